@@ -1,0 +1,85 @@
+"""Byte ledger and collective volumes of the pages (test infrastructure only).
+
+* Resident bytes per parameter ("07 · 显存模型", section 2.1 "每参数字节", and
+  "Parallelism strategies: which state to shard", section 九 Q1): bf16 param
+  (2 B), main grad (4 B fp32, or 2 B when grad_reduce_in_fp32 is off), fp32
+  master + Adam m + Adam v (12 B).  DDP keeps all of it; the distributed
+  optimizer (ZeRO-1) shards only the 12 B; ZeRO-2 also shards the grad; ZeRO-3 /
+  FSDP shards everything.
+* Per-rank send volume of a collective on n ranks with payload S bytes
+  ("Parallelism strategies: which state to shard", the ``coll_bytes`` listing in
+  its ledger appendix; section 一.1): all-reduce 2(n-1)/n S; all-gather,
+  reduce-scatter and all-to-all (n-1)/n S; send/recv S; nothing when n <= 1.
+* Dense GQA/SwiGLU/RMSNorm parameter count with a tied embedding ("07 · 显存模型",
+  section 2.2 "参数量估算"):
+  L [2 h q (1 + g/a) + 3 h ffn + 2 h] + V h, plus one final norm of h.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+PARAM_BYTES = 2          # bf16 param
+MASTER_ADAM_BYTES = 12   # fp32 master + m + v
+
+
+def bytes_per_param(scheme: str, n_d: int, grad_bytes: int = 4) -> Fraction:
+    """Resident bytes per parameter on one rank, as an exact fraction."""
+    n = Fraction(n_d)
+    p, g, k = PARAM_BYTES, grad_bytes, MASTER_ADAM_BYTES
+    if scheme == "ddp":
+        return Fraction(p + g + k)
+    if scheme in ("distopt", "zero1"):
+        return p + g + k / n
+    if scheme == "zero2":
+        return p + (g + k) / n
+    if scheme in ("fsdp", "zero3"):
+        return (p + g + k) / n
+    raise ValueError(scheme)
+
+
+def resident_bytes(scheme: str, n_params: int, n_d: int, grad_bytes: int = 4) -> Fraction:
+    return bytes_per_param(scheme, n_d, grad_bytes) * n_params
+
+
+def resident_breakdown_distopt(p_shard: int, dp: int, grad_bytes: int = 4) -> dict:
+    """(param, grad, optimizer) bytes of a DistOpt rank holding ``p_shard`` params."""
+    return {
+        "param": Fraction(PARAM_BYTES * p_shard),
+        "grad": Fraction(grad_bytes * p_shard),
+        "optimizer": Fraction(MASTER_ADAM_BYTES * p_shard, dp),
+    }
+
+
+def coll_bytes(kind: str, n: int, size: float) -> Fraction:
+    """Bytes one rank sends in a collective over ``n`` ranks with payload ``size``."""
+    s = Fraction(size)
+    if n <= 1 and kind != "send_recv":
+        return Fraction(0)
+    if kind == "all_reduce":
+        return 2 * Fraction(n - 1, n) * s
+    if kind in ("all_gather", "reduce_scatter", "all_to_all"):
+        return Fraction(n - 1, n) * s
+    if kind == "send_recv":
+        return s
+    raise ValueError(kind)
+
+
+def dense_param_count(h: int, layers: int, heads: int, kv_heads: int, head_dim: int, ffn: int,
+                      vocab: int, final_norm: bool = True, qk_norm: bool = False) -> int:
+    """Parameter count of a dense GQA / SwiGLU / RMSNorm stack with tied embedding.
+
+    ``qk_norm`` adds Qwen3's two head-dim RMSNorm weights per layer.
+    """
+    q = heads * head_dim
+    attn = Fraction(2 * h * q) * (1 + Fraction(kv_heads, heads))
+    per_layer = attn + 3 * h * ffn + 2 * h + (2 * head_dim if qk_norm else 0)
+    total = layers * per_layer + vocab * h + (h if final_norm else 0)
+    assert total.denominator == 1
+    return int(total)
+
+
+def sharded_step_bytes(n_d: int, grad_bytes: int) -> int:
+    """Minimum HBM bytes the fused step moves per valid element when N_d ranks
+    are buffers on one device: each rank's grad read once, fp32 master/m/v read
+    and written once, one bf16 param written per rank."""
+    return n_d * grad_bytes + 2 * MASTER_ADAM_BYTES + n_d * PARAM_BYTES
