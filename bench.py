@@ -1,0 +1,516 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 fused sharded mixed-precision step.
+
+Prints ONE JSON line (rank 0).  A "step" is one pass of the whole hot path -
+reduce-scatter of the N_d gradient buffers (rank-ordered fp32 sum / N_d),
+AdamW on the fp32 master/m/v shard, bf16 cast and all-gather into the N_d
+param buffers - over the workload's synthetic inputs, which are resident in
+HBM when the timed region starts.  Default workload: the Qwen3-0.6B-shaped
+stack with N_d = 8 in FSDP2 Shard(0) layout (596,049,920 params, 72 B moved
+per param).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|IDX]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Multi-GPU (torchrun, one rank per GPU): the step does not shard across GPUs
+(the N_d ranks already live on one device), so every GPU runs an independent
+replica; value = all ranks' params / max-over-ranks time ("weak" scaling).
+The control plane (barrier, max) uses gloo; the data path has no collective.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sharded-step params/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", "fsp_step.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------------
+# run-time context
+# --------------------------------------------------------------------------
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("fsp", "reference"), default="fsp")
+    ap.add_argument("--workload", default="qwen3_0p6b_fsdp2")
+    ap.add_argument("--param-slice", default=None,
+                    help="a:b - only params a..b-1 of the workload (small cases for profiling)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+class Dist:
+    """gloo control plane for barrier and max-over-ranks (no data-path use)."""
+
+    def __init__(self, n_gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+        if n_gpus != self.world and self.world > 1:
+            log(f"warning: --gpus {n_gpus} but WORLD_SIZE {self.world}")
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def traffic_per_elem(workload_name: str):
+    """ncu DRAM bytes per element of the step kernel, if the committed capture
+    was taken on the current kernel source and workload family."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_src") != kernel_src_hash():
+            return None
+        return float(kv[f"bytes_per_elem.{workload_name}"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if device_id:
+            cmd += ["-i", device_id]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception as e:  # no nvidia-smi
+            self.p, self.err = None, str(e)
+        self.t0 = self.t1 = None
+
+    def start_window(self):
+        time.sleep(1.0)
+        self.t0 = datetime.datetime.now()
+
+    def end_window(self):
+        self.t1 = datetime.datetime.now()
+        time.sleep(0.15)
+
+    def result(self) -> dict:
+        if self.p is None:
+            return {"error": self.err}
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except Exception:
+            self.p.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = []
+        for line in self.tmp.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
+                continue
+            rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"error": "no samples inside the timed region"}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())
+                if any(r[4].replace(".", "").isdigit() for r in rows) else None}
+
+
+def clocks_bad(c: dict) -> bool:
+    if "error" in c:
+        return False
+    if any(r in BAD_REASONS for r in c.get("reasons", [])):
+        return True
+    sm, mx = c.get("sm_mhz"), c.get("sm_max_mhz")
+    return bool(sm and mx and sm < 0.5 * mx and not c.get("reasons"))
+
+
+# --------------------------------------------------------------------------
+# workload on the device
+# --------------------------------------------------------------------------
+
+def resolve_workload(name: str, param_slice: str | None):
+    import synth_inputs as S
+    w = S.workload(int(name)) if name.isdigit() else S.workload(name)
+    shapes = w.shapes
+    label = w.name
+    if param_slice:
+        a, b = (int(x) if x else None for x in param_slice.split(":"))
+        shapes = shapes[a:b]
+        label = f"{w.name}[{param_slice}]"
+    return w, tuple(shapes), label
+
+
+class DeviceWorkload:
+    def __init__(self, w, shapes, device):
+        import torch
+        import fsdp_sharded_mixed_pass_gb300 as fsp
+        from synth_inputs import device as D
+        self.w, self.device = w, device
+        self.plan = fsp.plan_layout(shapes, w.n_d, w.mode)
+        p = self.plan
+        gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
+        self.grads = [torch.empty(p.full_len_padded, dtype=gdt, device=device) for _ in range(w.n_d)]
+        for q, g in enumerate(self.grads):
+            D.fill_grad(g, w.data_seed, q, w.grad_dtype)
+        self.state = [torch.zeros(p.state_len_total, dtype=torch.float32, device=device) for _ in range(3)]
+        D.fill_state_segments(*self.state, w.data_seed, [(s.full_off, s.state_off, s.length) for s in p.segments])
+        self.params = [torch.zeros(p.full_len_padded, dtype=torch.bfloat16, device=device) for _ in range(w.n_d)]
+        torch.cuda.synchronize(device)
+        self.t = w.step
+
+    def step(self, stream):
+        import fsdp_sharded_mixed_pass_gb300 as fsp
+        fsp.sharded_step(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t, stream=stream)
+        self.t += 1
+
+
+def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id):
+    import torch
+    stream = torch.cuda.Stream(device=wl.device)
+    for _ in range(warmup):
+        wl.step(stream)
+    stream.synchronize()
+    sampler = ClockSampler(clocks_id)
+    sampler.start_window()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(wl.device)
+    start.record(stream)
+    for _ in range(steps):
+        wl.step(stream)
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize(wl.device)
+    dist.barrier()
+    sampler.end_window()
+    ms = start.elapsed_time(end)
+    return ms, sampler.result()
+
+
+def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist):
+    """Same step through the public API with host (pinned) inputs and outputs:
+    every step copies the N_d gradient buffers host->device and reads the N_d
+    bf16 param buffers back, all inside the timed region."""
+    import torch
+    p = wl.plan
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in wl.grads]
+    host_p = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in wl.params]
+    for h, g in zip(host_g, wl.grads):
+        h.copy_(g)
+    stream = torch.cuda.Stream(device=wl.device)
+    import fsdp_sharded_mixed_pass_gb300 as fsp
+
+    def one():
+        with torch.cuda.stream(stream):
+            for d, h in zip(wl.grads, host_g):
+                d.copy_(h, non_blocking=True)
+            fsp.sharded_step(wl.plan, wl.grads, *wl.state, wl.params, wl.w.hparams(), wl.t, stream=stream)
+            wl.t += 1
+            for h, d in zip(host_p, wl.params):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    one()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    dist.barrier()
+    h2d = sum(g.numel() * g.element_size() for g in host_g)
+    d2h = sum(x.numel() * x.element_size() for x in host_p)
+    del host_g, host_p
+    return dt, h2d, d2h
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing
+# --------------------------------------------------------------------------
+
+def cpu_sample_shapes(w, max_elems=16_000_000):
+    """A contiguous run of the workload's params (skipping any single param over
+    32M elements, e.g. an embedding) of about ``max_elems`` elements."""
+    out, total = [], 0
+    for s in w.shapes:
+        n = 1
+        for d in s:
+            n *= d
+        if n > 32_000_000:
+            continue
+        if out and total + n > max_elems:
+            break
+        out.append(s)
+        total += n
+    return tuple(out), total
+
+
+def oracle_inputs(w, shapes, use_device: bool):
+    """Host inputs of the sample in the oracle's layout (generated on the device
+    by the shared generator when one is present - same bits as the host one)."""
+    import numpy as np
+    import synth_inputs as S
+    from oracle import plan as OP
+    op = OP.plan_layout(shapes, w.n_d, w.mode)
+    fi, si = OP.owned_indices(op)
+    n = op.full_len_padded
+    if use_device:
+        import torch
+        from synth_inputs import device as D
+        grads = []
+        for q in range(w.n_d):
+            t = torch.empty(n, dtype=torch.float32 if w.grad_dtype == "f32" else torch.bfloat16, device="cuda")
+            D.fill_grad(t, w.data_seed, q, w.grad_dtype)
+            a = t.cpu().numpy() if w.grad_dtype == "f32" else t.view(torch.int16).cpu().numpy().view(np.uint16)
+            grads.append(a)
+        del t
+    else:
+        idx = np.arange(n)
+        grads = [S.grad_f32(w.data_seed, q, idx) if w.grad_dtype == "f32" else S.grad_bf16_bits(w.data_seed, q, idx)
+                 for q in range(w.n_d)]
+    state = []
+    for fn in (S.master_f32, S.adam_m_f32, S.adam_v_f32):
+        a = np.zeros(op.state_len_total, np.float32)
+        a[si] = fn(w.data_seed, fi)
+        state.append(a)
+    params = [np.zeros(n, np.uint16) for _ in range(w.n_d)]
+    return op, grads, state, params
+
+
+def cpu_threads_used() -> int:
+    # numpy's elementwise kernels run on the calling thread
+    return 1
+
+
+def time_oracle(w, shapes, seconds: float, use_device: bool, max_reps: int = 1000):
+    from oracle import step as OS
+    op, grads, state, params = oracle_inputs(w, shapes, use_device)
+    t = w.step
+    reps, total = 0, 0.0
+    while total < seconds and reps < max_reps:
+        t0 = time.perf_counter()
+        OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+        total += time.perf_counter() - t0
+        reps += 1
+        t += 1
+    return op.valid_elems, reps, total
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def config_block(w, label, plan, l2_bytes=None):
+    per = w.n_d * w.grad_bytes + 24 + 2 * w.n_d
+    moved = per * plan.valid_elems
+    return {
+        "workload": label,
+        "n_d": w.n_d,
+        "mode": w.mode,
+        "grad_dtype": w.grad_dtype,
+        "params": plan.valid_elems,
+        "bytes_per_param": per,
+        "bytes_per_step": moved,
+        "l2": "inputs larger than L2: every step streams the whole working set" if moved > 4 * 129e6
+        else "working set fits in L2 (small case)",
+        "parallelism": "replicas",
+    }
+
+
+def run_fsp(args):
+    import torch
+    dist = Dist(args.gpus)
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w, shapes, label = resolve_workload(args.workload, args.param_slice)
+    wl = DeviceWorkload(w, shapes, dev)
+    plan = wl.plan
+    props = torch.cuda.get_device_properties(dev)
+    clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
+
+    ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id)
+    remeasured = False
+    if clocks_bad(clocks):
+        log(f"clocks rejected ({clocks}); measuring again")
+        ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id)
+        remeasured = True
+    ms_max = dist.max(ms)
+    P = plan.valid_elems
+    total_params = P * args.steps * dist.world
+    value = total_params / (ms_max / 1e3)
+    per = w.n_d * w.grad_bytes + 24 + 2 * w.n_d
+    launch_s = ms / 1e3 / args.steps
+    achieved = per * P / launch_s / 1e9
+    peak, peak_src = read_peak()
+    tpe = traffic_per_elem(w.name)
+
+    e2e = None
+    if not args.no_e2e:
+        dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist)
+        dt = dist.max(dt)
+        e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "fsdp_sharded_mixed_pass_gb300.sharded_step with pinned host copies (torch)"}
+
+    cpu = None
+    if dist.world == 1 and not args.no_cpu_baseline:
+        sshapes, _ = cpu_sample_shapes(w)
+        n, reps, secs = time_oracle(w, sshapes, args.cpu_seconds, use_device=True)
+        cpu = {"value": n * reps / secs, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": f"{len(sshapes)} params ({n} elements) of {w.name}, N_d={w.n_d}, "
+                         f"oracle step repeated {reps}x ({secs:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(w, label, plan),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "traffic": tpe * P if tpe is not None else None,
+                     "kernel": "sharded_step_kernel", "kernel_src": kernel_src_hash()},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if remeasured:
+        line["clocks_remeasured"] = True
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_reference(args):
+    dist_rank = int(os.environ.get("RANK", "0"))
+    if dist_rank != 0:
+        return
+    w, shapes, label = resolve_workload(args.workload, args.param_slice)
+    # per step, a bounded sample sized so the whole run stays within ~2 minutes
+    budget_elems = max(100_000, min(16_000_000, int(120 * 15e6 / max(1, args.steps + args.warmup))))
+    sshapes, _ = cpu_sample_shapes(w, budget_elems)
+    use_device = False
+    try:
+        import torch
+        use_device = torch.cuda.is_available()
+        if use_device:
+            from synth_inputs import device as D
+            D.lib()
+    except Exception:
+        use_device = False
+    from oracle import step as OS
+    op, grads, state, params = oracle_inputs(w, sshapes, use_device)
+    t = w.step
+    for _ in range(args.warmup):
+        OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+        t += 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+        t += 1
+    secs = time.perf_counter() - t0
+    value = op.valid_elems * args.steps / secs
+    plan_like = type("P", (), {"valid_elems": op.valid_elems})
+    cfg = config_block(w, label, plan_like)
+    cfg["sample_params"] = op.valid_elems
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+                         "sample": f"{len(sshapes)} params ({op.valid_elems} elements) of {w.name} per step, "
+                                   f"N_d={w.n_d}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_fsp(args)
+
+
+if __name__ == "__main__":
+    main()

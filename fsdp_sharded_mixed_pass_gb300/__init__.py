@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) sharded mixed-precision optimizer step.
+
+One data-parallel ZeRO / FSDP step with N_d ranks simulated as N_d buffers on
+one GPU: rank-ordered fp32 reduce-scatter averaged by N_d, AdamW on the fp32
+master / m / v shard, bf16 cast and all-gather into every rank's param buffer,
+fused into one streaming CUDA kernel behind the C ABI in ``include/fsp.h``.
+
+    from fsdp_sharded_mixed_pass_gb300 import plan_layout, sharded_step
+"""
+from .fsp import (  # noqa: F401
+    EXPORTS,
+    FspError,
+    Plan,
+    Segment,
+    lib,
+    plan_layout,
+    sharded_step,
+    sharded_step_debug,
+)

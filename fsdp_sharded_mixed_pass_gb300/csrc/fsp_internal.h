@@ -1,0 +1,60 @@
+// Internal declarations shared by the planner (fsp_plan.cpp) and the step
+// (fsp_step.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "fsp.h"
+
+namespace fsp {
+
+constexpr int kMaxRanks = 64;
+constexpr int kMaxDims = 8;
+// Work tiles never cross a multiple of this many elements of the full-size
+// buffers, so only a segment's first and last tile can start or end off a
+// vector boundary.
+constexpr int64_t kTileElems = 4096;
+// State segments start at a slot congruent to their full-buffer offset modulo
+// this, so grads, params and state share vector alignment.
+constexpr int64_t kStateAlign = 16;
+// DistOpt buffers are padded to a multiple of lcm(N_d, this).
+constexpr int64_t kDistOptAlign = 128;
+
+// One unit of work for a CTA: `len` elements starting at `full_begin` of every
+// full-size buffer and at `state_begin` of the state buffers.  32 bytes so a
+// descriptor is two aligned 16-byte loads.
+struct Tile {
+  int64_t full_begin;
+  int64_t state_begin;
+  int64_t len;
+  int64_t reserved;
+};
+static_assert(sizeof(Tile) == 32, "tile descriptor layout");
+
+}  // namespace fsp
+
+struct fsp_plan {
+  int32_t n_d = 0;
+  int32_t n_params = 0;
+  int32_t mode = 0;
+  int64_t valid_elems = 0;
+  int64_t full_len_padded = 0;
+  int64_t state_len_per_rank = 0;
+  int64_t state_len_total = 0;
+  std::vector<fsp_segment> segments;
+  std::vector<fsp::Tile> tiles;
+
+  // Device copies of `tiles`, one per device ordinal, uploaded on first use.
+  mutable std::mutex mu;
+  mutable std::map<int, fsp::Tile*> device_tiles;
+};
+
+namespace fsp {
+// Records the thread-local message behind an error status and returns it.
+fsp_status fail(fsp_status s, const std::string& msg);
+void clear_error();
+}  // namespace fsp

@@ -1,0 +1,222 @@
+"""ctypes binding of libfsp.so (``include/fsp.h``): argument marshalling only.
+
+Every step of the sharded update runs in the library's CUDA kernel; nothing
+here computes any of it, and there is no fallback: if the library is missing
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfsp.so")
+
+FSP_OK, FSP_EINVAL, FSP_ENOMEM, FSP_ECUDA, FSP_EUNSUPPORTED = range(5)
+MODES = {"fsdp2": 0, "distopt": 1}
+DTYPES = {"f32": 0, "bf16": 1}
+
+# Every symbol include/fsp.h declares.
+EXPORTS = ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
+           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_status_string", "fsp_last_error")
+
+
+class FspError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("n_d", ctypes.c_int32), ("n_params", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("tile_elems", ctypes.c_int32), ("valid_elems", ctypes.c_int64),
+                ("full_len_padded", ctypes.c_int64), ("state_len_per_rank", ctypes.c_int64),
+                ("state_len_total", ctypes.c_int64), ("n_segments", ctypes.c_int64), ("n_tiles", ctypes.c_int64)]
+
+
+class _Segment(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_int32), ("rank", ctypes.c_int32), ("full_off", ctypes.c_int64),
+                ("state_off", ctypes.c_int64), ("len", ctypes.c_int64), ("padded_len", ctypes.c_int64)]
+
+
+class _Ledger(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("resident_ddp", "resident_distopt", "resident_zero2",
+                                               "resident_fsdp", "reduce_scatter_sent", "all_gather_sent",
+                                               "step_hbm_bytes")]
+
+
+class _HParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with fsdp_sharded_mixed_pass_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.fsp_plan_layout.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32, i32,
+                                  ctypes.POINTER(vp)]
+    L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
+    L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
+    L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
+    L.fsp_plan_destroy.argtypes = [vp]
+    L.fsp_plan_destroy.restype = None
+    step_args = [vp, ctypes.POINTER(vp), i32, vp, vp, vp, ctypes.POINTER(vp), ctypes.POINTER(_HParams), i64]
+    L.fsp_sharded_step.argtypes = step_args + [vp]
+    L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
+    for fn in ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
+               "fsp_sharded_step_debug"):
+        getattr(L, fn).restype = ctypes.c_int
+    L.fsp_status_string.argtypes = [ctypes.c_int]
+    L.fsp_status_string.restype = ctypes.c_char_p
+    L.fsp_last_error.argtypes = []
+    L.fsp_last_error.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != FSP_OK:
+        L = lib()
+        raise FspError(status, f"{what}: {L.fsp_status_string(status).decode()}: {L.fsp_last_error().decode()}")
+
+
+@dataclass(frozen=True)
+class Segment:
+    param: int
+    rank: int
+    full_off: int
+    state_off: int
+    length: int
+    padded_len: int
+
+
+class Plan:
+    """A layout plan (owns the library handle)."""
+
+    def __init__(self, handle: int, shapes, mode: str):
+        self._h = ctypes.c_void_p(handle)
+        self.shapes = tuple(tuple(int(d) for d in s) for s in shapes)
+        self.mode = mode
+        info = _PlanInfo()
+        _check(lib().fsp_plan_info_get(self._h, ctypes.byref(info)), "fsp_plan_info_get")
+        self.n_d = info.n_d
+        self.n_params = info.n_params
+        self.tile_elems = info.tile_elems
+        self.valid_elems = info.valid_elems
+        self.full_len_padded = info.full_len_padded
+        self.state_len_per_rank = info.state_len_per_rank
+        self.state_len_total = info.state_len_total
+        self.n_segments = info.n_segments
+        self.n_tiles = info.n_tiles
+        self._segments = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def segments(self) -> tuple:
+        if self._segments is None:
+            out, seg = [], _Segment()
+            for i in range(self.n_segments):
+                _check(lib().fsp_plan_segment(self._h, i, ctypes.byref(seg)), "fsp_plan_segment")
+                out.append(Segment(seg.param, seg.rank, seg.full_off, seg.state_off, seg.len, seg.padded_len))
+            self._segments = tuple(out)
+        return self._segments
+
+    def ledger(self, grad_dtype: str = "f32") -> dict:
+        led = _Ledger()
+        _check(lib().fsp_plan_ledger(self._h, DTYPES[grad_dtype], ctypes.byref(led)), "fsp_plan_ledger")
+        return {n: getattr(led, n) for n, _ in _Ledger._fields_}
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            lib().fsp_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def plan_layout(shapes, n_d: int, mode: str = "fsdp2") -> Plan:
+    """FSDP2 Shard(0) (``mode="fsdp2"``) or DistOpt flat (``"distopt"``) plan."""
+    shapes = [tuple(int(d) for d in s) for s in shapes]
+    dims = [d for s in shapes for d in s]
+    nd = [len(s) for s in shapes]
+    dims_arr = (ctypes.c_int64 * max(1, len(dims)))(*dims)
+    nd_arr = (ctypes.c_int32 * max(1, len(nd)))(*nd)
+    out = ctypes.c_void_p()
+    if mode not in MODES:
+        raise ValueError(f"unknown mode {mode!r}")
+    _check(lib().fsp_plan_layout(dims_arr, nd_arr, len(shapes), int(n_d), MODES[mode], ctypes.byref(out)),
+           "fsp_plan_layout")
+    return Plan(out.value, shapes, mode)
+
+
+def _ptr(x) -> int:
+    return int(x) if isinstance(x, int) else int(x.data_ptr())
+
+
+def _grad_dtype(grad_bufs, grad_dtype):
+    if grad_dtype is not None:
+        return grad_dtype
+    import torch
+    dt = grad_bufs[0].dtype
+    if dt == torch.float32:
+        return "f32"
+    if dt == torch.bfloat16:
+        return "bf16"
+    raise TypeError(f"unsupported gradient dtype {dt}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _hp(hparams) -> _HParams:
+    h = _HParams()
+    for k in ("lr", "beta1", "beta2", "eps", "weight_decay"):
+        setattr(h, k, float(hparams[k]))
+    return h
+
+
+def _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype):
+    if len(grad_bufs) != plan.n_d or len(param_bufs) != plan.n_d:
+        raise ValueError(f"need {plan.n_d} grad and param buffers")
+    gd = _grad_dtype(grad_bufs, grad_dtype)
+    g = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in grad_bufs])
+    p = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
+    return [plan.handle, g, DTYPES[gd], ctypes.c_void_p(_ptr(master)), ctypes.c_void_p(_ptr(exp_avg)),
+            ctypes.c_void_p(_ptr(exp_avg_sq)), p, ctypes.byref(_hp(hparams)), int(step)]
+
+
+def sharded_step(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
+                 stream=None, grad_dtype: str | None = None) -> None:
+    """One fused reduce-scatter + AdamW + bf16 all-gather step (asynchronous)."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step(*args, ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step")
+
+
+def sharded_step_debug(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
+                       reduced_grad, stream=None, grad_dtype: str | None = None) -> None:
+    """``sharded_step`` that also stores the averaged shard gradient."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step_debug(*args, ctypes.c_void_p(_ptr(reduced_grad)),
+                                        ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_debug")

@@ -1,0 +1,187 @@
+/*
+ * fsp.h - C ABI of the GB300 sharded mixed-precision optimizer step.
+ *
+ * One data-parallel training step of ZeRO / FSDP with N_d ranks simulated as
+ * N_d separate buffers on one GPU:
+ *
+ *   (1) reduce-scatter: the owner of every element receives the sum over all
+ *       ranks of that element's gradient, taken as an fp32 left fold in rank
+ *       order 0..N_d-1, then divided (IEEE, round to nearest) by N_d.
+ *       "FSDP2 Qwen3 Decoder Layer Walkthrough", section "Backward 简述";
+ *       "Parallelism strategies: which state to shard", section 二.2.
+ *   (2) AdamW on the owner's fp32 master / Adam m / Adam v shard, with no
+ *       communication.  "07 · 显存模型", section 2.1 (fp32 master + m/v).
+ *   (3) cast of the new master to bf16 (round to nearest even) and all-gather
+ *       into every rank's full bf16 param buffer.
+ *       "FSDP2 Qwen3 Decoder Layer Walkthrough", section "Step 0".
+ *
+ * Steps (1)-(3) run as one fused streaming kernel: every gradient is read
+ * once, the fp32 state is read and written once, every bf16 copy is written
+ * once; the reduced gradient is never stored (except by the debug entry).
+ *
+ * Conventions for every function below:
+ *   - Return FSP_OK or an error status; fsp_last_error() then gives a
+ *     one-line, thread-local description.  Argument errors are detected on the
+ *     host before anything is launched; no function traps, asserts or waits on
+ *     the device.
+ *   - The caller owns every device buffer and the CUDA stream.  The library
+ *     owns plans and, per device, a small read-only table of work tiles that a
+ *     plan uploads on its first step on that device (one cudaMalloc and one
+ *     synchronous copy; make that first call outside any stream capture).
+ *   - Steps are asynchronous on the given stream (NULL = legacy default
+ *     stream) and run on the current CUDA device.
+ *   - A plan may be used from several threads at once; fsp_plan_destroy must
+ *     not race with any call or in-flight step using the same plan.
+ */
+#ifndef FSP_H
+#define FSP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FSP_OK = 0,
+  FSP_EINVAL = 1,        /* bad argument (null, range, alignment, overlap, size) */
+  FSP_ENOMEM = 2,        /* host or device allocation failed                       */
+  FSP_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed             */
+  FSP_EUNSUPPORTED = 4   /* valid request this build does not handle               */
+} fsp_status;
+
+typedef enum {
+  /* FSDP2 per-parameter Shard(0): each parameter is split on dim 0 into N_d
+   * chunks of c = ceil(rows / N_d) rows; rank r owns rows [r*c, min((r+1)*c,
+   * rows)) and holds a padded shard of c rows.  "FSDP2 Qwen3 Decoder Layer
+   * Walkthrough", section "FSDP2 设置"; "Parallelism strategies: which state to
+   * shard", section 二.5. */
+  FSP_MODE_FSDP2_SHARD0 = 0,
+  /* Megatron distributed optimizer (ZeRO-1): all parameters form one flat
+   * buffer padded to a multiple of lcm(N_d, 128) and cut into N_d equal
+   * contiguous shards that ignore parameter boundaries.  "07 · 显存模型",
+   * section 2.1 item 1 and section 8 item 4. */
+  FSP_MODE_DISTOPT_FLAT = 1
+} fsp_mode;
+
+typedef enum {
+  FSP_DTYPE_F32 = 0,     /* fp32 main grads (grad_reduce_in_fp32 on)            */
+  FSP_DTYPE_BF16 = 1     /* bf16 grads, widened exactly and reduced in fp32      */
+} fsp_dtype;
+
+typedef struct fsp_plan fsp_plan;   /* opaque; created by fsp_plan_layout */
+
+/* AdamW hyper-parameters (fp32).  Update index t is passed to the step.
+ * Requires lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0, weight_decay >= 0,
+ * all finite. */
+typedef struct {
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+} fsp_adamw_hparams;
+
+/* Sizes of the buffers a step on this plan reads and writes (in elements). */
+typedef struct {
+  int32_t n_d;
+  int32_t n_params;
+  int32_t mode;                 /* fsp_mode                                          */
+  int32_t tile_elems;           /* largest work tile                                 */
+  int64_t valid_elems;          /* P: parameters in the model                        */
+  int64_t full_len_padded;      /* length of each grad_bufs[r] and param_bufs[r]      */
+  int64_t state_len_per_rank;   /* one rank's shard of master / m / v                 */
+  int64_t state_len_total;      /* length of master, m and v: n_d * state_len_per_rank */
+  int64_t n_segments;
+  int64_t n_tiles;
+} fsp_plan_info;
+
+/* One contiguous run of a rank's shard.  Elements [full_off, full_off + len)
+ * of every full-size buffer live in slots [state_off, state_off + len) of
+ * master / m / v; slots [state_off + len, state_off + padded_len) are shard
+ * padding and are never written.  param = -1 for a DistOpt shard. */
+typedef struct {
+  int32_t param;
+  int32_t rank;
+  int64_t full_off;
+  int64_t state_off;
+  int64_t len;
+  int64_t padded_len;
+} fsp_segment;
+
+/* Per-rank byte ledger of this plan's model ("07 · 显存模型", section 2.1;
+ * "Parallelism strategies: which state to shard", section 九 Q1 and its
+ * coll_bytes listing), for the given gradient dtype. */
+typedef struct {
+  double resident_ddp;        /* (2 + g + 12) P                     */
+  double resident_distopt;    /* (2 + g) P + 12 P / N_d             */
+  double resident_zero2;      /* 2 P + (g + 12) P / N_d             */
+  double resident_fsdp;       /* (2 + g + 12) P / N_d               */
+  double reduce_scatter_sent; /* (N_d - 1) / N_d * g P              */
+  double all_gather_sent;     /* (N_d - 1) / N_d * 2 P              */
+  double step_hbm_bytes;      /* (N_d g + 24 + 2 N_d) P: one fused step on one GPU */
+} fsp_ledger;
+
+/* Plans the layout of n_params parameters over n_d simulated ranks.
+ *   dims:    the parameters' shapes, row-major, concatenated (sum of ndims
+ *            entries, each >= 0); host memory, read during the call only.
+ *   ndims:   number of dims of each parameter, 1..8.
+ *   n_params >= 0 (0 gives an empty plan), 1 <= n_d <= 64, mode an fsp_mode.
+ * FSDP2 state placement: master/m/v are rank-major (rank r's shard starts at
+ * r * state_len_per_rank); inside a rank, segments follow parameter order and
+ * each starts at the first slot at or after the previous one's end that is
+ * congruent to its full_off modulo 16.  DistOpt: state index = flat index.
+ * On success *out owns a new plan (free with fsp_plan_destroy). */
+fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                           int32_t n_d, int32_t mode, fsp_plan** out);
+
+fsp_status fsp_plan_info_get(const fsp_plan* plan, fsp_plan_info* out);
+
+/* Segment i (0 <= i < n_segments).  FSDP2: ordered by rank, then parameter.
+ * DistOpt: one segment per rank. */
+fsp_status fsp_plan_segment(const fsp_plan* plan, int64_t i, fsp_segment* out);
+
+fsp_status fsp_plan_ledger(const fsp_plan* plan, int32_t grad_dtype, fsp_ledger* out);
+
+/* Frees the plan and its device tile tables.  NULL is a no-op. */
+void fsp_plan_destroy(fsp_plan* plan);
+
+/* The fused step (1)-(3), asynchronous on `cuda_stream` (a cudaStream_t).
+ *   grad_bufs:  host array of n_d device pointers, each full_len_padded
+ *               elements of grad_dtype; only read.
+ *   master, exp_avg, exp_avg_sq: device, fp32, state_len_total elements each;
+ *               updated in place at owned slots only.
+ *   param_bufs: host array of n_d device pointers, each full_len_padded bf16
+ *               elements; owned elements written, padding untouched.
+ *   hp:         host pointer; step: t >= 1, the 1-based index of this update
+ *               (bias corrections use beta^t).
+ * Every device pointer must be 16-byte aligned and no two buffers may
+ * overlap.  Each device pointer must lie in a live CUDA allocation that holds
+ * the whole buffer (checked with the driver).  An empty plan returns FSP_OK
+ * and launches nothing. */
+fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
+                            float* master, float* exp_avg, float* exp_avg_sq,
+                            void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                            void* cuda_stream);
+
+/* As fsp_sharded_step, and also stores the averaged shard gradient of every
+ * owned element into reduced_grad (device, fp32, state layout,
+ * state_len_total elements; padding slots untouched).  For testing: it adds
+ * 8 bytes of traffic per element. */
+fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
+                                  float* master, float* exp_avg, float* exp_avg_sq,
+                                  void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                                  float* reduced_grad, void* cuda_stream);
+
+/* Message for a status code (static storage). */
+const char* fsp_status_string(fsp_status status);
+
+/* Description of the last error returned on the calling thread ("" if none). */
+const char* fsp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSP_H */

@@ -89,17 +89,28 @@ def _words(key: int, idx: np.ndarray, j: int) -> np.ndarray:
         return mix64(np.uint64(key) + np.uint64(GAMMA) * ctr)
 
 
+_CHUNK = 1 << 16   # elements per pass: keeps the temporaries in cache
+
+
+def _normal_chunk(key: int, flat: np.ndarray, sigma) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        ctr = flat.astype(np.uint64)[:, None] * np.uint64(3) + np.arange(1, 4, dtype=np.uint64)[None, :]
+        w = mix64(np.uint64(key) + np.uint64(GAMMA) * ctr)          # (n, 3) words
+    # the twelve 16-bit fields of the three words, summed (order-free)
+    s = w.view(np.uint16).reshape(-1, 12).sum(axis=1, dtype=np.int64)
+    n = 2 * s - 12 * 65535
+    unit = n.astype(np.float32) * np.float32(2.0 ** -17)  # exact: |n| < 2**24
+    return unit * np.float32(sigma)
+
+
 def normal_f32(key: int, idx: np.ndarray, sigma) -> np.ndarray:
     """Irwin-Hall(12) approximate N(0, sigma) in fp32 at logical indices ``idx``."""
     idx = np.asarray(idx, dtype=np.int64)
-    s = np.zeros(idx.shape, dtype=np.int64)
-    for j in range(3):
-        w = _words(key, idx, j)
-        for k in range(4):
-            s += ((w >> np.uint64(16 * k)) & np.uint64(0xFFFF)).astype(np.int64)
-    n = 2 * s - 12 * 65535
-    unit = n.astype(np.float32) * np.float32(2.0 ** -17)  # exact: |n| < 2**24
-    return (unit * np.float32(sigma)).astype(np.float32)
+    flat = idx.reshape(-1)
+    out = np.empty(flat.size, dtype=np.float32)
+    for a in range(0, flat.size, _CHUNK):
+        out[a:a + _CHUNK] = _normal_chunk(key, flat[a:a + _CHUNK], sigma)
+    return out.reshape(idx.shape)
 
 
 def uniform_f32(key: int, idx: np.ndarray, hi) -> np.ndarray:

@@ -1,0 +1,162 @@
+"""Shared machinery of the GPU parity tests: device buffers with guard bands,
+inputs from the seeded generator, and comparison with the oracle."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import fsdp_sharded_mixed_pass_gb300 as fsp
+import synth_inputs as S
+from oracle import plan as OP
+from oracle import step as OS
+from synth_inputs import device as D
+
+HP = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+GUARD_BYTES = 4096
+STATE_SENTINEL = 0x7FC0DEAD          # a NaN pattern no computation produces
+PARAM_SENTINEL = 0xFFFF              # bf16 NaN pattern
+GUARD_WORD = 0x5A5A5A5A
+
+
+def ensure_built():
+    from fsdp_sharded_mixed_pass_gb300 import build
+    from fsdp_sharded_mixed_pass_gb300 import fsp as B
+    if not os.path.exists(B.LIB_PATH):
+        build.build()
+    if not os.path.exists(D.LIB):
+        D.build()
+
+
+class Guarded:
+    """A device buffer of ``n`` elements with a guard band on both sides."""
+
+    def __init__(self, n: int, dtype: torch.dtype, fill_bits: int, device="cuda"):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        g = GUARD_BYTES // esz
+        self.g, self.n = g, n
+        int_dtype = {4: torch.int32, 2: torch.int16}[esz]
+        self.raw = torch.empty(n + 2 * g, dtype=int_dtype, device=device)
+        guard = np.array([GUARD_WORD], np.uint32).view(np.int32)[0] if esz == 4 else np.int16(0x5A5A)
+        self.raw.fill_(int(guard))
+        fill = np.array([fill_bits], np.uint32 if esz == 4 else np.uint16).view(
+            np.int32 if esz == 4 else np.int16)[0]
+        self.raw[g:g + n].fill_(int(fill))
+        self.t = self.raw[g:g + n].view(dtype)
+        self._guard = int(guard)
+
+    def guards_intact(self) -> bool:
+        return bool((self.raw[:self.g] == self._guard).all() and (self.raw[self.g + self.n:] == self._guard).all())
+
+    def bits(self) -> np.ndarray:
+        a = self.raw[self.g:self.g + self.n].cpu().numpy()
+        return a.view(np.uint32 if a.dtype == np.int32 else np.uint16)
+
+
+def ordered(bits: np.ndarray) -> np.ndarray:
+    """Bit patterns mapped to integers that order like the float values."""
+    if bits.dtype == np.uint32:
+        i = bits.view(np.int32).astype(np.int64)
+        return np.where(i < 0, -(2 ** 31) - i, i)
+    i = bits.view(np.int16).astype(np.int64)
+    return np.where(i < 0, -(2 ** 15) - i, i)
+
+
+def ulp_dist(a_bits, b_bits) -> np.ndarray:
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def within_tol(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """|got - ref| <= 1e-6 * max(1, |ref|) elementwise."""
+    g = got.astype(np.float64)
+    r = ref.astype(np.float64)
+    return np.abs(g - r) <= 1e-6 * np.maximum(1.0, np.abs(r))
+
+
+class DeviceCase:
+    """A plan plus guarded device buffers filled from the seeded generator."""
+
+    def __init__(self, shapes, n_d, mode, grad_dtype, seed):
+        self.shapes, self.n_d, self.mode, self.grad_dtype, self.seed = shapes, n_d, mode, grad_dtype, seed
+        self.plan = fsp.plan_layout(shapes, n_d, mode)
+        p = self.plan
+        gdt = torch.float32 if grad_dtype == "f32" else torch.bfloat16
+        self.grads = [Guarded(p.full_len_padded, gdt, 0) for _ in range(n_d)]
+        for q, g in enumerate(self.grads):
+            D.fill_grad(g.t, seed, q, grad_dtype)
+        self.state = [Guarded(p.state_len_total, torch.float32, STATE_SENTINEL) for _ in range(3)]
+        self.reduced = Guarded(p.state_len_total, torch.float32, STATE_SENTINEL)
+        D.fill_state_segments(self.state[0].t, self.state[1].t, self.state[2].t, seed,
+                              [(s.full_off, s.state_off, s.length) for s in p.segments])
+        self.params = [Guarded(p.full_len_padded, torch.bfloat16, PARAM_SENTINEL) for _ in range(n_d)]
+        torch.cuda.synchronize()
+
+    def step(self, t, debug=True, hp=HP):
+        st = [s.t for s in self.state]
+        if debug:
+            fsp.sharded_step_debug(self.plan, [g.t for g in self.grads], *st, [q.t for q in self.params], hp, t,
+                                   self.reduced.t)
+        else:
+            fsp.sharded_step(self.plan, [g.t for g in self.grads], *st, [q.t for q in self.params], hp, t)
+
+    def all_guards_intact(self):
+        return all(b.guards_intact() for b in self.grads + self.state + self.params + [self.reduced])
+
+
+class OracleCase:
+    """The same inputs on the host, from the oracle's planner and the host generator."""
+
+    def __init__(self, shapes, n_d, mode, grad_dtype, seed):
+        self.plan = OP.plan_layout(shapes, n_d, mode)
+        self.grad_dtype = grad_dtype
+        p = self.plan
+        idx = np.arange(p.full_len_padded)
+        if grad_dtype == "f32":
+            self.grads = [S.grad_f32(seed, q, idx) for q in range(n_d)]
+        else:
+            self.grads = [S.grad_bf16_bits(seed, q, idx) for q in range(n_d)]
+        self.fi, self.si = OP.owned_indices(p)
+        self.state = []
+        for fn in (S.master_f32, S.adam_m_f32, S.adam_v_f32):
+            a = np.full(p.state_len_total, STATE_SENTINEL, np.uint32).view(np.float32)
+            a[self.si] = fn(seed, self.fi)
+            self.state.append(a)
+        self.params = [np.full(p.full_len_padded, PARAM_SENTINEL, np.uint16) for _ in range(n_d)]
+        self.reduced = np.full(p.state_len_total, STATE_SENTINEL, np.uint32).view(np.float32)
+
+    def step(self, t, hp=HP):
+        OS.sharded_step(self.plan, self.grads, self.grad_dtype, *self.state, self.params, hp, t,
+                        reduced_out=self.reduced)
+
+
+def compare(dev: DeviceCase, ora: OracleCase, check_reduced=True) -> dict:
+    """Asserts parity; returns error statistics."""
+    si = ora.si
+    stats = {}
+    names = ("master", "exp_avg", "exp_avg_sq")
+    for name, d, o in zip(names, dev.state, ora.state):
+        got = d.bits()
+        want = o.view(np.uint32)
+        ok = within_tol(got[si].view(np.float32), want[si].view(np.float32))
+        assert ok.all(), f"{name}: {int((~ok).sum())} of {ok.size} outside 1e-6*max(1,|ref|)"
+        stats[name + "_max_ulp"] = int(ulp_dist(got[si], want[si]).max()) if si.size else 0
+        # slots nobody owns keep their sentinel
+        untouched = np.ones(got.size, bool)
+        untouched[si] = False
+        assert np.all(got[untouched] == STATE_SENTINEL), f"{name}: padding slot written"
+    if check_reduced:
+        got = dev.reduced.bits()
+        assert np.array_equal(got[si], ora.reduced.view(np.uint32)[si]), "reduced gradient not bit-exact"
+    master_bits = dev.state[0].bits()
+    cast = OS.bf16_rne(master_bits[si].view(np.float32))
+    p0 = dev.params[0].bits()
+    for q, prm in enumerate(dev.params):
+        got = prm.bits() if q else p0
+        assert np.array_equal(got, p0), f"param copy {q} differs from copy 0"
+        d = ulp_dist(got, ora.params[q])
+        assert d.max(initial=0) <= 1, f"param copy {q}: {int(d.max())} bf16 ulp from the oracle"
+    assert np.array_equal(p0[ora.fi], cast), "params != bf16_rne(device master)"
+    stats["param_max_ulp"] = int(ulp_dist(p0, ora.params[0]).max(initial=0))
+    assert dev.all_guards_intact(), "guard band overwritten"
+    return stats

@@ -1,0 +1,228 @@
+"""C-ABI library on the host: loads, exports what include/fsp.h declares, plans
+bit-exactly like the oracle, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import fsdp_sharded_mixed_pass_gb300 as fsp
+from fsdp_sharded_mixed_pass_gb300 import fsp as B
+from oracle import ledger as OL
+from oracle import plan as OP
+from synth_inputs import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HP = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(B.LIB_PATH):
+        from fsdp_sharded_mixed_pass_gb300 import build
+        build.build()
+    return B.lib()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fsp_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_exactly_the_binding_exports():
+    assert _declared() == set(fsp.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\b[TW] (fsp_\w+)$", out, flags=re.M))
+    missing = _declared() - exported
+    assert not missing, missing
+    for name in _declared():
+        assert getattr(B.lib(), name) is not None
+
+
+def _compare_plans(lib_plan, o):
+    assert lib_plan.n_d == o.n_d
+    assert lib_plan.valid_elems == o.valid_elems
+    assert lib_plan.full_len_padded == o.full_len_padded
+    assert lib_plan.state_len_per_rank == o.state_len_per_rank
+    assert lib_plan.state_len_total == o.state_len_total
+    # the library lists segments rank-major (its state order); the oracle by parameter
+    got = [(s.rank, s.param, s.full_off, s.state_off, s.length, s.padded_len) for s in lib_plan.segments]
+    want = sorted((s.rank, s.param, s.full_off, s.state_off, s.length, s.padded_len) for s in o.segments)
+    assert got == want
+    # tiles: one per started 4096-block of each non-empty segment
+    tiles = 0
+    for s in o.segments:
+        if s.length:
+            tiles += (s.full_off + s.length - 1) // 4096 - s.full_off // 4096 + 1
+    assert lib_plan.n_tiles == tiles
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_planner_matches_oracle_on_workloads(w):
+    _compare_plans(fsp.plan_layout(w.shapes, w.n_d, w.mode), OP.plan_layout(w.shapes, w.n_d, w.mode))
+
+
+@pytest.mark.parametrize("mode", ["fsdp2", "distopt"])
+@pytest.mark.parametrize("n_d", [1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 33, 64])
+def test_planner_matches_oracle_on_random_shapes(mode, n_d):
+    rng = np.random.default_rng(n_d * 31 + len(mode))
+    shapes = []
+    for _ in range(int(rng.integers(0, 40))):
+        nd = int(rng.integers(1, 4))
+        shape = [int(rng.integers(0, 3 * n_d + 5))] + [int(rng.choice([1, 2, 3, 7, 64])) for _ in range(nd - 1)]
+        shapes.append(tuple(shape))
+    _compare_plans(fsp.plan_layout(shapes, n_d, mode), OP.plan_layout(shapes, n_d, mode))
+
+
+def test_empty_plan():
+    p = fsp.plan_layout([], 4, "fsdp2")
+    assert (p.valid_elems, p.state_len_total, p.n_segments, p.n_tiles) == (0, 0, 0, 0)
+    p = fsp.plan_layout([], 4, "distopt")
+    assert (p.valid_elems, p.full_len_padded, p.n_tiles) == (0, 0, 0)
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_ledger_matches_oracle(w):
+    led = fsp.plan_layout(w.shapes, w.n_d, w.mode).ledger(w.grad_dtype)
+    P, n, g = w.numel, w.n_d, w.grad_bytes
+    want = {
+        "resident_ddp": OL.resident_bytes("ddp", P, n, g),
+        "resident_distopt": OL.resident_bytes("distopt", P, n, g),
+        "resident_zero2": OL.resident_bytes("zero2", P, n, g),
+        "resident_fsdp": OL.resident_bytes("fsdp", P, n, g),
+        "reduce_scatter_sent": OL.coll_bytes("reduce_scatter", n, g * P),
+        "all_gather_sent": OL.coll_bytes("all_gather", n, 2 * P),
+        "step_hbm_bytes": OL.sharded_step_bytes(n, g) * P,
+    }
+    for k, v in want.items():
+        assert led[k] == pytest.approx(float(v), rel=1e-12), k
+
+
+# ---- argument errors, all detected on the host before any CUDA call ----------
+
+def _raw_layout(dims, ndims, n_params, n_d, mode):
+    L = B.lib()
+    out = ctypes.c_void_p()
+    d = (ctypes.c_int64 * max(1, len(dims)))(*dims)
+    nd = (ctypes.c_int32 * max(1, len(ndims)))(*ndims)
+    st = L.fsp_plan_layout(d, nd, n_params, n_d, mode, ctypes.byref(out))
+    if out.value:
+        L.fsp_plan_destroy(out)
+    return st
+
+
+@pytest.mark.parametrize("dims,ndims,n_params,n_d,mode", [
+    ([4], [1], 1, 0, 0),        # n_d < 1
+    ([4], [1], 1, 65, 0),       # n_d > 64
+    ([4], [1], 1, 2, 7),        # unknown mode
+    ([-1], [1], 1, 2, 0),       # negative dim
+    ([4], [0], 1, 2, 0),        # ndims < 1
+    ([4] * 9, [9], 1, 2, 0),    # ndims > 8
+    ([4], [1], -1, 2, 0),       # n_params < 0
+    ([1 << 40, 1 << 20], [2], 1, 2, 0),   # too many elements
+])
+def test_plan_layout_rejects(dims, ndims, n_params, n_d, mode):
+    assert _raw_layout(dims, ndims, n_params, n_d, mode) == B.FSP_EINVAL
+    assert B.lib().fsp_last_error().decode() != ""
+
+
+def test_plan_layout_null_out():
+    L = B.lib()
+    d = (ctypes.c_int64 * 1)(4)
+    nd = (ctypes.c_int32 * 1)(1)
+    assert L.fsp_plan_layout(d, nd, 1, 2, 0, None) == B.FSP_EINVAL
+
+
+def test_segment_index_out_of_range():
+    p = fsp.plan_layout([(8,)], 2)
+    seg = B._Segment()
+    assert B.lib().fsp_plan_segment(p.handle, 2, ctypes.byref(seg)) == B.FSP_EINVAL
+    assert B.lib().fsp_plan_segment(p.handle, -1, ctypes.byref(seg)) == B.FSP_EINVAL
+
+
+class _Fake:
+    """A stand-in buffer with a chosen address; never dereferenced."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def _fakes(plan, base=1 << 40, align=0):
+    gstride = plan.full_len_padded * 4 + 4096
+    grads = [_Fake(base + q * gstride + align) for q in range(plan.n_d)]
+    pbase = base + plan.n_d * gstride
+    params = [_Fake(pbase + q * gstride) for q in range(plan.n_d)]
+    sbase = pbase + plan.n_d * gstride
+    sstride = plan.state_len_total * 4 + 4096
+    return grads, [_Fake(sbase + i * sstride) for i in range(3)], params
+
+
+def _step_status(plan, grads, state, params, hp=HP, step=1, dtype="f32"):
+    try:
+        fsp.sharded_step(plan, grads, *state, params, hp, step, stream=0, grad_dtype=dtype)
+    except fsp.FspError as e:
+        return e.status, str(e)
+    return B.FSP_OK, ""
+
+
+def test_step_rejects_bad_arguments_on_host():
+    plan = fsp.plan_layout([(64, 8)], 4)
+    grads, state, params = _fakes(plan)
+    assert _step_status(plan, grads, state, params, step=0)[0] == B.FSP_EINVAL
+    assert _step_status(plan, grads, state, params, step=-3)[0] == B.FSP_EINVAL
+    for bad in (dict(HP, beta1=1.0), dict(HP, beta2=-0.1), dict(HP, lr=-1.0), dict(HP, eps=float("nan")),
+                dict(HP, weight_decay=float("inf"))):
+        assert _step_status(plan, grads, state, params, hp=bad)[0] == B.FSP_EINVAL
+    g2, s2, p2 = _fakes(plan, align=4)
+    st, msg = _step_status(plan, g2, s2, p2)
+    assert st == B.FSP_EINVAL and "aligned" in msg
+    # overlapping buffers: param 1 inside grad 0
+    g3, s3, p3 = _fakes(plan)
+    p3[1] = _Fake(g3[0].addr + 64)
+    st, msg = _step_status(plan, g3, s3, p3)
+    assert st == B.FSP_EINVAL and "overlaps" in msg
+    # null state pointer
+    g4, s4, p4 = _fakes(plan)
+    s4[1] = _Fake(0)
+    assert _step_status(plan, g4, s4, p4)[0] == B.FSP_EINVAL
+    g5, s5, p5 = _fakes(plan)
+    p5[2] = _Fake(0)
+    assert _step_status(plan, g5, s5, p5)[0] == B.FSP_EINVAL
+
+
+def test_step_rejects_wrong_buffer_count_and_dtype():
+    plan = fsp.plan_layout([(64, 8)], 4)
+    grads, state, params = _fakes(plan)
+    with pytest.raises(ValueError):
+        fsp.sharded_step(plan, grads[:3], *state, params, HP, 1, stream=0, grad_dtype="f32")
+    L = B.lib()
+    args = B._step_args(plan, grads, *state, params, HP, 1, "f32")
+    args[2] = 9   # unknown dtype
+    assert L.fsp_sharded_step(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+    assert L.fsp_sharded_step(None, *args[1:], ctypes.c_void_p(0)) == B.FSP_EINVAL
+
+
+def test_empty_plan_step_is_a_noop():
+    plan = fsp.plan_layout([(0, 5)], 3)
+    grads, state, params = _fakes(plan)
+    assert _step_status(plan, grads, state, params)[0] == B.FSP_OK
+
+
+def test_status_strings():
+    L = B.lib()
+    for s in range(5):
+        assert L.fsp_status_string(s)
+    assert L.fsp_status_string(99) == b"unknown status"
