@@ -281,12 +281,11 @@ int grid_for(KernelFn fn) {
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
 
 fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
-                    float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
+                    float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step, bool debug,
                     float* reduced, void* stream) {
   clear_error();
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
-  if (!master || !m || !v) return fail(FSP_EINVAL, "master, exp_avg or exp_avg_sq is NULL");
   if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
   if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
@@ -310,9 +309,10 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   bufs.push_back({master, sbytes, "master"});
   bufs.push_back({m, sbytes, "exp_avg"});
   bufs.push_back({v, sbytes, "exp_avg_sq"});
-  if (reduced) bufs.push_back({reduced, sbytes, "reduced_grad"});
+  if (debug) bufs.push_back({reduced, sbytes, "reduced_grad"});
   for (const Buf& b : bufs) {
-    if (!b.ptr) return fail(FSP_EINVAL, b.name + " is NULL");
+    // NULL stands for a buffer of zero bytes (e.g. every buffer of an empty plan)
+    if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
     if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
   }
   std::vector<size_t> order(bufs.size());
@@ -323,7 +323,7 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   for (size_t i = 1; i < order.size(); ++i) {
     const Buf& lo = bufs[order[i - 1]];
     const Buf& hi = bufs[order[i]];
-    if (lo.bytes && hi.bytes &&
+    if (lo.ptr && lo.bytes && hi.bytes &&
         reinterpret_cast<uintptr_t>(lo.ptr) + lo.bytes > reinterpret_cast<uintptr_t>(hi.ptr))
       return fail(FSP_EINVAL, lo.name + " overlaps " + hi.name);
   }
@@ -376,8 +376,8 @@ extern "C" fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* 
                                        float* master, float* exp_avg, float* exp_avg_sq,
                                        void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                        void* cuda_stream) {
-  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, nullptr,
-                       cuda_stream);
+  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, false,
+                       nullptr, cuda_stream);
 }
 
 extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs,
@@ -385,7 +385,6 @@ extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* c
                                              float* exp_avg_sq, void* const* param_bufs,
                                              const fsp_adamw_hparams* hp, int64_t step, float* reduced_grad,
                                              void* cuda_stream) {
-  if (!reduced_grad) return fsp::fail(FSP_EINVAL, "reduced_grad is NULL");
-  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, true,
                        reduced_grad, cuda_stream);
 }

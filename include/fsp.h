@@ -158,8 +158,9 @@ void fsp_plan_destroy(fsp_plan* plan);
  *               (bias corrections use beta^t).
  * Every device pointer must be 16-byte aligned and no two buffers may
  * overlap.  Each device pointer must lie in a live CUDA allocation that holds
- * the whole buffer (checked with the driver).  An empty plan returns FSP_OK
- * and launches nothing. */
+ * the whole buffer (checked with the driver).  A pointer may be NULL only
+ * where its buffer has zero elements.  An empty plan returns FSP_OK and
+ * launches nothing. */
 fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
                             float* master, float* exp_avg, float* exp_avg_sq,
                             void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,

@@ -12,7 +12,8 @@ from oracle import step as OS
 from synth_inputs import device as D
 from synth_inputs import workload
 
-from gpu_cases import HP, PARAM_SENTINEL, STATE_SENTINEL, Guarded, ensure_built, ulp_dist, within_tol
+from gpu_cases import (HP, PARAM_SENTINEL, SCALED_BOUND, STATE_SENTINEL, Guarded, ensure_built, state_errors,
+                       ulp_dist, within_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,11 +78,13 @@ def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
         cols = [S.grad_f32(seed, q, f) for q in range(n_d)]
     else:
         cols = [S.grad_bf16_bits(seed, q, f) for q in range(n_d)]
-    th, mm, vv, b, _ = OS.elementwise_step(cols, grad_dtype, S.master_f32(seed, f), S.adam_m_f32(seed, f),
-                                           S.adam_v_f32(seed, f), HP, t)
-    for name, g_, r_ in zip(("master", "exp_avg", "exp_avg_sq"), got, (th, mm, vv)):
+    olds = (S.master_f32(seed, f), S.adam_m_f32(seed, f), S.adam_v_f32(seed, f))
+    th, mm, vv, b, _ = OS.elementwise_step(cols, grad_dtype, *olds, HP, t)
+    errs = state_errors(got, (th, mm, vv), olds)
+    for name, g_, r_, se in zip(("master", "exp_avg", "exp_avg_sq"), got, (th, mm, vv), errs):
         ok = within_tol(g_, r_)
         assert ok.all(), f"{name}: {int((~ok).sum())} of {ok.size} sampled elements out of tolerance"
+        assert np.all(se <= SCALED_BOUND * 2 ** 24), f"{name}: error {se.max():.1f} x 2^-24 of the terms' scale"
     for q in range(n_d):
         assert ulp_dist(got_p[q], b).max(initial=0) <= 1, f"param copy {q} off by more than 1 bf16 ulp"
 

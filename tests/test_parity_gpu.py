@@ -69,7 +69,7 @@ def test_several_tiles_ragged(n_d, mode):
 def test_qwen3_layer_workload_both_entries():
     w = workload(0)
     stats = _run(w.shapes, w.n_d, w.mode, w.grad_dtype, w.data_seed)
-    assert stats["master_max_ulp"] <= 64
+    assert stats["master_max_scaled_err"] <= 16 and stats["exp_avg_sq_max_scaled_err"] <= 16
     # the production entry writes the same bits as the debug entry
     a = DeviceCase(w.shapes, w.n_d, w.mode, w.grad_dtype, w.data_seed)
     b = DeviceCase(w.shapes, w.n_d, w.mode, w.grad_dtype, w.data_seed)
