@@ -16,4 +16,5 @@ from .fsp import (  # noqa: F401
     plan_layout,
     sharded_step,
     sharded_step_debug,
+    sharded_step_noalloc,
 )

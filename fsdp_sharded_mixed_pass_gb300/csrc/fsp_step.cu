@@ -388,3 +388,145 @@ extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* c
   return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, true,
                        reduced_grad, cuda_stream);
 }
+
+// ---- entry point that allocates nothing --------------------------------------
+//
+// For callers that cannot call cudaMalloc: code running while a framework's
+// allocator owns all device memory, inside a memory pool that must not grow,
+// or on a path that must never touch the CUDA allocator.  fsp_sharded_step
+// allocates one tile table per plan and device on its first call; this entry
+// point instead keeps the tile list in a fixed array of device memory that
+// the library declares at file scope (kNoAllocMaxTiles tiles, 8 MiB, held on
+// every device that loads the library until the process exits), rewrites it
+// with a stream-ordered copy on every call, and runs the same kernel on it.
+
+namespace fsp {
+namespace {
+
+constexpr int64_t kNoAllocMaxTiles = 262144;   // 8 MiB of 32-byte tile descriptors
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) Tile g_noalloc_tiles[kNoAllocMaxTiles];
+
+// Device address of g_noalloc_tiles on each device (the name itself is a host
+// stand-in in host code), resolved once per device with that device current.
+std::mutex g_noalloc_mu;
+Tile* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+fsp_status noalloc_tiles_on_current_device(Tile** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FSP_EUNSUPPORTED, "device ordinal above 63");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_tiles);
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetSymbolAddress(g_noalloc_tiles)", e));
+    g_noalloc_addr[dev] = static_cast<Tile*>(ptr);
+  }
+  *out = g_noalloc_addr[dev];
+  return FSP_OK;
+}
+
+fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
+                            float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
+                            void* stream) {
+  clear_error();
+  if (!p) return fail(FSP_EINVAL, "plan is NULL");
+  if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
+  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
+  if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
+  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
+  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
+      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
+    return fail(FSP_EINVAL, "hyper-parameters out of range");
+  if (int64_t(p->tiles.size()) > kNoAllocMaxTiles)
+    return fail(FSP_EUNSUPPORTED, "plan needs " + std::to_string(p->tiles.size()) +
+                                      " work tiles; fsp_sharded_step_noalloc holds at most 262144");
+
+  // The same buffer checks as fsp_sharded_step, on fixed storage.
+  const int n = p->n_d;
+  const size_t gsize = dtype == FSP_DTYPE_F32 ? 4 : 2;
+  const size_t fbytes = size_t(p->full_len_padded), sbytes = size_t(p->state_len_total) * 4;
+  const void* ptrs[2 * kMaxRanks + 3];
+  size_t sizes[2 * kMaxRanks + 3];
+  int nb = 0;
+  for (int q = 0; q < n; ++q) {
+    ptrs[nb] = grads[q];
+    sizes[nb++] = fbytes * gsize;
+    ptrs[nb] = params[q];
+    sizes[nb++] = fbytes * 2;
+  }
+  ptrs[nb] = master;
+  sizes[nb++] = sbytes;
+  ptrs[nb] = m;
+  sizes[nb++] = sbytes;
+  ptrs[nb] = v;
+  sizes[nb++] = sbytes;
+  for (int i = 0; i < nb; ++i) {
+    if (!ptrs[i] && sizes[i]) return fail(FSP_EINVAL, "a buffer is NULL");
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0) return fail(FSP_EINVAL, "a buffer is not 16-byte aligned");
+  }
+  for (int i = 0; i < nb; ++i) {
+    for (int j = i + 1; j < nb; ++j) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(ptrs[i]), b0 = reinterpret_cast<uintptr_t>(ptrs[j]);
+      if (ptrs[i] && ptrs[j] && sizes[i] && sizes[j] && a0 < b0 + sizes[j] && b0 < a0 + sizes[i])
+        return fail(FSP_EINVAL, "two buffers overlap");
+    }
+  }
+  if (p->tiles.empty()) return FSP_OK;
+  for (int i = 0; i < nb; ++i) {
+    fsp_status s = check_allocation(ptrs[i], sizes[i], "a buffer");
+    if (s != FSP_OK) return s;
+  }
+
+  Tile* tiles = nullptr;
+  fsp_status s = noalloc_tiles_on_current_device(&tiles);
+  if (s != FSP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(tiles, p->tiles.data(), p->tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemcpyAsync (tile list)", e));
+
+  StepArgs a{};
+  for (int q = 0; q < n; ++q) {
+    a.grads[q] = grads[q];
+    a.params[q] = static_cast<uint16_t*>(params[q]);
+  }
+  a.master = master;
+  a.m = m;
+  a.v = v;
+  a.reduced = nullptr;
+  a.tiles = tiles;
+  a.n_tiles = int64_t(p->tiles.size());
+  a.n_d = n;
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
+  const double bc1 = 1.0 - std::pow(b1, double(step));
+  const double bc2 = 1.0 - std::pow(b2, double(step));
+  a.c.beta1 = hp->beta1;
+  a.c.one_minus_beta1 = float(1.0 - b1);
+  a.c.beta2 = hp->beta2;
+  a.c.one_minus_beta2 = float(1.0 - b2);
+  a.c.decay = float(1.0 - lr * wd);
+  a.c.step_size = float(lr / bc1);
+  a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+  a.c.eps = hp->eps;
+
+  KernelFn fn = dtype == FSP_DTYPE_F32 ? F32Kernels::get(n) : BF16Kernels::get(n);
+  const int grid = int(std::min<int64_t>(grid_for(fn), a.n_tiles));
+  fn<<<grid, kThreads, 0, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("sharded_step_kernel launch", e));
+  return FSP_OK;
+}
+
+}  // namespace
+}  // namespace fsp
+
+extern "C" fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* grad_bufs,
+                                               int32_t grad_dtype, float* master, float* exp_avg,
+                                               float* exp_avg_sq, void* const* param_bufs,
+                                               const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream) {
+  return fsp::run_step_noalloc(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                               cuda_stream);
+}

@@ -19,7 +19,8 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_status_string", "fsp_last_error")
+           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_sharded_step_noalloc", "fsp_status_string",
+           "fsp_last_error")
 
 
 class FspError(RuntimeError):
@@ -72,8 +73,9 @@ def lib():
     step_args = [vp, ctypes.POINTER(vp), i32, vp, vp, vp, ctypes.POINTER(vp), ctypes.POINTER(_HParams), i64]
     L.fsp_sharded_step.argtypes = step_args + [vp]
     L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
+    L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
     for fn in ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
-               "fsp_sharded_step_debug"):
+               "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_status_string.argtypes = [ctypes.c_int]
     L.fsp_status_string.restype = ctypes.c_char_p
@@ -220,3 +222,12 @@ def sharded_step_debug(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_debug(*args, ctypes.c_void_p(_ptr(reduced_grad)),
                                         ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_debug")
+
+
+def sharded_step_noalloc(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
+                         stream=None, grad_dtype: str | None = None) -> None:
+    """``sharded_step`` that allocates no device memory (for callers that cannot
+    call cudaMalloc); see ``fsp_sharded_step_noalloc`` in include/fsp.h for its
+    size limit and the rule that overlapping calls race."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step_noalloc(*args, ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_noalloc")

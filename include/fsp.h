@@ -175,6 +175,27 @@ fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_
                                   void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                   float* reduced_grad, void* cuda_stream);
 
+/* fsp_sharded_step for callers that cannot allocate device memory (a
+ * framework's allocator owns the device, a fixed memory pool must not grow,
+ * or the call sits on a path that must never reach cudaMalloc).  The pages
+ * have no counterpart: this is a property of the library, not of the step.
+ *   Same arguments, results and checks as fsp_sharded_step; it allocates
+ *   nothing.  The plan's work-tile list goes into a fixed array of device
+ *   memory declared by the library (262144 tiles, 8 MiB, present on every
+ *   device that loads the library until the process exits), copied there on
+ *   `cuda_stream` before the kernel on every call.  Plans with more tiles
+ *   (roughly more than 1.07e9 elements) return FSP_EUNSUPPORTED.
+ *   The first call on a device looks up that array's device address (with the
+ *   device current); make that first call before any stream capture.
+ *   Every call shares the one array: calls that can overlap on the GPU (other
+ *   streams, other threads) race and must be ordered by the caller.  Nothing
+ *   in the array needs clearing between calls: each call writes the whole
+ *   tile list it uses. */
+fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
+                                    float* master, float* exp_avg, float* exp_avg_sq,
+                                    void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                                    void* cuda_stream);
+
 /* Message for a status code (static storage). */
 const char* fsp_status_string(fsp_status status);
 
