@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps in one CUDA graph (removes host launch overhead; small cases)")
     return ap.parse_args(argv)
 
 
@@ -240,12 +242,21 @@ class DeviceWorkload:
         self.t += 1
 
 
-def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id):
+def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False):
     import torch
     stream = torch.cuda.Stream(device=wl.device)
     for _ in range(warmup):
         wl.step(stream)
     stream.synchronize()
+    g = None
+    if graph:
+        # the K timed launches (each with its own update index t) as one graph
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for _ in range(steps):
+                wl.step(stream)
+        g.replay()          # warm replay
+        stream.synchronize()
     sampler = ClockSampler(clocks_id)
     sampler.start_window()
     start = torch.cuda.Event(enable_timing=True)
@@ -253,8 +264,12 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
     dist.barrier()
     torch.cuda.synchronize(wl.device)
     start.record(stream)
-    for _ in range(steps):
-        wl.step(stream)
+    if g is not None:
+        with torch.cuda.stream(stream):
+            g.replay()
+    else:
+        for _ in range(steps):
+            wl.step(stream)
     end.record(stream)
     end.synchronize()
     torch.cuda.synchronize(wl.device)
@@ -304,11 +319,11 @@ def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist):
 # CPU oracle timing
 # --------------------------------------------------------------------------
 
-def cpu_sample_shapes(w, max_elems=16_000_000):
+def cpu_sample_shapes(shapes, max_elems=16_000_000):
     """A contiguous run of the workload's params (skipping any single param over
     32M elements, e.g. an embedding) of about ``max_elems`` elements."""
     out, total = [], 0
-    for s in w.shapes:
+    for s in shapes:
         n = 1
         for d in s:
             n *= d
@@ -404,11 +419,11 @@ def run_fsp(args):
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
 
-    ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id)
+    ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph)
     remeasured = False
     if clocks_bad(clocks):
         log(f"clocks rejected ({clocks}); measuring again")
-        ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id)
+        ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph)
         remeasured = True
     ms_max = dist.max(ms)
     P = plan.valid_elems
@@ -430,7 +445,7 @@ def run_fsp(args):
 
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:
-        sshapes, _ = cpu_sample_shapes(w)
+        sshapes, _ = cpu_sample_shapes(shapes)
         n, reps, secs = time_oracle(w, sshapes, args.cpu_seconds, use_device=True)
         cpu = {"value": n * reps / secs, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
                "sample": f"{len(sshapes)} params ({n} elements) of {w.name}, N_d={w.n_d}, "
@@ -450,6 +465,7 @@ def run_fsp(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps,
+        "launch": "one CUDA graph of the K steps" if args.graph else "one launch per step from the host",
         "clocks": clocks,
     }
     if remeasured:
@@ -466,7 +482,7 @@ def run_reference(args):
     w, shapes, label = resolve_workload(args.workload, args.param_slice)
     # per step, a bounded sample sized so the whole run stays within ~2 minutes
     budget_elems = max(100_000, min(16_000_000, int(120 * 15e6 / max(1, args.steps + args.warmup))))
-    sshapes, _ = cpu_sample_shapes(w, budget_elems)
+    sshapes, _ = cpu_sample_shapes(shapes, budget_elems)
     use_device = False
     try:
         import torch

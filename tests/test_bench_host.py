@@ -1,0 +1,98 @@
+"""bench.py's host logic on CPU: the gloo control plane of the replica path
+(world size 2), the reference arm's JSON line, and the clock check."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    d = bench.Dist(world)
+    d.barrier()
+    m = d.max(10.0 * rank + 0.5)
+    d.barrier()
+    d.close()
+    with open(os.path.join(out_dir, f"r{rank}.txt"), "w") as f:
+        f.write(f"{d.rank} {d.world} {m}")
+
+
+def test_replica_control_plane_two_ranks(tmp_path):
+    mp.start_processes(_rank_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, start_method="spawn")
+    got = sorted(open(tmp_path / f"r{r}.txt").read().split() for r in range(2))
+    assert got == [["0", "2", "10.5"], ["1", "2", "10.5"]]
+
+
+def test_single_process_dist_is_a_noop():
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        os.environ.pop(k, None)
+    d = bench.Dist(1)
+    d.barrier()
+    assert (d.rank, d.world, d.max(3.0)) == (0, 1, 3.0)
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True,
+                          text=True, env=env, cwd=ROOT, timeout=600)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_bench(["--impl", "reference", "--workload", "0", "--param-slice", "0:4", "--steps", "2",
+                    "--warmup", "1"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference"
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["value"] > 0 and line["unit"] == "params/s"
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    r = _run_bench(["--impl", "reference", "--workload", "0", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_fsp_arm_fails_loudly_without_a_gpu():
+    r = _run_bench(["--workload", "0", "--steps", "1", "--warmup", "0"])
+    assert r.returncode != 0
+
+
+@pytest.mark.parametrize("clocks,bad", [
+    ({"sm_mhz": 2070, "sm_max_mhz": 2070, "reasons": []}, False),
+    ({"sm_mhz": 1900, "sm_max_mhz": 2070, "reasons": ["sw_power_cap"]}, False),
+    ({"sm_mhz": 1500, "sm_max_mhz": 2070, "reasons": ["hw_slowdown"]}, True),
+    ({"sm_mhz": 1500, "sm_max_mhz": 2070, "reasons": ["sw_thermal_slowdown"]}, True),
+    ({"sm_mhz": 600, "sm_max_mhz": 2070, "reasons": []}, True),
+    ({"error": "no nvidia-smi"}, False),
+])
+def test_clock_rejection_rule(clocks, bad):
+    assert bench.clocks_bad(clocks) == bad
+
+
+def test_cpu_sample_is_whole_params_and_skips_embeddings():
+    from synth_inputs import workload
+    shapes, n = bench.cpu_sample_shapes(workload(1).shapes)
+    assert shapes[0] == (1024,) and n <= 16_000_000 and len(shapes) == 12
