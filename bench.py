@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 METRIC = "sharded-step params/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", "fsp_step.cu")
+KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", "fsp_kernels.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -111,6 +111,7 @@ def read_peak():
 
 
 def kernel_src_hash() -> str:
+    """sha256 prefix of the device code (the kernels' source file)."""
     with open(KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:12]
 

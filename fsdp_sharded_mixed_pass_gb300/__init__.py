@@ -12,6 +12,7 @@ from .fsp import (  # noqa: F401
     FspError,
     Plan,
     Segment,
+    device_error,
     lib,
     plan_layout,
     sharded_step,

@@ -1,0 +1,505 @@
+// Device code of the fused sharded step (sm_103a): reduce-scatter (rank-
+// ordered fp32 sum, divided by N_d) + AdamW on the fp32 shard + bf16 cast +
+// all-gather, in one streaming pass over the plan's tiles.
+//
+// Stages: "Parallelism strategies: which state to shard", section 二.2 (ZeRO-1
+// puts the optimizer between the two halves of an all-reduce); "FSDP2 Qwen3
+// Decoder Layer Walkthrough", sections "Step 0" (all-gather) and "Backward 简述"
+// (reduce-scatter with averaging, then a communication-free update of the
+// local shard); "07 · 显存模型", section 2.1 (fp32 master + Adam m/v, bf16
+// params, fp32 or bf16 main grads).
+//
+// The step moves (N_d * sizeof(grad) + 24 + 2 N_d) bytes per element at ~0.3
+// flop/byte: it is bound by HBM bandwidth and has no contraction for tensor
+// cores.  Two kernels:
+//
+//  * sharded_step_kernel<N, GradT> (N_d known at compile time): one CTA per
+//    SM, warp-specialised.  A producer thread streams every chunk of up to E
+//    aligned elements of the N_d gradient slices and the three state slices
+//    into a ring of S shared-memory stages with 1-D bulk asynchronous copies
+//    (cp.async.bulk, completion counted on an mbarrier); eight consumer warps
+//    fold, update and cast from shared memory, leaving the new master/m/v in
+//    place and one bf16 tile beside them; a storer thread writes the chunk
+//    back with bulk stores: three state slices and the same bf16 tile to each
+//    of the N_d param buffers (the all-gather is N_d bulk copies of one tile).
+//    Segment edges that are not 16-byte aligned take a scalar path from
+//    global memory.
+//  * sharded_step_generic_kernel<0, GradT> (any N_d up to 64): the same
+//    arithmetic with vectorised per-thread loads and stores.
+//
+// Every wait is bounded: an mbarrier wait gives up after ~2 s, records a bit in
+// g_fsp_device_error, lets its own copies land and returns.  No trap, assert
+// or unbounded loop exists.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fsp_internal.h"
+
+namespace fsp {
+
+constexpr int kGenericThreads = 256;
+constexpr int kConsumerThreads = 256;                  // 8 consumer warps
+constexpr int kBulkThreads = kConsumerThreads + 64;    // + producer warp + storer warp
+constexpr int kBulkSmemBudget = 196608;                // stage ring, bytes
+constexpr int kBulkStageBudget = 49152;                // one stage, bytes
+
+// Device error bits (sticky until read by fsp_device_error).
+constexpr unsigned kErrConsumerWait = 1u;
+constexpr unsigned kErrProducerWait = 2u;
+static __device__ unsigned int g_fsp_device_error = 0;
+
+// Scalars of one AdamW update, from the fp32 hyper-parameters and t in double.
+struct Coeffs {
+  float beta1, one_minus_beta1;
+  float beta2, one_minus_beta2;
+  float decay;          // 1 - lr * weight_decay
+  float step_size;      // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+  float eps;
+};
+
+struct StepArgs {
+  const void* grads[kMaxRanks];
+  uint16_t* params[kMaxRanks];
+  float* master;
+  float* m;
+  float* v;
+  float* reduced;   // averaged shard gradient (state layout); nullptr in production
+  const Tile* tiles;
+  int64_t n_tiles;
+  int n_d;
+  Coeffs c;
+};
+
+// Chunk size E and stage count S of the bulk kernel for N ranks of grad type G.
+template <int N, typename GradT>
+struct BulkCfg {
+  static constexpr int kBytesPerElem = N * int(sizeof(GradT)) + 12 + 2;   // grads, state, bf16 out
+  static constexpr int E = 1024 * kBytesPerElem <= kBulkStageBudget  ? 1024
+                           : 512 * kBytesPerElem <= kBulkStageBudget ? 512
+                                                                     : 256;
+  static constexpr int kStageBytes = E * kBytesPerElem;
+  static constexpr int kS0 = kBulkSmemBudget / kStageBytes;
+  static constexpr int S = kS0 > 8 ? 8 : (kS0 < 2 ? 2 : kS0);
+  static constexpr int kGradOff = 0;                                  // [N][E] GradT
+  static constexpr int kStateOff = N * E * int(sizeof(GradT));        // [3][E] float
+  static constexpr int kParamOff = kStateOff + 3 * E * 4;             // [E] bf16
+  static constexpr int kBarrierBytes = 256;                           // full, computed, empty [S]
+  static constexpr int kSmemBytes = kBarrierBytes + S * kStageBytes;
+  static_assert(kStageBytes % 128 == 0, "stage alignment");
+  static_assert(3 * S * 8 <= kBarrierBytes, "barrier area");
+};
+
+// ---- element math -------------------------------------------------------------
+
+// AdamW on one element: updates m, v, theta in place (fp32).
+__device__ __forceinline__ void adamw(float g, float& theta, float& m, float& v, const Coeffs& c) {
+  m = fmaf(c.beta1, m, c.one_minus_beta1 * g);
+  v = fmaf(c.beta2, v, c.one_minus_beta2 * (g * g));
+  const float denom = fmaf(sqrtf(v), c.inv_sqrt_bc2, c.eps);
+  theta = fmaf(theta, c.decay, -(c.step_size * (m / denom)));
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+__device__ __forceinline__ uint2 pack_bf16x4(float4 t) {
+  uint2 b;
+  b.x = uint32_t(bf16_bits(t.x)) | (uint32_t(bf16_bits(t.y)) << 16);
+  b.y = uint32_t(bf16_bits(t.z)) | (uint32_t(bf16_bits(t.w)) << 16);
+  return b;
+}
+
+// ---- gradient element access ------------------------------------------------------
+
+template <typename GradT>
+struct GradIO;
+
+template <>
+struct GradIO<float> {
+  static __device__ __forceinline__ float4 load4(const void* base, int64_t i) {
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+  }
+  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
+    return __ldcs(static_cast<const float*>(base) + i);
+  }
+  static __device__ __forceinline__ float4 smem4(const unsigned char* base, int i) {
+    return *reinterpret_cast<const float4*>(base + 4 * i);
+  }
+};
+
+template <>
+struct GradIO<__nv_bfloat16> {
+  static __device__ __forceinline__ float4 widen(uint2 w) {
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+  }
+  static __device__ __forceinline__ float4 load4(const void* base, int64_t i) {
+    return widen(__ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i)));
+  }
+  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
+    const uint16_t h = __ldcs(static_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(uint32_t(h) << 16);
+  }
+  static __device__ __forceinline__ float4 smem4(const unsigned char* base, int i) {
+    return widen(*reinterpret_cast<const uint2*>(base + 2 * i));
+  }
+};
+
+// ---- one element from global memory (segment edges, generic kernel) -----------
+
+template <int NT, typename GradT>
+__device__ __forceinline__ void step_one(const StepArgs& a, int n, int64_t f, int64_t s) {
+  float acc = 0.f;
+#pragma unroll
+  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
+    if (NT == 0 && q >= n) break;
+    acc += GradIO<GradT>::load1(a.grads[q], f);
+  }
+  acc = acc / float(NT > 0 ? NT : n);
+  float th = a.master[s], mm = a.m[s], vv = a.v[s];
+  adamw(acc, th, mm, vv, a.c);
+  a.master[s] = th;
+  a.m[s] = mm;
+  a.v[s] = vv;
+  if (a.reduced) a.reduced[s] = acc;
+  const uint16_t b = bf16_bits(th);
+#pragma unroll
+  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
+    if (NT == 0 && q >= n) break;
+    a.params[q][f] = b;
+  }
+}
+
+// ---- generic kernel: per-thread vector loads and stores ---------------------------
+
+// f: full index (multiple of 4); s: state index (same residue mod 16).
+template <int NT, typename GradT>
+__device__ __forceinline__ void step_group(const StepArgs& a, int n, int64_t f, int64_t s) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
+    if (NT == 0 && q >= n) break;
+    const float4 g = GradIO<GradT>::load4(a.grads[q], f);
+    acc.x += g.x;
+    acc.y += g.y;
+    acc.z += g.z;
+    acc.w += g.w;
+  }
+  const float nd = float(NT > 0 ? NT : n);
+  acc.x = acc.x / nd;
+  acc.y = acc.y / nd;
+  acc.z = acc.z / nd;
+  acc.w = acc.w / nd;
+  float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + s));
+  float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m + s));
+  float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v + s));
+  adamw(acc.x, th.x, mm.x, vv.x, a.c);
+  adamw(acc.y, th.y, mm.y, vv.y, a.c);
+  adamw(acc.z, th.z, mm.z, vv.z, a.c);
+  adamw(acc.w, th.w, mm.w, vv.w, a.c);
+  __stcs(reinterpret_cast<float4*>(a.master + s), th);
+  __stcs(reinterpret_cast<float4*>(a.m + s), mm);
+  __stcs(reinterpret_cast<float4*>(a.v + s), vv);
+  if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + s), acc);
+  const uint2 b = pack_bf16x4(th);
+#pragma unroll
+  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
+    if (NT == 0 && q >= n) break;
+    __stcs(reinterpret_cast<uint2*>(a.params[q] + f), b);
+  }
+}
+
+// NT > 0: N_d fixed at compile time; NT == 0: N_d = a.n_d (up to 64).
+template <int NT, typename GradT>
+__global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
+  const int n = NT > 0 ? NT : a.n_d;
+  for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const int64_t f0 = tile.full_begin;
+    const int64_t delta = tile.state_begin - tile.full_begin;
+    const int64_t len = tile.len;
+    // [0, head): before the first multiple of 4; [head, tail): 4-element
+    // groups; [tail, len): the remainder.
+    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
+    const int64_t groups = (len - head) >> 2;
+    const int64_t tail = head + groups * 4;
+    for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+      const int64_t f = f0 + head + 4 * i;
+      step_group<NT, GradT>(a, n, f, f + delta);
+    }
+    const int64_t n_scalar = head + (len - tail);
+    if (threadIdx.x < n_scalar) {
+      const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
+      step_one<NT, GradT>(a, n, f0 + e, f0 + e + delta);
+    }
+  }
+}
+
+// ---- PTX: mbarrier, bulk asynchronous copies, fences --------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of parity `parity` to complete; false after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Aligned body [b0, b1) of a tile: 8-element (16-byte) boundaries in the full
+// index, so every bulk copy starts and ends on 16 bytes for fp32 and bf16.
+struct Body {
+  int64_t b0, b1;
+};
+__device__ __forceinline__ Body tile_body(const Tile& t) {
+  const int64_t end = t.full_begin + t.len;
+  int64_t b0 = (t.full_begin + 7) & ~int64_t(7);
+  int64_t b1 = end & ~int64_t(7);
+  if (b1 < b0) b0 = b1 = end;   // no aligned body: everything is edge
+  return {b0, b1};
+}
+
+// ---- bulk kernel --------------------------------------------------------------------
+
+// Roles (warp index): 0-7 consumers, 8 producer (lane 0), 9 storer (lane 0).
+// Per stage s of the ring three mbarriers carry the hand-offs:
+//   full[s]      producer -> consumers: the chunk's N_d + 3 slices have landed
+//   computed[s]  consumers -> storer: all 8 warps left results in the stage
+//   empty[s]     storer -> producer: the bulk stores have read the stage out
+template <int N, typename GradT>
+__global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __grid_constant__ StepArgs a) {
+  using Cfg = BulkCfg<N, GradT>;
+  constexpr int E = Cfg::E, S = Cfg::S, G = int(sizeof(GradT));
+  constexpr int kConsumerWarps = kConsumerThreads / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* computed = full + S;
+  uint64_t* empty = full + 2 * S;
+  unsigned char* stages = smem + Cfg::kBarrierBytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);                  // producer's arrive (+ the copies' bytes)
+      mbar_init(smem_addr(&computed[s]), kConsumerWarps); // one arrive per consumer warp
+      mbar_init(smem_addr(&empty[s]), 1);                 // storer's arrive
+    }
+    fence_mbar_init();
+    fence_async_smem();
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one thread streams chunks into the ring ----------------
+    if (lane != 0) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;   // stages that ever received copies (bit s)
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < a.n_tiles; t += gridDim.x) {
+      const Tile tile = a.tiles[t];
+      const Body body = tile_body(tile);
+      const int64_t delta = tile.state_begin - tile.full_begin;
+      for (int64_t c = body.b0; c < body.b1; c += E) {
+        const uint32_t len = uint32_t(min(int64_t(E), body.b1 - c));
+        if (!mbar_wait(smem_addr(&empty[stage]), phase ^ 1u)) {
+          atomicOr(&g_fsp_device_error, kErrProducerWait);
+          ok = false;
+          break;
+        }
+        unsigned char* st = stages + stage * Cfg::kStageBytes;
+        const uint32_t bar = smem_addr(&full[stage]);
+        mbar_arrive_expect_tx(bar, len * uint32_t(N * G + 12));
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+          bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+                    len * G, bar);
+        const int64_t s = c + delta;
+        bulk_load(smem_addr(st + Cfg::kStateOff), a.master + s, len * 4, bar);
+        bulk_load(smem_addr(st + Cfg::kStateOff + E * 4), a.m + s, len * 4, bar);
+        bulk_load(smem_addr(st + Cfg::kStateOff + 2 * E * 4), a.v + s, len * 4, bar);
+        armed |= 1u << stage;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      // Let every issued copy land before this CTA can retire: the most recent
+      // phase armed on stage s has parity `phase` for s < stage, else phase ^ 1.
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) mbar_wait(smem_addr(&full[s]), s < stage ? phase : phase ^ 1u);
+    }
+    return;
+  }
+
+  if (warp == kConsumerWarps + 1) {
+    // ---------------- storer: one thread writes finished stages back ----------------
+    if (lane != 0) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+      const Tile tile = a.tiles[t];
+      const Body body = tile_body(tile);
+      const int64_t delta = tile.state_begin - tile.full_begin;
+      for (int64_t c = body.b0; c < body.b1; c += E) {
+        const uint32_t len = uint32_t(min(int64_t(E), body.b1 - c));
+        if (!mbar_wait(smem_addr(&computed[stage]), phase)) {
+          atomicOr(&g_fsp_device_error, kErrConsumerWait);
+          bulk_wait_all();
+          return;
+        }
+        unsigned char* st = stages + stage * Cfg::kStageBytes;
+        const uint32_t th_s = smem_addr(st + Cfg::kStateOff);
+        const uint32_t p_s = smem_addr(st + Cfg::kParamOff);
+        const int64_t s = c + delta;
+        bulk_store(a.master + s, th_s, len * 4);
+        bulk_store(a.m + s, th_s + E * 4, len * 4);
+        bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
+#pragma unroll
+        for (int q = 0; q < N; ++q) bulk_store(a.params[q] + c, p_s, len * 2);   // the all-gather
+        bulk_commit();
+        bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out
+        mbar_arrive(smem_addr(&empty[stage]));
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    bulk_wait_all();
+    return;
+  }
+
+  // ---------------- consumers: fold, update, cast in shared memory ----------------
+  const int tid = threadIdx.x;
+  int stage = 0;
+  uint32_t phase = 0;
+  int64_t t = blockIdx.x;
+  Tile next = t < a.n_tiles ? a.tiles[t] : Tile{0, 0, 0, 0};
+  for (; t < a.n_tiles; t += gridDim.x) {
+    const Tile tile = next;
+    if (t + gridDim.x < a.n_tiles) next = a.tiles[t + gridDim.x];   // prefetch the next descriptor
+    const Body body = tile_body(tile);
+    const int64_t delta = tile.state_begin - tile.full_begin;
+    const int64_t end = tile.full_begin + tile.len;
+
+    // unaligned edges, straight from global memory (fewer than 16 elements)
+    const int64_t n_head = body.b0 - tile.full_begin, n_tail = end - body.b1;
+    if (tid < n_head + n_tail) {
+      const int64_t f = tid < n_head ? tile.full_begin + tid : body.b1 + (tid - n_head);
+      step_one<N, GradT>(a, N, f, f + delta);
+    }
+
+    for (int64_t c = body.b0; c < body.b1; c += E) {
+      const int len = int(min(int64_t(E), body.b1 - c));
+      // a warp-uniform decision, so that a wait running out ends the whole warp
+      const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_addr(&full[stage]), phase));
+      if (!landed) return;   // the storer's bounded wait records the error
+      unsigned char* st = stages + stage * Cfg::kStageBytes;
+      float* th_s = reinterpret_cast<float*>(st + Cfg::kStateOff);
+      float* m_s = th_s + E;
+      float* v_s = th_s + 2 * E;
+      uint16_t* p_s = reinterpret_cast<uint16_t*>(st + Cfg::kParamOff);
+      for (int j = 4 * tid; j < len; j += 4 * kConsumerThreads) {
+        // (1) reduce-scatter: left fold in rank order, then divide by N_d
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          const float4 g = GradIO<GradT>::smem4(st + Cfg::kGradOff + q * E * G, j);
+          acc.x += g.x;
+          acc.y += g.y;
+          acc.z += g.z;
+          acc.w += g.w;
+        }
+        acc.x = acc.x / float(N);
+        acc.y = acc.y / float(N);
+        acc.z = acc.z / float(N);
+        acc.w = acc.w / float(N);
+        // (2) AdamW on the shard, in place in the stage
+        float4 th = *reinterpret_cast<float4*>(th_s + j);
+        float4 mm = *reinterpret_cast<float4*>(m_s + j);
+        float4 vv = *reinterpret_cast<float4*>(v_s + j);
+        adamw(acc.x, th.x, mm.x, vv.x, a.c);
+        adamw(acc.y, th.y, mm.y, vv.y, a.c);
+        adamw(acc.z, th.z, mm.z, vv.z, a.c);
+        adamw(acc.w, th.w, mm.w, vv.w, a.c);
+        *reinterpret_cast<float4*>(th_s + j) = th;
+        *reinterpret_cast<float4*>(m_s + j) = mm;
+        *reinterpret_cast<float4*>(v_s + j) = vv;
+        if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + c + delta + j), acc);
+        // (3) bf16 cast, one tile for all ranks
+        *reinterpret_cast<uint2*>(p_s + j) = pack_bf16x4(th);
+      }
+      fence_async_smem();   // this thread's shared-memory writes -> visible to the bulk stores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&computed[stage]));
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
+}  // namespace fsp

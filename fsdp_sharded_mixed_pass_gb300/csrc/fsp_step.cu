@@ -1,22 +1,5 @@
-// The fused sharded step for sm_103a: reduce-scatter (rank-ordered fp32 sum,
-// averaged by N_d) + AdamW on the fp32 shard + bf16 cast + all-gather, in one
-// streaming pass over the plan's tiles.
-//
-// Stages: "Parallelism strategies: which state to shard", section 二.2 (ZeRO-1
-// puts the optimizer between the two halves of an all-reduce); "FSDP2 Qwen3
-// Decoder Layer Walkthrough", sections "Step 0" (all-gather) and "Backward 简述"
-// (reduce-scatter with averaging, then a communication-free update of the
-// local shard); "07 · 显存模型", section 2.1 (fp32 master + Adam m/v, bf16
-// params, fp32 or bf16 main grads).
-//
-// Design: the step moves (N_d * sizeof(grad) + 24 + 2 N_d) bytes per element
-// at ~0.3 flop/byte, so it is bound by HBM bandwidth and uses no tensor cores.
-// A persistent grid (a multiple of the SM count) walks fixed 4096-element
-// tiles round-robin; inside a tile each thread handles 4-element groups with
-// 16-byte (fp32) or 8-byte (bf16) vector accesses, so a warp touches 512 or
-// 256 contiguous bytes of each of the 2 N_d + 3 streams per access.  Streaming
-// cache hints (.cs) keep the once-touched data from displacing anything in L2.
-// Nothing waits on anything: there are no barriers, atomics or spin loops.
+// Host side of the fused sharded step: argument checks, launch selection and
+// the C entry points.  The kernels are in fsp_kernels.cuh.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -27,181 +10,31 @@
 #include <vector>
 
 #include "fsp_internal.h"
+#include "fsp_kernels.cuh"
 
 namespace fsp {
 namespace {
 
-constexpr int kThreads = 256;
-
-// Scalars of one AdamW update, from the fp32 hyper-parameters and t in double.
-struct Coeffs {
-  float beta1, one_minus_beta1;
-  float beta2, one_minus_beta2;
-  float decay;          // 1 - lr * weight_decay
-  float step_size;      // lr / (1 - beta1^t)
-  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
-  float eps;
-};
-
-struct StepArgs {
-  const void* grads[kMaxRanks];
-  uint16_t* params[kMaxRanks];
-  float* master;
-  float* m;
-  float* v;
-  float* reduced;   // averaged shard gradient (state layout); nullptr in production
-  const Tile* tiles;
-  int64_t n_tiles;
-  int n_d;
-  Coeffs c;
-};
-
-// ---- element math ---------------------------------------------------------
-
-// AdamW on one element: updates m, v, theta in place (fp32).
-__device__ __forceinline__ void adamw(float g, float& theta, float& m, float& v, const Coeffs& c) {
-  m = fmaf(c.beta1, m, c.one_minus_beta1 * g);
-  v = fmaf(c.beta2, v, c.one_minus_beta2 * (g * g));
-  const float denom = fmaf(sqrtf(v), c.inv_sqrt_bc2, c.eps);
-  theta = fmaf(theta, c.decay, -(c.step_size * (m / denom)));
-}
-
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-// ---- loads / stores -------------------------------------------------------
-
-template <typename GradT> struct GradIO;
-
-template <> struct GradIO<float> {
-  static __device__ __forceinline__ float4 load4(const void* base, int64_t i) {
-    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
-  }
-  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
-    return __ldcs(static_cast<const float*>(base) + i);
-  }
-};
-
-template <> struct GradIO<__nv_bfloat16> {
-  static __device__ __forceinline__ float4 load4(const void* base, int64_t i) {
-    const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i));
-    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
-                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-  }
-  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
-    const uint16_t h = __ldcs(static_cast<const unsigned short*>(base) + i);
-    return __uint_as_float(uint32_t(h) << 16);
-  }
-};
-
-// ---- one 4-element group and one scalar element ---------------------------
-
-// f: full index (multiple of 4); s: state index (same residue mod 16).
-template <int NT, typename GradT>
-__device__ __forceinline__ void step_group(const StepArgs& a, int n, int64_t f, int64_t s) {
-  // (1) reduce-scatter: left fold in rank order, then divide by N_d
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    const float4 g = GradIO<GradT>::load4(a.grads[q], f);
-    acc.x += g.x;
-    acc.y += g.y;
-    acc.z += g.z;
-    acc.w += g.w;
-  }
-  const float nd = float(NT > 0 ? NT : n);
-  acc.x = acc.x / nd;
-  acc.y = acc.y / nd;
-  acc.z = acc.z / nd;
-  acc.w = acc.w / nd;
-
-  // (2) AdamW on the shard
-  float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + s));
-  float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m + s));
-  float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v + s));
-  adamw(acc.x, th.x, mm.x, vv.x, a.c);
-  adamw(acc.y, th.y, mm.y, vv.y, a.c);
-  adamw(acc.z, th.z, mm.z, vv.z, a.c);
-  adamw(acc.w, th.w, mm.w, vv.w, a.c);
-  __stcs(reinterpret_cast<float4*>(a.master + s), th);
-  __stcs(reinterpret_cast<float4*>(a.m + s), mm);
-  __stcs(reinterpret_cast<float4*>(a.v + s), vv);
-  if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + s), acc);
-
-  // (3) bf16 cast + all-gather into every rank's buffer
-  uint2 b;
-  b.x = uint32_t(bf16_bits(th.x)) | (uint32_t(bf16_bits(th.y)) << 16);
-  b.y = uint32_t(bf16_bits(th.z)) | (uint32_t(bf16_bits(th.w)) << 16);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    __stcs(reinterpret_cast<uint2*>(a.params[q] + f), b);
-  }
-}
-
-template <int NT, typename GradT>
-__device__ __forceinline__ void step_one(const StepArgs& a, int n, int64_t f, int64_t s) {
-  float acc = 0.f;
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    acc += GradIO<GradT>::load1(a.grads[q], f);
-  }
-  acc = acc / float(NT > 0 ? NT : n);
-  float th = a.master[s], mm = a.m[s], vv = a.v[s];
-  adamw(acc, th, mm, vv, a.c);
-  a.master[s] = th;
-  a.m[s] = mm;
-  a.v[s] = vv;
-  if (a.reduced) a.reduced[s] = acc;
-  const uint16_t b = bf16_bits(th);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    a.params[q][f] = b;
-  }
-}
-
-// ---- the kernel -------------------------------------------------------------
-
-// NT > 0: N_d fixed at compile time; NT == 0: N_d = a.n_d (up to 64).
-template <int NT, typename GradT>
-__global__ void __launch_bounds__(kThreads) sharded_step_kernel(const __grid_constant__ StepArgs a) {
-  const int n = NT > 0 ? NT : a.n_d;
-  for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const Tile tile = a.tiles[t];
-    const int64_t f0 = tile.full_begin;
-    const int64_t delta = tile.state_begin - tile.full_begin;
-    const int64_t len = tile.len;
-    // [0, head): before the first multiple of 4; [head, tail): 4-element
-    // groups; [tail, len): the remainder.
-    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
-    const int64_t groups = (len - head) >> 2;
-    const int64_t tail = head + groups * 4;
-    for (int64_t i = threadIdx.x; i < groups; i += kThreads) {
-      const int64_t f = f0 + head + 4 * i;
-      step_group<NT, GradT>(a, n, f, f + delta);
-    }
-    const int64_t n_scalar = head + (len - tail);
-    if (threadIdx.x < n_scalar) {
-      const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<NT, GradT>(a, n, f0 + e, f0 + e + delta);
-    }
-  }
-}
-
 // ---- host side -------------------------------------------------------------
 
-using KernelFn = void (*)(StepArgs);
+// Which kernel runs for (N_d, grad dtype): the bulk-copy pipeline for the
+// N_d it is instantiated for, the generic kernel otherwise.
+struct KernelInfo {
+  const void* fn;
+  int threads;
+  int smem;
+};
 
 template <typename GradT, int... Ns>
 struct KernelTable {
-  static KernelFn get(int n) {
-    KernelFn fn = sharded_step_kernel<0, GradT>;
-    ((n == Ns ? (fn = sharded_step_kernel<Ns, GradT>, 0) : 0), ...);
-    return fn;
+  static KernelInfo get(int n) {
+    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<0, GradT>), kGenericThreads, 0};
+    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<Ns, GradT>), kBulkThreads,
+                                BulkCfg<Ns, GradT>::kSmemBytes},
+                 0)
+              : 0),
+     ...);
+    return k;
   }
 };
 using F32Kernels = KernelTable<float, 1, 2, 3, 4, 5, 6, 7, 8, 12, 16>;
@@ -260,22 +93,64 @@ fsp_status device_tiles(const fsp_plan* p, const Tile** out) {
   return FSP_OK;
 }
 
-int grid_for(KernelFn fn) {
-  // Cached per (kernel, device): SM count times resident CTAs per SM.
+// Grid for a kernel on the current device: SM count times resident CTAs
+// (one for the bulk kernel), after allowing its dynamic shared memory.
+// Cached per (kernel, device).
+fsp_status grid_for(const KernelInfo& k, int* grid) {
   static std::mutex mu;
-  static std::map<std::pair<KernelFn, int>, int> cache;
+  static std::map<std::pair<const void*, int>, int> cache;
   int dev = 0;
-  cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
   std::lock_guard<std::mutex> lock(mu);
-  auto key = std::make_pair(fn, dev);
+  auto key = std::make_pair(k.fn, dev);
   auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
+  if (it != cache.end()) {
+    *grid = it->second;
+    return FSP_OK;
+  }
+  if (k.smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaFuncSetAttribute", e));
+  }
   int sms = 0, per_sm = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(fn), kThreads, 0);
-  const int g = std::max(1, sms) * std::max(1, per_sm);
-  cache[key] = g;
-  return g;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaDeviceGetAttribute", e));
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e));
+  if (per_sm < 1) return fail(FSP_ECUDA, "the step kernel cannot be resident on this device");
+  *grid = sms * per_sm;
+  cache[key] = *grid;
+  return FSP_OK;
+}
+
+// Fills the AdamW scalars of update t (bias corrections in double).
+void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step) {
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
+  const double bc1 = 1.0 - std::pow(b1, double(step));
+  const double bc2 = 1.0 - std::pow(b2, double(step));
+  a.c.beta1 = hp->beta1;
+  a.c.one_minus_beta1 = float(1.0 - b1);
+  a.c.beta2 = hp->beta2;
+  a.c.one_minus_beta2 = float(1.0 - b2);
+  a.c.decay = float(1.0 - lr * wd);
+  a.c.step_size = float(lr / bc1);
+  a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+  a.c.eps = hp->eps;
+}
+
+// Launches the step for argument block `a` (tiles already on the device).
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream) {
+  const KernelInfo k = dtype == FSP_DTYPE_F32 ? F32Kernels::get(a.n_d) : BF16Kernels::get(a.n_d);
+  int grid = 0;
+  fsp_status s = grid_for(k, &grid);
+  if (s != FSP_OK) return s;
+  grid = int(std::min<int64_t>(grid, a.n_tiles));
+  void* args[] = {&a};
+  cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(k.threads), args, size_t(k.smem),
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("sharded step kernel launch", e));
+  return FSP_OK;
 }
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
@@ -349,24 +224,8 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
   a.n_d = n;
-  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  const double bc1 = 1.0 - std::pow(b1, double(step));
-  const double bc2 = 1.0 - std::pow(b2, double(step));
-  a.c.beta1 = hp->beta1;
-  a.c.one_minus_beta1 = float(1.0 - b1);
-  a.c.beta2 = hp->beta2;
-  a.c.one_minus_beta2 = float(1.0 - b2);
-  a.c.decay = float(1.0 - lr * wd);
-  a.c.step_size = float(lr / bc1);
-  a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
-  a.c.eps = hp->eps;
-
-  KernelFn fn = dtype == FSP_DTYPE_F32 ? F32Kernels::get(n) : BF16Kernels::get(n);
-  const int grid = int(std::min<int64_t>(grid_for(fn), a.n_tiles));
-  fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("sharded_step_kernel launch", e));
-  return FSP_OK;
+  set_coeffs(a, hp, step);
+  return launch(a, dtype, stream);
 }
 
 }  // namespace
@@ -500,24 +359,8 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
   a.n_d = n;
-  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  const double bc1 = 1.0 - std::pow(b1, double(step));
-  const double bc2 = 1.0 - std::pow(b2, double(step));
-  a.c.beta1 = hp->beta1;
-  a.c.one_minus_beta1 = float(1.0 - b1);
-  a.c.beta2 = hp->beta2;
-  a.c.one_minus_beta2 = float(1.0 - b2);
-  a.c.decay = float(1.0 - lr * wd);
-  a.c.step_size = float(lr / bc1);
-  a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
-  a.c.eps = hp->eps;
-
-  KernelFn fn = dtype == FSP_DTYPE_F32 ? F32Kernels::get(n) : BF16Kernels::get(n);
-  const int grid = int(std::min<int64_t>(grid_for(fn), a.n_tiles));
-  fn<<<grid, kThreads, 0, st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("sharded_step_kernel launch", e));
-  return FSP_OK;
+  set_coeffs(a, hp, step);
+  return launch(a, dtype, st);
 }
 
 }  // namespace
@@ -529,4 +372,17 @@ extern "C" fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void*
                                                const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream) {
   return fsp::run_step_noalloc(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
                                cuda_stream);
+}
+
+extern "C" fsp_status fsp_device_error(uint32_t* bits) {
+  fsp::clear_error();
+  if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, fsp::g_fsp_device_error, sizeof(v));
+  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("reading the device error word", e));
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(fsp::g_fsp_device_error, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("clearing the device error word", e));
+  *bits = v;
+  return FSP_OK;
 }

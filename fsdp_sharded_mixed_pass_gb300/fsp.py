@@ -19,8 +19,8 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_sharded_step_noalloc", "fsp_status_string",
-           "fsp_last_error")
+           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_sharded_step_noalloc", "fsp_device_error",
+           "fsp_status_string", "fsp_last_error")
 
 
 class FspError(RuntimeError):
@@ -77,6 +77,8 @@ def lib():
     for fn in ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
                "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
+    L.fsp_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.fsp_device_error.restype = ctypes.c_int
     L.fsp_status_string.argtypes = [ctypes.c_int]
     L.fsp_status_string.restype = ctypes.c_char_p
     L.fsp_last_error.argtypes = []
@@ -231,3 +233,11 @@ def sharded_step_noalloc(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, par
     size limit and the rule that overlapping calls race."""
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_noalloc(*args, ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_noalloc")
+
+
+def device_error() -> int:
+    """Reads and clears the device error word (0: every step since the last
+    read completed; see ``fsp_device_error``).  Synchronous."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().fsp_device_error(ctypes.byref(bits)), "fsp_device_error")
+    return int(bits.value)

@@ -18,6 +18,10 @@
  * Steps (1)-(3) run as one fused streaming kernel: every gradient is read
  * once, the fp32 state is read and written once, every bf16 copy is written
  * once; the reduced gradient is never stored (except by the debug entry).
+ * For N_d in {1..8, 12, 16} the kernel stages the gradient and state slices
+ * in shared memory with bulk asynchronous copies and writes the N_d bf16
+ * copies as bulk stores of one tile; other N_d (up to 64) use per-thread
+ * vector loads and stores.
  *
  * Conventions for every function below:
  *   - Return FSP_OK or an error status; fsp_last_error() then gives a
@@ -195,6 +199,14 @@ fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* gra
                                     float* master, float* exp_avg, float* exp_avg_sq,
                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                     void* cuda_stream);
+
+/* Reads and clears the device error word of the current device (synchronous:
+ * waits for the device).  The step kernel's waits on its own copy pipeline
+ * are bounded (about 2 s); one that runs out sets a bit here (1: a consumer
+ * waited for data, 2: the producer waited for a free stage), lets its copies
+ * land and ends the kernel, leaving that step's results incomplete.  0 means
+ * every step since the last read completed normally. */
+fsp_status fsp_device_error(uint32_t* bits);
 
 /* Message for a status code (static storage). */
 const char* fsp_status_string(fsp_status status);

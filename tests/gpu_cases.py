@@ -206,4 +206,5 @@ def compare(dev: DeviceCase, ora: OracleCase, check_reduced=True) -> dict:
     assert np.array_equal(p0[ora.fi], cast), "params != bf16_rne(device master)"
     stats["param_max_ulp"] = int(ulp_dist(p0, ora.params[0]).max(initial=0))
     assert dev.all_guards_intact(), "guard band overwritten"
+    assert fsp.device_error() == 0, "a bounded wait in the step kernel ran out"
     return stats

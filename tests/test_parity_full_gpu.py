@@ -108,6 +108,7 @@ def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
         n_sent = int((st.t.view(torch.int32) == int(np.uint32(STATE_SENTINEL).view(np.int32))).sum())
         assert n_sent == padding, "a padding slot of the state was written (or an owned one was not)"
     assert all(x.guards_intact() for x in grads + state + params), "guard band overwritten"
+    assert fsp.device_error() == 0, "a bounded wait in the step kernel ran out"
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2, 3, 4], ids=lambda i: workload(i).name)
