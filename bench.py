@@ -60,6 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--param-slice", default=None,
                     help="a:b - only params a..b-1 of the workload (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk", type=int, default=0, help="elements per host-pipeline chunk (0: library default)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -280,27 +281,26 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
     return ms, sampler.result()
 
 
-def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist):
-    """Same step through the public API with host (pinned) inputs and outputs:
-    every step copies the N_d gradient buffers host->device and reads the N_d
-    bf16 param buffers back, all inside the timed region."""
+def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist, chunk_elems: int = 0):
+    """The same step through the C ABI's host-buffer entry point: every step
+    copies the N_d gradient buffers from pinned host memory to the device and
+    the N_d bf16 param buffers back (chunked, H2D / kernel / D2H overlapped),
+    all inside the timed region; the fp32 state stays on the device."""
     import torch
+    import fsdp_sharded_mixed_pass_gb300 as fsp
     p = wl.plan
     host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in wl.grads]
     host_p = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in wl.params]
     for h, g in zip(host_g, wl.grads):
         h.copy_(g)
+    ws = torch.empty(fsp.host_step_workspace_bytes(p, wl.w.grad_dtype, chunk_elems), dtype=torch.uint8,
+                     device=wl.device)
     stream = torch.cuda.Stream(device=wl.device)
-    import fsdp_sharded_mixed_pass_gb300 as fsp
 
     def one():
-        with torch.cuda.stream(stream):
-            for d, h in zip(wl.grads, host_g):
-                d.copy_(h, non_blocking=True)
-            fsp.sharded_step(wl.plan, wl.grads, *wl.state, wl.params, wl.w.hparams(), wl.t, stream=stream)
-            wl.t += 1
-            for h, d in zip(host_p, wl.params):
-                h.copy_(d, non_blocking=True)
+        fsp.sharded_step_host(p, host_g, *wl.state, host_p, wl.w.hparams(), wl.t, ws, chunk_elems=chunk_elems,
+                              stream=stream)
+        wl.t += 1
         stream.synchronize()
 
     one()
@@ -310,9 +310,9 @@ def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist):
         one()
     dt = time.perf_counter() - t0
     dist.barrier()
-    h2d = sum(g.numel() * g.element_size() for g in host_g)
-    d2h = sum(x.numel() * x.element_size() for x in host_p)
-    del host_g, host_p
+    h2d = p.valid_elems * wl.w.n_d * wl.w.grad_bytes
+    d2h = p.valid_elems * wl.w.n_d * 2
+    del host_g, host_p, ws
     return dt, h2d, d2h
 
 
@@ -438,11 +438,12 @@ def run_fsp(args):
 
     e2e = None
     if not args.no_e2e:
-        dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist)
+        dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist, args.e2e_chunk)
         dt = dist.max(dt)
         e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "api": "fsdp_sharded_mixed_pass_gb300.sharded_step with pinned host copies (torch)"}
+               "api": "fsp_sharded_step_host (C ABI): pinned host grads in, pinned host bf16 params out, "
+                      "chunked H2D / kernel / D2H pipeline"}
 
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:

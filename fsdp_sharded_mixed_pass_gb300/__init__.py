@@ -17,5 +17,7 @@ from .fsp import (  # noqa: F401
     plan_layout,
     sharded_step,
     sharded_step_debug,
+    sharded_step_host,
+    host_step_workspace_bytes,
     sharded_step_noalloc,
 )

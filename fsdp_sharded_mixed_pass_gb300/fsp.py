@@ -19,8 +19,8 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_sharded_step_noalloc", "fsp_device_error",
-           "fsp_status_string", "fsp_last_error")
+           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
+           "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_status_string", "fsp_last_error")
 
 
 class FspError(RuntimeError):
@@ -77,6 +77,10 @@ def lib():
     for fn in ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
                "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
+    L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
+    L.fsp_host_step_workspace_bytes.restype = ctypes.c_int
+    L.fsp_sharded_step_host.argtypes = step_args + [vp, ctypes.c_size_t, i64, vp]
+    L.fsp_sharded_step_host.restype = ctypes.c_int
     L.fsp_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.fsp_device_error.restype = ctypes.c_int
     L.fsp_status_string.argtypes = [ctypes.c_int]
@@ -241,3 +245,22 @@ def device_error() -> int:
     bits = ctypes.c_uint32(0)
     _check(lib().fsp_device_error(ctypes.byref(bits)), "fsp_device_error")
     return int(bits.value)
+
+
+def host_step_workspace_bytes(plan: Plan, grad_dtype: str = "f32", chunk_elems: int = 0) -> int:
+    """Device workspace bytes ``sharded_step_host`` needs (chunk_elems 0: 2^24)."""
+    out = ctypes.c_size_t(0)
+    _check(lib().fsp_host_step_workspace_bytes(plan.handle, DTYPES[grad_dtype], int(chunk_elems), ctypes.byref(out)),
+           "fsp_host_step_workspace_bytes")
+    return int(out.value)
+
+
+def sharded_step_host(plan: Plan, host_grads, master, exp_avg, exp_avg_sq, host_params, hparams: dict, step: int,
+                      workspace, chunk_elems: int = 0, stream=None, grad_dtype: str | None = None) -> None:
+    """The step with gradients and bf16 params in host (pinned) memory and the
+    fp32 state on the device; ``workspace`` is a device tensor of at least
+    ``host_step_workspace_bytes`` bytes.  Asynchronous on ``stream``."""
+    args = _step_args(plan, host_grads, master, exp_avg, exp_avg_sq, host_params, hparams, step, grad_dtype)
+    nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else 0
+    _check(lib().fsp_sharded_step_host(*args, ctypes.c_void_p(_ptr(workspace)), nbytes, int(chunk_elems),
+                                       ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_host")

@@ -179,6 +179,30 @@ fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_
                                   void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                   float* reduced_grad, void* cuda_stream);
 
+/* Device workspace, in bytes, that fsp_sharded_step_host needs for this plan,
+ * gradient dtype and chunk size (chunk_elems >= 0; 0 selects 2^24). */
+fsp_status fsp_host_step_workspace_bytes(const fsp_plan* plan, int32_t grad_dtype, int64_t chunk_elems,
+                                         size_t* bytes);
+
+/* The fused step with the N_d gradient buffers and the N_d bf16 param buffers
+ * in HOST memory (pinned memory for full speed; pageable works, slower) and
+ * master / exp_avg / exp_avg_sq on the device, as a pipeline over chunks of
+ * about chunk_elems elements: host-to-device copies of chunk k+1's gradient
+ * slices, the step kernel on chunk k and device-to-host copies of chunk k-1's
+ * bf16 result to every rank's host buffer overlap, on two library-owned copy
+ * streams (created once per device, kept until exit) and `cuda_stream`.
+ *   host_grads[r], host_params[r]: full_len_padded elements each; only the
+ *               P owned elements are copied (padding is left alone).
+ *   workspace:  device, 256-byte aligned, at least
+ *               fsp_host_step_workspace_bytes(...) bytes; two staging slots.
+ * Asynchronous: returns once everything is enqueued; `cuda_stream` completes
+ * after the last copy back, and the host buffers and the workspace must stay
+ * valid and untouched until then.  Same results as fsp_sharded_step. */
+fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_grads, int32_t grad_dtype,
+                                 float* master, float* exp_avg, float* exp_avg_sq, void* const* host_params,
+                                 const fsp_adamw_hparams* hp, int64_t step, void* workspace,
+                                 size_t workspace_bytes, int64_t chunk_elems, void* cuda_stream);
+
 /* fsp_sharded_step for callers that cannot allocate device memory (a
  * framework's allocator owns the device, a fixed memory pool must not grow,
  * or the call sits on a path that must never reach cudaMalloc).  The pages
