@@ -37,6 +37,25 @@ def bytes_per_param(scheme: str, n_d: int, grad_bytes: int = 4) -> Fraction:
     raise ValueError(scheme)
 
 
+def hsdp_bytes_per_param(n_shard: int, grad_bytes: int = 4) -> Fraction:
+    """HSDP: ZeRO-3 inside an N_s-rank shard group, plain replication across
+    groups, so a rank keeps (2 + g + 12) / N_s bytes per parameter
+    ("Parallelism strategies: which state to shard", section 二.6)."""
+    return Fraction(PARAM_BYTES + grad_bytes + MASTER_ADAM_BYTES, n_shard)
+
+
+def hsdp_step_sent(n_rep: int, n_shard: int, grad_payload: float, param_payload: float) -> dict:
+    """Bytes one rank sends for the optimizer-side collectives of an HSDP step:
+    reduce-scatter and all-gather inside the shard group, all-reduce of its
+    1/N_s gradient shard across the N_r replica groups (the pages' ledger
+    listing, the HSDP branch of its DP section)."""
+    return {
+        "reduce_scatter": coll_bytes("reduce_scatter", n_shard, grad_payload),
+        "all_gather": coll_bytes("all_gather", n_shard, param_payload),
+        "cross_group_all_reduce": coll_bytes("all_reduce", n_rep, Fraction(grad_payload) / n_shard),
+    }
+
+
 def resident_bytes(scheme: str, n_params: int, n_d: int, grad_bytes: int = 4) -> Fraction:
     return bytes_per_param(scheme, n_d, grad_bytes) * n_params
 
@@ -78,8 +97,9 @@ def dense_param_count(h: int, layers: int, heads: int, kv_heads: int, head_dim: 
     return int(total)
 
 
-def sharded_step_bytes(n_d: int, grad_bytes: int) -> int:
+def sharded_step_bytes(n_d: int, grad_bytes: int, n_rep: int = 1) -> int:
     """Minimum HBM bytes the fused step moves per valid element when N_d ranks
-    are buffers on one device: each rank's grad read once, fp32 master/m/v read
-    and written once, one bf16 param written per rank."""
-    return n_d * grad_bytes + 2 * MASTER_ADAM_BYTES + n_d * PARAM_BYTES
+    are buffers on one device: each rank's grad read once, each of the N_r
+    copies of fp32 master/m/v read and written once, one bf16 param written per
+    rank."""
+    return n_d * grad_bytes + 2 * MASTER_ADAM_BYTES * n_rep + n_d * PARAM_BYTES

@@ -25,6 +25,12 @@ State placement (FSDP2; the pages are silent): the fp32 master/m/v buffers are
     so that both sides line up for vector access.  ``state_len_per_rank`` is the
     largest rank's extent rounded up to 16.  Gaps and shard padding are never
     written.
+
+HSDP ("Parallelism strategies: which state to shard", section 二.6): the N_d
+    ranks form an N_r x N_s mesh (replicate, shard); global rank = r * N_s + j.
+    Inside each replica group the parameters are FSDP2 Shard(0) over N_s ranks;
+    the N_r groups hold identical copies.  State: N_r copies of the N_s-rank
+    FSDP2 state, replica r's copy at r * (N_s * state_len_per_rank).
 """
 from __future__ import annotations
 
@@ -55,6 +61,11 @@ class Plan:
     full_len_padded: int      # length of each grad / param buffer
     state_len_per_rank: int
     segments: tuple
+    n_rep: int = 1            # HSDP replica groups (1 otherwise)
+
+    @property
+    def n_shard(self) -> int:
+        return self.n_d // self.n_rep
 
     @property
     def state_len_total(self) -> int:
@@ -129,16 +140,31 @@ def plan_distopt(shapes, n_d: int) -> Plan:
     return Plan("distopt", n_d, shapes, offs, total, padded, shard, segs)
 
 
-def plan_layout(shapes, n_d: int, mode: str) -> Plan:
+def plan_hsdp(shapes, n_rep: int, n_shard: int) -> Plan:
+    """N_r replica groups of an N_s-rank FSDP2 layout; segment ranks are global."""
+    inner = plan_fsdp2(shapes, n_shard)
+    copy = n_shard * inner.state_len_per_rank
+    segs = tuple(Segment(s.param, r * n_shard + s.rank, s.full_off, r * copy + s.state_off, s.length, s.padded_len)
+                 for r in range(n_rep) for s in inner.segments)
+    return Plan("hsdp", n_rep * n_shard, inner.shapes, inner.param_offsets, inner.valid_elems,
+                inner.full_len_padded, inner.state_len_per_rank, segs, n_rep)
+
+
+def plan_layout(shapes, n_d: int, mode: str, n_rep: int = 1) -> Plan:
     if mode == "fsdp2":
         return plan_fsdp2(shapes, n_d)
     if mode == "distopt":
         return plan_distopt(shapes, n_d)
+    if mode == "hsdp":
+        if n_rep < 1 or n_d % n_rep:
+            raise ValueError("N_d must be a multiple of the replica count")
+        return plan_hsdp(shapes, n_rep, n_d // n_rep)
     raise ValueError(mode)
 
 
 def owned_indices(plan: Plan):
-    """(full index, state index) for every valid element, in segment order."""
+    """(full index, state index) for every valid element, in segment order
+    (HSDP: every replica's copy, so each full index appears N_r times)."""
     import numpy as np
     full, state = [], []
     for s in plan.segments:

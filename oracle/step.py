@@ -83,21 +83,33 @@ def average(summed: np.ndarray, n_d: int) -> np.ndarray:
     return (summed / np.float32(n_d)).astype(np.float32)
 
 
+def hybrid_sum(slices, n_rep: int):
+    """HSDP reduction ("Parallelism strategies: which state to shard", section
+    二.6): a reduce-scatter inside each replica group - the rank-ordered fold of
+    that group's N_s slices - then an all-reduce across the N_r groups - the
+    fold of the groups' partial sums in group order.  Global rank = r*N_s + j.
+    With N_r = 1 or N_s = 1 it is the plain rank-ordered fold."""
+    n_shard = len(slices) // n_rep
+    partials = [rank_ordered_sum(slices[r * n_shard:(r + 1) * n_shard]) for r in range(n_rep)]
+    return rank_ordered_sum(partials)
+
+
 def reduce_scatter(plan: Plan, grads, grad_dtype: str = "f32", mean: bool = True):
     """Per segment (in plan order), the owner's reduced slice of the gradient."""
     out = []
     for seg in plan.segments:
         sl = slice(seg.full_off, seg.full_off + seg.length)
-        s = rank_ordered_sum([grads_as_f32(g[sl], grad_dtype) for g in grads])
+        s = hybrid_sum([grads_as_f32(g[sl], grad_dtype) for g in grads], plan.n_rep)
         out.append(average(s, plan.n_d) if mean else s)
     return out
 
 
-def all_reduce(grads, grad_dtype: str = "f32", length: int | None = None, mean: bool = True):
-    """Unsharded counterpart: every element reduced, nobody owns anything."""
+def all_reduce(grads, grad_dtype: str = "f32", length: int | None = None, mean: bool = True, n_rep: int = 1):
+    """Unsharded counterpart: every element reduced, nobody owns anything
+    (with the HSDP grouping when n_rep > 1)."""
     n = len(grads)
     sl = slice(0, length)
-    s = rank_ordered_sum([grads_as_f32(g[sl], grad_dtype) for g in grads])
+    s = hybrid_sum([grads_as_f32(g[sl], grad_dtype) for g in grads], n_rep)
     return average(s, n) if mean else s
 
 
@@ -132,10 +144,13 @@ def adamw(theta, m, v, g, hp: dict, t: int):
 # ---------------------------------------------------------------------------
 
 def all_gather(plan: Plan, per_segment_values, params) -> None:
-    """Write each owner's values into every rank's full buffer."""
+    """Write each owner's values into the full buffer of every rank of its
+    group (all N_d ranks; HSDP: the N_s ranks of the owner's replica group)."""
+    group = plan.n_shard
     for seg, vals in zip(plan.segments, per_segment_values):
         sl = slice(seg.full_off, seg.full_off + seg.length)
-        for q in range(plan.n_d):
+        first = (seg.rank // group) * group
+        for q in range(first, first + group):
             params[q][sl] = vals
 
 
@@ -164,25 +179,26 @@ def sharded_step(plan: Plan, grads, grad_dtype: str, master, m, v, params, hp: d
     all_gather(plan, casts, params)
 
 
-def unsharded_step(grads, grad_dtype: str, theta_full, m_full, v_full, n_valid: int, hp: dict, t: int):
+def unsharded_step(grads, grad_dtype: str, theta_full, m_full, v_full, n_valid: int, hp: dict, t: int,
+                   n_rep: int = 1):
     """Plain data-parallel definition on logical (full-index) arrays.
 
     Returns (theta', m', v', bf16 bits) over the first ``n_valid`` elements; each
     of the N_d ranks would hold a copy of the bf16 bits.
     """
-    g = all_reduce(grads, grad_dtype, n_valid, mean=True)
+    g = all_reduce(grads, grad_dtype, n_valid, mean=True, n_rep=n_rep)
     th, mm, vv = adamw(theta_full[:n_valid], m_full[:n_valid], v_full[:n_valid], g, hp, t)
     return th, mm, vv, bf16_rne(th)
 
 
-def elementwise_step(grad_columns, grad_dtype: str, theta, m, v, hp: dict, t: int):
+def elementwise_step(grad_columns, grad_dtype: str, theta, m, v, hp: dict, t: int, n_rep: int = 1):
     """The step for a sample of elements given their inputs directly.
 
     ``grad_columns[q]`` holds rank q's gradient at the sampled elements.  Used to
     check full-size runs one element at a time; it composes the same stages.
     """
     n_d = len(grad_columns)
-    g = average(rank_ordered_sum([grads_as_f32(c, grad_dtype) for c in grad_columns]), n_d)
+    g = average(hybrid_sum([grads_as_f32(c, grad_dtype) for c in grad_columns], n_rep), n_d)
     th, mm, vv = adamw(theta, m, v, g, hp, t)
     return th, mm, vv, bf16_rne(th), g
 
