@@ -226,7 +226,7 @@ class DeviceWorkload:
         import fsdp_sharded_mixed_pass_gb300 as fsp
         from synth_inputs import device as D
         self.w, self.device = w, device
-        self.plan = fsp.plan_layout(shapes, w.n_d, w.mode)
+        self.plan = fsp.plan_layout(shapes, w.n_d, w.mode, n_replicate=w.n_rep)
         p = self.plan
         gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
         self.grads = [torch.empty(p.full_len_padded, dtype=gdt, device=device) for _ in range(w.n_d)]
@@ -343,7 +343,7 @@ def oracle_inputs(w, shapes, use_device: bool):
     import numpy as np
     import synth_inputs as S
     from oracle import plan as OP
-    op = OP.plan_layout(shapes, w.n_d, w.mode)
+    op = OP.plan_layout(shapes, w.n_d, w.mode, n_rep=w.n_rep)
     fi, si = OP.owned_indices(op)
     n = op.full_len_padded
     if use_device:
@@ -393,12 +393,13 @@ def time_oracle(w, shapes, seconds: float, use_device: bool, max_reps: int = 100
 # --------------------------------------------------------------------------
 
 def config_block(w, label, plan, l2_bytes=None):
-    per = w.n_d * w.grad_bytes + 24 + 2 * w.n_d
+    per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
     moved = per * plan.valid_elems
     return {
         "workload": label,
         "n_d": w.n_d,
         "mode": w.mode,
+        "n_replicate": w.n_rep,
         "grad_dtype": w.grad_dtype,
         "params": plan.valid_elems,
         "bytes_per_param": per,
@@ -430,7 +431,7 @@ def run_fsp(args):
     P = plan.valid_elems
     total_params = P * args.steps * dist.world
     value = total_params / (ms_max / 1e3)
-    per = w.n_d * w.grad_bytes + 24 + 2 * w.n_d
+    per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
     launch_s = ms / 1e3 / args.steps
     achieved = per * P / launch_s / 1e9
     peak, peak_src = read_peak()

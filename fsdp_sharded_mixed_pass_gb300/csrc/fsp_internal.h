@@ -39,14 +39,17 @@ static_assert(sizeof(Tile) == 32, "tile descriptor layout");
 
 struct fsp_plan {
   int32_t n_d = 0;
+  int32_t n_rep = 1;      // HSDP replica groups; 1 for FSDP2 and DistOpt
+  int32_t n_shard = 0;    // ranks per shard group (= n_d when n_rep == 1)
   int32_t n_params = 0;
   int32_t mode = 0;
+  int64_t rep_stride = 0; // state elements between two replicas' copies
   int64_t valid_elems = 0;
   int64_t full_len_padded = 0;
   int64_t state_len_per_rank = 0;
   int64_t state_len_total = 0;
   std::vector<fsp_segment> segments;
-  std::vector<fsp::Tile> tiles;
+  std::vector<fsp::Tile> tiles;   // one replica's elements (replica 0's state offsets)
 
   // Device copies of `tiles`, one per device ordinal, uploaded on first use.
   mutable std::mutex mu;

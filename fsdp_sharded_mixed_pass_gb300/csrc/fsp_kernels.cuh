@@ -13,7 +13,9 @@
 // flop/byte: it is bound by HBM bandwidth and has no contraction for tensor
 // cores.  Two kernels:
 //
-//  * sharded_step_kernel<N, GradT> (N_d known at compile time): one CTA per
+//  * sharded_step_kernel<NS, NR, GradT> (N_d = NS x NR known at compile time;
+//    NR > 1 is HSDP: NR replica groups of NS shard ranks, each group with its
+//    own copy of the fp32 state): one CTA per
 //    SM, warp-specialised.  A producer thread streams every chunk of up to E
 //    aligned elements of the N_d gradient slices and the three state slices
 //    into a ring of S shared-memory stages with 1-D bulk asynchronous copies
@@ -24,8 +26,8 @@
 //    of the N_d param buffers (the all-gather is N_d bulk copies of one tile).
 //    Segment edges that are not 16-byte aligned take a scalar path from
 //    global memory.
-//  * sharded_step_generic_kernel<0, GradT> (any N_d up to 64): the same
-//    arithmetic with vectorised per-thread loads and stores.
+//  * sharded_step_generic_kernel<GradT> (any N_d up to 64, any grouping): the
+//    same arithmetic with vectorised per-thread loads and stores.
 //
 // Every wait is bounded: an mbarrier wait gives up after ~2 s, records a bit in
 // g_fsp_device_error, lets its own copies land and returns.  No trap, assert
@@ -71,14 +73,20 @@ struct StepArgs {
   float* reduced;   // averaged shard gradient (state layout); nullptr in production
   const Tile* tiles;
   int64_t n_tiles;
-  int n_d;
+  int n_d;             // = n_rep * n_shard
+  int n_rep;           // HSDP replica groups (1: FSDP2 / DistOpt)
+  int n_shard;         // ranks per shard group; rank q = r * n_shard + j
+  int64_t rep_stride;  // state elements between replica r's copy and r + 1's
   Coeffs c;
 };
 
-// Chunk size E and stage count S of the bulk kernel for N ranks of grad type G.
-template <int N, typename GradT>
+// Chunk size E and stage count S of the bulk kernel for NS x NR ranks (NR
+// replica groups of NS shard ranks) with grads of type GradT.
+template <int NS, int NR, typename GradT>
 struct BulkCfg {
-  static constexpr int kBytesPerElem = N * int(sizeof(GradT)) + 12 + 2;   // grads, state, bf16 out
+  static constexpr int N = NS * NR;
+  // per element: N grads, NR copies of master/m/v, NR bf16 tiles
+  static constexpr int kBytesPerElem = N * int(sizeof(GradT)) + NR * (12 + 2);
   static constexpr int E = 1024 * kBytesPerElem <= kBulkStageBudget  ? 1024
                            : 512 * kBytesPerElem <= kBulkStageBudget ? 512
                                                                      : 256;
@@ -86,8 +94,8 @@ struct BulkCfg {
   static constexpr int kS0 = kBulkSmemBudget / kStageBytes;
   static constexpr int S = kS0 > 8 ? 8 : (kS0 < 2 ? 2 : kS0);
   static constexpr int kGradOff = 0;                                  // [N][E] GradT
-  static constexpr int kStateOff = N * E * int(sizeof(GradT));        // [3][E] float
-  static constexpr int kParamOff = kStateOff + 3 * E * 4;             // [E] bf16
+  static constexpr int kStateOff = N * E * int(sizeof(GradT));        // [NR][3][E] float
+  static constexpr int kParamOff = kStateOff + NR * 3 * E * 4;        // [NR][E] bf16
   static constexpr int kBarrierBytes = 256;                           // full, computed, empty [S]
   static constexpr int kSmemBytes = kBarrierBytes + S * kStageBytes;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
@@ -151,72 +159,86 @@ struct GradIO<__nv_bfloat16> {
 
 // ---- one element from global memory (segment edges, generic kernel) -----------
 
-template <int NT, typename GradT>
-__device__ __forceinline__ void step_one(const StepArgs& a, int n, int64_t f, int64_t s) {
+// NS / NR > 0: fixed at compile time; 0: taken from the arguments.
+// Reduce: inside replica group r the rank-ordered fold of its NS slices (the
+// reduce-scatter), then the rank-ordered fold of the NR partial sums (the
+// all-reduce across groups); with NR = 1 it is the plain rank-ordered fold.
+template <int NS, int NR, typename GradT>
+__device__ __forceinline__ void step_one(const StepArgs& a, int64_t f, int64_t s) {
+  const int ns = NS > 0 ? NS : a.n_shard;
+  const int nr = NR > 0 ? NR : a.n_rep;
   float acc = 0.f;
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    acc += GradIO<GradT>::load1(a.grads[q], f);
+#pragma unroll(NR > 0 ? NR : 1)
+  for (int r = 0; r < nr; ++r) {
+    float part = 0.f;
+#pragma unroll(NS > 0 ? NS : 1)
+    for (int j = 0; j < ns; ++j) part += GradIO<GradT>::load1(a.grads[r * ns + j], f);
+    acc = r == 0 ? part : acc + part;
   }
-  acc = acc / float(NT > 0 ? NT : n);
-  float th = a.master[s], mm = a.m[s], vv = a.v[s];
-  adamw(acc, th, mm, vv, a.c);
-  a.master[s] = th;
-  a.m[s] = mm;
-  a.v[s] = vv;
-  if (a.reduced) a.reduced[s] = acc;
-  const uint16_t b = bf16_bits(th);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    a.params[q][f] = b;
+  acc = acc / float(ns * nr);
+#pragma unroll(NR > 0 ? NR : 1)
+  for (int r = 0; r < nr; ++r) {
+    const int64_t sr = s + r * a.rep_stride;
+    float th = a.master[sr], mm = a.m[sr], vv = a.v[sr];
+    adamw(acc, th, mm, vv, a.c);
+    a.master[sr] = th;
+    a.m[sr] = mm;
+    a.v[sr] = vv;
+    if (a.reduced) a.reduced[sr] = acc;
+    const uint16_t b = bf16_bits(th);
+#pragma unroll(NS > 0 ? NS : 1)
+    for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
   }
 }
 
 // ---- generic kernel: per-thread vector loads and stores ---------------------------
 
+__device__ __forceinline__ void add4(float4& a, float4 b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
 // f: full index (multiple of 4); s: state index (same residue mod 16).
-template <int NT, typename GradT>
-__device__ __forceinline__ void step_group(const StepArgs& a, int n, int64_t f, int64_t s) {
+template <typename GradT>
+__device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t s) {
+  const int ns = a.n_shard, nr = a.n_rep;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    const float4 g = GradIO<GradT>::load4(a.grads[q], f);
-    acc.x += g.x;
-    acc.y += g.y;
-    acc.z += g.z;
-    acc.w += g.w;
+  for (int r = 0; r < nr; ++r) {
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < ns; ++j) add4(part, GradIO<GradT>::load4(a.grads[r * ns + j], f));
+    if (r == 0)
+      acc = part;
+    else
+      add4(acc, part);
   }
-  const float nd = float(NT > 0 ? NT : n);
+  const float nd = float(ns * nr);
   acc.x = acc.x / nd;
   acc.y = acc.y / nd;
   acc.z = acc.z / nd;
   acc.w = acc.w / nd;
-  float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + s));
-  float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m + s));
-  float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v + s));
-  adamw(acc.x, th.x, mm.x, vv.x, a.c);
-  adamw(acc.y, th.y, mm.y, vv.y, a.c);
-  adamw(acc.z, th.z, mm.z, vv.z, a.c);
-  adamw(acc.w, th.w, mm.w, vv.w, a.c);
-  __stcs(reinterpret_cast<float4*>(a.master + s), th);
-  __stcs(reinterpret_cast<float4*>(a.m + s), mm);
-  __stcs(reinterpret_cast<float4*>(a.v + s), vv);
-  if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + s), acc);
-  const uint2 b = pack_bf16x4(th);
-#pragma unroll
-  for (int q = 0; q < (NT > 0 ? NT : kMaxRanks); ++q) {
-    if (NT == 0 && q >= n) break;
-    __stcs(reinterpret_cast<uint2*>(a.params[q] + f), b);
+  for (int r = 0; r < nr; ++r) {
+    const int64_t sr = s + r * a.rep_stride;
+    float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + sr));
+    float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m + sr));
+    float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v + sr));
+    adamw(acc.x, th.x, mm.x, vv.x, a.c);
+    adamw(acc.y, th.y, mm.y, vv.y, a.c);
+    adamw(acc.z, th.z, mm.z, vv.z, a.c);
+    adamw(acc.w, th.w, mm.w, vv.w, a.c);
+    __stcs(reinterpret_cast<float4*>(a.master + sr), th);
+    __stcs(reinterpret_cast<float4*>(a.m + sr), mm);
+    __stcs(reinterpret_cast<float4*>(a.v + sr), vv);
+    if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + sr), acc);
+    const uint2 b = pack_bf16x4(th);
+    for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(a.params[r * ns + j] + f), b);
   }
 }
 
-// NT > 0: N_d fixed at compile time; NT == 0: N_d = a.n_d (up to 64).
-template <int NT, typename GradT>
+// Any N_d up to 64 and any replica grouping.
+template <typename GradT>
 __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
-  const int n = NT > 0 ? NT : a.n_d;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     const int64_t f0 = tile.full_begin;
@@ -229,12 +251,12 @@ __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(c
     const int64_t tail = head + groups * 4;
     for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
       const int64_t f = f0 + head + 4 * i;
-      step_group<NT, GradT>(a, n, f, f + delta);
+      step_group<GradT>(a, f, f + delta);
     }
     const int64_t n_scalar = head + (len - tail);
     if (threadIdx.x < n_scalar) {
       const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<NT, GradT>(a, n, f0 + e, f0 + e + delta);
+      step_one<0, 0, GradT>(a, f0 + e, f0 + e + delta);
     }
   }
 }
@@ -323,9 +345,10 @@ __device__ __forceinline__ Body tile_body(const Tile& t) {
 //   full[s]      producer -> consumers: the chunk's N_d + 3 slices have landed
 //   computed[s]  consumers -> storer: all 8 warps left results in the stage
 //   empty[s]     storer -> producer: the bulk stores have read the stage out
-template <int N, typename GradT>
+template <int NS, int NR, typename GradT>
 __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __grid_constant__ StepArgs a) {
-  using Cfg = BulkCfg<N, GradT>;
+  using Cfg = BulkCfg<NS, NR, GradT>;
+  constexpr int N = NS * NR;
   constexpr int E = Cfg::E, S = Cfg::S, G = int(sizeof(GradT));
   constexpr int kConsumerWarps = kConsumerThreads / 32;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -368,15 +391,19 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         }
         unsigned char* st = stages + stage * Cfg::kStageBytes;
         const uint32_t bar = smem_addr(&full[stage]);
-        mbar_arrive_expect_tx(bar, len * uint32_t(N * G + 12));
+        mbar_arrive_expect_tx(bar, len * uint32_t(N * G + NR * 12));
 #pragma unroll
         for (int q = 0; q < N; ++q)
           bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
                     len * G, bar);
-        const int64_t s = c + delta;
-        bulk_load(smem_addr(st + Cfg::kStateOff), a.master + s, len * 4, bar);
-        bulk_load(smem_addr(st + Cfg::kStateOff + E * 4), a.m + s, len * 4, bar);
-        bulk_load(smem_addr(st + Cfg::kStateOff + 2 * E * 4), a.v + s, len * 4, bar);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const int64_t s = c + delta + r * a.rep_stride;
+          unsigned char* sb = st + Cfg::kStateOff + r * 3 * E * 4;
+          bulk_load(smem_addr(sb), a.master + s, len * 4, bar);
+          bulk_load(smem_addr(sb + E * 4), a.m + s, len * 4, bar);
+          bulk_load(smem_addr(sb + 2 * E * 4), a.v + s, len * 4, bar);
+        }
         armed |= 1u << stage;
         if (++stage == S) {
           stage = 0;
@@ -410,14 +437,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           return;
         }
         unsigned char* st = stages + stage * Cfg::kStageBytes;
-        const uint32_t th_s = smem_addr(st + Cfg::kStateOff);
-        const uint32_t p_s = smem_addr(st + Cfg::kParamOff);
-        const int64_t s = c + delta;
-        bulk_store(a.master + s, th_s, len * 4);
-        bulk_store(a.m + s, th_s + E * 4, len * 4);
-        bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
 #pragma unroll
-        for (int q = 0; q < N; ++q) bulk_store(a.params[q] + c, p_s, len * 2);   // the all-gather
+        for (int r = 0; r < NR; ++r) {
+          const uint32_t th_s = smem_addr(st + Cfg::kStateOff + r * 3 * E * 4);
+          const uint32_t p_s = smem_addr(st + Cfg::kParamOff + r * E * 2);
+          const int64_t s = c + delta + r * a.rep_stride;
+          bulk_store(a.master + s, th_s, len * 4);
+          bulk_store(a.m + s, th_s + E * 4, len * 4);
+          bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
+#pragma unroll
+          for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + c, p_s, len * 2);   // the all-gather
+        }
         bulk_commit();
         bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out
         mbar_arrive(smem_addr(&empty[stage]));
@@ -448,7 +478,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     const int64_t n_head = body.b0 - tile.full_begin, n_tail = end - body.b1;
     if (tid < n_head + n_tail) {
       const int64_t f = tid < n_head ? tile.full_begin + tid : body.b1 + (tid - n_head);
-      step_one<N, GradT>(a, N, f, f + delta);
+      step_one<NS, NR, GradT>(a, f, f + delta);
     }
 
     for (int64_t c = body.b0; c < body.b1; c += E) {
@@ -457,39 +487,45 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
       const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_addr(&full[stage]), phase));
       if (!landed) return;   // the storer's bounded wait records the error
       unsigned char* st = stages + stage * Cfg::kStageBytes;
-      float* th_s = reinterpret_cast<float*>(st + Cfg::kStateOff);
-      float* m_s = th_s + E;
-      float* v_s = th_s + 2 * E;
-      uint16_t* p_s = reinterpret_cast<uint16_t*>(st + Cfg::kParamOff);
       for (int j = 4 * tid; j < len; j += 4 * kConsumerThreads) {
-        // (1) reduce-scatter: left fold in rank order, then divide by N_d
+        // (1) reduce-scatter (inside each replica group) and all-reduce (across
+        // groups): rank-ordered folds, then divide by N_d
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < N; ++q) {
-          const float4 g = GradIO<GradT>::smem4(st + Cfg::kGradOff + q * E * G, j);
-          acc.x += g.x;
-          acc.y += g.y;
-          acc.z += g.z;
-          acc.w += g.w;
+        for (int r = 0; r < NR; ++r) {
+          float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < NS; ++q) add4(part, GradIO<GradT>::smem4(st + Cfg::kGradOff + (r * NS + q) * E * G, j));
+          if (r == 0)
+            acc = part;
+          else
+            add4(acc, part);
         }
         acc.x = acc.x / float(N);
         acc.y = acc.y / float(N);
         acc.z = acc.z / float(N);
         acc.w = acc.w / float(N);
-        // (2) AdamW on the shard, in place in the stage
-        float4 th = *reinterpret_cast<float4*>(th_s + j);
-        float4 mm = *reinterpret_cast<float4*>(m_s + j);
-        float4 vv = *reinterpret_cast<float4*>(v_s + j);
-        adamw(acc.x, th.x, mm.x, vv.x, a.c);
-        adamw(acc.y, th.y, mm.y, vv.y, a.c);
-        adamw(acc.z, th.z, mm.z, vv.z, a.c);
-        adamw(acc.w, th.w, mm.w, vv.w, a.c);
-        *reinterpret_cast<float4*>(th_s + j) = th;
-        *reinterpret_cast<float4*>(m_s + j) = mm;
-        *reinterpret_cast<float4*>(v_s + j) = vv;
-        if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + c + delta + j), acc);
-        // (3) bf16 cast, one tile for all ranks
-        *reinterpret_cast<uint2*>(p_s + j) = pack_bf16x4(th);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          // (2) AdamW on replica r's copy of the shard, in place in the stage
+          float* th_s = reinterpret_cast<float*>(st + Cfg::kStateOff + r * 3 * E * 4);
+          float* m_s = th_s + E;
+          float* v_s = th_s + 2 * E;
+          uint16_t* p_s = reinterpret_cast<uint16_t*>(st + Cfg::kParamOff + r * E * 2);
+          float4 th = *reinterpret_cast<float4*>(th_s + j);
+          float4 mm = *reinterpret_cast<float4*>(m_s + j);
+          float4 vv = *reinterpret_cast<float4*>(v_s + j);
+          adamw(acc.x, th.x, mm.x, vv.x, a.c);
+          adamw(acc.y, th.y, mm.y, vv.y, a.c);
+          adamw(acc.z, th.z, mm.z, vv.z, a.c);
+          adamw(acc.w, th.w, mm.w, vv.w, a.c);
+          *reinterpret_cast<float4*>(th_s + j) = th;
+          *reinterpret_cast<float4*>(m_s + j) = mm;
+          *reinterpret_cast<float4*>(v_s + j) = vv;
+          if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + c + delta + r * a.rep_stride + j), acc);
+          // (3) bf16 cast, one tile for the replica group's ranks
+          *reinterpret_cast<uint2*>(p_s + j) = pack_bf16x4(th);
+        }
       }
       fence_async_smem();   // this thread's shared-memory writes -> visible to the bulk stores
       __syncwarp();

@@ -70,20 +70,18 @@ extern "C" const char* fsp_status_string(fsp_status s) {
   return "unknown status";
 }
 
-extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_params,
-                                      int32_t n_d, int32_t mode, fsp_plan** out) {
-  fsp::clear_error();
-  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout: out is NULL");
-  *out = nullptr;
+namespace {
+
+// Rows (dim 0), cols (product of the other dims) and flat start of each param.
+fsp_status parse_shapes(const int64_t* dims, const int32_t* ndims, int32_t n_params, std::vector<int64_t>& rows,
+                        std::vector<int64_t>& cols, std::vector<int64_t>& start, int64_t& total) {
   if (n_params < 0) return fail(FSP_EINVAL, "fsp_plan_layout: n_params < 0");
   if (n_params > 0 && (!dims || !ndims)) return fail(FSP_EINVAL, "fsp_plan_layout: dims or ndims is NULL");
-  if (n_d < 1 || n_d > fsp::kMaxRanks) return fail(FSP_EINVAL, "fsp_plan_layout: n_d must be in [1, 64]");
-  if (mode != FSP_MODE_FSDP2_SHARD0 && mode != FSP_MODE_DISTOPT_FLAT)
-    return fail(FSP_EINVAL, "fsp_plan_layout: unknown mode");
-
-  // Per parameter: rows (dim 0) and cols (product of the other dims).
-  std::vector<int64_t> rows(n_params), cols(n_params), start(n_params);
-  int64_t cursor = 0, total = 0;
+  rows.assign(n_params, 0);
+  cols.assign(n_params, 0);
+  start.assign(n_params, 0);
+  int64_t cursor = 0;
+  total = 0;
   for (int32_t i = 0; i < n_params; ++i) {
     if (ndims[i] < 1 || ndims[i] > fsp::kMaxDims)
       return fail(FSP_EINVAL, "fsp_plan_layout: ndims[" + std::to_string(i) + "] must be in [1, 8]");
@@ -105,58 +103,90 @@ extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims,
     total += rows[i] * c;
     if (total > fsp::kMaxElems) return fail(FSP_EINVAL, "fsp_plan_layout: model too large");
   }
+  return FSP_OK;
+}
 
+// FSDP2 Shard(0) over n_shard ranks, repeated for n_rep replica groups.
+void build_fsdp2(fsp_plan* p, const std::vector<int64_t>& rows, const std::vector<int64_t>& cols,
+                 const std::vector<int64_t>& start, int32_t n_shard, int32_t n_rep) {
+  const int32_t n_params = int32_t(rows.size());
+  p->full_len_padded = p->valid_elems;
+  // each shard rank's local slot for each (param, rank)
+  std::vector<int64_t> local(size_t(n_params) * n_shard);
+  int64_t widest = 0;
+  for (int32_t r = 0; r < n_shard; ++r) {
+    int64_t at = 0;
+    for (int32_t i = 0; i < n_params; ++i) {
+      const int64_t c = (rows[i] + n_shard - 1) / n_shard;  // padded shard height
+      const int64_t first = std::min<int64_t>(int64_t(r) * c, rows[i]);
+      const int64_t full_off = start[i] + first * cols[i];
+      // first slot >= at with slot == full_off (mod kStateAlign)
+      const int64_t want = full_off % fsp::kStateAlign;
+      const int64_t have = at % fsp::kStateAlign;
+      at += (want - have + fsp::kStateAlign) % fsp::kStateAlign;
+      local[size_t(r) * n_params + i] = at;
+      at += c * cols[i];
+    }
+    widest = std::max(widest, at);
+  }
+  p->state_len_per_rank = fsp::round_up(widest, fsp::kStateAlign);
+  p->rep_stride = p->state_len_per_rank * n_shard;
+  p->state_len_total = p->rep_stride * n_rep;
+  p->segments.reserve(size_t(n_params) * n_shard * n_rep);
+  for (int32_t g = 0; g < n_rep; ++g) {
+    for (int32_t r = 0; r < n_shard; ++r) {
+      for (int32_t i = 0; i < n_params; ++i) {
+        const int64_t c = (rows[i] + n_shard - 1) / n_shard;
+        const int64_t first = std::min<int64_t>(int64_t(r) * c, rows[i]);
+        const int64_t owned_rows = std::min<int64_t>(c, rows[i] - first);
+        fsp_segment s;
+        s.param = i;
+        s.rank = g * n_shard + r;
+        s.full_off = start[i] + first * cols[i];
+        s.state_off = g * p->rep_stride + int64_t(r) * p->state_len_per_rank + local[size_t(r) * n_params + i];
+        s.len = owned_rows * cols[i];
+        s.padded_len = c * cols[i];
+        p->segments.push_back(s);
+      }
+    }
+  }
+}
+
+// Tiles of replica 0's segments, in full-index order so a CTA's consecutive
+// tiles are neighbours in every buffer.
+void build_tiles(fsp_plan* p) {
+  std::vector<const fsp_segment*> order;
+  order.reserve(p->segments.size());
+  for (const auto& s : p->segments)
+    if (s.len > 0 && s.rank < p->n_shard) order.push_back(&s);
+  std::sort(order.begin(), order.end(),
+            [](const fsp_segment* a, const fsp_segment* b) { return a->full_off < b->full_off; });
+  p->tiles.reserve(size_t(p->valid_elems / fsp::kTileElems + 2 * order.size() + 1));
+  for (const fsp_segment* s : order) fsp::append_tiles(*s, p->tiles);
+}
+
+fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params, int32_t n_rep, int32_t n_shard,
+                     int32_t mode, fsp_plan** out) {
+  std::vector<int64_t> rows, cols, start;
+  int64_t total = 0;
+  fsp_status st = parse_shapes(dims, ndims, n_params, rows, cols, start, total);
+  if (st != FSP_OK) return st;
   fsp_plan* p = new (std::nothrow) fsp_plan();
   if (!p) return fail(FSP_ENOMEM, "fsp_plan_layout: host allocation failed");
   try {
-    p->n_d = n_d;
+    p->n_d = n_rep * n_shard;
+    p->n_rep = n_rep;
+    p->n_shard = n_shard;
     p->n_params = n_params;
     p->mode = mode;
     p->valid_elems = total;
-
-    if (mode == FSP_MODE_FSDP2_SHARD0) {
-      p->full_len_padded = total;
-      // Pass 1: each rank's local slot for each (param, rank), in rank order.
-      std::vector<int64_t> local(size_t(n_params) * n_d);
-      int64_t widest = 0;
-      for (int32_t r = 0; r < n_d; ++r) {
-        int64_t at = 0;
-        for (int32_t i = 0; i < n_params; ++i) {
-          const int64_t c = (rows[i] + n_d - 1) / n_d;  // padded shard height
-          const int64_t first = std::min<int64_t>(int64_t(r) * c, rows[i]);
-          const int64_t full_off = start[i] + first * cols[i];
-          // first slot >= at with slot == full_off (mod kStateAlign)
-          const int64_t want = full_off % fsp::kStateAlign;
-          const int64_t have = at % fsp::kStateAlign;
-          at += (want - have + fsp::kStateAlign) % fsp::kStateAlign;
-          local[size_t(r) * n_params + i] = at;
-          at += c * cols[i];
-        }
-        widest = std::max(widest, at);
-      }
-      p->state_len_per_rank = fsp::round_up(widest, fsp::kStateAlign);
-      p->state_len_total = p->state_len_per_rank * n_d;
-      p->segments.reserve(size_t(n_params) * n_d);
-      for (int32_t r = 0; r < n_d; ++r) {
-        for (int32_t i = 0; i < n_params; ++i) {
-          const int64_t c = (rows[i] + n_d - 1) / n_d;
-          const int64_t first = std::min<int64_t>(int64_t(r) * c, rows[i]);
-          const int64_t owned_rows = std::min<int64_t>(c, rows[i] - first);
-          fsp_segment s;
-          s.param = i;
-          s.rank = r;
-          s.full_off = start[i] + first * cols[i];
-          s.state_off = int64_t(r) * p->state_len_per_rank + local[size_t(r) * n_params + i];
-          s.len = owned_rows * cols[i];
-          s.padded_len = c * cols[i];
-          p->segments.push_back(s);
-        }
-      }
-    } else {
+    if (mode == FSP_MODE_DISTOPT_FLAT) {
+      const int32_t n_d = n_shard;
       const int64_t unit = int64_t(n_d) / fsp::gcd64(n_d, fsp::kDistOptAlign) * fsp::kDistOptAlign;
       p->full_len_padded = fsp::round_up(total, unit);
       p->state_len_per_rank = p->full_len_padded / n_d;
       p->state_len_total = p->full_len_padded;
+      p->rep_stride = p->state_len_total;
       for (int32_t r = 0; r < n_d; ++r) {
         fsp_segment s;
         s.param = -1;
@@ -167,24 +197,39 @@ extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims,
         s.padded_len = p->state_len_per_rank;
         p->segments.push_back(s);
       }
+    } else {
+      build_fsdp2(p, rows, cols, start, n_shard, n_rep);
     }
-
-    // Tiles, in full-index order so a CTA's consecutive tiles are neighbours
-    // in every buffer.
-    std::vector<const fsp_segment*> order;
-    order.reserve(p->segments.size());
-    for (const auto& s : p->segments)
-      if (s.len > 0) order.push_back(&s);
-    std::sort(order.begin(), order.end(),
-              [](const fsp_segment* a, const fsp_segment* b) { return a->full_off < b->full_off; });
-    p->tiles.reserve(size_t(total / fsp::kTileElems + 2 * order.size() + 1));
-    for (const fsp_segment* s : order) fsp::append_tiles(*s, p->tiles);
+    build_tiles(p);
   } catch (const std::bad_alloc&) {
     delete p;
     return fail(FSP_ENOMEM, "fsp_plan_layout: host allocation failed");
   }
   *out = p;
   return FSP_OK;
+}
+
+}  // namespace
+
+extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                                      int32_t n_d, int32_t mode, fsp_plan** out) {
+  fsp::clear_error();
+  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout: out is NULL");
+  *out = nullptr;
+  if (n_d < 1 || n_d > fsp::kMaxRanks) return fail(FSP_EINVAL, "fsp_plan_layout: n_d must be in [1, 64]");
+  if (mode != FSP_MODE_FSDP2_SHARD0 && mode != FSP_MODE_DISTOPT_FLAT)
+    return fail(FSP_EINVAL, "fsp_plan_layout: unknown mode");
+  return make_plan(dims, ndims, n_params, 1, n_d, mode, out);
+}
+
+extern "C" fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                                           int32_t n_replicate, int32_t n_shard, fsp_plan** out) {
+  fsp::clear_error();
+  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: out is NULL");
+  *out = nullptr;
+  if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
+    return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: need n_replicate, n_shard >= 1 and their product <= 64");
+  return make_plan(dims, ndims, n_params, n_replicate, n_shard, FSP_MODE_HSDP, out);
 }
 
 extern "C" fsp_status fsp_plan_info_get(const fsp_plan* p, fsp_plan_info* out) {
@@ -200,6 +245,8 @@ extern "C" fsp_status fsp_plan_info_get(const fsp_plan* p, fsp_plan_info* out) {
   out->state_len_total = p->state_len_total;
   out->n_segments = int64_t(p->segments.size());
   out->n_tiles = int64_t(p->tiles.size());
+  out->n_replicate = p->n_rep;
+  out->n_shard = p->n_shard;
   return FSP_OK;
 }
 
@@ -217,14 +264,18 @@ extern "C" fsp_status fsp_plan_ledger(const fsp_plan* p, int32_t grad_dtype, fsp
   if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16)
     return fail(FSP_EINVAL, "fsp_plan_ledger: unknown grad dtype");
   const double P = double(p->valid_elems), n = double(p->n_d);
+  const double ns = double(p->n_shard), nr = double(p->n_rep);
   const double g = grad_dtype == FSP_DTYPE_F32 ? 4.0 : 2.0;
   out->resident_ddp = (2.0 + g + 12.0) * P;
   out->resident_distopt = (2.0 + g) * P + 12.0 * P / n;
   out->resident_zero2 = 2.0 * P + (g + 12.0) * P / n;
   out->resident_fsdp = (2.0 + g + 12.0) * P / n;
-  out->reduce_scatter_sent = (n - 1.0) / n * g * P;
-  out->all_gather_sent = (n - 1.0) / n * 2.0 * P;
-  out->step_hbm_bytes = (n * g + 24.0 + 2.0 * n) * P;
+  // collectives of this plan's own layout (the shard group for HSDP)
+  out->reduce_scatter_sent = (ns - 1.0) / ns * g * P;
+  out->all_gather_sent = (ns - 1.0) / ns * 2.0 * P;
+  out->step_hbm_bytes = (n * g + 24.0 * nr + 2.0 * n) * P;
+  out->resident_hsdp = (2.0 + g + 12.0) * P / ns;
+  out->cross_group_all_reduce_sent = nr > 1.0 ? 2.0 * (nr - 1.0) / nr * g * P / ns : 0.0;
   return FSP_OK;
 }
 

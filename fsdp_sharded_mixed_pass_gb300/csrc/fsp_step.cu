@@ -25,20 +25,32 @@ struct KernelInfo {
   int smem;
 };
 
-template <typename GradT, int... Ns>
-struct KernelTable {
-  static KernelInfo get(int n) {
-    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<0, GradT>), kGenericThreads, 0};
-    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<Ns, GradT>), kBulkThreads,
-                                BulkCfg<Ns, GradT>::kSmemBytes},
-                 0)
-              : 0),
+// (N_s, N_r) pairs with a bulk-copy instantiation: FSDP2 / DistOpt (N_r = 1)
+// and the common HSDP meshes.
+template <int NS, int NR>
+struct Mesh {};
+
+template <typename GradT, typename... Ms>
+struct KernelTable;
+
+template <typename GradT, int... NS, int... NR>
+struct KernelTable<GradT, Mesh<NS, NR>...> {
+  static KernelInfo get(int n_shard, int n_rep) {
+    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<GradT>), kGenericThreads, 0};
+    ((n_shard == NS && n_rep == NR
+          ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<NS, NR, GradT>), kBulkThreads,
+                            BulkCfg<NS, NR, GradT>::kSmemBytes},
+             0)
+          : 0),
      ...);
     return k;
   }
 };
-using F32Kernels = KernelTable<float, 1, 2, 3, 4, 5, 6, 7, 8, 12, 16>;
-using BF16Kernels = KernelTable<__nv_bfloat16, 1, 2, 3, 4, 5, 6, 7, 8, 12, 16>;
+
+template <typename GradT>
+using Kernels = KernelTable<GradT, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
+                            Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>, Mesh<2, 2>, Mesh<4, 2>, Mesh<8, 2>,
+                            Mesh<2, 4>, Mesh<4, 4>>;
 
 std::string cuda_msg(const char* what, cudaError_t e) {
   return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -139,9 +151,18 @@ void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step) {
   a.c.eps = hp->eps;
 }
 
+// Rank layout of the plan in the argument block.
+void set_mesh(StepArgs& a, const fsp_plan* p) {
+  a.n_d = p->n_d;
+  a.n_rep = p->n_rep;
+  a.n_shard = p->n_shard;
+  a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
+}
+
 // Launches the step for argument block `a` (tiles already on the device).
 fsp_status launch(StepArgs& a, int32_t dtype, void* stream) {
-  const KernelInfo k = dtype == FSP_DTYPE_F32 ? F32Kernels::get(a.n_d) : BF16Kernels::get(a.n_d);
+  const KernelInfo k = dtype == FSP_DTYPE_F32 ? Kernels<float>::get(a.n_shard, a.n_rep)
+                                              : Kernels<__nv_bfloat16>::get(a.n_shard, a.n_rep);
   int grid = 0;
   fsp_status s = grid_for(k, &grid);
   if (s != FSP_OK) return s;
@@ -223,7 +244,7 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   a.reduced = reduced;
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
-  a.n_d = n;
+  set_mesh(a, p);
   set_coeffs(a, hp, step);
   return launch(a, dtype, stream);
 }
@@ -358,7 +379,7 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   a.reduced = nullptr;
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
-  a.n_d = n;
+  set_mesh(a, p);
   set_coeffs(a, hp, step);
   return launch(a, dtype, st);
 }
@@ -408,7 +429,7 @@ int64_t host_slot_elems(int64_t chunk_elems) {
 
 size_t host_workspace_bytes(const fsp_plan* p, int32_t dtype, int64_t chunk_elems) {
   const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
-  return 2 * size_t(host_slot_elems(chunk_elems)) * (size_t(p->n_d) * g + 2);
+  return 2 * size_t(host_slot_elems(chunk_elems)) * (size_t(p->n_d) * g + 2 * size_t(p->n_rep));
 }
 
 // Copies of different ranks' slices run on several streams at once so that
@@ -522,7 +543,11 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   auto stg_grad = [&](int sl, int q) { return ws + (size_t(sl) * n + q) * size_t(slot) * g; };
-  auto stg_param = [&](int sl) { return ws + 2 * size_t(n) * size_t(slot) * g + size_t(sl) * size_t(slot) * 2; };
+  const int n_rep = p->n_rep, n_shard = p->n_shard;
+  // one bf16 tile per replica group per slot
+  auto stg_param = [&](int sl, int r) {
+    return ws + 2 * size_t(n) * size_t(slot) * g + (size_t(sl) * n_rep + r) * size_t(slot) * 2;
+  };
 
   cudaStream_t cs_main = static_cast<cudaStream_t>(stream);
   const int lanes = std::min(kCopyLanes, n);
@@ -550,7 +575,7 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
   a.m = m;
   a.v = v;
   a.reduced = nullptr;
-  a.n_d = n;
+  set_mesh(a, p);
   set_coeffs(a, hp, step);
 
   cudaError_t e = cudaEventRecord(entry, cs_main);   // copies start after earlier work on the stream
@@ -581,7 +606,7 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
     for (int q = 0; q < n; ++q) {
       // staging holds full indices [f0, f1): index it with the full index
       a.grads[q] = stg_grad(sl, q) - size_t(f0) * g;
-      a.params[q] = reinterpret_cast<uint16_t*>(stg_param(sl)) - f0;   // one bf16 tile serves every rank
+      a.params[q] = reinterpret_cast<uint16_t*>(stg_param(sl, q / n_shard)) - f0;   // one tile per group
     }
     a.tiles = dtiles + cuts[k];
     a.n_tiles = int64_t(cuts[k + 1] - cuts[k]);
@@ -595,8 +620,8 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
     for (int j = 0; e == cudaSuccess && j < lanes; ++j) {
       e = cudaStreamWaitEvent(cs.d2h[j], ev_kern(k), 0);
       for (int q = j; e == cudaSuccess && q < n; q += lanes)
-        e = cudaMemcpyAsync(static_cast<unsigned char*>(host_params[q]) + size_t(f0) * 2, stg_param(sl), len * 2,
-                            cudaMemcpyDeviceToHost, cs.d2h[j]);
+        e = cudaMemcpyAsync(static_cast<unsigned char*>(host_params[q]) + size_t(f0) * 2, stg_param(sl, q / n_shard),
+                            len * 2, cudaMemcpyDeviceToHost, cs.d2h[j]);
       if (e == cudaSuccess) e = cudaEventRecord(ev_d2h(k, j), cs.d2h[j]);
     }
   }

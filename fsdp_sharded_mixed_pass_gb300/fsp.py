@@ -14,11 +14,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libfsp.so")
 
 FSP_OK, FSP_EINVAL, FSP_ENOMEM, FSP_ECUDA, FSP_EUNSUPPORTED = range(5)
-MODES = {"fsdp2": 0, "distopt": 1}
+MODES = {"fsdp2": 0, "distopt": 1, "hsdp": 2}
 DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
-EXPORTS = ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
+EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
            "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_status_string", "fsp_last_error")
 
@@ -33,7 +33,8 @@ class _PlanInfo(ctypes.Structure):
     _fields_ = [("n_d", ctypes.c_int32), ("n_params", ctypes.c_int32), ("mode", ctypes.c_int32),
                 ("tile_elems", ctypes.c_int32), ("valid_elems", ctypes.c_int64),
                 ("full_len_padded", ctypes.c_int64), ("state_len_per_rank", ctypes.c_int64),
-                ("state_len_total", ctypes.c_int64), ("n_segments", ctypes.c_int64), ("n_tiles", ctypes.c_int64)]
+                ("state_len_total", ctypes.c_int64), ("n_segments", ctypes.c_int64), ("n_tiles", ctypes.c_int64),
+                ("n_replicate", ctypes.c_int32), ("n_shard", ctypes.c_int32)]
 
 
 class _Segment(ctypes.Structure):
@@ -44,7 +45,7 @@ class _Segment(ctypes.Structure):
 class _Ledger(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in ("resident_ddp", "resident_distopt", "resident_zero2",
                                                "resident_fsdp", "reduce_scatter_sent", "all_gather_sent",
-                                               "step_hbm_bytes")]
+                                               "step_hbm_bytes", "resident_hsdp", "cross_group_all_reduce_sent")]
 
 
 class _HParams(ctypes.Structure):
@@ -65,6 +66,8 @@ def lib():
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     L.fsp_plan_layout.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32, i32,
                                   ctypes.POINTER(vp)]
+    L.fsp_plan_layout_hsdp.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32,
+                                       i32, ctypes.POINTER(vp)]
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
     L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
@@ -74,7 +77,7 @@ def lib():
     L.fsp_sharded_step.argtypes = step_args + [vp]
     L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
-    for fn in ("fsp_plan_layout", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
+    for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
                "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
@@ -125,6 +128,8 @@ class Plan:
         self.state_len_total = info.state_len_total
         self.n_segments = info.n_segments
         self.n_tiles = info.n_tiles
+        self.n_replicate = info.n_replicate
+        self.n_shard = info.n_shard
         self._segments = None
 
     @property
@@ -158,8 +163,9 @@ class Plan:
             pass
 
 
-def plan_layout(shapes, n_d: int, mode: str = "fsdp2") -> Plan:
-    """FSDP2 Shard(0) (``mode="fsdp2"``) or DistOpt flat (``"distopt"``) plan."""
+def plan_layout(shapes, n_d: int, mode: str = "fsdp2", n_replicate: int = 1) -> Plan:
+    """FSDP2 Shard(0) (``mode="fsdp2"``), DistOpt flat (``"distopt"``) or HSDP
+    (``"hsdp"``: ``n_replicate`` groups of ``n_d // n_replicate`` shard ranks)."""
     shapes = [tuple(int(d) for d in s) for s in shapes]
     dims = [d for s in shapes for d in s]
     nd = [len(s) for s in shapes]
@@ -168,8 +174,14 @@ def plan_layout(shapes, n_d: int, mode: str = "fsdp2") -> Plan:
     out = ctypes.c_void_p()
     if mode not in MODES:
         raise ValueError(f"unknown mode {mode!r}")
-    _check(lib().fsp_plan_layout(dims_arr, nd_arr, len(shapes), int(n_d), MODES[mode], ctypes.byref(out)),
-           "fsp_plan_layout")
+    if mode == "hsdp":
+        if n_replicate < 1 or n_d % n_replicate:
+            raise ValueError("n_d must be a multiple of n_replicate")
+        _check(lib().fsp_plan_layout_hsdp(dims_arr, nd_arr, len(shapes), int(n_replicate), int(n_d // n_replicate),
+                                          ctypes.byref(out)), "fsp_plan_layout_hsdp")
+    else:
+        _check(lib().fsp_plan_layout(dims_arr, nd_arr, len(shapes), int(n_d), MODES[mode], ctypes.byref(out)),
+               "fsp_plan_layout")
     return Plan(out.value, shapes, mode)
 
 

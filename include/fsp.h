@@ -66,7 +66,16 @@ typedef enum {
    * buffer padded to a multiple of lcm(N_d, 128) and cut into N_d equal
    * contiguous shards that ignore parameter boundaries.  "07 · 显存模型",
    * section 2.1 item 1 and section 8 item 4. */
-  FSP_MODE_DISTOPT_FLAT = 1
+  FSP_MODE_DISTOPT_FLAT = 1,
+  /* HSDP: the N_d = N_r * N_s ranks form a (replicate, shard) mesh, rank
+   * q = r * N_s + j.  Each replica group r shards the parameters FSDP2-style
+   * over its N_s ranks and keeps its own copy of the fp32 state; gradients are
+   * reduce-scattered inside each group (rank-ordered fp32 fold over its N_s
+   * ranks), then all-reduced across the N_r groups (fold of the partial sums in
+   * group order), divided by N_d; each group all-gathers its bf16 params.
+   * "Parallelism strategies: which state to shard", section 二.6.  Created by
+   * fsp_plan_layout_hsdp. */
+  FSP_MODE_HSDP = 2
 } fsp_mode;
 
 typedef enum {
@@ -99,12 +108,16 @@ typedef struct {
   int64_t state_len_total;      /* length of master, m and v: n_d * state_len_per_rank */
   int64_t n_segments;
   int64_t n_tiles;
+  int32_t n_replicate;          /* N_r: HSDP replica groups (1 otherwise)            */
+  int32_t n_shard;              /* N_s: ranks per shard group (n_d otherwise)         */
 } fsp_plan_info;
 
 /* One contiguous run of a rank's shard.  Elements [full_off, full_off + len)
  * of every full-size buffer live in slots [state_off, state_off + len) of
  * master / m / v; slots [state_off + len, state_off + padded_len) are shard
- * padding and are never written.  param = -1 for a DistOpt shard. */
+ * padding and are never written.  param = -1 for a DistOpt shard.  HSDP:
+ * replica group r's copy of the state is the state_len_total / N_r slots
+ * starting at r * state_len_total / N_r. */
 typedef struct {
   int32_t param;
   int32_t rank;
@@ -122,9 +135,11 @@ typedef struct {
   double resident_distopt;    /* (2 + g) P + 12 P / N_d             */
   double resident_zero2;      /* 2 P + (g + 12) P / N_d             */
   double resident_fsdp;       /* (2 + g + 12) P / N_d               */
-  double reduce_scatter_sent; /* (N_d - 1) / N_d * g P              */
-  double all_gather_sent;     /* (N_d - 1) / N_d * 2 P              */
-  double step_hbm_bytes;      /* (N_d g + 24 + 2 N_d) P: one fused step on one GPU */
+  double reduce_scatter_sent; /* (N_s - 1) / N_s * g P  (N_s = N_d unless HSDP) */
+  double all_gather_sent;     /* (N_s - 1) / N_s * 2 P              */
+  double step_hbm_bytes;      /* (N_d g + 24 N_r + 2 N_d) P: one fused step on one GPU */
+  double resident_hsdp;       /* (2 + g + 12) P / N_s               */
+  double cross_group_all_reduce_sent; /* 2 (N_r - 1) / N_r * g P / N_s (0 when N_r = 1) */
 } fsp_ledger;
 
 /* Plans the layout of n_params parameters over n_d simulated ranks.
@@ -140,10 +155,17 @@ typedef struct {
 fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_params,
                            int32_t n_d, int32_t mode, fsp_plan** out);
 
+/* HSDP plan (FSP_MODE_HSDP) of n_replicate groups of n_shard ranks each
+ * (n_replicate, n_shard >= 1, product <= 64); dims / ndims / n_params as for
+ * fsp_plan_layout.  master / m / v then hold n_replicate copies of the
+ * n_shard-rank FSDP2 state (state_len_total covers all of them). */
+fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                                int32_t n_replicate, int32_t n_shard, fsp_plan** out);
+
 fsp_status fsp_plan_info_get(const fsp_plan* plan, fsp_plan_info* out);
 
-/* Segment i (0 <= i < n_segments).  FSDP2: ordered by rank, then parameter.
- * DistOpt: one segment per rank. */
+/* Segment i (0 <= i < n_segments).  FSDP2 and HSDP: ordered by rank, then
+ * parameter.  DistOpt: one segment per rank. */
 fsp_status fsp_plan_segment(const fsp_plan* plan, int64_t i, fsp_segment* out);
 
 fsp_status fsp_plan_ledger(const fsp_plan* plan, int32_t grad_dtype, fsp_ledger* out);

@@ -1,4 +1,4 @@
-"""The five synthetic workloads: parameter shapes, N_d, layout mode, grad dtype.
+"""The synthetic workloads: parameter shapes, N_d, layout mode, grad dtype.
 
 Shapes follow the model descriptions they stand for (no weights or data are
 involved; values come from the seeded generator in this package):
@@ -18,6 +18,9 @@ involved; values come from the seeded generator in this package):
 * ``dense_1p5b_bf16grad`` - 24 layers of d=2048, 16 q / 4 kv heads of 128,
   ffn 5632 (no embedding, no q/k-norm named): 216 params, 1,082,228,736
   elements; N_d=16, bf16 gradients reduced in fp32.
+* ``qwen3_0p6b_hsdp_2x4`` - the Qwen3-0.6B-shaped stack under HSDP
+  ("Parallelism strategies: which state to shard", section 二.6): 2 replica
+  groups of 4 shard ranks (N_d=8), fp32 grads.
 
 All share AdamW lr 3e-4, betas (0.9, 0.95), eps 1e-8, weight decay 0.1 and
 update index t=10; data seed 0x5EED0000 + workload index.
@@ -43,8 +46,9 @@ class Workload:
     name: str
     shapes: tuple
     n_d: int
-    mode: str            # "fsdp2" | "distopt"
+    mode: str            # "fsdp2" | "distopt" | "hsdp"
     grad_dtype: str      # "f32" | "bf16"
+    n_rep: int = 1       # HSDP replica groups (N_d = n_rep x shard-group size)
     lr: float = 3e-4
     beta1: float = 0.9
     beta2: float = 0.95
@@ -131,6 +135,8 @@ WORKLOADS = (
              description="500 ragged params, N_d=6, FSDP2 Shard(0) with padding, fp32 grads"),
     Workload(4, "dense_1p5b_bf16grad", dense_1p5b_shapes(), 16, "fsdp2", "bf16",
              description="24-layer d=2048 GQA/SwiGLU stack, N_d=16, FSDP2, bf16 grads reduced in fp32"),
+    Workload(5, "qwen3_0p6b_hsdp_2x4", qwen3_0p6b_shapes(), 8, "hsdp", "f32", n_rep=2,
+             description="Qwen3-0.6B-shaped stack, HSDP: 2 replica groups x 4 shard ranks, fp32 grads"),
 )
 
 

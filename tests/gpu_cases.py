@@ -117,9 +117,9 @@ def state_errors(got, ref, old, hp=HP):
 class DeviceCase:
     """A plan plus guarded device buffers filled from the seeded generator."""
 
-    def __init__(self, shapes, n_d, mode, grad_dtype, seed):
+    def __init__(self, shapes, n_d, mode, grad_dtype, seed, n_rep=1):
         self.shapes, self.n_d, self.mode, self.grad_dtype, self.seed = shapes, n_d, mode, grad_dtype, seed
-        self.plan = fsp.plan_layout(shapes, n_d, mode)
+        self.plan = fsp.plan_layout(shapes, n_d, mode, n_replicate=n_rep)
         p = self.plan
         gdt = torch.float32 if grad_dtype == "f32" else torch.bfloat16
         self.grads = [Guarded(p.full_len_padded, gdt, 0) for _ in range(n_d)]
@@ -147,8 +147,8 @@ class DeviceCase:
 class OracleCase:
     """The same inputs on the host, from the oracle's planner and the host generator."""
 
-    def __init__(self, shapes, n_d, mode, grad_dtype, seed):
-        self.plan = OP.plan_layout(shapes, n_d, mode)
+    def __init__(self, shapes, n_d, mode, grad_dtype, seed, n_rep=1):
+        self.plan = OP.plan_layout(shapes, n_d, mode, n_rep=n_rep)
         self.grad_dtype = grad_dtype
         p = self.plan
         idx = np.arange(p.full_len_padded)

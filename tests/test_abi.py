@@ -59,17 +59,27 @@ def _compare_plans(lib_plan, o):
     got = [(s.rank, s.param, s.full_off, s.state_off, s.length, s.padded_len) for s in lib_plan.segments]
     want = sorted((s.rank, s.param, s.full_off, s.state_off, s.length, s.padded_len) for s in o.segments)
     assert got == want
-    # tiles: one per started 4096-block of each non-empty segment
+    # tiles: one per started 4096-block of each non-empty segment of one replica
     tiles = 0
     for s in o.segments:
-        if s.length:
+        if s.length and s.rank < o.n_shard:
             tiles += (s.full_off + s.length - 1) // 4096 - s.full_off // 4096 + 1
     assert lib_plan.n_tiles == tiles
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
 def test_planner_matches_oracle_on_workloads(w):
-    _compare_plans(fsp.plan_layout(w.shapes, w.n_d, w.mode), OP.plan_layout(w.shapes, w.n_d, w.mode))
+    lib_plan = fsp.plan_layout(w.shapes, w.n_d, w.mode, n_replicate=w.n_rep)
+    _compare_plans(lib_plan, OP.plan_layout(w.shapes, w.n_d, w.mode, n_rep=w.n_rep))
+    assert (lib_plan.n_replicate, lib_plan.n_shard) == (w.n_rep, w.n_d // w.n_rep)
+
+
+@pytest.mark.parametrize("n_rep,n_shard", [(1, 1), (1, 5), (2, 1), (2, 2), (2, 3), (4, 4), (3, 7), (8, 8), (16, 4)])
+def test_hsdp_planner_matches_oracle(n_rep, n_shard):
+    rng = np.random.default_rng(n_rep * 100 + n_shard)
+    shapes = [(int(rng.integers(0, 3 * n_shard + 5)), int(rng.choice([1, 3, 64]))) for _ in range(int(rng.integers(0, 25)))]
+    _compare_plans(fsp.plan_layout(shapes, n_rep * n_shard, "hsdp", n_replicate=n_rep),
+                   OP.plan_layout(shapes, n_rep * n_shard, "hsdp", n_rep=n_rep))
 
 
 @pytest.mark.parametrize("mode", ["fsdp2", "distopt"])
@@ -93,16 +103,20 @@ def test_empty_plan():
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
 def test_ledger_matches_oracle(w):
-    led = fsp.plan_layout(w.shapes, w.n_d, w.mode).ledger(w.grad_dtype)
-    P, n, g = w.numel, w.n_d, w.grad_bytes
+    led = fsp.plan_layout(w.shapes, w.n_d, w.mode, n_replicate=w.n_rep).ledger(w.grad_dtype)
+    P, n, g, nr = w.numel, w.n_d, w.grad_bytes, w.n_rep
+    ns = n // nr
+    sent = OL.hsdp_step_sent(nr, ns, g * P, 2 * P)
     want = {
         "resident_ddp": OL.resident_bytes("ddp", P, n, g),
         "resident_distopt": OL.resident_bytes("distopt", P, n, g),
         "resident_zero2": OL.resident_bytes("zero2", P, n, g),
         "resident_fsdp": OL.resident_bytes("fsdp", P, n, g),
-        "reduce_scatter_sent": OL.coll_bytes("reduce_scatter", n, g * P),
-        "all_gather_sent": OL.coll_bytes("all_gather", n, 2 * P),
-        "step_hbm_bytes": OL.sharded_step_bytes(n, g) * P,
+        "reduce_scatter_sent": sent["reduce_scatter"],
+        "all_gather_sent": sent["all_gather"],
+        "step_hbm_bytes": OL.sharded_step_bytes(n, g, nr) * P,
+        "resident_hsdp": OL.hsdp_bytes_per_param(ns, g) * P,
+        "cross_group_all_reduce_sent": sent["cross_group_all_reduce"],
     }
     for k, v in want.items():
         assert led[k] == pytest.approx(float(v), rel=1e-12), k
@@ -119,6 +133,16 @@ def _raw_layout(dims, ndims, n_params, n_d, mode):
     if out.value:
         L.fsp_plan_destroy(out)
     return st
+
+
+def test_hsdp_layout_rejects():
+    L = B.lib()
+    d = (ctypes.c_int64 * 1)(4)
+    nd = (ctypes.c_int32 * 1)(1)
+    out = ctypes.c_void_p()
+    for nr, ns in ((0, 4), (2, 0), (8, 9), (-1, 2)):
+        assert L.fsp_plan_layout_hsdp(d, nd, 1, nr, ns, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_plan_layout_hsdp(d, nd, 1, 2, 2, None) == B.FSP_EINVAL
 
 
 @pytest.mark.parametrize("dims,ndims,n_params,n_d,mode", [

@@ -29,10 +29,17 @@ CASES = [
 ]
 
 
+CASES += [
+    (((3001, 7), (12289,), (9, 5)), 8, "hsdp", "f32", 11, 4096),   # 2 x 4 mesh
+    (((3001, 7), (12289,), (9, 5)), 6, "hsdp", "bf16", 12, 8192),  # 2 x 3 mesh (generic kernel)
+]
+
+
 @pytest.mark.parametrize("shapes,n_d,mode,grad_dtype,seed,chunk", CASES)
 def test_host_step_matches_device_step(shapes, n_d, mode, grad_dtype, seed, chunk):
-    ref = DeviceCase(shapes, n_d, mode, grad_dtype, seed)
-    hst = DeviceCase(shapes, n_d, mode, grad_dtype, seed)
+    n_rep = 2 if mode == "hsdp" else 1
+    ref = DeviceCase(shapes, n_d, mode, grad_dtype, seed, n_rep)
+    hst = DeviceCase(shapes, n_d, mode, grad_dtype, seed, n_rep)
     plan = hst.plan
     host_g = [g.t.cpu().pin_memory() for g in hst.grads]
     host_p = [torch.full((plan.full_len_padded,), PARAM_SENTINEL - 65536, dtype=torch.int16).view(torch.bfloat16)

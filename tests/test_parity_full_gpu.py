@@ -43,16 +43,17 @@ def _sample_indices(oplan, rng, n_random):
 
 
 def _state_index(oplan, f):
-    segs = sorted((s for s in oplan.segments if s.length), key=lambda s: s.full_off)
+    """Replica 0's state slot of each full index."""
+    segs = sorted((s for s in oplan.segments if s.length and s.rank < oplan.n_shard), key=lambda s: s.full_off)
     starts = np.array([s.full_off for s in segs], np.int64)
     k = np.searchsorted(starts, f, side="right") - 1
     offs = np.array([s.state_off - s.full_off for s in segs], np.int64)
     return f + offs[k]
 
 
-def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
-    plan = fsp.plan_layout(shapes, n_d, mode)
-    oplan = OP.plan_layout(shapes, n_d, mode)
+def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000, n_rep=1):
+    plan = fsp.plan_layout(shapes, n_d, mode, n_replicate=n_rep)
+    oplan = OP.plan_layout(shapes, n_d, mode, n_rep=n_rep)
     gdt = torch.float32 if grad_dtype == "f32" else torch.bfloat16
     grads = [Guarded(plan.full_len_padded, gdt, 0) for _ in range(n_d)]
     for q, g in enumerate(grads):
@@ -73,13 +74,17 @@ def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
     fd = torch.from_numpy(f).cuda()
     sd = torch.from_numpy(s).cuda()
     got = [st.t[sd].cpu().numpy() for st in state]
+    for r in range(1, n_rep):   # every replica group's copy of the state is the same
+        for st in state:
+            assert np.array_equal(st.t[sd + r * (plan.state_len_total // n_rep)].cpu().numpy().view(np.uint32),
+                                  got[state.index(st)].view(np.uint32))
     got_p = [p.t.view(torch.int16)[fd].cpu().numpy().view(np.uint16) for p in params]
     if grad_dtype == "f32":
         cols = [S.grad_f32(seed, q, f) for q in range(n_d)]
     else:
         cols = [S.grad_bf16_bits(seed, q, f) for q in range(n_d)]
     olds = (S.master_f32(seed, f), S.adam_m_f32(seed, f), S.adam_v_f32(seed, f))
-    th, mm, vv, b, _ = OS.elementwise_step(cols, grad_dtype, *olds, HP, t)
+    th, mm, vv, b, _ = OS.elementwise_step(cols, grad_dtype, *olds, HP, t, n_rep=n_rep)
     errs = state_errors(got, (th, mm, vv), olds)
     for name, g_, r_, se in zip(("master", "exp_avg", "exp_avg_sq"), got, (th, mm, vv), errs):
         ok = within_tol(g_, r_)
@@ -103,7 +108,7 @@ def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
                 a, c = sg.full_off, sg.state_off
                 assert torch.equal(p0[a:a + sg.length],
                                    master[c:c + sg.length].to(torch.bfloat16).view(torch.int16))
-    padding = plan.state_len_total - plan.valid_elems
+    padding = plan.state_len_total - plan.valid_elems * n_rep
     for st in state:
         n_sent = int((st.t.view(torch.int32) == int(np.uint32(STATE_SENTINEL).view(np.int32))).sum())
         assert n_sent == padding, "a padding slot of the state was written (or an owned one was not)"
@@ -111,11 +116,11 @@ def _full_size_case(shapes, n_d, mode, grad_dtype, seed, t, n_random=200_000):
     assert fsp.device_error() == 0, "a bounded wait in the step kernel ran out"
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4], ids=lambda i: workload(i).name)
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4, 5], ids=lambda i: workload(i).name)
 def test_workload_full_size(idx):
     w = workload(idx)
     try:
-        _full_size_case(w.shapes, w.n_d, w.mode, w.grad_dtype, w.data_seed, w.step)
+        _full_size_case(w.shapes, w.n_d, w.mode, w.grad_dtype, w.data_seed, w.step, n_rep=w.n_rep)
     finally:
         torch.cuda.empty_cache()
 

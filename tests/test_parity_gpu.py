@@ -29,9 +29,9 @@ def _tiny_shapes(rng, n_d):
     return shapes
 
 
-def _run(shapes, n_d, mode, grad_dtype, seed, steps=(10, 11)):
-    dev = DeviceCase(shapes, n_d, mode, grad_dtype, seed)
-    ora = OracleCase(shapes, n_d, mode, grad_dtype, seed)
+def _run(shapes, n_d, mode, grad_dtype, seed, steps=(10, 11), n_rep=1):
+    dev = DeviceCase(shapes, n_d, mode, grad_dtype, seed, n_rep)
+    ora = OracleCase(shapes, n_d, mode, grad_dtype, seed, n_rep)
     stats = None
     for t in steps:
         dev.step(t)
@@ -55,6 +55,17 @@ def test_generic_rank_count(n_d, grad_dtype):
     """N_d without a specialised kernel, up to the maximum of 64."""
     rng = np.random.default_rng(n_d)
     _run(_tiny_shapes(rng, n_d) + [(3 * n_d + 1, 17)], n_d, "fsdp2", grad_dtype, seed=2000 + n_d)
+
+
+@pytest.mark.parametrize("n_rep,n_shard", [(2, 2), (2, 4), (2, 8), (4, 2), (4, 4),   # bulk-copy kernels
+                                           (2, 3), (3, 2), (2, 1), (4, 1), (8, 8)])  # generic kernel
+@pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
+def test_hsdp_cases(n_rep, n_shard, grad_dtype):
+    """HSDP: reduce-scatter inside each replica group, all-reduce across groups,
+    each group's own copy of the state, gather within the group."""
+    rng = np.random.default_rng(n_rep * 31 + n_shard)
+    shapes = _tiny_shapes(rng, n_shard) + [(4097,), (3 * n_shard + 1, 67)]
+    _run(shapes, n_rep * n_shard, "hsdp", grad_dtype, seed=3000 + n_rep * n_shard, n_rep=n_rep)
 
 
 @pytest.mark.parametrize("n_d,mode", [(3, "fsdp2"), (6, "fsdp2"), (6, "distopt"), (8, "fsdp2")])
