@@ -15,6 +15,7 @@ from .fsp import (  # noqa: F401
     device_error,
     lib,
     plan_layout,
+    selftest_bounded_wait,
     sharded_step,
     sharded_step_debug,
     sharded_step_host,

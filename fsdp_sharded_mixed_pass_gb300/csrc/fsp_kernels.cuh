@@ -298,13 +298,16 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Waits for the phase of parity `parity` to complete; false after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Waits for the phase of parity `parity` to complete; false once `limit_ns`
+// has passed (or after 2^30 polls, whichever comes first).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
@@ -325,6 +328,18 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// ever arrives at; the wait must give up after `limit_ns` and report through
+// the device error word, exactly as the step kernel's waits do.
+constexpr unsigned kErrSelfTest = 4u;
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_addr(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait(smem_addr(&bar), 0, limit_ns)) atomicOr(&g_fsp_device_error, kErrSelfTest);
+}
+
 // Aligned body [b0, b1) of a tile: 8-element (16-byte) boundaries in the full
 // index, so every bulk copy starts and ends on 16 bytes for fp32 and bf16.
 struct Body {

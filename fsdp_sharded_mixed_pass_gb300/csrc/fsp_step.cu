@@ -68,6 +68,13 @@ fsp_status check_allocation(const void* ptr, size_t bytes, const char* name) {
     return reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
   }();
   if (!get_range) return fail(FSP_ECUDA, "cannot resolve cuMemGetAddressRange");
+  // The driver call needs a current context on this thread; a thread that has
+  // made no runtime call yet has none, so bind the current device's primary
+  // context (cudaSetDevice does that, and nothing else, when it is current).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("binding the device context", e));
   CUdeviceptr base = 0;
   size_t size = 0;
   if (get_range(&base, &size, reinterpret_cast<CUdeviceptr>(ptr)) != CUDA_SUCCESS)
@@ -653,4 +660,21 @@ extern "C" fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* co
                                             void* cuda_stream) {
   return fsp::run_step_host(plan, host_grads, grad_dtype, master, exp_avg, exp_avg_sq, host_params, hp, step,
                             workspace, workspace_bytes, chunk_elems, cuda_stream);
+}
+
+extern "C" fsp_status fsp_selftest_bounded_wait(uint32_t limit_ms, uint32_t* bits) {
+  fsp::clear_error();
+  if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
+  if (limit_ms < 1 || limit_ms > 2000) return fsp::fail(FSP_EINVAL, "limit_ms must be in [1, 2000]");
+  uint32_t before = 0;
+  fsp_status s = fsp_device_error(&before);   // start from a clear word
+  if (s != FSP_OK) return s;
+  fsp::bounded_wait_selftest_kernel<<<1, 32>>>(uint64_t(limit_ms) * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("bounded-wait self-test", e));
+  s = fsp_device_error(bits);
+  if (s != FSP_OK) return s;
+  *bits |= before;
+  return FSP_OK;
 }

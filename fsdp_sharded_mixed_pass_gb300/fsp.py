@@ -20,7 +20,8 @@ DTYPES = {"f32": 0, "bf16": 1}
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
-           "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_status_string", "fsp_last_error")
+           "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
+           "fsp_last_error")
 
 
 class FspError(RuntimeError):
@@ -86,6 +87,8 @@ def lib():
     L.fsp_sharded_step_host.restype = ctypes.c_int
     L.fsp_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.fsp_device_error.restype = ctypes.c_int
+    L.fsp_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]
+    L.fsp_selftest_bounded_wait.restype = ctypes.c_int
     L.fsp_status_string.argtypes = [ctypes.c_int]
     L.fsp_status_string.restype = ctypes.c_char_p
     L.fsp_last_error.argtypes = []
@@ -276,3 +279,11 @@ def sharded_step_host(plan: Plan, host_grads, master, exp_avg, exp_avg_sq, host_
     nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else 0
     _check(lib().fsp_sharded_step_host(*args, ctypes.c_void_p(_ptr(workspace)), nbytes, int(chunk_elems),
                                        ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_host")
+
+
+def selftest_bounded_wait(limit_ms: int = 100) -> int:
+    """Runs the bounded-wait self-test (a wait nothing completes) and returns
+    the device error word it left (bit 4 when the bound worked)."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().fsp_selftest_bounded_wait(int(limit_ms), ctypes.byref(bits)), "fsp_selftest_bounded_wait")
+    return int(bits.value)

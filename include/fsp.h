@@ -248,11 +248,19 @@ fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* gra
 
 /* Reads and clears the device error word of the current device (synchronous:
  * waits for the device).  The step kernel's waits on its own copy pipeline
- * are bounded (about 2 s); one that runs out sets a bit here (1: a consumer
- * waited for data, 2: the producer waited for a free stage), lets its copies
- * land and ends the kernel, leaving that step's results incomplete.  0 means
- * every step since the last read completed normally. */
+ * are bounded (about 2 s); one that runs out sets a bit here (1: the storer
+ * waited for the consumers' results, 2: the producer waited for a free
+ * stage; 4: the self-test below), lets its copies land and ends the kernel,
+ * leaving that step's results incomplete.  0 means every step since the last
+ * read completed normally. */
 fsp_status fsp_device_error(uint32_t* bits);
+
+/* Self-test of the step kernel's bounded waits: runs one thread that waits
+ * on an mbarrier nothing ever arrives at, with the step kernel's wait routine
+ * and a limit of limit_ms (1..2000) milliseconds, synchronises the device and
+ * returns the device error word in *bits (cleared afterwards).  A working
+ * bound gives bit 4 after about limit_ms; the device stays usable. */
+fsp_status fsp_selftest_bounded_wait(uint32_t limit_ms, uint32_t* bits);
 
 /* Message for a status code (static storage). */
 const char* fsp_status_string(fsp_status status);
