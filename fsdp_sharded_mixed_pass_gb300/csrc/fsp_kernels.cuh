@@ -47,7 +47,7 @@ constexpr int kGenericThreads = 256;
 constexpr int kConsumerThreads = 256;                  // 8 consumer warps
 constexpr int kBulkThreads = kConsumerThreads + 64;    // + producer warp + storer warp
 constexpr int kBulkSmemBudget = 196608;                // stage ring, bytes
-constexpr int kBulkStageBudget = 49152;                // one stage, bytes
+constexpr int kBulkStageBudget = 65536;                // one stage, bytes
 
 // Device error bits (sticky until read by fsp_device_error).
 constexpr unsigned kErrConsumerWait = 1u;
