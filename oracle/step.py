@@ -213,3 +213,60 @@ def rs_update_ag(plan: Plan, grads, update) -> list:
     outs = [np.full(plan.full_len_padded, np.nan, dtype=np.float32) for _ in range(plan.n_d)]
     all_gather(plan, [np.asarray(update(s), dtype=np.float32) for s in sums], outs)
     return outs
+
+
+# ---------------------------------------------------------------------------
+# Megatron distributed-optimizer flow with gradient clipping
+# ---------------------------------------------------------------------------
+#
+# The reduce-scatter leaves each rank's averaged shard of the gradient in that
+# rank's own 1/N_d slice of its grad buffer ("07 · 显存模型", section 2.1 item 1:
+# the buffer stays full size, the result is written back into the rank's
+# slice).  Global-norm clipping is not on the pages; the reading taken is
+# PyTorch's clip_grad_norm_: total norm = sqrt of the sum of squares of every
+# reduced gradient element (each counted once), coefficient =
+# min(1, max_norm / (norm + 1e-6)), every gradient element multiplied by it
+# in fp32 before the optimizer.  Here the norm is taken in fp64 and the
+# coefficient is rounded once to fp32.
+
+def reduce_scatter_write_back(plan: Plan, grads, grad_dtype: str = "f32"):
+    """Averaged shard gradients, also written into each owner's grad slice."""
+    if grad_dtype != "f32":
+        raise ValueError("write-back is defined for fp32 grad buffers")
+    reduced = reduce_scatter(plan, grads, grad_dtype, mean=True)
+    for seg, g in zip(plan.segments, reduced):
+        grads[seg.rank][seg.full_off:seg.full_off + seg.length] = g
+    return reduced
+
+
+def global_grad_norm(reduced) -> float:
+    """sqrt(sum of squares) over every reduced gradient element, in fp64."""
+    total = 0.0
+    for g in reduced:
+        g64 = np.asarray(g, dtype=np.float32).astype(np.float64)
+        total += float(np.dot(g64, g64))
+    return float(np.sqrt(total))
+
+
+def clip_coefficient(norm: float, max_norm) -> np.float32:
+    c = float(np.float32(max_norm)) / (norm + 1e-6)
+    return np.float32(min(1.0, c))
+
+
+def sharded_step_clipped(plan: Plan, grads, master, m, v, params, hp: dict, t: int, max_norm):
+    """reduce-scatter with write-back -> global norm -> clip -> AdamW -> cast ->
+    all-gather.  Returns (norm, coefficient).  fp32 grads, one replica group."""
+    if plan.n_rep != 1:
+        raise ValueError("clipping is defined here for FSDP2 and DistOpt plans")
+    reduced = reduce_scatter_write_back(plan, grads, "f32")
+    norm = global_grad_norm(reduced)
+    coef = clip_coefficient(norm, max_norm)
+    casts = []
+    for seg, g in zip(plan.segments, reduced):
+        st = slice(seg.state_off, seg.state_off + seg.length)
+        gc = (g * coef).astype(np.float32)
+        th, mm, vv = adamw(master[st], m[st], v[st], gc, hp, t)
+        master[st], m[st], v[st] = th, mm, vv
+        casts.append(bf16_rne(th))
+    all_gather(plan, casts, params)
+    return norm, coef
