@@ -64,6 +64,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--clip", type=float, default=None, metavar="MAX_NORM",
+                    help="time the distributed-optimizer flow instead: reduce-scatter written back into the "
+                         "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the timed steps in one CUDA graph (removes host launch overhead; small cases)")
     return ap.parse_args(argv)
@@ -237,11 +240,24 @@ class DeviceWorkload:
         self.params = [torch.zeros(p.full_len_padded, dtype=torch.bfloat16, device=device) for _ in range(w.n_d)]
         torch.cuda.synchronize(device)
         self.t = w.step
+        self.clip = None
+        self.norm_out = torch.zeros(4, dtype=torch.float32, device=device)
 
     def step(self, stream):
         import fsdp_sharded_mixed_pass_gb300 as fsp
-        fsp.sharded_step(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t, stream=stream)
+        if self.clip is not None:
+            fsp.sharded_step_clipped(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
+                                     self.clip, self.norm_out, stream=stream)
+        else:
+            fsp.sharded_step(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
+                             stream=stream)
         self.t += 1
+
+    def bytes_per_param(self) -> int:
+        w = self.w
+        if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
+            return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+        return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
 
 
 def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False):
@@ -417,6 +433,7 @@ def run_fsp(args):
     torch.cuda.set_device(dev)
     w, shapes, label = resolve_workload(args.workload, args.param_slice)
     wl = DeviceWorkload(w, shapes, dev)
+    wl.clip = args.clip
     plan = wl.plan
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
@@ -431,14 +448,14 @@ def run_fsp(args):
     P = plan.valid_elems
     total_params = P * args.steps * dist.world
     value = total_params / (ms_max / 1e3)
-    per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+    per = wl.bytes_per_param()
     launch_s = ms / 1e3 / args.steps
     achieved = per * P / launch_s / 1e9
     peak, peak_src = read_peak()
     tpe = traffic_per_elem(w.name)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.clip is None:
         dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist, args.e2e_chunk)
         dt = dist.max(dt)
         e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
@@ -458,16 +475,18 @@ def run_fsp(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_block(w, label, plan),
+        "config": dict(config_block(w, label, plan), bytes_per_param=per, **(
+            {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (3 kernels per step)"}
+            if args.clip is not None else {})),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "traffic": tpe * P if tpe is not None else None,
+                     "traffic": tpe * P if tpe is not None and args.clip is None else None,
                      "kernel": "sharded_step_kernel", "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if args.clip is not None else 1),
         "launch": "one CUDA graph of the K steps" if args.graph else "one launch per step from the host",
         "clocks": clocks,
     }

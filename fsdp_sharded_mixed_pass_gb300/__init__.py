@@ -17,6 +17,7 @@ from .fsp import (  # noqa: F401
     plan_layout,
     selftest_bounded_wait,
     sharded_step,
+    sharded_step_clipped,
     sharded_step_debug,
     sharded_step_host,
     host_step_workspace_bytes,

@@ -25,13 +25,14 @@ constexpr int64_t kStateAlign = 16;
 constexpr int64_t kDistOptAlign = 128;
 
 // One unit of work for a CTA: `len` elements starting at `full_begin` of every
-// full-size buffer and at `state_begin` of the state buffers.  32 bytes so a
-// descriptor is two aligned 16-byte loads.
+// full-size buffer and at `state_begin` of the state buffers, owned by `rank`
+// (the rank whose shard the elements are; replica group 0 for HSDP).  32 bytes
+// so a descriptor is two aligned 16-byte loads.
 struct Tile {
   int64_t full_begin;
   int64_t state_begin;
   int64_t len;
-  int64_t reserved;
+  int64_t rank;
 };
 static_assert(sizeof(Tile) == 32, "tile descriptor layout");
 
@@ -51,9 +52,11 @@ struct fsp_plan {
   std::vector<fsp_segment> segments;
   std::vector<fsp::Tile> tiles;   // one replica's elements (replica 0's state offsets)
 
-  // Device copies of `tiles`, one per device ordinal, uploaded on first use.
+  // Device copies of `tiles`, one per device ordinal, uploaded on first use,
+  // and per device the per-CTA partial sums of the clipped step's norm.
   mutable std::mutex mu;
   mutable std::map<int, fsp::Tile*> device_tiles;
+  mutable std::map<int, double*> device_partials;
 };
 
 namespace fsp {

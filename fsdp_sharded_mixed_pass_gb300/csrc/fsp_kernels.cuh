@@ -77,24 +77,27 @@ struct StepArgs {
   int n_rep;           // HSDP replica groups (1: FSDP2 / DistOpt)
   int n_shard;         // ranks per shard group; rank q = r * n_shard + j
   int64_t rep_stride;  // state elements between replica r's copy and r + 1's
+  const float* clip;   // clipped update: {norm, coefficient} on the device
   Coeffs c;
 };
 
 // Chunk size E and stage count S of the bulk kernel for NS x NR ranks (NR
 // replica groups of NS shard ranks) with grads of type GradT.
-template <int NS, int NR, typename GradT>
+// NG: gradient slices staged per chunk (N_d, or 1 for the clipped update,
+// which reads the already-reduced gradient from its owner's slice).
+template <int NS, int NR, typename GradT, int NG = NS * NR>
 struct BulkCfg {
   static constexpr int N = NS * NR;
-  // per element: N grads, NR copies of master/m/v, NR bf16 tiles
-  static constexpr int kBytesPerElem = N * int(sizeof(GradT)) + NR * (12 + 2);
+  // per element: NG grads, NR copies of master/m/v, NR bf16 tiles
+  static constexpr int kBytesPerElem = NG * int(sizeof(GradT)) + NR * (12 + 2);
   static constexpr int E = 1024 * kBytesPerElem <= kBulkStageBudget  ? 1024
                            : 512 * kBytesPerElem <= kBulkStageBudget ? 512
                                                                      : 256;
   static constexpr int kStageBytes = E * kBytesPerElem;
   static constexpr int kS0 = kBulkSmemBudget / kStageBytes;
   static constexpr int S = kS0 > 8 ? 8 : (kS0 < 2 ? 2 : kS0);
-  static constexpr int kGradOff = 0;                                  // [N][E] GradT
-  static constexpr int kStateOff = N * E * int(sizeof(GradT));        // [NR][3][E] float
+  static constexpr int kGradOff = 0;                                  // [NG][E] GradT
+  static constexpr int kStateOff = NG * E * int(sizeof(GradT));       // [NR][3][E] float
   static constexpr int kParamOff = kStateOff + NR * 3 * E * 4;        // [NR][E] bf16
   static constexpr int kBarrierBytes = 256;                           // full, computed, empty [S]
   static constexpr int kSmemBytes = kBarrierBytes + S * kStageBytes;
@@ -163,19 +166,25 @@ struct GradIO<__nv_bfloat16> {
 // Reduce: inside replica group r the rank-ordered fold of its NS slices (the
 // reduce-scatter), then the rank-ordered fold of the NR partial sums (the
 // all-reduce across groups); with NR = 1 it is the plain rank-ordered fold.
-template <int NS, int NR, typename GradT>
-__device__ __forceinline__ void step_one(const StepArgs& a, int64_t f, int64_t s) {
+// kClip: the clipped update - the gradient is already reduced and sits in
+// its owner's slice, and is multiplied by the clip coefficient instead.
+template <int NS, int NR, typename GradT, bool kClip>
+__device__ __forceinline__ void step_one(const StepArgs& a, int64_t f, int64_t s, int64_t owner, float coef) {
   const int ns = NS > 0 ? NS : a.n_shard;
   const int nr = NR > 0 ? NR : a.n_rep;
   float acc = 0.f;
+  if (kClip) {
+    acc = GradIO<GradT>::load1(a.grads[owner], f) * coef;
+  } else {
 #pragma unroll(NR > 0 ? NR : 1)
-  for (int r = 0; r < nr; ++r) {
-    float part = 0.f;
+    for (int r = 0; r < nr; ++r) {
+      float part = 0.f;
 #pragma unroll(NS > 0 ? NS : 1)
-    for (int j = 0; j < ns; ++j) part += GradIO<GradT>::load1(a.grads[r * ns + j], f);
-    acc = r == 0 ? part : acc + part;
+      for (int j = 0; j < ns; ++j) part += GradIO<GradT>::load1(a.grads[r * ns + j], f);
+      acc = r == 0 ? part : acc + part;
+    }
+    acc = acc / float(ns * nr);
   }
-  acc = acc / float(ns * nr);
 #pragma unroll(NR > 0 ? NR : 1)
   for (int r = 0; r < nr; ++r) {
     const int64_t sr = s + r * a.rep_stride;
@@ -201,23 +210,31 @@ __device__ __forceinline__ void add4(float4& a, float4 b) {
 }
 
 // f: full index (multiple of 4); s: state index (same residue mod 16).
-template <typename GradT>
-__device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t s) {
+template <typename GradT, bool kClip>
+__device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t s, int64_t owner, float coef) {
   const int ns = a.n_shard, nr = a.n_rep;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r = 0; r < nr; ++r) {
-    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < ns; ++j) add4(part, GradIO<GradT>::load4(a.grads[r * ns + j], f));
-    if (r == 0)
-      acc = part;
-    else
-      add4(acc, part);
+  if (kClip) {
+    acc = GradIO<GradT>::load4(a.grads[owner], f);
+    acc.x *= coef;
+    acc.y *= coef;
+    acc.z *= coef;
+    acc.w *= coef;
+  } else {
+    for (int r = 0; r < nr; ++r) {
+      float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < ns; ++j) add4(part, GradIO<GradT>::load4(a.grads[r * ns + j], f));
+      if (r == 0)
+        acc = part;
+      else
+        add4(acc, part);
+    }
+    const float nd = float(ns * nr);
+    acc.x = acc.x / nd;
+    acc.y = acc.y / nd;
+    acc.z = acc.z / nd;
+    acc.w = acc.w / nd;
   }
-  const float nd = float(ns * nr);
-  acc.x = acc.x / nd;
-  acc.y = acc.y / nd;
-  acc.z = acc.z / nd;
-  acc.w = acc.w / nd;
   for (int r = 0; r < nr; ++r) {
     const int64_t sr = s + r * a.rep_stride;
     float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + sr));
@@ -237,8 +254,9 @@ __device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t
 }
 
 // Any N_d up to 64 and any replica grouping.
-template <typename GradT>
+template <typename GradT, bool kClip>
 __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
+  const float coef = kClip ? a.clip[1] : 1.f;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     const int64_t f0 = tile.full_begin;
@@ -251,13 +269,86 @@ __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(c
     const int64_t tail = head + groups * 4;
     for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
       const int64_t f = f0 + head + 4 * i;
-      step_group<GradT>(a, f, f + delta);
+      step_group<GradT, kClip>(a, f, f + delta, tile.rank, coef);
     }
     const int64_t n_scalar = head + (len - tail);
     if (threadIdx.x < n_scalar) {
       const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<0, 0, GradT>(a, f0 + e, f0 + e + delta);
+      step_one<0, 0, GradT, kClip>(a, f0 + e, f0 + e + delta, tile.rank, coef);
     }
+  }
+}
+
+// ---- distributed-optimizer pass 1: reduce-scatter into the owner's slice + norm ----
+
+// Every element's averaged gradient (rank-ordered fp32 fold / N_d) is written
+// into its owner's slice of that rank's own grad buffer (fp32), and each CTA
+// leaves the fp64 sum of squares of the elements it reduced in partials[cta].
+// One replica group (FSDP2 / DistOpt).  NT > 0: N_d fixed; 0: a.n_d.
+template <int NT>
+__global__ void __launch_bounds__(kGenericThreads) rs_writeback_norm_kernel(const __grid_constant__ StepArgs a,
+                                                                            double* partials) {
+  const int n = NT > 0 ? NT : a.n_d;
+  double sq = 0.0;
+  for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const int64_t f0 = tile.full_begin, len = tile.len;
+    float* own = static_cast<float*>(const_cast<void*>(a.grads[tile.rank]));
+    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
+    const int64_t groups = (len - head) >> 2;
+    const int64_t tail = head + groups * 4;
+    for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+      const int64_t f = f0 + head + 4 * i;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(NT > 0 ? NT : 1)
+      for (int q = 0; q < n; ++q) add4(acc, GradIO<float>::load4(a.grads[q], f));
+      acc.x = acc.x / float(n);
+      acc.y = acc.y / float(n);
+      acc.z = acc.z / float(n);
+      acc.w = acc.w / float(n);
+      *reinterpret_cast<float4*>(own + f) = acc;
+      sq += double(acc.x) * acc.x + double(acc.y) * acc.y + double(acc.z) * acc.z + double(acc.w) * acc.w;
+    }
+    const int64_t n_scalar = head + (len - tail);
+    if (threadIdx.x < n_scalar) {
+      const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
+      float acc = 0.f;
+#pragma unroll(NT > 0 ? NT : 1)
+      for (int q = 0; q < n; ++q) acc += GradIO<float>::load1(a.grads[q], f);
+      acc = acc / float(n);
+      own[f] = acc;
+      sq += double(acc) * acc;
+    }
+  }
+  // CTA sum in a fixed order: warp shuffles, then warp 0 over the warp sums
+  __shared__ double warp_sums[kGenericThreads / 32];
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_down_sync(0xffffffffu, sq, o);
+  if (threadIdx.x % 32 == 0) warp_sums[threadIdx.x / 32] = sq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    for (int w = 0; w < kGenericThreads / 32; ++w) total += warp_sums[w];
+    partials[blockIdx.x] = total;
+  }
+}
+
+// pass 2: out = {sqrt(sum of partials), min(1, max_norm / (norm + 1e-6))}.
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const double* partials, int n_partials, float max_norm,
+                                                            float* out) {
+  __shared__ double s[256];
+  double x = 0.0;
+  for (int i = threadIdx.x; i < n_partials; i += 256) x += partials[i];
+  s[threadIdx.x] = x;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(s[0]);
+    const double c = double(max_norm) / (norm + 1e-6);
+    out[0] = float(norm);
+    out[1] = float(c < 1.0 ? c : 1.0);
   }
 }
 
@@ -360,10 +451,11 @@ __device__ __forceinline__ Body tile_body(const Tile& t) {
 //   full[s]      producer -> consumers: the chunk's N_d + 3 slices have landed
 //   computed[s]  consumers -> storer: all 8 warps left results in the stage
 //   empty[s]     storer -> producer: the bulk stores have read the stage out
-template <int NS, int NR, typename GradT>
+template <int NS, int NR, typename GradT, bool kClip>
 __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __grid_constant__ StepArgs a) {
-  using Cfg = BulkCfg<NS, NR, GradT>;
   constexpr int N = NS * NR;
+  constexpr int NG = kClip ? 1 : N;   // gradient slices staged per chunk
+  using Cfg = BulkCfg<NS, NR, GradT, NG>;
   constexpr int E = Cfg::E, S = Cfg::S, G = int(sizeof(GradT));
   constexpr int kConsumerWarps = kConsumerThreads / 32;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -406,11 +498,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         }
         unsigned char* st = stages + stage * Cfg::kStageBytes;
         const uint32_t bar = smem_addr(&full[stage]);
-        mbar_arrive_expect_tx(bar, len * uint32_t(N * G + NR * 12));
-#pragma unroll
-        for (int q = 0; q < N; ++q)
-          bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+        mbar_arrive_expect_tx(bar, len * uint32_t(NG * G + NR * 12));
+        if (kClip) {   // the reduced gradient, from its owner's slice
+          bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(a.grads[tile.rank]) + c * G,
                     len * G, bar);
+        } else {
+#pragma unroll
+          for (int q = 0; q < N; ++q)
+            bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+                      len * G, bar);
+        }
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const int64_t s = c + delta + r * a.rep_stride;
@@ -478,6 +575,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
 
   // ---------------- consumers: fold, update, cast in shared memory ----------------
   const int tid = threadIdx.x;
+  const float coef = kClip ? a.clip[1] : 1.f;
   int stage = 0;
   uint32_t phase = 0;
   int64_t t = blockIdx.x;
@@ -493,7 +591,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     const int64_t n_head = body.b0 - tile.full_begin, n_tail = end - body.b1;
     if (tid < n_head + n_tail) {
       const int64_t f = tid < n_head ? tile.full_begin + tid : body.b1 + (tid - n_head);
-      step_one<NS, NR, GradT>(a, f, f + delta);
+      step_one<NS, NR, GradT, kClip>(a, f, f + delta, tile.rank, coef);
     }
 
     for (int64_t c = body.b0; c < body.b1; c += E) {
@@ -506,20 +604,29 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         // (1) reduce-scatter (inside each replica group) and all-reduce (across
         // groups): rank-ordered folds, then divide by N_d
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kClip) {
+          acc = GradIO<GradT>::smem4(st + Cfg::kGradOff, j);
+          acc.x *= coef;
+          acc.y *= coef;
+          acc.z *= coef;
+          acc.w *= coef;
+        } else {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int r = 0; r < NR; ++r) {
+            float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < NS; ++q) add4(part, GradIO<GradT>::smem4(st + Cfg::kGradOff + (r * NS + q) * E * G, j));
-          if (r == 0)
-            acc = part;
-          else
-            add4(acc, part);
+            for (int q = 0; q < NS; ++q)
+              add4(part, GradIO<GradT>::smem4(st + Cfg::kGradOff + (r * NS + q) * E * G, j));
+            if (r == 0)
+              acc = part;
+            else
+              add4(acc, part);
+          }
+          acc.x = acc.x / float(N);
+          acc.y = acc.y / float(N);
+          acc.z = acc.z / float(N);
+          acc.w = acc.w / float(N);
         }
-        acc.x = acc.x / float(N);
-        acc.y = acc.y / float(N);
-        acc.z = acc.z / float(N);
-        acc.w = acc.w / float(N);
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           // (2) AdamW on replica r's copy of the shard, in place in the stage

@@ -39,7 +39,7 @@ void append_tiles(const fsp_segment& s, std::vector<Tile>& out) {
   const int64_t end = s.full_off + s.len;
   while (f < end) {
     int64_t stop = std::min(end, (f / kTileElems + 1) * kTileElems);
-    out.push_back(Tile{f, s.state_off + (f - s.full_off), stop - f, 0});
+    out.push_back(Tile{f, s.state_off + (f - s.full_off), stop - f, s.rank});
     f = stop;
   }
 }
@@ -281,15 +281,19 @@ extern "C" fsp_status fsp_plan_ledger(const fsp_plan* p, int32_t grad_dtype, fsp
 
 extern "C" void fsp_plan_destroy(fsp_plan* p) {
   if (!p) return;
-  if (!p->device_tiles.empty()) {
+  if (!p->device_tiles.empty() || !p->device_partials.empty()) {
     std::lock_guard<std::mutex> lock(p->mu);
     int prev = -1;
     const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
     for (auto& kv : p->device_tiles) {
       if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second);
     }
+    for (auto& kv : p->device_partials) {
+      if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second);
+    }
     if (have_prev) cudaSetDevice(prev);
     p->device_tiles.clear();
+    p->device_partials.clear();
   }
   delete p;
 }

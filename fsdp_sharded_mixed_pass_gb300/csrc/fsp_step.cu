@@ -35,11 +35,13 @@ struct KernelTable;
 
 template <typename GradT, int... NS, int... NR>
 struct KernelTable<GradT, Mesh<NS, NR>...> {
+  // kClip: the clipped update of the distributed-optimizer flow
+  template <bool kClip>
   static KernelInfo get(int n_shard, int n_rep) {
-    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<GradT>), kGenericThreads, 0};
+    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<GradT, kClip>), kGenericThreads, 0};
     ((n_shard == NS && n_rep == NR
-          ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<NS, NR, GradT>), kBulkThreads,
-                            BulkCfg<NS, NR, GradT>::kSmemBytes},
+          ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<NS, NR, GradT, kClip>), kBulkThreads,
+                            BulkCfg<NS, NR, GradT, kClip ? 1 : NS * NR>::kSmemBytes},
              0)
           : 0),
      ...);
@@ -51,6 +53,23 @@ template <typename GradT>
 using Kernels = KernelTable<GradT, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
                             Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>, Mesh<2, 2>, Mesh<4, 2>, Mesh<8, 2>,
                             Mesh<2, 4>, Mesh<4, 4>>;
+// the clipped update exists for one replica group and fp32 grads only
+using ClipKernels = KernelTable<float, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
+                                Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>>;
+
+// Pass 1 of the clipped flow for N_d ranks.
+template <int... Ns>
+struct NormKernelTable {
+  static KernelInfo get(int n) {
+    KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0>), kGenericThreads, 0};
+    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0},
+                 0)
+              : 0),
+     ...);
+    return k;
+  }
+};
+using NormKernels = NormKernelTable<1, 2, 3, 4, 5, 6, 7, 8, 12, 16>;
 
 std::string cuda_msg(const char* what, cudaError_t e) {
   return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -166,10 +185,12 @@ void set_mesh(StepArgs& a, const fsp_plan* p) {
   a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
 }
 
-// Launches the step for argument block `a` (tiles already on the device).
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream) {
-  const KernelInfo k = dtype == FSP_DTYPE_F32 ? Kernels<float>::get(a.n_shard, a.n_rep)
-                                              : Kernels<__nv_bfloat16>::get(a.n_shard, a.n_rep);
+// Launches the step for argument block `a` (tiles already on the device);
+// `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false) {
+  const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
+                       : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
+                                                : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
   int grid = 0;
   fsp_status s = grid_for(k, &grid);
   if (s != FSP_OK) return s;
@@ -183,10 +204,18 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream) {
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
 
-fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
-                    float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step, bool debug,
-                    float* reduced, void* stream) {
-  clear_error();
+struct Buf {
+  const void* ptr;
+  size_t bytes;
+  std::string name;
+};
+
+// Host-side checks shared by the device-buffer entry points: arguments,
+// hyper-parameters, NULL / alignment / overlap of every buffer (the step's and
+// `extra`), and - for a non-empty plan - that each lies in a live allocation.
+fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
+                             float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
+                             const std::vector<Buf>& extra) {
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
   if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
@@ -198,11 +227,6 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
 
   const int n = p->n_d;
   const size_t gsize = dtype == FSP_DTYPE_F32 ? 4 : 2;
-  struct Buf {
-    const void* ptr;
-    size_t bytes;
-    std::string name;
-  };
   std::vector<Buf> bufs;
   for (int q = 0; q < n; ++q) {
     bufs.push_back({grads[q], size_t(p->full_len_padded) * gsize, "grad_bufs[" + std::to_string(q) + "]"});
@@ -212,7 +236,7 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   bufs.push_back({master, sbytes, "master"});
   bufs.push_back({m, sbytes, "exp_avg"});
   bufs.push_back({v, sbytes, "exp_avg_sq"});
-  if (debug) bufs.push_back({reduced, sbytes, "reduced_grad"});
+  for (const Buf& b : extra) bufs.push_back(b);
   for (const Buf& b : bufs) {
     // NULL stands for a buffer of zero bytes (e.g. every buffer of an empty plan)
     if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
@@ -235,25 +259,111 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
     fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
     if (s != FSP_OK) return s;
   }
+  return FSP_OK;
+}
 
+// Argument block for the plan's tiles on the current device.
+fsp_status step_args(const fsp_plan* p, const void* const* grads, float* master, float* m, float* v,
+                     void* const* params, const fsp_adamw_hparams* hp, int64_t step, StepArgs* a) {
   const Tile* tiles = nullptr;
   fsp_status s = device_tiles(p, &tiles);
   if (s != FSP_OK) return s;
-
-  StepArgs a{};
-  for (int q = 0; q < n; ++q) {
-    a.grads[q] = grads[q];
-    a.params[q] = static_cast<uint16_t*>(params[q]);
+  *a = StepArgs{};
+  for (int q = 0; q < p->n_d; ++q) {
+    a->grads[q] = grads[q];
+    a->params[q] = static_cast<uint16_t*>(params[q]);
   }
-  a.master = master;
-  a.m = m;
-  a.v = v;
+  a->master = master;
+  a->m = m;
+  a->v = v;
+  a->tiles = tiles;
+  a->n_tiles = int64_t(p->tiles.size());
+  set_mesh(*a, p);
+  set_coeffs(*a, hp, step);
+  return FSP_OK;
+}
+
+fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
+                    float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step, bool debug,
+                    float* reduced, void* stream) {
+  clear_error();
+  std::vector<Buf> extra;
+  if (debug && p) extra.push_back({reduced, size_t(p->state_len_total) * 4, "reduced_grad"});
+  fsp_status s = check_device_step(p, grads, dtype, master, m, v, params, hp, step, extra);
+  if (s != FSP_OK || p->tiles.empty()) return s;
+  StepArgs a;
+  s = step_args(p, grads, master, m, v, params, hp, step, &a);
+  if (s != FSP_OK) return s;
   a.reduced = reduced;
-  a.tiles = tiles;
-  a.n_tiles = int64_t(p->tiles.size());
-  set_mesh(a, p);
-  set_coeffs(a, hp, step);
   return launch(a, dtype, stream);
+}
+
+constexpr int kMaxNormPartials = 4096;
+
+// Per-CTA partial sums of the clipped step's norm, one array per plan and device.
+fsp_status device_partials(const fsp_plan* p, double** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  std::lock_guard<std::mutex> lock(p->mu);
+  auto it = p->device_partials.find(dev);
+  if (it != p->device_partials.end()) {
+    *out = it->second;
+    return FSP_OK;
+  }
+  double* d = nullptr;
+  e = cudaMalloc(&d, kMaxNormPartials * sizeof(double));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FSP_ENOMEM, cuda_msg("cudaMalloc (norm partials)", e));
+  }
+  p->device_partials[dev] = d;
+  *out = d;
+  return FSP_OK;
+}
+
+fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype, float* master, float* m, float* v,
+                            void* const* params, const fsp_adamw_hparams* hp, int64_t step, float max_norm,
+                            float* norm_out, void* stream) {
+  clear_error();
+  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 and DistOpt plans");
+  if (dtype != FSP_DTYPE_F32) return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 grad buffers");
+  if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");
+  std::vector<Buf> extra{{norm_out, 2 * sizeof(float), "norm_out"}};
+  fsp_status s = check_device_step(p, reinterpret_cast<const void* const*>(grads), dtype, master, m, v, params, hp,
+                                   step, extra);
+  if (s != FSP_OK) return s;
+  if (p->tiles.empty()) {   // nothing to reduce: norm 0, coefficient 1
+    const float out[2] = {0.f, 1.f};
+    cudaError_t e = cudaMemcpyAsync(norm_out, out, sizeof(out), cudaMemcpyHostToDevice,
+                                    static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FSP_OK : fail(FSP_ECUDA, cuda_msg("writing norm_out", e));
+  }
+  StepArgs a;
+  s = step_args(p, reinterpret_cast<const void* const*>(grads), master, m, v, params, hp, step, &a);
+  if (s != FSP_OK) return s;
+  double* partials = nullptr;
+  s = device_partials(p, &partials);
+  if (s != FSP_OK) return s;
+
+  // pass 1: reduce-scatter into the owners' slices, per-CTA sums of squares
+  const KernelInfo k1 = NormKernels::get(p->n_d);
+  int grid = 0;
+  s = grid_for(k1, &grid);
+  if (s != FSP_OK) return s;
+  grid = int(std::min<int64_t>(std::min(grid, kMaxNormPartials), a.n_tiles));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* args1[] = {&a, &partials};
+  cudaError_t e = cudaLaunchKernel(k1.fn, dim3(grid), dim3(k1.threads), args1, 0, st);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("reduce-scatter / norm kernel launch", e));
+  // pass 2: the norm and the clip coefficient
+  norm_finalize_kernel<<<1, 256, 0, st>>>(partials, grid, max_norm, norm_out);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("norm kernel launch", e));
+  // pass 3: AdamW on the clipped gradient read from the owners' slices
+  a.clip = norm_out;
+  return launch(a, dtype, stream, true);
 }
 
 }  // namespace
@@ -265,6 +375,14 @@ extern "C" fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* 
                                        void* cuda_stream) {
   return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, false,
                        nullptr, cuda_stream);
+}
+
+extern "C" fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
+                                               float* master, float* exp_avg, float* exp_avg_sq,
+                                               void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                                               float max_norm, float* norm_out, void* cuda_stream) {
+  return fsp::run_step_clipped(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                               max_norm, norm_out, cuda_stream);
 }
 
 extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs,

@@ -19,7 +19,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
+           "fsp_sharded_step", "fsp_sharded_step_clipped", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
            "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
 
@@ -78,6 +78,8 @@ def lib():
     L.fsp_sharded_step.argtypes = step_args + [vp]
     L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
+    L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
+    L.fsp_sharded_step_clipped.restype = ctypes.c_int
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
                "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
@@ -287,3 +289,13 @@ def selftest_bounded_wait(limit_ms: int = 100) -> int:
     bits = ctypes.c_uint32(0)
     _check(lib().fsp_selftest_bounded_wait(int(limit_ms), ctypes.byref(bits)), "fsp_selftest_bounded_wait")
     return int(bits.value)
+
+
+def sharded_step_clipped(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
+                         max_norm: float, norm_out, stream=None, grad_dtype: str | None = None) -> None:
+    """Reduce-scatter with write-back into the owners' grad slices, global-norm
+    clipping, AdamW, cast, all-gather; ``norm_out`` (device, 2 floats) receives
+    {norm, coefficient}.  fp32 grads, FSDP2 or DistOpt plans."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step_clipped(*args, float(max_norm), ctypes.c_void_p(_ptr(norm_out)),
+                                          ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_clipped")

@@ -192,6 +192,26 @@ fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* grad_bufs, 
                             void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                             void* cuda_stream);
 
+/* The Megatron distributed-optimizer flow with global-norm gradient clipping,
+ * for FSDP2 and DistOpt plans with fp32 grads (others: FSP_EUNSUPPORTED):
+ *   1. reduce-scatter with write-back: every element's averaged gradient
+ *      (the rank-ordered fp32 fold / N_d) is stored into its owner's slice of
+ *      the owner's own grad buffer ("07 · 显存模型", section 2.1 item 1); the
+ *      rest of each grad buffer is left as it was;
+ *   2. norm = sqrt(sum of squares of every reduced element), taken in fp64,
+ *      and coefficient = min(1, max_norm / (norm + 1e-6)) rounded to fp32
+ *      (the pages are silent on clipping; this is clip_grad_norm_'s rule);
+ *   3. AdamW on coefficient * gradient (one fp32 multiply), bf16 cast and
+ *      all-gather, as in fsp_sharded_step.
+ *   max_norm: finite, > 0.  norm_out: device, 2 floats, 16-byte aligned;
+ *   receives {norm, coefficient}.  Three kernels on `cuda_stream`; the plan
+ *   owns a small per-device array of partial sums (allocated on first use),
+ *   so clipped steps on one plan must be ordered on the device. */
+fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
+                                    float* master, float* exp_avg, float* exp_avg_sq,
+                                    void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                                    float max_norm, float* norm_out, void* cuda_stream);
+
 /* As fsp_sharded_step, and also stores the averaged shard gradient of every
  * owned element into reduced_grad (device, fp32, state layout,
  * state_len_total elements; padding slots untouched).  For testing: it adds

@@ -250,3 +250,16 @@ def test_status_strings():
     for s in range(5):
         assert L.fsp_status_string(s)
     assert L.fsp_status_string(99) == b"unknown status"
+
+
+def test_clipped_step_rejects_on_host():
+    L = B.lib()
+    hsdp = fsp.plan_layout([(64, 8)], 4, "hsdp", n_replicate=2)
+    fsdp = fsp.plan_layout([(64, 8)], 4)
+    for plan, dtype, max_norm, want in ((hsdp, "f32", 1.0, B.FSP_EUNSUPPORTED),
+                                        (fsdp, "bf16", 1.0, B.FSP_EUNSUPPORTED),
+                                        (fsdp, "f32", 0.0, B.FSP_EINVAL),
+                                        (fsdp, "f32", float("inf"), B.FSP_EINVAL)):
+        grads, state, params = _fakes(plan)
+        args = B._step_args(plan, grads, *state, params, HP, 1, dtype)
+        assert L.fsp_sharded_step_clipped(*args, max_norm, ctypes.c_void_p(1 << 44), ctypes.c_void_p(0)) == want
