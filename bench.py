@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--clip", type=float, default=None, metavar="MAX_NORM",
                     help="time the distributed-optimizer flow instead: reduce-scatter written back into the "
                          "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt)")
+    ap.add_argument("--unshard", action="store_true",
+                    help="time the FSDP2 unshard instead (fp32 shards -> bf16 -> every rank's full buffer)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the timed steps in one CUDA graph (removes host launch overhead; small cases)")
     return ap.parse_args(argv)
@@ -241,11 +243,14 @@ class DeviceWorkload:
         torch.cuda.synchronize(device)
         self.t = w.step
         self.clip = None
+        self.unshard = False
         self.norm_out = torch.zeros(4, dtype=torch.float32, device=device)
 
     def step(self, stream):
         import fsdp_sharded_mixed_pass_gb300 as fsp
-        if self.clip is not None:
+        if self.unshard:
+            fsp.unshard(self.plan, self.state[0], self.params, stream=stream)
+        elif self.clip is not None:
             fsp.sharded_step_clipped(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
                                      self.clip, self.norm_out, stream=stream)
         else:
@@ -255,6 +260,8 @@ class DeviceWorkload:
 
     def bytes_per_param(self) -> int:
         w = self.w
+        if self.unshard:            # fp32 master in, one bf16 per rank of its group out
+            return 4 * w.n_rep + 2 * w.n_d
         if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
             return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
@@ -434,6 +441,7 @@ def run_fsp(args):
     w, shapes, label = resolve_workload(args.workload, args.param_slice)
     wl = DeviceWorkload(w, shapes, dev)
     wl.clip = args.clip
+    wl.unshard = args.unshard
     plan = wl.plan
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
@@ -455,7 +463,7 @@ def run_fsp(args):
     tpe = traffic_per_elem(w.name)
 
     e2e = None
-    if not args.no_e2e and args.clip is None:
+    if not args.no_e2e and args.clip is None and not args.unshard:
         dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist, args.e2e_chunk)
         dt = dist.max(dt)
         e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
@@ -477,13 +485,15 @@ def run_fsp(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(config_block(w, label, plan), bytes_per_param=per, **(
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (3 kernels per step)"}
-            if args.clip is not None else {})),
+            if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
+            if args.unshard else {})),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "traffic": tpe * P if tpe is not None and args.clip is None else None,
-                     "kernel": "sharded_step_kernel", "kernel_src": kernel_src_hash()},
+                     "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard else None,
+                     "kernel": "unshard_kernel" if args.unshard else "sharded_step_kernel",
+                     "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps * (3 if args.clip is not None else 1),

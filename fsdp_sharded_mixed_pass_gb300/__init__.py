@@ -22,4 +22,5 @@ from .fsp import (  # noqa: F401
     sharded_step_host,
     host_step_workspace_bytes,
     sharded_step_noalloc,
+    unshard,
 )

@@ -20,7 +20,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_clipped", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
-           "fsp_sharded_step_noalloc", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
+           "fsp_sharded_step_noalloc", "fsp_unshard", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
 
 
@@ -80,6 +80,8 @@ def lib():
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
     L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
     L.fsp_sharded_step_clipped.restype = ctypes.c_int
+    L.fsp_unshard.argtypes = [vp, vp, ctypes.POINTER(vp), vp]
+    L.fsp_unshard.restype = ctypes.c_int
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
                "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
@@ -299,3 +301,13 @@ def sharded_step_clipped(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, par
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_clipped(*args, float(max_norm), ctypes.c_void_p(_ptr(norm_out)),
                                           ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_clipped")
+
+
+def unshard(plan: Plan, master, param_bufs, stream=None) -> None:
+    """FSDP2 unshard: cast every rank's fp32 shard to bf16 and gather it into
+    every rank's full param buffer (of its group).  Asynchronous."""
+    if len(param_bufs) != plan.n_d:
+        raise ValueError(f"need {plan.n_d} param buffers")
+    p = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
+    _check(lib().fsp_unshard(plan.handle, ctypes.c_void_p(_ptr(master)), p, ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_unshard")

@@ -212,6 +212,19 @@ fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs
                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                     float max_norm, float* norm_out, void* cuda_stream);
 
+/* FSDP2 unshard of the plan's parameters (the all-gather before forward and
+ * before backward in ZeRO-3 / FSDP2, with a bf16 MixedPrecisionPolicy): every
+ * rank's fp32 shard - its owned slots of `master` - is cast to bf16 (round to
+ * nearest even) and gathered into the full buffer of every rank of its group
+ * (all N_d ranks; HSDP: the N_s ranks of each replica group, from that group's
+ * state copy).  "Parallelism strategies: which state to shard", section 二.5
+ * (copy-in, one all-gather, copy-out); "FSDP2 Qwen3 Decoder Layer
+ * Walkthrough", section "Step 0".  master: device, state layout,
+ * state_len_total fp32; param_bufs: host array of n_d device pointers,
+ * full_len_padded bf16 each (padding untouched).  Asynchronous on
+ * `cuda_stream`; one kernel reading 4 B and writing 2 N_s B per element. */
+fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs, void* cuda_stream);
+
 /* As fsp_sharded_step, and also stores the averaged shard gradient of every
  * owned element into reduced_grad (device, fp32, state layout,
  * state_len_total elements; padding slots untouched).  For testing: it adds

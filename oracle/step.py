@@ -270,3 +270,18 @@ def sharded_step_clipped(plan: Plan, grads, master, m, v, params, hp: dict, t: i
         casts.append(bf16_rne(th))
     all_gather(plan, casts, params)
     return norm, coef
+
+
+# ---------------------------------------------------------------------------
+# FSDP2 unshard (all-gather before forward / backward)
+# ---------------------------------------------------------------------------
+
+def unshard(plan: Plan, master, params) -> None:
+    """FSDP2's unshard of a parameter group: every rank's sharded fp32 param
+    (here: its slots of the master buffer) is cast to the all-gather dtype
+    (bf16, round to nearest even - MixedPrecisionPolicy's param dtype) and
+    all-gathered into every rank's full buffer of its group ("Parallelism
+    strategies: which state to shard", section 二.5: copy-in, one all-gather,
+    copy-out; "FSDP2 Qwen3 Decoder Layer Walkthrough", section "Step 0")."""
+    casts = [bf16_rne(master[seg.state_off:seg.state_off + seg.length]) for seg in plan.segments]
+    all_gather(plan, casts, params)

@@ -1,0 +1,69 @@
+"""GPU parity of the FSDP2 unshard (fp32 shards -> bf16 -> every rank's full buffer)."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_mixed_pass_gb300 as fsp
+from oracle import step as OS
+from synth_inputs import workload
+
+from gpu_cases import PARAM_SENTINEL, DeviceCase, Guarded, OracleCase, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+CASES = [("fsdp2", 4, 1), ("fsdp2", 1, 1), ("fsdp2", 6, 1), ("fsdp2", 16, 1), ("fsdp2", 33, 1), ("distopt", 8, 1),
+         ("distopt", 6, 1), ("hsdp", 8, 2), ("hsdp", 6, 3)]
+SHAPES = [(3001, 7), (12289,), (9, 5), (1,), (5, 4099), (2, 3, 5)]
+
+
+@pytest.mark.parametrize("mode,n_d,n_rep", CASES)
+def test_unshard_matches_oracle(mode, n_d, n_rep):
+    dev = DeviceCase(SHAPES, n_d, mode, "f32", 17, n_rep)
+    ora = OracleCase(SHAPES, n_d, mode, "f32", 17, n_rep)
+    fsp.unshard(dev.plan, dev.state[0].t, [p.t for p in dev.params])
+    OS.unshard(ora.plan, ora.state[0], ora.params)
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        assert np.array_equal(dev.params[q].bits(), ora.params[q]), f"rank {q}"
+    n = dev.plan.valid_elems
+    assert all(np.all(p.bits()[n:] == PARAM_SENTINEL) for p in dev.params)
+    assert dev.all_guards_intact()
+
+
+@pytest.mark.parametrize("mode,n_d,n_rep", [("fsdp2", 8, 1), ("distopt", 8, 1), ("hsdp", 8, 2), ("fsdp2", 9, 1)])
+def test_unshard_after_step_reproduces_its_params(mode, n_d, n_rep):
+    dev = DeviceCase(SHAPES, n_d, mode, "f32", 18, n_rep)
+    dev.step(10, debug=False)
+    fresh = [Guarded(dev.plan.full_len_padded, torch.bfloat16, PARAM_SENTINEL) for _ in range(n_d)]
+    fsp.unshard(dev.plan, dev.state[0].t, [p.t for p in fresh])
+    torch.cuda.synchronize()
+    for a, b in zip(dev.params, fresh):
+        assert np.array_equal(a.bits(), b.bits())
+        assert b.guards_intact()
+
+
+def test_unshard_full_size_qwen3():
+    w = workload(1)
+    dev = DeviceCase(w.shapes, w.n_d, w.mode, "f32", w.data_seed)
+    try:
+        fsp.unshard(dev.plan, dev.state[0].t, [p.t for p in dev.params])
+        torch.cuda.synchronize()
+        p0 = dev.params[0].t.view(torch.int16)
+        for q in range(1, w.n_d):
+            assert torch.equal(dev.params[q].t.view(torch.int16), p0)
+        master = dev.state[0].t
+        for sg in dev.plan.segments:
+            if sg.length:
+                a, c = sg.full_off, sg.state_off
+                assert torch.equal(p0[a:a + sg.length], master[c:c + sg.length].to(torch.bfloat16).view(torch.int16))
+    finally:
+        del dev
+        torch.cuda.empty_cache()
