@@ -19,6 +19,7 @@ from .fsp import (  # noqa: F401
     sharded_step,
     sharded_step_clipped,
     sharded_step_debug,
+    sharded_step_device_t,
     sharded_step_host,
     host_step_workspace_bytes,
     sharded_step_noalloc,

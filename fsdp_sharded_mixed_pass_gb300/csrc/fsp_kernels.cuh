@@ -78,8 +78,30 @@ struct StepArgs {
   int n_shard;         // ranks per shard group; rank q = r * n_shard + j
   int64_t rep_stride;  // state elements between replica r's copy and r + 1's
   const float* clip;   // clipped update: {norm, coefficient} on the device
+  const int64_t* step_dev;  // update index t in device memory (nullptr: t is folded into c)
+  float lr;                 // kept to rebuild c's t-dependent scalars from *step_dev
   Coeffs c;
 };
+
+constexpr unsigned kErrStepIndex = 8u;   // *step_dev < 1 (treated as 1)
+
+// The AdamW scalars of this launch: from the host (c) or, when the update
+// index lives in device memory, with the bias corrections of t = *step_dev
+// computed here in double exactly as the host computes them.
+__device__ __forceinline__ Coeffs coeffs_of(const StepArgs& a) {
+  if (!a.step_dev) return a.c;
+  int64_t t = *a.step_dev;
+  if (t < 1) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_fsp_device_error, kErrStepIndex);
+    t = 1;
+  }
+  Coeffs c = a.c;
+  const double bc1 = 1.0 - pow(double(a.c.beta1), double(t));
+  const double bc2 = 1.0 - pow(double(a.c.beta2), double(t));
+  c.step_size = float(double(a.lr) / bc1);
+  c.inv_sqrt_bc2 = float(1.0 / sqrt(bc2));
+  return c;
+}
 
 // Chunk size E and stage count S of the bulk kernel for NS x NR ranks (NR
 // replica groups of NS shard ranks) with grads of type GradT.
@@ -169,7 +191,8 @@ struct GradIO<__nv_bfloat16> {
 // kClip: the clipped update - the gradient is already reduced and sits in
 // its owner's slice, and is multiplied by the clip coefficient instead.
 template <int NS, int NR, typename GradT, bool kClip>
-__device__ __forceinline__ void step_one(const StepArgs& a, int64_t f, int64_t s, int64_t owner, float coef) {
+__device__ __forceinline__ void step_one(const StepArgs& a, const Coeffs& cf, int64_t f, int64_t s, int64_t owner,
+                                         float coef) {
   const int ns = NS > 0 ? NS : a.n_shard;
   const int nr = NR > 0 ? NR : a.n_rep;
   float acc = 0.f;
@@ -189,7 +212,7 @@ __device__ __forceinline__ void step_one(const StepArgs& a, int64_t f, int64_t s
   for (int r = 0; r < nr; ++r) {
     const int64_t sr = s + r * a.rep_stride;
     float th = a.master[sr], mm = a.m[sr], vv = a.v[sr];
-    adamw(acc, th, mm, vv, a.c);
+    adamw(acc, th, mm, vv, cf);
     a.master[sr] = th;
     a.m[sr] = mm;
     a.v[sr] = vv;
@@ -211,7 +234,8 @@ __device__ __forceinline__ void add4(float4& a, float4 b) {
 
 // f: full index (multiple of 4); s: state index (same residue mod 16).
 template <typename GradT, bool kClip>
-__device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t s, int64_t owner, float coef) {
+__device__ __forceinline__ void step_group(const StepArgs& a, const Coeffs& cf, int64_t f, int64_t s, int64_t owner,
+                                           float coef) {
   const int ns = a.n_shard, nr = a.n_rep;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (kClip) {
@@ -240,10 +264,10 @@ __device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t
     float4 th = __ldcs(reinterpret_cast<const float4*>(a.master + sr));
     float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m + sr));
     float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v + sr));
-    adamw(acc.x, th.x, mm.x, vv.x, a.c);
-    adamw(acc.y, th.y, mm.y, vv.y, a.c);
-    adamw(acc.z, th.z, mm.z, vv.z, a.c);
-    adamw(acc.w, th.w, mm.w, vv.w, a.c);
+    adamw(acc.x, th.x, mm.x, vv.x, cf);
+    adamw(acc.y, th.y, mm.y, vv.y, cf);
+    adamw(acc.z, th.z, mm.z, vv.z, cf);
+    adamw(acc.w, th.w, mm.w, vv.w, cf);
     __stcs(reinterpret_cast<float4*>(a.master + sr), th);
     __stcs(reinterpret_cast<float4*>(a.m + sr), mm);
     __stcs(reinterpret_cast<float4*>(a.v + sr), vv);
@@ -257,6 +281,7 @@ __device__ __forceinline__ void step_group(const StepArgs& a, int64_t f, int64_t
 template <typename GradT, bool kClip>
 __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
   const float coef = kClip ? a.clip[1] : 1.f;
+  const Coeffs cf = coeffs_of(a);
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     const int64_t f0 = tile.full_begin;
@@ -269,12 +294,12 @@ __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(c
     const int64_t tail = head + groups * 4;
     for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
       const int64_t f = f0 + head + 4 * i;
-      step_group<GradT, kClip>(a, f, f + delta, tile.rank, coef);
+      step_group<GradT, kClip>(a, cf, f, f + delta, tile.rank, coef);
     }
     const int64_t n_scalar = head + (len - tail);
     if (threadIdx.x < n_scalar) {
       const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<0, 0, GradT, kClip>(a, f0 + e, f0 + e + delta, tile.rank, coef);
+      step_one<0, 0, GradT, kClip>(a, cf, f0 + e, f0 + e + delta, tile.rank, coef);
     }
   }
 }
@@ -431,6 +456,9 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
   if (!mbar_wait(smem_addr(&bar), 0, limit_ns)) atomicOr(&g_fsp_device_error, kErrSelfTest);
 }
 
+// t <- t + 1 after a step that read its update index from device memory.
+__global__ void step_advance_kernel(int64_t* step_dev) { *step_dev += 1; }
+
 // Aligned body [b0, b1) of a tile: 8-element (16-byte) boundaries in the full
 // index, so every bulk copy starts and ends on 16 bytes for fp32 and bf16.
 struct Body {
@@ -576,6 +604,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   // ---------------- consumers: fold, update, cast in shared memory ----------------
   const int tid = threadIdx.x;
   const float coef = kClip ? a.clip[1] : 1.f;
+  const Coeffs cf = coeffs_of(a);
   int stage = 0;
   uint32_t phase = 0;
   int64_t t = blockIdx.x;
@@ -591,7 +620,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     const int64_t n_head = body.b0 - tile.full_begin, n_tail = end - body.b1;
     if (tid < n_head + n_tail) {
       const int64_t f = tid < n_head ? tile.full_begin + tid : body.b1 + (tid - n_head);
-      step_one<NS, NR, GradT, kClip>(a, f, f + delta, tile.rank, coef);
+      step_one<NS, NR, GradT, kClip>(a, cf, f, f + delta, tile.rank, coef);
     }
 
     for (int64_t c = body.b0; c < body.b1; c += E) {
@@ -637,10 +666,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           float4 th = *reinterpret_cast<float4*>(th_s + j);
           float4 mm = *reinterpret_cast<float4*>(m_s + j);
           float4 vv = *reinterpret_cast<float4*>(v_s + j);
-          adamw(acc.x, th.x, mm.x, vv.x, a.c);
-          adamw(acc.y, th.y, mm.y, vv.y, a.c);
-          adamw(acc.z, th.z, mm.z, vv.z, a.c);
-          adamw(acc.w, th.w, mm.w, vv.w, a.c);
+          adamw(acc.x, th.x, mm.x, vv.x, cf);
+          adamw(acc.y, th.y, mm.y, vv.y, cf);
+          adamw(acc.z, th.z, mm.z, vv.z, cf);
+          adamw(acc.w, th.w, mm.w, vv.w, cf);
           *reinterpret_cast<float4*>(th_s + j) = th;
           *reinterpret_cast<float4*>(m_s + j) = mm;
           *reinterpret_cast<float4*>(v_s + j) = vv;

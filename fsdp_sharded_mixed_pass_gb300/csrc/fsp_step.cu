@@ -175,6 +175,7 @@ void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step) {
   a.c.step_size = float(lr / bc1);
   a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
   a.c.eps = hp->eps;
+  a.lr = hp->lr;
 }
 
 // Rank layout of the plan in the argument block.
@@ -383,6 +384,36 @@ extern "C" fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const
                                                float max_norm, float* norm_out, void* cuda_stream) {
   return fsp::run_step_clipped(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
                                max_norm, norm_out, cuda_stream);
+}
+
+extern "C" fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void* const* grad_bufs,
+                                                int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
+                                                void* const* param_bufs, const fsp_adamw_hparams* hp,
+                                                int64_t* step_dev, int32_t advance, void* cuda_stream) {
+  using namespace fsp;
+  clear_error();
+  if (!step_dev) return fail(FSP_EINVAL, "step_dev is NULL");
+  if (reinterpret_cast<uintptr_t>(step_dev) % 8 != 0) return fail(FSP_EINVAL, "step_dev is not 8-byte aligned");
+  // t only enters the bias corrections, which the kernel recomputes from *step_dev
+  fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, {});
+  if (s != FSP_OK) return s;
+  s = check_allocation(step_dev, sizeof(int64_t), "step_dev");
+  if (s != FSP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (!plan->tiles.empty()) {
+    StepArgs a;
+    s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, &a);
+    if (s != FSP_OK) return s;
+    a.step_dev = step_dev;
+    s = launch(a, grad_dtype, cuda_stream);
+    if (s != FSP_OK) return s;
+  }
+  if (advance) {
+    step_advance_kernel<<<1, 1, 0, st>>>(step_dev);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("step counter advance", e));
+  }
+  return FSP_OK;
 }
 
 extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs,

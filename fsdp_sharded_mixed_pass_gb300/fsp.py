@@ -19,7 +19,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_clipped", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
+           "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
            "fsp_sharded_step_noalloc", "fsp_unshard", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
 
@@ -80,6 +80,8 @@ def lib():
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
     L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
     L.fsp_sharded_step_clipped.restype = ctypes.c_int
+    L.fsp_sharded_step_device_t.argtypes = step_args[:-1] + [vp, i32, vp]
+    L.fsp_sharded_step_device_t.restype = ctypes.c_int
     L.fsp_unshard.argtypes = [vp, vp, ctypes.POINTER(vp), vp]
     L.fsp_unshard.restype = ctypes.c_int
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
@@ -311,3 +313,13 @@ def unshard(plan: Plan, master, param_bufs, stream=None) -> None:
     p = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
     _check(lib().fsp_unshard(plan.handle, ctypes.c_void_p(_ptr(master)), p, ctypes.c_void_p(_stream_handle(stream))),
            "fsp_unshard")
+
+
+def sharded_step_device_t(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step_dev,
+                          advance: bool = True, stream=None, grad_dtype: str | None = None) -> None:
+    """``sharded_step`` with the update index in device memory (``step_dev``: a
+    one-element int64 CUDA tensor), advanced by one after the step when
+    ``advance`` - the form to capture once in a CUDA graph and replay."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, 1, grad_dtype)[:-1]
+    _check(lib().fsp_sharded_step_device_t(*args, ctypes.c_void_p(_ptr(step_dev)), int(bool(advance)),
+                                           ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_device_t")

@@ -192,6 +192,19 @@ fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* grad_bufs, 
                             void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                             void* cuda_stream);
 
+/* fsp_sharded_step with the update index t read from device memory, for
+ * loops captured once in a CUDA graph and replayed: the kernel computes the
+ * bias corrections of t = *step_dev (in double, as the host would) and, when
+ * `advance` is non-zero, a one-thread kernel then adds 1 to *step_dev on the
+ * same stream, so each replay applies the next update.  step_dev: device,
+ * 8-byte aligned int64 inside a live allocation; a value below 1 is treated as
+ * 1 and sets bit 8 of the device error word.  Everything else as
+ * fsp_sharded_step (make the first call on a device outside any capture). */
+fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
+                                     float* master, float* exp_avg, float* exp_avg_sq,
+                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t* step_dev,
+                                     int32_t advance, void* cuda_stream);
+
 /* The Megatron distributed-optimizer flow with global-norm gradient clipping,
  * for FSDP2 and DistOpt plans with fp32 grads (others: FSP_EUNSUPPORTED):
  *   1. reduce-scatter with write-back: every element's averaged gradient
@@ -283,7 +296,8 @@ fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* gra
  * waits for the device).  The step kernel's waits on its own copy pipeline
  * are bounded (about 2 s); one that runs out sets a bit here (1: the storer
  * waited for the consumers' results, 2: the producer waited for a free
- * stage; 4: the self-test below), lets its copies land and ends the kernel,
+ * stage; 4: the self-test below; 8: a device-resident update index below 1),
+ * lets its copies land and ends the kernel,
  * leaving that step's results incomplete.  0 means every step since the last
  * read completed normally. */
 fsp_status fsp_device_error(uint32_t* bits);
