@@ -116,10 +116,18 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_src_hash() -> str:
-    """sha256 prefix of the device code (the kernels' source file)."""
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+def kernel_src_hash(text: str | None = None) -> str:
+    """sha256 prefix of the device code (the kernels' source file) with its
+    comments and whitespace removed, so that only a change of code makes a
+    stored ncu capture stale."""
+    import re
+    if text is None:
+        with open(KERNEL_SRC, encoding="utf-8") as f:
+            text = f.read()
+    code = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    code = re.sub(r"//[^\n]*", " ", code)
+    code = " ".join(code.split())
+    return hashlib.sha256(code.encode()).hexdigest()[:12]
 
 
 def traffic_per_elem(workload_name: str):

@@ -3,31 +3,41 @@
 // all-gather, in one streaming pass over the plan's tiles.
 //
 // Stages: "Parallelism strategies: which state to shard", section 二.2 (ZeRO-1
-// puts the optimizer between the two halves of an all-reduce); "FSDP2 Qwen3
-// Decoder Layer Walkthrough", sections "Step 0" (all-gather) and "Backward 简述"
-// (reduce-scatter with averaging, then a communication-free update of the
-// local shard); "07 · 显存模型", section 2.1 (fp32 master + Adam m/v, bf16
-// params, fp32 or bf16 main grads).
+// puts the optimizer between the two halves of an all-reduce) and 二.6 (HSDP);
+// "FSDP2 Qwen3 Decoder Layer Walkthrough", sections "Step 0" (all-gather) and
+// "Backward 简述" (reduce-scatter with averaging, then a communication-free
+// update of the local shard); "07 · 显存模型", section 2.1 (fp32 master + Adam
+// m/v, bf16 params, fp32 or bf16 main grads; the reduce-scatter result lands in
+// the rank's own slice of its grad buffer).
 //
-// The step moves (N_d * sizeof(grad) + 24 + 2 N_d) bytes per element at ~0.3
-// flop/byte: it is bound by HBM bandwidth and has no contraction for tensor
-// cores.  Two kernels:
+// The step moves (N_d * sizeof(grad) + 24 N_r + 2 N_d) bytes per element at
+// ~0.3 flop/byte: it is bound by HBM bandwidth and has no contraction for
+// tensor cores.  Kernels:
 //
-//  * sharded_step_kernel<NS, NR, GradT> (N_d = NS x NR known at compile time;
-//    NR > 1 is HSDP: NR replica groups of NS shard ranks, each group with its
-//    own copy of the fp32 state): one CTA per
-//    SM, warp-specialised.  A producer thread streams every chunk of up to E
-//    aligned elements of the N_d gradient slices and the three state slices
-//    into a ring of S shared-memory stages with 1-D bulk asynchronous copies
-//    (cp.async.bulk, completion counted on an mbarrier); eight consumer warps
-//    fold, update and cast from shared memory, leaving the new master/m/v in
-//    place and one bf16 tile beside them; a storer thread writes the chunk
-//    back with bulk stores: three state slices and the same bf16 tile to each
-//    of the N_d param buffers (the all-gather is N_d bulk copies of one tile).
-//    Segment edges that are not 16-byte aligned take a scalar path from
-//    global memory.
-//  * sharded_step_generic_kernel<GradT> (any N_d up to 64, any grouping): the
-//    same arithmetic with vectorised per-thread loads and stores.
+//  * sharded_step_kernel<NS, NR, GradT, kClip> (N_d = NS x NR known at compile
+//    time; NR > 1 is HSDP: NR replica groups of NS shard ranks, each group with
+//    its own copy of the fp32 state): one CTA per SM, warp-specialised.  A
+//    producer thread streams every chunk of up to E aligned elements of the
+//    N_d gradient slices and the NR x 3 state slices into a ring of S
+//    shared-memory stages with 1-D bulk asynchronous copies (cp.async.bulk,
+//    completion counted on an mbarrier); eight consumer warps fold, update and
+//    cast from shared memory, leaving the new master/m/v in place and one bf16
+//    tile per replica group beside them; a storer thread writes the chunk back
+//    with bulk stores: the state slices and the same bf16 tile to each rank of
+//    the group (the all-gather is N_s bulk copies of one tile).  Segment edges
+//    that are not 16-byte aligned take a scalar path from global memory.
+//    kClip: the clipped update of the distributed-optimizer flow - one slice,
+//    the already-reduced gradient in its owner's grad buffer, scaled by the
+//    clip coefficient.
+//  * sharded_step_generic_kernel<GradT, kClip> (any N_d up to 64, any
+//    grouping): the same arithmetic with vectorised per-thread loads/stores.
+//  * rs_writeback_norm_kernel<N_d> + norm_finalize_kernel: passes 1 and 2 of
+//    the clipped flow (reduce-scatter into the owners' slices with per-CTA
+//    fp64 sums of squares; the norm and the clip coefficient).
+//  * step_advance_kernel: t += 1 for steps whose update index is in device
+//    memory (coeffs_of rebuilds the t-dependent scalars on the device).
+//  * bounded_wait_selftest_kernel: the bounded wait against an mbarrier that
+//    nothing completes.
 //
 // Every wait is bounded: an mbarrier wait gives up after ~2 s, records a bit in
 // g_fsp_device_error, lets its own copies land and returns.  No trap, assert
