@@ -320,8 +320,18 @@ def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist, chunk_elems: int = 0):
     import torch
     import fsdp_sharded_mixed_pass_gb300 as fsp
     p = wl.plan
-    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in wl.grads]
-    host_p = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in wl.params]
+    need = sum(g.numel() * g.element_size() for g in wl.grads) + sum(x.numel() * x.element_size() for x in wl.params)
+    pinned = True
+    try:
+        host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in wl.grads]
+        host_p = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in wl.params]
+    except RuntimeError as e:   # pinned memory exhausted: pageable buffers work too, slower
+        log(f"pinning {need / 1e9:.1f} GB of host memory failed ({e}); using pageable buffers")
+        host_g = host_p = None
+        torch.cuda.empty_cache()
+        pinned = False
+        host_g = [torch.empty(g.shape, dtype=g.dtype) for g in wl.grads]
+        host_p = [torch.empty(x.shape, dtype=x.dtype) for x in wl.params]
     for h, g in zip(host_g, wl.grads):
         h.copy_(g)
     ws = torch.empty(fsp.host_step_workspace_bytes(p, wl.w.grad_dtype, chunk_elems), dtype=torch.uint8,
@@ -344,7 +354,18 @@ def time_e2e(wl: DeviceWorkload, steps: int, dist: Dist, chunk_elems: int = 0):
     h2d = p.valid_elems * wl.w.n_d * wl.w.grad_bytes
     d2h = p.valid_elems * wl.w.n_d * 2
     del host_g, host_p, ws
-    return dt, h2d, d2h
+    return dt, h2d, d2h, pinned
+
+
+def host_memory_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
 
 
 # --------------------------------------------------------------------------
@@ -472,12 +493,22 @@ def run_fsp(args):
 
     e2e = None
     if not args.no_e2e and args.clip is None and not args.unshard:
-        dt, h2d, d2h = time_e2e(wl, args.e2e_steps, dist, args.e2e_chunk)
-        dt = dist.max(dt)
-        e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "api": "fsp_sharded_step_host (C ABI): pinned host grads in, pinned host bf16 params out, "
-                      "chunked H2D / kernel / D2H pipeline"}
+        # every rank on this node needs its own host copy of the grads and params
+        per_rank = P * w.n_d * (w.grad_bytes + 2)
+        local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
+        avail = host_memory_available()
+        too_big = bool(avail) and per_rank * local > 0.8 * avail
+        if dist.max(1.0 if too_big else 0.0) > 0:   # every rank takes the same branch
+            e2e = {"error": f"host memory: {local} ranks x {per_rank / 1e9:.1f} GB of host buffers "
+                            f"exceed 80% of the {avail / 1e9:.0f} GB available"}
+        else:
+            dt, h2d, d2h, pinned = time_e2e(wl, args.e2e_steps, dist, args.e2e_chunk)
+            dt = dist.max(dt)
+            kind = "pinned" if pinned else "pageable"
+            e2e = {"value": P * args.e2e_steps * dist.world / dt, "unit": UNIT,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "api": f"fsp_sharded_step_host (C ABI): {kind} host grads in, {kind} host bf16 params out, "
+                          "chunked H2D / kernel / D2H pipeline"}
 
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:
