@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--clip", type=float, default=None, metavar="MAX_NORM",
                     help="time the distributed-optimizer flow instead: reduce-scatter written back into the "
                          "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt)")
+    ap.add_argument("--no-gather", action="store_true",
+                    help="time the ZeRO-3 step instead: reduce-scatter + AdamW, parameters left sharded")
     ap.add_argument("--unshard", action="store_true",
                     help="time the FSDP2 unshard instead (fp32 shards -> bf16 -> every rank's full buffer)")
     ap.add_argument("--graph", action="store_true",
@@ -252,6 +254,7 @@ class DeviceWorkload:
         self.t = w.step
         self.clip = None
         self.unshard = False
+        self.no_gather = False
         self.norm_out = torch.zeros(4, dtype=torch.float32, device=device)
 
     def step(self, stream):
@@ -262,14 +265,16 @@ class DeviceWorkload:
             fsp.sharded_step_clipped(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
                                      self.clip, self.norm_out, stream=stream)
         else:
-            fsp.sharded_step(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
-                             stream=stream)
+            fsp.sharded_step(self.plan, self.grads, *self.state, None if self.no_gather else self.params,
+                             self.w.hparams(), self.t, stream=stream)
         self.t += 1
 
     def bytes_per_param(self) -> int:
         w = self.w
         if self.unshard:            # fp32 master in, one bf16 per rank of its group out
             return 4 * w.n_rep + 2 * w.n_d
+        if self.no_gather:          # grads in, state in and out, no params
+            return w.n_d * w.grad_bytes + 24 * w.n_rep
         if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
             return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
@@ -471,6 +476,7 @@ def run_fsp(args):
     wl = DeviceWorkload(w, shapes, dev)
     wl.clip = args.clip
     wl.unshard = args.unshard
+    wl.no_gather = args.no_gather
     plan = wl.plan
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
@@ -492,7 +498,7 @@ def run_fsp(args):
     tpe = traffic_per_elem(w.name)
 
     e2e = None
-    if not args.no_e2e and args.clip is None and not args.unshard:
+    if not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather:
         # every rank on this node needs its own host copy of the grads and params
         per_rank = P * w.n_d * (w.grad_bytes + 2)
         local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
@@ -525,12 +531,14 @@ def run_fsp(args):
         "config": dict(config_block(w, label, plan), bytes_per_param=per, **(
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (3 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
-            if args.unshard else {})),
+            if args.unshard else {"flow": "ZeRO-3 step: reduce-scatter + AdamW, no all-gather"}
+            if args.no_gather else {})),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard else None,
+                     "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
+                     and not args.no_gather else None,
                      "kernel": "unshard_kernel" if args.unshard else "sharded_step_kernel",
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,

@@ -89,6 +89,7 @@ struct StepArgs {
   int64_t rep_stride;  // state elements between replica r's copy and r + 1's
   const float* clip;   // clipped update: {norm, coefficient} on the device
   const int64_t* step_dev;  // update index t in device memory (nullptr: t is folded into c)
+  int gather;               // 0: ZeRO-3 / FSDP2 reshard - no all-gather, params untouched
   float lr;                 // kept to rebuild c's t-dependent scalars from *step_dev
   Coeffs c;
 };
@@ -229,7 +230,8 @@ __device__ __forceinline__ void step_one(const StepArgs& a, const Coeffs& cf, in
     if (a.reduced) a.reduced[sr] = acc;
     const uint16_t b = bf16_bits(th);
 #pragma unroll(NS > 0 ? NS : 1)
-    for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
+    if (a.gather)
+      for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
   }
 }
 
@@ -282,8 +284,10 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const Coeffs& cf, 
     __stcs(reinterpret_cast<float4*>(a.m + sr), mm);
     __stcs(reinterpret_cast<float4*>(a.v + sr), vv);
     if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + sr), acc);
-    const uint2 b = pack_bf16x4(th);
-    for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(a.params[r * ns + j] + f), b);
+    if (a.gather) {
+      const uint2 b = pack_bf16x4(th);
+      for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(a.params[r * ns + j] + f), b);
+    }
   }
 }
 
@@ -596,7 +600,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
 #pragma unroll
-          for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + c, p_s, len * 2);   // the all-gather
+          if (a.gather)
+            for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + c, p_s, len * 2);   // the all-gather
         }
         bulk_commit();
         bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out

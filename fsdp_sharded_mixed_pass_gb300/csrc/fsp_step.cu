@@ -218,7 +218,7 @@ fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_
                              float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
                              const std::vector<Buf>& extra) {
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
-  if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
+  if (!grads) return fail(FSP_EINVAL, "grad_bufs is NULL");   // param_bufs NULL: no all-gather
   if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
   if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
@@ -231,7 +231,8 @@ fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_
   std::vector<Buf> bufs;
   for (int q = 0; q < n; ++q) {
     bufs.push_back({grads[q], size_t(p->full_len_padded) * gsize, "grad_bufs[" + std::to_string(q) + "]"});
-    bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
+    if (params)
+      bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
   }
   const size_t sbytes = size_t(p->state_len_total) * 4;
   bufs.push_back({master, sbytes, "master"});
@@ -272,8 +273,9 @@ fsp_status step_args(const fsp_plan* p, const void* const* grads, float* master,
   *a = StepArgs{};
   for (int q = 0; q < p->n_d; ++q) {
     a->grads[q] = grads[q];
-    a->params[q] = static_cast<uint16_t*>(params[q]);
+    a->params[q] = params ? static_cast<uint16_t*>(params[q]) : nullptr;
   }
+  a->gather = params ? 1 : 0;
   a->master = master;
   a->m = m;
   a->v = v;
@@ -533,6 +535,7 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   a.m = m;
   a.v = v;
   a.reduced = nullptr;
+  a.gather = 1;
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
   set_mesh(a, p);
@@ -731,6 +734,7 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
   a.m = m;
   a.v = v;
   a.reduced = nullptr;
+  a.gather = 1;
   set_mesh(a, p);
   set_coeffs(a, hp, step);
 

@@ -227,18 +227,21 @@ def _hp(hparams) -> _HParams:
 
 
 def _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype):
-    if len(grad_bufs) != plan.n_d or len(param_bufs) != plan.n_d:
+    if len(grad_bufs) != plan.n_d or (param_bufs is not None and len(param_bufs) != plan.n_d):
         raise ValueError(f"need {plan.n_d} grad and param buffers")
     gd = _grad_dtype(grad_bufs, grad_dtype)
     g = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in grad_bufs])
-    p = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
+    # param_bufs None: no all-gather (ZeRO-3 / FSDP2 reshard; gather later with unshard)
+    p = None if param_bufs is None else (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
     return [plan.handle, g, DTYPES[gd], ctypes.c_void_p(_ptr(master)), ctypes.c_void_p(_ptr(exp_avg)),
             ctypes.c_void_p(_ptr(exp_avg_sq)), p, ctypes.byref(_hp(hparams)), int(step)]
 
 
 def sharded_step(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
                  stream=None, grad_dtype: str | None = None) -> None:
-    """One fused reduce-scatter + AdamW + bf16 all-gather step (asynchronous)."""
+    """One fused reduce-scatter + AdamW + bf16 all-gather step (asynchronous).
+    ``param_bufs=None`` skips the all-gather (ZeRO-3: gather later with
+    ``unshard``)."""
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step(*args, ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step")
 

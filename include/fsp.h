@@ -179,7 +179,10 @@ void fsp_plan_destroy(fsp_plan* plan);
  *   master, exp_avg, exp_avg_sq: device, fp32, state_len_total elements each;
  *               updated in place at owned slots only.
  *   param_bufs: host array of n_d device pointers, each full_len_padded bf16
- *               elements; owned elements written, padding untouched.
+ *               elements; owned elements written, padding untouched.  NULL:
+ *               no all-gather - the ZeRO-3 / FSDP2 step that leaves the
+ *               parameters sharded (only master/m/v change; gather them
+ *               later with fsp_unshard).
  *   hp:         host pointer; step: t >= 1, the 1-based index of this update
  *               (bias corrections use beta^t).
  * Every device pointer must be 16-byte aligned and no two buffers may

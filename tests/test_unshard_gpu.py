@@ -7,7 +7,7 @@ import fsdp_sharded_mixed_pass_gb300 as fsp
 from oracle import step as OS
 from synth_inputs import workload
 
-from gpu_cases import PARAM_SENTINEL, DeviceCase, Guarded, OracleCase, ensure_built
+from gpu_cases import HP, PARAM_SENTINEL, DeviceCase, Guarded, OracleCase, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -67,3 +67,26 @@ def test_unshard_full_size_qwen3():
     finally:
         del dev
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode,n_d,n_rep", [("fsdp2", 8, 1), ("distopt", 6, 1), ("hsdp", 8, 2), ("fsdp2", 9, 1)])
+def test_zero3_step_then_unshard_equals_the_gathering_step(mode, n_d, n_rep):
+    """The step without all-gather leaves every param buffer alone and updates
+    the state exactly like the full step; unsharding afterwards gives the full
+    step's params."""
+    full = DeviceCase(SHAPES, n_d, mode, "f32", 19, n_rep)
+    z3 = DeviceCase(SHAPES, n_d, mode, "f32", 19, n_rep)
+    before = [p.bits().copy() for p in z3.params]
+    for t in (10, 11):
+        full.step(t, debug=False)
+        fsp.sharded_step(z3.plan, [g.t for g in z3.grads], *[s.t for s in z3.state], None, HP, t)
+    torch.cuda.synchronize()
+    for a, b in zip(full.state, z3.state):
+        assert np.array_equal(a.bits(), b.bits())
+    for p, b in zip(z3.params, before):
+        assert np.array_equal(p.bits(), b)
+    fsp.unshard(z3.plan, z3.state[0].t, [p.t for p in z3.params])
+    torch.cuda.synchronize()
+    for a, b in zip(full.params, z3.params):
+        assert np.array_equal(a.bits(), b.bits())
+    assert fsp.device_error() == 0
