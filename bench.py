@@ -37,7 +37,8 @@ if ROOT not in sys.path:
 METRIC = "sharded-step params/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", "fsp_kernels.cuh")
+KERNEL_SRC = tuple(os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", f)
+                   for f in ("fsp_args.h", "fsp_kernels.cuh"))
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -119,13 +120,15 @@ def read_peak():
 
 
 def kernel_src_hash(text: str | None = None) -> str:
-    """sha256 prefix of the device code (the kernels' source file) with its
-    comments and whitespace removed, so that only a change of code makes a
-    stored ncu capture stale."""
+    """sha256 prefix of the step kernels' code (their argument block and
+    device source) with comments and whitespace removed, so that only a
+    change of code makes a stored ncu capture stale."""
     import re
     if text is None:
-        with open(KERNEL_SRC, encoding="utf-8") as f:
-            text = f.read()
+        text = ""
+        for path in KERNEL_SRC:
+            with open(path, encoding="utf-8") as f:
+                text += f.read() + "\n"
     code = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     code = re.sub(r"//[^\n]*", " ", code)
     code = " ".join(code.split())

@@ -1,0 +1,42 @@
+// Argument block of the step kernels, shared by the host code that fills it
+// (fsp_step.cu, fsp_host.cu) and the device code that reads it
+// (fsp_kernels.cuh).  Plain data: passed by value as a __grid_constant__.
+#pragma once
+
+#include <cstdint>
+
+#include "fsp_internal.h"
+
+namespace fsp {
+
+// Scalars of one AdamW update, from the fp32 hyper-parameters and t in double.
+struct Coeffs {
+  float beta1, one_minus_beta1;
+  float beta2, one_minus_beta2;
+  float decay;          // 1 - lr * weight_decay
+  float step_size;      // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+  float eps;
+};
+
+struct StepArgs {
+  const void* grads[kMaxRanks];
+  uint16_t* params[kMaxRanks];
+  float* master;
+  float* m;
+  float* v;
+  float* reduced;   // averaged shard gradient (state layout); nullptr in production
+  const Tile* tiles;
+  int64_t n_tiles;
+  int n_d;             // = n_rep * n_shard
+  int n_rep;           // HSDP replica groups (1: FSDP2 / DistOpt)
+  int n_shard;         // ranks per shard group; rank q = r * n_shard + j
+  int64_t rep_stride;  // state elements between replica r's copy and r + 1's
+  const float* clip;   // clipped update: {norm, coefficient} on the device
+  const int64_t* step_dev;  // update index t in device memory (nullptr: t is folded into c)
+  int gather;               // 0: ZeRO-3 / FSDP2 reshard - no all-gather, params untouched
+  float lr;                 // kept to rebuild c's t-dependent scalars from *step_dev
+  Coeffs c;
+};
+
+}  // namespace fsp

@@ -1,0 +1,33 @@
+// Host-side helpers shared by the translation units that launch kernels
+// (defined in fsp_step.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime_api.h>
+
+#include <string>
+
+#include "fsp_args.h"
+#include "fsp_internal.h"
+
+namespace fsp {
+
+// A buffer an entry point validates: pointer, bytes, name for messages.
+struct Buf {
+  const void* ptr;
+  size_t bytes;
+  std::string name;
+};
+
+std::string cuda_msg(const char* what, cudaError_t e);
+bool finite_nonneg(float x);
+// Whether [ptr, ptr + bytes) lies inside one live allocation of the driver.
+fsp_status check_allocation(const void* ptr, size_t bytes, const char* name);
+// The plan's tile table on the current device (uploaded on first use).
+fsp_status device_tiles(const fsp_plan* p, const Tile** out);
+// AdamW scalars of update t, and the plan's rank layout, into `a`.
+void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step);
+void set_mesh(StepArgs& a, const fsp_plan* p);
+// Launches the step kernel for `a` (clip: the clipped update).
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false);
+
+}  // namespace fsp

@@ -49,6 +49,7 @@
 
 #include <cstdint>
 
+#include "fsp_args.h"
 #include "fsp_internal.h"
 
 namespace fsp {
@@ -63,36 +64,6 @@ constexpr int kBulkStageBudget = 65536;                // one stage, bytes
 constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 static __device__ unsigned int g_fsp_device_error = 0;
-
-// Scalars of one AdamW update, from the fp32 hyper-parameters and t in double.
-struct Coeffs {
-  float beta1, one_minus_beta1;
-  float beta2, one_minus_beta2;
-  float decay;          // 1 - lr * weight_decay
-  float step_size;      // lr / (1 - beta1^t)
-  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
-  float eps;
-};
-
-struct StepArgs {
-  const void* grads[kMaxRanks];
-  uint16_t* params[kMaxRanks];
-  float* master;
-  float* m;
-  float* v;
-  float* reduced;   // averaged shard gradient (state layout); nullptr in production
-  const Tile* tiles;
-  int64_t n_tiles;
-  int n_d;             // = n_rep * n_shard
-  int n_rep;           // HSDP replica groups (1: FSDP2 / DistOpt)
-  int n_shard;         // ranks per shard group; rank q = r * n_shard + j
-  int64_t rep_stride;  // state elements between replica r's copy and r + 1's
-  const float* clip;   // clipped update: {norm, coefficient} on the device
-  const int64_t* step_dev;  // update index t in device memory (nullptr: t is folded into c)
-  int gather;               // 0: ZeRO-3 / FSDP2 reshard - no all-gather, params untouched
-  float lr;                 // kept to rebuild c's t-dependent scalars from *step_dev
-  Coeffs c;
-};
 
 constexpr unsigned kErrStepIndex = 8u;   // *step_dev < 1 (treated as 1)
 
@@ -229,9 +200,10 @@ __device__ __forceinline__ void step_one(const StepArgs& a, const Coeffs& cf, in
     a.v[sr] = vv;
     if (a.reduced) a.reduced[sr] = acc;
     const uint16_t b = bf16_bits(th);
+    if (a.gather) {
 #pragma unroll(NS > 0 ? NS : 1)
-    if (a.gather)
       for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
+    }
   }
 }
 
@@ -599,9 +571,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.master + s, th_s, len * 4);
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
+          if (a.gather) {
 #pragma unroll
-          if (a.gather)
             for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + c, p_s, len * 2);   // the all-gather
+          }
         }
         bulk_commit();
         bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out

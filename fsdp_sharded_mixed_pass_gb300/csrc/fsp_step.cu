@@ -1,5 +1,8 @@
-// Host side of the fused sharded step: argument checks, launch selection and
-// the C entry points.  The kernels are in fsp_kernels.cuh.
+// Host side of the fused sharded step: kernel selection and launch, argument
+// checks, and the C entry points that take device buffers (the step, its
+// debug / device-t / clipped / no-allocation variants, the device error word
+// and the bounded-wait self-test).  The kernels are in fsp_kernels.cuh; the
+// host-buffer pipeline is in fsp_host.cu and the unshard in fsp_unshard.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -9,11 +12,11 @@
 #include <string>
 #include <vector>
 
+#include "fsp_host.h"
 #include "fsp_internal.h"
 #include "fsp_kernels.cuh"
 
 namespace fsp {
-namespace {
 
 // ---- host side -------------------------------------------------------------
 
@@ -188,7 +191,7 @@ void set_mesh(StepArgs& a, const fsp_plan* p) {
 
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false) {
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip) {
   const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
                        : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
                                                 : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
@@ -204,12 +207,6 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false) {
 }
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
-
-struct Buf {
-  const void* ptr;
-  size_t bytes;
-  std::string name;
-};
 
 // Host-side checks shared by the device-buffer entry points: arguments,
 // hyper-parameters, NULL / alignment / overlap of every buffer (the step's and
@@ -369,7 +366,6 @@ fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype
   return launch(a, dtype, stream, true);
 }
 
-}  // namespace
 }  // namespace fsp
 
 extern "C" fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
@@ -567,254 +563,6 @@ extern "C" fsp_status fsp_device_error(uint32_t* bits) {
   return FSP_OK;
 }
 
-// ---- step with the gradients and params in host memory --------------------------
-//
-// The N_d gradient buffers come from host memory and the N_d bf16 param buffers
-// go back to it, while master/m/v stay on the device.  The plan's tiles are cut
-// into chunks of about `chunk_elems` elements (at 4096-element tile boundaries);
-// chunk k's gradient slices are copied into one of two device staging slots on
-// a host-to-device stream, the kernel runs on the caller's stream, and the bf16
-// result is copied from a staging slot to every rank's host buffer on a
-// device-to-host stream, so H2D of chunk k+1, the kernel on chunk k and D2H of
-// chunk k-1 overlap (NVLink-C2C carries both directions at once).
-
-namespace fsp {
-namespace {
-
-int64_t host_slot_elems(int64_t chunk_elems) {
-  const int64_t c = chunk_elems > 0 ? chunk_elems : (int64_t(1) << 24);
-  return (c + kTileElems - 1) / kTileElems * kTileElems + kTileElems;
-}
-
-size_t host_workspace_bytes(const fsp_plan* p, int32_t dtype, int64_t chunk_elems) {
-  const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
-  return 2 * size_t(host_slot_elems(chunk_elems)) * (size_t(p->n_d) * g + 2 * size_t(p->n_rep));
-}
-
-// Copies of different ranks' slices run on several streams at once so that
-// several copy engines share each direction of the link.
-constexpr int kCopyLanes = 4;
-
-struct CopyStreams {
-  cudaStream_t h2d[kCopyLanes] = {}, d2h[kCopyLanes] = {};
-};
-
-// 2 x kCopyLanes non-blocking copy streams per device, created on first use
-// and kept for the life of the process.
-fsp_status copy_streams(CopyStreams* out) {
-  static std::mutex mu;
-  static std::map<int, CopyStreams> cache;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(dev);
-  if (it != cache.end()) {
-    *out = it->second;
-    return FSP_OK;
-  }
-  CopyStreams s;
-  for (int j = 0; e == cudaSuccess && j < kCopyLanes; ++j) {
-    e = cudaStreamCreateWithFlags(&s.h2d[j], cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s.d2h[j], cudaStreamNonBlocking);
-  }
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaStreamCreateWithFlags", e));
-  cache[dev] = s;
-  *out = s;
-  return FSP_OK;
-}
-
-bool is_host_pointer(const void* ptr) {
-  cudaPointerAttributes attr{};
-  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return attr.type == cudaMemoryTypeHost || attr.type == cudaMemoryTypeUnregistered;
-}
-
-fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32_t dtype, float* master, float* m,
-                         float* v, void* const* host_params, const fsp_adamw_hparams* hp, int64_t step,
-                         void* workspace, size_t workspace_bytes, int64_t chunk_elems, void* stream) {
-  clear_error();
-  if (!p) return fail(FSP_EINVAL, "plan is NULL");
-  if (!host_grads || !host_params) return fail(FSP_EINVAL, "host_grads or host_params is NULL");
-  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
-  if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
-  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
-  if (chunk_elems < 0) return fail(FSP_EINVAL, "chunk_elems must be >= 0 (0: default)");
-  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
-      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
-    return fail(FSP_EINVAL, "hyper-parameters out of range");
-  const int n = p->n_d;
-  const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
-  const size_t sbytes = size_t(p->state_len_total) * 4;
-  const float* state[3] = {master, m, v};
-  const char* names[3] = {"master", "exp_avg", "exp_avg_sq"};
-  for (int i = 0; i < 3; ++i) {
-    if (!state[i] && sbytes) return fail(FSP_EINVAL, std::string(names[i]) + " is NULL");
-    if (reinterpret_cast<uintptr_t>(state[i]) % 16) return fail(FSP_EINVAL, std::string(names[i]) + " is not 16-byte aligned");
-  }
-  for (int i = 0; i < 3; ++i)
-    for (int j = i + 1; j < 3; ++j) {
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(state[i]), b0 = reinterpret_cast<uintptr_t>(state[j]);
-      if (sbytes && a0 < b0 + sbytes && b0 < a0 + sbytes) return fail(FSP_EINVAL, "state buffers overlap");
-    }
-  const size_t need = host_workspace_bytes(p, dtype, chunk_elems);
-  if (p->tiles.empty()) return FSP_OK;
-  for (int q = 0; q < n; ++q) {
-    if (!host_grads[q] || !host_params[q]) return fail(FSP_EINVAL, "a host buffer is NULL");
-    if (!is_host_pointer(host_grads[q]) || !is_host_pointer(host_params[q]))
-      return fail(FSP_EINVAL, "host_grads / host_params must be host memory");
-  }
-  if (!workspace) return fail(FSP_EINVAL, "workspace is NULL");
-  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(FSP_EINVAL, "workspace is not 256-byte aligned");
-  if (workspace_bytes < need)
-    return fail(FSP_EINVAL, "workspace too small: " + std::to_string(need) + " bytes needed");
-  for (int i = 0; i < 3; ++i) {
-    fsp_status s = check_allocation(state[i], sbytes, names[i]);
-    if (s != FSP_OK) return s;
-  }
-  fsp_status s = check_allocation(workspace, need, "workspace");
-  if (s != FSP_OK) return s;
-
-  const Tile* dtiles = nullptr;
-  s = device_tiles(p, &dtiles);
-  if (s != FSP_OK) return s;
-  CopyStreams cs;
-  s = copy_streams(&cs);
-  if (s != FSP_OK) return s;
-
-  // chunk k = tiles [cuts[k], cuts[k+1]), a contiguous full-index range
-  const int64_t slot = host_slot_elems(chunk_elems);
-  const int64_t target = slot - kTileElems;
-  std::vector<size_t> cuts{0};
-  int64_t start = p->tiles[0].full_begin;
-  for (size_t i = 1; i < p->tiles.size(); ++i) {
-    const Tile& t = p->tiles[i];
-    if (t.full_begin % kTileElems == 0 && t.full_begin - start >= target) {
-      cuts.push_back(i);
-      start = t.full_begin;
-    }
-  }
-  cuts.push_back(p->tiles.size());
-  const size_t n_chunks = cuts.size() - 1;
-
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  auto stg_grad = [&](int sl, int q) { return ws + (size_t(sl) * n + q) * size_t(slot) * g; };
-  const int n_rep = p->n_rep, n_shard = p->n_shard;
-  // one bf16 tile per replica group per slot
-  auto stg_param = [&](int sl, int r) {
-    return ws + 2 * size_t(n) * size_t(slot) * g + (size_t(sl) * n_rep + r) * size_t(slot) * 2;
-  };
-
-  cudaStream_t cs_main = static_cast<cudaStream_t>(stream);
-  const int lanes = std::min(kCopyLanes, n);
-  // per chunk: `lanes` H2D events, one kernel event, `lanes` D2H events
-  const size_t per = size_t(2 * lanes + 1);
-  std::vector<cudaEvent_t> ev(per * n_chunks + 1, nullptr);
-  auto cleanup = [&]() {
-    for (cudaEvent_t x : ev)
-      if (x) cudaEventDestroy(x);
-  };
-  for (auto& x : ev) {
-    cudaError_t e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      cleanup();
-      return fail(FSP_ECUDA, cuda_msg("cudaEventCreateWithFlags", e));
-    }
-  }
-  cudaEvent_t entry = ev[per * n_chunks];
-  auto ev_h2d = [&](size_t k, int j) { return ev[per * k + j]; };
-  auto ev_kern = [&](size_t k) { return ev[per * k + lanes]; };
-  auto ev_d2h = [&](size_t k, int j) { return ev[per * k + lanes + 1 + j]; };
-
-  StepArgs a{};
-  a.master = master;
-  a.m = m;
-  a.v = v;
-  a.reduced = nullptr;
-  a.gather = 1;
-  set_mesh(a, p);
-  set_coeffs(a, hp, step);
-
-  cudaError_t e = cudaEventRecord(entry, cs_main);   // copies start after earlier work on the stream
-  for (int j = 0; e == cudaSuccess && j < lanes; ++j) {
-    e = cudaStreamWaitEvent(cs.h2d[j], entry, 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.d2h[j], entry, 0);
-  }
-  for (size_t k = 0; e == cudaSuccess && k < n_chunks; ++k) {
-    const int sl = int(k % 2);
-    const Tile& first = p->tiles[cuts[k]];
-    const Tile& last = p->tiles[cuts[k + 1] - 1];
-    const int64_t f0 = first.full_begin, f1 = last.full_begin + last.len;
-    const size_t len = size_t(f1 - f0);
-    // H2D, rank q on lane q % lanes: this slot's previous reader (the kernel of
-    // chunk k-2) must be done
-    for (int j = 0; e == cudaSuccess && j < lanes; ++j) {
-      if (k >= 2) e = cudaStreamWaitEvent(cs.h2d[j], ev_kern(k - 2), 0);
-      for (int q = j; e == cudaSuccess && q < n; q += lanes)
-        e = cudaMemcpyAsync(stg_grad(sl, q), static_cast<const unsigned char*>(host_grads[q]) + size_t(f0) * g,
-                            len * g, cudaMemcpyHostToDevice, cs.h2d[j]);
-      if (e == cudaSuccess) e = cudaEventRecord(ev_h2d(k, j), cs.h2d[j]);
-      // the kernel waits for every lane's gradients ...
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(cs_main, ev_h2d(k, j), 0);
-      // ... and for the D2H of chunk k-2, which read this slot's bf16 tile
-      if (e == cudaSuccess && k >= 2) e = cudaStreamWaitEvent(cs_main, ev_d2h(k - 2, j), 0);
-    }
-    if (e != cudaSuccess) break;
-    for (int q = 0; q < n; ++q) {
-      // staging holds full indices [f0, f1): index it with the full index
-      a.grads[q] = stg_grad(sl, q) - size_t(f0) * g;
-      a.params[q] = reinterpret_cast<uint16_t*>(stg_param(sl, q / n_shard)) - f0;   // one tile per group
-    }
-    a.tiles = dtiles + cuts[k];
-    a.n_tiles = int64_t(cuts[k + 1] - cuts[k]);
-    s = launch(a, dtype, cs_main);
-    if (s != FSP_OK) {
-      cleanup();
-      return s;
-    }
-    e = cudaEventRecord(ev_kern(k), cs_main);
-    // D2H: the all-gather into every rank's host buffer
-    for (int j = 0; e == cudaSuccess && j < lanes; ++j) {
-      e = cudaStreamWaitEvent(cs.d2h[j], ev_kern(k), 0);
-      for (int q = j; e == cudaSuccess && q < n; q += lanes)
-        e = cudaMemcpyAsync(static_cast<unsigned char*>(host_params[q]) + size_t(f0) * 2, stg_param(sl, q / n_shard),
-                            len * 2, cudaMemcpyDeviceToHost, cs.d2h[j]);
-      if (e == cudaSuccess) e = cudaEventRecord(ev_d2h(k, j), cs.d2h[j]);
-    }
-  }
-  // the caller's stream completes only after every copy back
-  for (size_t k = n_chunks >= 2 ? n_chunks - 2 : 0; e == cudaSuccess && k < n_chunks; ++k)
-    for (int j = 0; e == cudaSuccess && j < lanes; ++j) e = cudaStreamWaitEvent(cs_main, ev_d2h(k, j), 0);
-  cleanup();
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("host-buffer step pipeline", e));
-  return FSP_OK;
-}
-
-}  // namespace
-}  // namespace fsp
-
-extern "C" fsp_status fsp_host_step_workspace_bytes(const fsp_plan* plan, int32_t grad_dtype, int64_t chunk_elems,
-                                                    size_t* bytes) {
-  fsp::clear_error();
-  if (!plan || !bytes) return fsp::fail(FSP_EINVAL, "NULL argument");
-  if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16) return fsp::fail(FSP_EINVAL, "unknown grad dtype");
-  if (chunk_elems < 0) return fsp::fail(FSP_EINVAL, "chunk_elems must be >= 0 (0: default)");
-  *bytes = fsp::host_workspace_bytes(plan, grad_dtype, chunk_elems);
-  return FSP_OK;
-}
-
-extern "C" fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_grads, int32_t grad_dtype,
-                                            float* master, float* exp_avg, float* exp_avg_sq,
-                                            void* const* host_params, const fsp_adamw_hparams* hp, int64_t step,
-                                            void* workspace, size_t workspace_bytes, int64_t chunk_elems,
-                                            void* cuda_stream) {
-  return fsp::run_step_host(plan, host_grads, grad_dtype, master, exp_avg, exp_avg_sq, host_params, hp, step,
-                            workspace, workspace_bytes, chunk_elems, cuda_stream);
-}
-
 extern "C" fsp_status fsp_selftest_bounded_wait(uint32_t limit_ms, uint32_t* bits) {
   fsp::clear_error();
   if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
@@ -830,59 +578,4 @@ extern "C" fsp_status fsp_selftest_bounded_wait(uint32_t limit_ms, uint32_t* bit
   if (s != FSP_OK) return s;
   *bits |= before;
   return FSP_OK;
-}
-
-
-// ---- FSDP2 unshard ------------------------------------------------------------------
-
-namespace fsp {
-namespace {
-
-fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* params, void* stream) {
-  clear_error();
-  if (!p) return fail(FSP_EINVAL, "plan is NULL");
-  if (!params) return fail(FSP_EINVAL, "param_bufs is NULL");
-  std::vector<Buf> bufs;
-  for (int q = 0; q < p->n_d; ++q)
-    bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
-  bufs.push_back({master, size_t(p->state_len_total) * 4, "master"});
-  for (const Buf& b : bufs) {
-    if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
-    if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
-  }
-  for (size_t i = 0; i < bufs.size(); ++i)
-    for (size_t j = i + 1; j < bufs.size(); ++j) {
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(bufs[i].ptr), b0 = reinterpret_cast<uintptr_t>(bufs[j].ptr);
-      if (bufs[i].bytes && bufs[j].bytes && a0 < b0 + bufs[j].bytes && b0 < a0 + bufs[i].bytes)
-        return fail(FSP_EINVAL, bufs[i].name + " overlaps " + bufs[j].name);
-    }
-  if (p->tiles.empty()) return FSP_OK;
-  for (const Buf& b : bufs) {
-    fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
-    if (s != FSP_OK) return s;
-  }
-  const Tile* tiles = nullptr;
-  fsp_status s = device_tiles(p, &tiles);
-  if (s != FSP_OK) return s;
-  UnshardArgs a{};
-  a.master = master;
-  for (int q = 0; q < p->n_d; ++q) a.params[q] = static_cast<uint16_t*>(params[q]);
-  a.tiles = tiles;
-  a.n_tiles = int64_t(p->tiles.size());
-  a.n_rep = p->n_rep;
-  a.n_shard = p->n_shard;
-  a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
-  int grid = 0;
-  cudaError_t e = unshard_grid(&grid);
-  if (e == cudaSuccess) e = launch_unshard(a, int(std::min<int64_t>(grid, a.n_tiles)), stream);
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("unshard kernel launch", e));
-  return FSP_OK;
-}
-
-}  // namespace
-}  // namespace fsp
-
-extern "C" fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs,
-                                  void* cuda_stream) {
-  return fsp::run_unshard(plan, master, param_bufs, cuda_stream);
 }

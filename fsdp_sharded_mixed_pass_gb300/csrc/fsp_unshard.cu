@@ -14,7 +14,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <string>
+#include <vector>
 
+#include "fsp_host.h"
 #include "fsp_internal.h"
 
 namespace fsp {
@@ -77,3 +80,57 @@ cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream) {
 }
 
 }  // namespace fsp
+
+// ---- FSDP2 unshard ------------------------------------------------------------------
+
+namespace fsp {
+namespace {
+
+fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* params, void* stream) {
+  clear_error();
+  if (!p) return fail(FSP_EINVAL, "plan is NULL");
+  if (!params) return fail(FSP_EINVAL, "param_bufs is NULL");
+  std::vector<Buf> bufs;
+  for (int q = 0; q < p->n_d; ++q)
+    bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
+  bufs.push_back({master, size_t(p->state_len_total) * 4, "master"});
+  for (const Buf& b : bufs) {
+    if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
+    if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
+  }
+  for (size_t i = 0; i < bufs.size(); ++i)
+    for (size_t j = i + 1; j < bufs.size(); ++j) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(bufs[i].ptr), b0 = reinterpret_cast<uintptr_t>(bufs[j].ptr);
+      if (bufs[i].bytes && bufs[j].bytes && a0 < b0 + bufs[j].bytes && b0 < a0 + bufs[i].bytes)
+        return fail(FSP_EINVAL, bufs[i].name + " overlaps " + bufs[j].name);
+    }
+  if (p->tiles.empty()) return FSP_OK;
+  for (const Buf& b : bufs) {
+    fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
+    if (s != FSP_OK) return s;
+  }
+  const Tile* tiles = nullptr;
+  fsp_status s = device_tiles(p, &tiles);
+  if (s != FSP_OK) return s;
+  UnshardArgs a{};
+  a.master = master;
+  for (int q = 0; q < p->n_d; ++q) a.params[q] = static_cast<uint16_t*>(params[q]);
+  a.tiles = tiles;
+  a.n_tiles = int64_t(p->tiles.size());
+  a.n_rep = p->n_rep;
+  a.n_shard = p->n_shard;
+  a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
+  int grid = 0;
+  cudaError_t e = unshard_grid(&grid);
+  if (e == cudaSuccess) e = launch_unshard(a, int(std::min<int64_t>(grid, a.n_tiles)), stream);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("unshard kernel launch", e));
+  return FSP_OK;
+}
+
+}  // namespace
+}  // namespace fsp
+
+extern "C" fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs,
+                                  void* cuda_stream) {
+  return fsp::run_unshard(plan, master, param_bufs, cuda_stream);
+}

@@ -263,3 +263,11 @@ def test_clipped_step_rejects_on_host():
         grads, state, params = _fakes(plan)
         args = B._step_args(plan, grads, *state, params, HP, 1, dtype)
         assert L.fsp_sharded_step_clipped(*args, max_norm, ctypes.c_void_p(1 << 44), ctypes.c_void_p(0)) == want
+
+
+def test_build_is_free_of_compiler_warnings():
+    log = B.LIB_PATH + ".ptxas.txt"
+    if not os.path.exists(log):
+        pytest.skip("library built without a log")
+    text = open(log).read()
+    assert "warning" not in text.lower(), [l for l in text.splitlines() if "warning" in l.lower()][:5]
