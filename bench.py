@@ -23,6 +23,7 @@ import argparse
 import datetime
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -40,6 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = tuple(os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", f)
                    for f in ("fsp_args.h", "fsp_kernels.cuh"))
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+# Working sets under this many L2 sizes get an L2 flush before every timed step.
+L2_FLUSH_FACTOR = 4
+L2_BYTES = 129_000_000      # GB300's L2; the device's own figure is used when a GPU is present
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -283,40 +287,64 @@ class DeviceWorkload:
         return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
 
 
-def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False):
+def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False,
+                flush_bytes: int = 0):
+    """Device time of ``steps`` steps on one stream, in ms.
+
+    With ``flush_bytes`` > 0 (working sets that fit in L2) every timed step is
+    preceded by an untimed write of ``flush_bytes`` to a scratch buffer, so each
+    step starts from a cold L2; each step then has its own event pair and the
+    result is the sum of the steps' own durations."""
     import torch
     stream = torch.cuda.Stream(device=wl.device)
     for _ in range(warmup):
         wl.step(stream)
     stream.synchronize()
-    g = None
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=wl.device) if flush_bytes > 0 else None
+    graphs = []
     if graph:
-        # the K timed launches (each with its own update index t) as one graph
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            for _ in range(steps):
-                wl.step(stream)
-        g.replay()          # warm replay
+        # the K timed launches (each with its own update index t) as one graph,
+        # or, with flushes between them, one graph per step
+        for _ in range(steps if flush is not None else 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for _ in range(1 if flush is not None else steps):
+                    wl.step(stream)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for g in graphs:
+                g.replay()  # warm replay
         stream.synchronize()
     sampler = ClockSampler(clocks_id)
     sampler.start_window()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    n_ev = steps if flush is not None else 1
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     dist.barrier()
     torch.cuda.synchronize(wl.device)
-    start.record(stream)
-    if g is not None:
-        with torch.cuda.stream(stream):
-            g.replay()
-    else:
-        for _ in range(steps):
-            wl.step(stream)
-    end.record(stream)
-    end.synchronize()
+    with torch.cuda.stream(stream):
+        if flush is None:
+            starts[0].record(stream)
+            if graphs:
+                graphs[0].replay()
+            else:
+                for _ in range(steps):
+                    wl.step(stream)
+            ends[0].record(stream)
+        else:
+            for i in range(steps):
+                flush.fill_(i & 0xFF)
+                starts[i].record(stream)
+                if graphs:
+                    graphs[i].replay()
+                else:
+                    wl.step(stream)
+                ends[i].record(stream)
+    ends[-1].synchronize()
     torch.cuda.synchronize(wl.device)
     dist.barrier()
     sampler.end_window()
-    ms = start.elapsed_time(end)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
     return ms, sampler.result()
 
 
@@ -452,9 +480,8 @@ def time_oracle(w, shapes, seconds: float, use_device: bool, max_reps: int = 100
 # arms
 # --------------------------------------------------------------------------
 
-def config_block(w, label, plan, l2_bytes=None):
+def config_block(w, label, plan):
     per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
-    moved = per * plan.valid_elems
     return {
         "workload": label,
         "n_d": w.n_d,
@@ -463,11 +490,15 @@ def config_block(w, label, plan, l2_bytes=None):
         "grad_dtype": w.grad_dtype,
         "params": plan.valid_elems,
         "bytes_per_param": per,
-        "bytes_per_step": moved,
-        "l2": "inputs larger than L2: every step streams the whole working set" if moved > 4 * 129e6
-        else "working set fits in L2 (small case)",
+        "bytes_per_step": per * plan.valid_elems,
         "parallelism": "replicas",
     }
+
+
+def l2_note(moved: int, flush_bytes: int) -> str:
+    if flush_bytes:
+        return f"L2 flushed before every timed step (an untimed {flush_bytes / 1e6:.0f} MB write)"
+    return f"inputs larger than L2: every step streams the whole {moved / 1e9:.2f} GB working set"
 
 
 def run_fsp(args):
@@ -484,11 +515,13 @@ def run_fsp(args):
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
 
-    ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_BYTES)
+    flush_bytes = 2 * l2 if wl.bytes_per_param() * plan.valid_elems <= L2_FLUSH_FACTOR * l2 else 0
+    ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph, flush_bytes)
     remeasured = False
     if clocks_bad(clocks):
         log(f"clocks rejected ({clocks}); measuring again")
-        ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph)
+        ms, clocks = time_device(wl, args.steps, args.warmup, dist, clocks_id, args.graph, flush_bytes)
         remeasured = True
     ms_max = dist.max(ms)
     P = plan.valid_elems
@@ -531,7 +564,8 @@ def run_fsp(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_block(w, label, plan), bytes_per_param=per, **(
+        "config": dict(config_block(w, label, plan), bytes_per_param=per,
+                       l2=l2_note(per * P, flush_bytes), **(
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (3 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
             if args.unshard else {"flow": "ZeRO-3 step: reduce-scatter + AdamW, no all-gather"}
@@ -586,7 +620,9 @@ def run_reference(args):
         t += 1
     secs = time.perf_counter() - t0
     value = op.valid_elems * args.steps / secs
-    plan_like = type("P", (), {"valid_elems": op.valid_elems})
+    # the config of the workload itself (as the GPU arm reports it), the sample beside it
+    full_p = sum(math.prod(sh) for sh in shapes)
+    plan_like = type("P", (), {"valid_elems": full_p})
     cfg = config_block(w, label, plan_like)
     cfg["sample_params"] = op.valid_elems
     line = {

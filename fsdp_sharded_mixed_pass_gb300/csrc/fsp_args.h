@@ -28,6 +28,9 @@ struct StepArgs {
   float* reduced;   // averaged shard gradient (state layout); nullptr in production
   const Tile* tiles;
   int64_t n_tiles;
+  // Bulk kernel: tiles are taken in order from this counter (zeroed before the
+  // launch, one per launch); nullptr: CTA b takes tiles b, b + grid, ...
+  unsigned long long* tile_ctr;
   int n_d;             // = n_rep * n_shard
   int n_rep;           // HSDP replica groups (1: FSDP2 / DistOpt)
   int n_shard;         // ranks per shard group; rank q = r * n_shard + j

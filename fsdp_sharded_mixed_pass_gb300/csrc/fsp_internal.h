@@ -63,23 +63,6 @@ struct fsp_plan {
 
 namespace fsp {
 
-// Arguments of the FSDP2 unshard kernel (fsp_unshard.cu).
-struct UnshardArgs {
-  const float* master;
-  uint16_t* params[kMaxRanks];
-  const Tile* tiles;
-  int64_t n_tiles;
-  int n_rep;
-  int n_shard;
-  int64_t rep_stride;
-};
-
-// Launches the unshard kernel on `stream` with `grid` CTAs (fsp_unshard.cu);
-// unshard_grid gives SM count x resident CTAs for the current device.
-int unshard_threads();
-cudaError_t unshard_grid(int* grid);
-cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream);
-
 // Records the thread-local message behind an error status and returns it.
 fsp_status fail(fsp_status s, const std::string& msg);
 void clear_error();

@@ -104,9 +104,12 @@ struct BulkCfg {
   static constexpr int kStateOff = NG * E * int(sizeof(GradT));       // [NR][3][E] float
   static constexpr int kParamOff = kStateOff + NR * 3 * E * 4;        // [NR][E] bf16
   static constexpr int kBarrierBytes = 256;                           // full, computed, empty [S]
-  static constexpr int kSmemBytes = kBarrierBytes + S * kStageBytes;
+  static constexpr int kHeaderOff = kBarrierBytes;                    // StageHdr [S]
+  static constexpr int kMetaBytes = kBarrierBytes + 8 * 64;           // barriers + headers
+  static constexpr int kSmemBytes = kMetaBytes + S * kStageBytes;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
   static_assert(3 * S * 8 <= kBarrierBytes, "barrier area");
+  static_assert(S <= 8, "header area");
 };
 
 // ---- element math -------------------------------------------------------------
@@ -460,9 +463,34 @@ __device__ __forceinline__ Body tile_body(const Tile& t) {
 
 // ---- bulk kernel --------------------------------------------------------------------
 
+// What the producer puts in a stage besides the data: which chunk it holds and
+// the unaligned edges of its tile (on the tile's first stage only).  len > 0:
+// a chunk of len elements at full index c; 0: edges only; -1: no more work.
+struct StageHdr {
+  int64_t c;        // first element of the chunk (full index)
+  int64_t delta;    // state index - full index, replica group 0
+  int64_t edge_f0;  // the tile's first element (head edge starts here)
+  int64_t edge_b1;  // end of the tile's aligned body (tail edge starts here)
+  int32_t len;
+  int32_t n_head;   // head / tail edge elements to do with this stage
+  int32_t n_tail;
+  int32_t rank;     // owner rank of the tile
+};
+static_assert(sizeof(StageHdr) == 48, "stage header layout");
+
+// Next work tile of this CTA: from the launch's tile counter when there is one
+// (tiles are handed out in order, so the CTAs' traffic stays in one compact,
+// moving window of the buffers), else the static stride blockIdx.x + k * grid.
+__device__ __forceinline__ int64_t next_tile(const StepArgs& a, int64_t k) {
+  if (a.tile_ctr) return int64_t(atomicAdd(a.tile_ctr, 1ull));
+  return int64_t(blockIdx.x) + k * int64_t(gridDim.x);
+}
+
 // Roles (warp index): 0-7 consumers, 8 producer (lane 0), 9 storer (lane 0).
-// Per stage s of the ring three mbarriers carry the hand-offs:
-//   full[s]      producer -> consumers: the chunk's N_d + 3 slices have landed
+// The producer alone picks tiles; every stage carries a StageHdr, so the
+// consumers and the storer follow the producer's sequence.  Per stage s of the
+// ring three mbarriers carry the hand-offs:
+//   full[s]      producer -> consumers: header written, the chunk's N_d + 3 slices landed
 //   computed[s]  consumers -> storer: all 8 warps left results in the stage
 //   empty[s]     storer -> producer: the bulk stores have read the stage out
 template <int NS, int NR, typename GradT, bool kClip>
@@ -476,7 +504,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* computed = full + S;
   uint64_t* empty = full + 2 * S;
-  unsigned char* stages = smem + Cfg::kBarrierBytes;
+  StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + Cfg::kHeaderOff);
+  unsigned char* stages = smem + Cfg::kMetaBytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -493,55 +522,83 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   const int lane = threadIdx.x % 32;
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one thread streams chunks into the ring ----------------
+    // ---------------- producer: one thread picks tiles and streams chunks into the ring ----------------
     if (lane != 0) return;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed = 0;   // stages that ever received copies (bit s)
+    uint32_t used = 0;   // stages that ever received a header (bit s)
     bool ok = true;
-    for (int64_t t = blockIdx.x; ok && t < a.n_tiles; t += gridDim.x) {
-      const Tile tile = a.tiles[t];
-      const Body body = tile_body(tile);
+    // the next tile and its descriptor are fetched one tile ahead
+    int64_t k = 0;
+    int64_t t_next = next_tile(a, k++);
+    Tile d_next = t_next < a.n_tiles ? a.tiles[t_next] : Tile{0, 0, 0, 0};
+    for (;;) {
+      const int64_t t = t_next;
+      const Tile tile = d_next;
+      const bool done = t >= a.n_tiles;
+      if (!done) {
+        t_next = next_tile(a, k++);
+        if (t_next < a.n_tiles) d_next = a.tiles[t_next];
+      }
+      const Body body = done ? Body{0, 0} : tile_body(tile);
       const int64_t delta = tile.state_begin - tile.full_begin;
-      for (int64_t c = body.b0; c < body.b1; c += E) {
-        const uint32_t len = uint32_t(min(int64_t(E), body.b1 - c));
+      int64_t c = body.b0;
+      bool first = true;
+      do {
+        const int32_t len = done ? -1 : int32_t(min(int64_t(E), body.b1 - c));
         if (!mbar_wait(smem_addr(&empty[stage]), phase ^ 1u)) {
           atomicOr(&g_fsp_device_error, kErrProducerWait);
           ok = false;
           break;
         }
-        unsigned char* st = stages + stage * Cfg::kStageBytes;
+        StageHdr& h = hdr[stage];
+        h.c = c;
+        h.delta = delta;
+        h.edge_f0 = tile.full_begin;
+        h.edge_b1 = body.b1;
+        h.len = len;
+        h.n_head = first && !done ? int32_t(body.b0 - tile.full_begin) : 0;
+        h.n_tail = first && !done ? int32_t(tile.full_begin + tile.len - body.b1) : 0;
+        h.rank = int32_t(tile.rank);
         const uint32_t bar = smem_addr(&full[stage]);
-        mbar_arrive_expect_tx(bar, len * uint32_t(NG * G + NR * 12));
-        if (kClip) {   // the reduced gradient, from its owner's slice
-          bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(a.grads[tile.rank]) + c * G,
-                    len * G, bar);
-        } else {
-#pragma unroll
-          for (int q = 0; q < N; ++q)
-            bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+        if (len > 0) {
+          unsigned char* st = stages + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(bar, uint32_t(len) * uint32_t(NG * G + NR * 12));
+          if (kClip) {   // the reduced gradient, from its owner's slice
+            bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(a.grads[tile.rank]) + c * G,
                       len * G, bar);
-        }
+          } else {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const int64_t s = c + delta + r * a.rep_stride;
-          unsigned char* sb = st + Cfg::kStateOff + r * 3 * E * 4;
-          bulk_load(smem_addr(sb), a.master + s, len * 4, bar);
-          bulk_load(smem_addr(sb + E * 4), a.m + s, len * 4, bar);
-          bulk_load(smem_addr(sb + 2 * E * 4), a.v + s, len * 4, bar);
+            for (int q = 0; q < N; ++q)
+              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G),
+                        static_cast<const unsigned char*>(a.grads[q]) + c * G, len * G, bar);
+          }
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            const int64_t s = c + delta + r * a.rep_stride;
+            unsigned char* sb = st + Cfg::kStateOff + r * 3 * E * 4;
+            bulk_load(smem_addr(sb), a.master + s, len * 4, bar);
+            bulk_load(smem_addr(sb + E * 4), a.m + s, len * 4, bar);
+            bulk_load(smem_addr(sb + 2 * E * 4), a.v + s, len * 4, bar);
+          }
+        } else {
+          mbar_arrive(bar);   // header only: edges, or the end of the work
         }
-        armed |= 1u << stage;
+        used |= 1u << stage;
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
-      }
+        first = false;
+        c += E;
+      } while (!done && c < body.b1);
+      if (!ok || done) break;
     }
     if (!ok) {
       // Let every issued copy land before this CTA can retire: the most recent
-      // phase armed on stage s has parity `phase` for s < stage, else phase ^ 1.
+      // phase used on stage s has parity `phase` for s < stage, else phase ^ 1.
       for (int s = 0; s < S; ++s)
-        if (armed & (1u << s)) mbar_wait(smem_addr(&full[s]), s < stage ? phase : phase ^ 1u);
+        if (used & (1u << s)) mbar_wait(smem_addr(&full[s]), s < stage ? phase : phase ^ 1u);
     }
     return;
   }
@@ -551,38 +608,36 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     if (lane != 0) return;
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-      const Tile tile = a.tiles[t];
-      const Body body = tile_body(tile);
-      const int64_t delta = tile.state_begin - tile.full_begin;
-      for (int64_t c = body.b0; c < body.b1; c += E) {
-        const uint32_t len = uint32_t(min(int64_t(E), body.b1 - c));
-        if (!mbar_wait(smem_addr(&computed[stage]), phase)) {
-          atomicOr(&g_fsp_device_error, kErrConsumerWait);
-          bulk_wait_all();
-          return;
-        }
+    for (;;) {
+      if (!mbar_wait(smem_addr(&computed[stage]), phase)) {
+        atomicOr(&g_fsp_device_error, kErrConsumerWait);
+        break;
+      }
+      const StageHdr h = hdr[stage];
+      if (h.len < 0) break;
+      if (h.len > 0) {
+        const uint32_t len = uint32_t(h.len);
         unsigned char* st = stages + stage * Cfg::kStageBytes;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const uint32_t th_s = smem_addr(st + Cfg::kStateOff + r * 3 * E * 4);
           const uint32_t p_s = smem_addr(st + Cfg::kParamOff + r * E * 2);
-          const int64_t s = c + delta + r * a.rep_stride;
+          const int64_t s = h.c + h.delta + r * a.rep_stride;
           bulk_store(a.master + s, th_s, len * 4);
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
           if (a.gather) {
 #pragma unroll
-            for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + c, p_s, len * 2);   // the all-gather
+            for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + h.c, p_s, len * 2);   // the all-gather
           }
         }
         bulk_commit();
         bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out
-        mbar_arrive(smem_addr(&empty[stage]));
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      mbar_arrive(smem_addr(&empty[stage]));
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     bulk_wait_all();
@@ -595,27 +650,19 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   const Coeffs cf = coeffs_of(a);
   int stage = 0;
   uint32_t phase = 0;
-  int64_t t = blockIdx.x;
-  Tile next = t < a.n_tiles ? a.tiles[t] : Tile{0, 0, 0, 0};
-  for (; t < a.n_tiles; t += gridDim.x) {
-    const Tile tile = next;
-    if (t + gridDim.x < a.n_tiles) next = a.tiles[t + gridDim.x];   // prefetch the next descriptor
-    const Body body = tile_body(tile);
-    const int64_t delta = tile.state_begin - tile.full_begin;
-    const int64_t end = tile.full_begin + tile.len;
-
-    // unaligned edges, straight from global memory (fewer than 16 elements)
-    const int64_t n_head = body.b0 - tile.full_begin, n_tail = end - body.b1;
-    if (tid < n_head + n_tail) {
-      const int64_t f = tid < n_head ? tile.full_begin + tid : body.b1 + (tid - n_head);
-      step_one<NS, NR, GradT, kClip>(a, cf, f, f + delta, tile.rank, coef);
-    }
-
-    for (int64_t c = body.b0; c < body.b1; c += E) {
-      const int len = int(min(int64_t(E), body.b1 - c));
-      // a warp-uniform decision, so that a wait running out ends the whole warp
-      const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_addr(&full[stage]), phase));
-      if (!landed) return;   // the storer's bounded wait records the error
+  for (;;) {
+    // a warp-uniform decision, so that a wait running out ends the whole warp
+    const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_addr(&full[stage]), phase));
+    if (!landed) return;   // the storer's bounded wait records the error
+    const StageHdr h = hdr[stage];
+    if (h.len >= 0) {
+      // unaligned edges of the tile, straight from global memory (fewer than 16 elements)
+      if (tid < h.n_head + h.n_tail) {
+        const int64_t f = tid < h.n_head ? h.edge_f0 + tid : h.edge_b1 + (tid - h.n_head);
+        step_one<NS, NR, GradT, kClip>(a, cf, f, f + h.delta, h.rank, coef);
+      }
+      const int len = h.len;
+      const int64_t c = h.c, delta = h.delta;
       unsigned char* st = stages + stage * Cfg::kStageBytes;
       for (int j = 4 * tid; j < len; j += 4 * kConsumerThreads) {
         // (1) reduce-scatter (inside each replica group) and all-reduce (across
@@ -667,12 +714,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         }
       }
       fence_async_smem();   // this thread's shared-memory writes -> visible to the bulk stores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&computed[stage]));
-      if (++stage == S) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&computed[stage]));
+    if (h.len < 0) return;
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
 }

@@ -26,6 +26,7 @@ struct KernelInfo {
   const void* fn;
   int threads;
   int smem;
+  bool bulk;   // the bulk-copy pipeline (takes StepArgs::tile_ctr)
 };
 
 // (N_s, N_r) pairs with a bulk-copy instantiation: FSDP2 / DistOpt (N_r = 1)
@@ -41,10 +42,11 @@ struct KernelTable<GradT, Mesh<NS, NR>...> {
   // kClip: the clipped update of the distributed-optimizer flow
   template <bool kClip>
   static KernelInfo get(int n_shard, int n_rep) {
-    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<GradT, kClip>), kGenericThreads, 0};
+    KernelInfo k{reinterpret_cast<const void*>(&sharded_step_generic_kernel<GradT, kClip>), kGenericThreads, 0,
+                 false};
     ((n_shard == NS && n_rep == NR
           ? (k = KernelInfo{reinterpret_cast<const void*>(&sharded_step_kernel<NS, NR, GradT, kClip>), kBulkThreads,
-                            BulkCfg<NS, NR, GradT, kClip ? 1 : NS * NR>::kSmemBytes},
+                            BulkCfg<NS, NR, GradT, kClip ? 1 : NS * NR>::kSmemBytes, true},
              0)
           : 0),
      ...);
@@ -64,8 +66,8 @@ using ClipKernels = KernelTable<float, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<
 template <int... Ns>
 struct NormKernelTable {
   static KernelInfo get(int n) {
-    KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0>), kGenericThreads, 0};
-    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0},
+    KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0>), kGenericThreads, 0, false};
+    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0, false},
                  0)
               : 0),
      ...);
@@ -189,19 +191,78 @@ void set_mesh(StepArgs& a, const fsp_plan* p) {
   a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
 }
 
+// Pool of the launches' tile counters on the current device: 8-byte
+// stream-ordered allocations, memory kept by the pool between launches.
+fsp_status counter_pool(cudaMemPool_t* out) {
+  static std::mutex mu;
+  static std::map<int, cudaMemPool_t> pools;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = pools.find(dev);
+  if (it != pools.end()) {
+    *out = it->second;
+    return FSP_OK;
+  }
+  cudaMemPoolProps props{};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool = nullptr;
+  e = cudaMemPoolCreate(&pool, &props);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemPoolCreate (tile counters)", e));
+  uint64_t keep = ~uint64_t(0);
+  e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  if (e != cudaSuccess) {
+    cudaMemPoolDestroy(pool);
+    return fail(FSP_ECUDA, cuda_msg("cudaMemPoolSetAttribute (tile counters)", e));
+  }
+  pools[dev] = pool;
+  *out = pool;
+  return FSP_OK;
+}
+
+// Bulk-kernel plans with at least this many tiles per CTA hand their tiles out
+// in order from a counter: with a fixed stride the CTAs drift apart over a long
+// launch, their copies spread over the whole buffers, and HBM throughput drops
+// (smaller plans finish before that matters).
+constexpr int64_t kOrderedMinTilesPerCta = 16;
+
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip) {
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, bool ordered) {
   const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
                        : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
                                                 : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
   int grid = 0;
   fsp_status s = grid_for(k, &grid);
   if (s != FSP_OK) return s;
-  grid = int(std::min<int64_t>(grid, a.n_tiles));
+  // The generic kernel runs one CTA per tile: the block scheduler hands the
+  // tiles out in order.  The bulk kernel keeps one CTA per SM.
+  grid = int(std::min<int64_t>(k.bulk ? grid : int64_t(INT32_MAX), a.n_tiles));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  a.tile_ctr = nullptr;
+  if (ordered && k.bulk && a.n_tiles >= kOrderedMinTilesPerCta * grid) {
+    cudaMemPool_t pool = nullptr;
+    s = counter_pool(&pool);
+    if (s != FSP_OK) return s;
+    void* ctr = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ctr, sizeof(unsigned long long), pool, st);
+    if (e != cudaSuccess) return fail(FSP_ENOMEM, cuda_msg("cudaMallocFromPoolAsync (tile counter)", e));
+    e = cudaMemsetAsync(ctr, 0, sizeof(unsigned long long), st);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ctr, st);
+      return fail(FSP_ECUDA, cuda_msg("cudaMemsetAsync (tile counter)", e));
+    }
+    a.tile_ctr = static_cast<unsigned long long*>(ctr);
+  }
   void* args[] = {&a};
-  cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(k.threads), args, size_t(k.smem),
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(k.threads), args, size_t(k.smem), st);
+  if (a.tile_ctr) {
+    const cudaError_t f = cudaFreeAsync(a.tile_ctr, st);
+    if (e == cudaSuccess) e = f;
+  }
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("sharded step kernel launch", e));
   return FSP_OK;
 }
@@ -536,7 +597,7 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   a.n_tiles = int64_t(p->tiles.size());
   set_mesh(a, p);
   set_coeffs(a, hp, step);
-  return launch(a, dtype, st);
+  return launch(a, dtype, st, false, /*ordered=*/false);   // static tile stride: no counter to allocate
 }
 
 }  // namespace

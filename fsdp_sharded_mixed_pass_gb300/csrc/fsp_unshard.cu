@@ -7,9 +7,10 @@
 // copy-in / all-gather / copy-out collapse into one pass: each element is read
 // once (4 B) and written once per rank of its group (2 B each).
 //
-// Persistent grid over the plan's tiles; each thread takes 8-element groups
-// (two 16-byte loads of the master, one 16-byte store per rank); unaligned
-// segment edges are done one element at a time.  No waits of any kind.
+// One CTA per tile (the loop over tiles also serves any smaller grid); each
+// thread takes 8-element groups (two 16-byte loads of the master, one 16-byte
+// store per rank); unaligned segment edges are done one element at a time.
+// No waits of any kind.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -24,6 +25,17 @@ namespace fsp {
 namespace {
 
 constexpr int kUnshardThreads = 256;
+
+// Arguments of the unshard kernel.
+struct UnshardArgs {
+  const float* master;
+  uint16_t* params[kMaxRanks];
+  const Tile* tiles;
+  int64_t n_tiles;
+  int n_rep;
+  int n_shard;
+  int64_t rep_stride;
+};
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
@@ -61,30 +73,12 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
   }
 }
 
-}  // namespace
-
-int unshard_threads() { return kUnshardThreads; }
-
-cudaError_t unshard_grid(int* grid) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, unshard_kernel, kUnshardThreads, 0);
-  if (e == cudaSuccess) *grid = std::max(1, sms) * std::max(1, per_sm);
-  return e;
-}
-
 cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream) {
   unshard_kernel<<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError();
 }
 
-}  // namespace fsp
-
-// ---- FSDP2 unshard ------------------------------------------------------------------
-
-namespace fsp {
-namespace {
+// ---- FSDP2 unshard: host side -----------------------------------------------------------
 
 fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* params, void* stream) {
   clear_error();
@@ -120,9 +114,10 @@ fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* para
   a.n_rep = p->n_rep;
   a.n_shard = p->n_shard;
   a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
-  int grid = 0;
-  cudaError_t e = unshard_grid(&grid);
-  if (e == cudaSuccess) e = launch_unshard(a, int(std::min<int64_t>(grid, a.n_tiles)), stream);
+  // one CTA per tile: the block scheduler hands the tiles out in order, which
+  // keeps the writes in one compact, moving window of the param buffers
+  const int grid = int(std::min<int64_t>(INT32_MAX, a.n_tiles));
+  cudaError_t e = launch_unshard(a, grid, stream);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("unshard kernel launch", e));
   return FSP_OK;
 }

@@ -120,3 +120,84 @@ def test_first_use_of_a_plan_from_several_host_threads():
         for a, b in zip(first, _bits(c)):
             assert np.array_equal(a, b)
     assert fsp.device_error() == 0
+
+
+# --- tiles handed out in order from a per-launch counter (plans with many tiles per CTA) ---
+
+BIG = ((6100, 4096), (4099,), (77, 3))   # ~25M elements: thousands of tiles per CTA group
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _noalloc(case, t, stream):
+    """The no-allocation entry keeps the static tile stride: the reference schedule."""
+    grads, state, params = _step_args(case)
+    fsp.sharded_step_noalloc(case.plan, grads, *state, params, HP, t, stream=stream)
+
+
+@pytest.mark.parametrize("n_d,mode,n_rep,gd", [(4, "fsdp2", 1, "f32"), (8, "hsdp", 2, "f32"), (6, "fsdp2", 1, "bf16")])
+def test_ordered_tiles_equal_static_stride(n_d, mode, n_rep, gd):
+    ordered = DeviceCase(BIG, n_d, mode, gd, 51, n_rep)
+    static = DeviceCase(BIG, n_d, mode, gd, 51, n_rep)
+    assert ordered.plan.n_tiles >= 16 * _sms()     # large enough for the counter schedule
+    stream = torch.cuda.current_stream()
+    for t in (10, 11):
+        ordered.step(t, debug=False)
+        _noalloc(static, t, stream)
+    torch.cuda.synchronize()
+    for a, b in zip(_bits(ordered), _bits(static)):
+        assert np.array_equal(a, b)
+    assert ordered.all_guards_intact() and static.all_guards_intact()
+    assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("mode", ["relaxed", "global"])
+def test_cuda_graph_of_ordered_steps(mode):
+    eager = DeviceCase(BIG, 4, "fsdp2", "f32", 53)
+    graphed = DeviceCase(BIG, 4, "fsdp2", "f32", 53)
+    fresh = DeviceCase(BIG, 4, "fsdp2", "f32", 53)
+    assert graphed.plan.n_tiles >= 16 * _sms()
+    graphed.step(1, debug=False)      # first use outside capture (tile table, counter pool)
+    torch.cuda.synchronize()
+    for dst, src in zip(graphed.state + graphed.params, fresh.state + fresh.params):
+        dst.raw.copy_(src.raw)
+    del fresh
+    grads, state, params = _step_args(graphed)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode=mode):
+        for t in (10, 11):
+            fsp.sharded_step(graphed.plan, grads, *state, params, HP, t, stream=stream)
+    for _ in range(2):                # each replay zeroes its counters again
+        g.replay()
+        for t in (10, 11):
+            eager.step(t, debug=False)
+        torch.cuda.synchronize()
+        for a, b in zip(_bits(eager), _bits(graphed)):
+            assert np.array_equal(a, b)
+    assert graphed.all_guards_intact()
+    assert fsp.device_error() == 0
+
+
+def test_one_plan_on_concurrent_streams_with_ordered_tiles():
+    cases = [DeviceCase(BIG, 4, "fsdp2", "f32", 61 + i) for i in range(2)]
+    refs = [DeviceCase(BIG, 4, "fsdp2", "f32", 61 + i) for i in range(2)]
+    plan = cases[0].plan                       # one plan, two sets of buffers, in flight together
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for t in (10, 11, 12):
+        for c, s in zip(cases, streams):
+            grads, state, params = _step_args(c)
+            fsp.sharded_step(plan, grads, *state, params, HP, t, stream=s)
+    torch.cuda.synchronize()
+    for r in refs:
+        for t in (10, 11, 12):
+            r.step(t, debug=False)
+    torch.cuda.synchronize()
+    for c, r in zip(cases, refs):
+        for a, b in zip(_bits(c), _bits(r)):
+            assert np.array_equal(a, b)
+    assert fsp.device_error() == 0
