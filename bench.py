@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("fsp", "reference"), default="fsp")
     ap.add_argument("--workload", default="qwen3_0p6b_fsdp2")
+    ap.add_argument("--n-d", type=int, default=None,
+                    help="run the workload with this many data-parallel ranks instead of its own N_d")
     ap.add_argument("--param-slice", default=None,
                     help="a:b - only params a..b-1 of the workload (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -137,6 +139,11 @@ def kernel_src_hash(text: str | None = None) -> str:
     code = re.sub(r"//[^\n]*", " ", code)
     code = " ".join(code.split())
     return hashlib.sha256(code.encode()).hexdigest()[:12]
+
+
+def workload_own_n_d(name: str) -> int:
+    import synth_inputs as S
+    return (S.workload(int(name)) if name.isdigit() else S.workload(name)).n_d
 
 
 def traffic_per_elem(workload_name: str):
@@ -230,15 +237,23 @@ def clocks_bad(c: dict) -> bool:
 # workload on the device
 # --------------------------------------------------------------------------
 
-def resolve_workload(name: str, param_slice: str | None):
+def resolve_workload(name: str, param_slice: str | None, n_d: int | None = None):
+    """The named workload, optionally on params a..b-1 only and/or with another
+    rank count N_d (HSDP keeps its replica groups; N_d must be a multiple)."""
+    import dataclasses
     import synth_inputs as S
     w = S.workload(int(name)) if name.isdigit() else S.workload(name)
-    shapes = w.shapes
     label = w.name
+    if n_d is not None and n_d != w.n_d:
+        if not 1 <= n_d <= 64 or n_d % w.n_rep:
+            raise SystemExit(f"--n-d {n_d}: need 1..64 and a multiple of the {w.n_rep} replica groups")
+        w = dataclasses.replace(w, n_d=n_d)
+        label = f"{w.name}@N_d={n_d}"
+    shapes = w.shapes
     if param_slice:
         a, b = (int(x) if x else None for x in param_slice.split(":"))
         shapes = shapes[a:b]
-        label = f"{w.name}[{param_slice}]"
+        label = f"{label}[{param_slice}]"
     return w, tuple(shapes), label
 
 
@@ -506,7 +521,7 @@ def run_fsp(args):
     dist = Dist(args.gpus)
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
-    w, shapes, label = resolve_workload(args.workload, args.param_slice)
+    w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
     wl = DeviceWorkload(w, shapes, dev)
     wl.clip = args.clip
     wl.unshard = args.unshard
@@ -531,7 +546,8 @@ def run_fsp(args):
     launch_s = ms / 1e3 / args.steps
     achieved = per * P / launch_s / 1e9
     peak, peak_src = read_peak()
-    tpe = traffic_per_elem(w.name)
+    # per-element traffic was captured at each workload's own N_d
+    tpe = traffic_per_elem(w.name) if args.n_d in (None, workload_own_n_d(args.workload)) else None
 
     e2e = None
     if not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather:
@@ -566,7 +582,7 @@ def run_fsp(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(config_block(w, label, plan), bytes_per_param=per,
                        l2=l2_note(per * P, flush_bytes), **(
-            {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (3 kernels per step)"}
+            {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (4 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
             if args.unshard else {"flow": "ZeRO-3 step: reduce-scatter + AdamW, no all-gather"}
             if args.no_gather else {})),
@@ -580,7 +596,7 @@ def run_fsp(args):
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps * (3 if args.clip is not None else 1),
+        "gpu_launches": args.steps * (4 if args.clip is not None else 1),
         "launch": "one CUDA graph of the K steps" if args.graph else "one launch per step from the host",
         "clocks": clocks,
     }
@@ -595,7 +611,7 @@ def run_reference(args):
     dist_rank = int(os.environ.get("RANK", "0"))
     if dist_rank != 0:
         return
-    w, shapes, label = resolve_workload(args.workload, args.param_slice)
+    w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
     # per step, a bounded sample sized so the whole run stays within ~2 minutes
     budget_elems = max(100_000, min(16_000_000, int(120 * 15e6 / max(1, args.steps + args.warmup))))
     sshapes, _ = cpu_sample_shapes(shapes, budget_elems)

@@ -359,9 +359,8 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   return launch(a, dtype, stream);
 }
 
-constexpr int kMaxNormPartials = 4096;
-
-// Per-CTA partial sums of the clipped step's norm, one array per plan and device.
+// Partial sums of the clipped step's norm, one array per plan and device: one
+// double per work tile, then one per block of kNormBlock tiles.
 fsp_status device_partials(const fsp_plan* p, double** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -373,7 +372,8 @@ fsp_status device_partials(const fsp_plan* p, double** out) {
     return FSP_OK;
   }
   double* d = nullptr;
-  e = cudaMalloc(&d, kMaxNormPartials * sizeof(double));
+  const size_t n = p->tiles.size();
+  e = cudaMalloc(&d, std::max<size_t>(1, n + (n + kNormBlock - 1) / kNormBlock) * sizeof(double));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(FSP_ENOMEM, cuda_msg("cudaMalloc (norm partials)", e));
@@ -408,18 +408,22 @@ fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype
   s = device_partials(p, &partials);
   if (s != FSP_OK) return s;
 
-  // pass 1: reduce-scatter into the owners' slices, per-CTA sums of squares
+  // pass 1: reduce-scatter into the owners' slices and each tile's sum of
+  // squares, one CTA per tile (the block scheduler takes the tiles in order)
+  if (a.n_tiles > INT32_MAX) return fail(FSP_EUNSUPPORTED, "the clipped step takes at most 2^31 - 1 work tiles");
   const KernelInfo k1 = NormKernels::get(p->n_d);
-  int grid = 0;
-  s = grid_for(k1, &grid);
-  if (s != FSP_OK) return s;
-  grid = int(std::min<int64_t>(std::min(grid, kMaxNormPartials), a.n_tiles));
+  const int grid = int(a.n_tiles);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* args1[] = {&a, &partials};
   cudaError_t e = cudaLaunchKernel(k1.fn, dim3(grid), dim3(k1.threads), args1, 0, st);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("reduce-scatter / norm kernel launch", e));
-  // pass 2: the norm and the clip coefficient
-  norm_finalize_kernel<<<1, 256, 0, st>>>(partials, grid, max_norm, norm_out);
+  // pass 2: the norm (the tiles' sums added in a fixed order) and the clip coefficient
+  const int n_blocks = int((a.n_tiles + kNormBlock - 1) / kNormBlock);
+  double* block_sums = partials + a.n_tiles;
+  norm_block_sums_kernel<<<n_blocks, kNormBlockThreads, 0, st>>>(partials, grid, block_sums);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("norm block-sum kernel launch", e));
+  norm_finalize_kernel<<<1, kNormFinalizeThreads, 0, st>>>(block_sums, n_blocks, max_norm, norm_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("norm kernel launch", e));
   // pass 3: AdamW on the clipped gradient read from the owners' slices

@@ -7,10 +7,12 @@
 // copy-in / all-gather / copy-out collapse into one pass: each element is read
 // once (4 B) and written once per rank of its group (2 B each).
 //
-// One CTA per tile (the loop over tiles also serves any smaller grid); each
-// thread takes 8-element groups (two 16-byte loads of the master, one 16-byte
-// store per rank); unaligned segment edges are done one element at a time.
-// No waits of any kind.
+// One CTA per tile (the loop over tiles also serves any smaller grid): the
+// threads read the tile's fp32 master with 16-byte loads and cast it into
+// shared memory; one thread then writes the bf16 tile to every rank's buffer
+// with bulk asynchronous copies.  Unaligned segment edges are done one element
+// at a time.  The only waits are the bulk-copy group waits on this CTA's own
+// stores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,35 +44,76 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
          (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(static_cast<uint32_t>(__cvta_generic_to_shared(src))), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N committed bulk groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// A tile is at most kTileElems elements: two 8-element groups per thread.
+static_assert(kTileElems == 2 * 8 * kUnshardThreads, "unshard covers a tile in one pass of the CTA");
+
+// Per tile and replica group: the threads cast the master's aligned body to
+// bf16 in shared memory, then one thread writes it to each rank of the group
+// with a bulk copy (one 8 KB store per rank for a full tile).  Two buffers
+// alternate, so replica r + 1 is cast while r's stores drain.
 __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_constant__ UnshardArgs a) {
+  __shared__ __align__(128) uint16_t cast[2][kTileElems];
   const int ns = a.n_shard, nr = a.n_rep;
+  const int i0 = threadIdx.x, i1 = threadIdx.x + kUnshardThreads;
+  int buf = 0;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
-    const int64_t f0 = tile.full_begin, len = tile.len;
+    const int64_t f0 = tile.full_begin, end = f0 + tile.len;
     const int64_t delta = tile.state_begin - tile.full_begin;
-    // [0, head): before the first multiple of 8; [head, tail): 8-element groups
-    const int64_t head = min(len, (8 - (f0 & 7)) & 7);
-    const int64_t groups = (len - head) >> 3;
-    const int64_t tail = head + groups * 8;
-    for (int64_t i = threadIdx.x; i < groups; i += kUnshardThreads) {
-      const int64_t f = f0 + head + 8 * i;
+    // aligned body [b0, b1): 8-element (16-byte bf16) boundaries of the full index
+    int64_t b0 = (f0 + 7) & ~int64_t(7), b1 = end & ~int64_t(7);
+    if (b1 < b0) b0 = b1 = end;
+    const int groups = int((b1 - b0) >> 3);
+    if (groups > 0) {
       for (int r = 0; r < nr; ++r) {
-        const float* src = a.master + f + delta + r * a.rep_stride;
-        const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
-        const float4 y = __ldcs(reinterpret_cast<const float4*>(src + 4));
-        const uint4 b = make_uint4(pack2(x.x, x.y), pack2(x.z, x.w), pack2(y.x, y.y), pack2(y.z, y.w));
-        for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint4*>(a.params[r * ns + j] + f), b);
+        const float* src = a.master + b0 + delta + r * a.rep_stride;
+        float4 x0, y0, x1, y1;
+        if (i0 < groups) {
+          x0 = __ldcs(reinterpret_cast<const float4*>(src + 8 * i0));
+          y0 = __ldcs(reinterpret_cast<const float4*>(src + 8 * i0 + 4));
+        }
+        if (i1 < groups) {
+          x1 = __ldcs(reinterpret_cast<const float4*>(src + 8 * i1));
+          y1 = __ldcs(reinterpret_cast<const float4*>(src + 8 * i1 + 4));
+        }
+        if (threadIdx.x == 0) bulk_wait_read<1>();   // this buffer's previous stores have read it
+        __syncthreads();
+        uint4* d = reinterpret_cast<uint4*>(cast[buf]);
+        if (i0 < groups) d[i0] = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(y0.x, y0.y), pack2(y0.z, y0.w));
+        if (i1 < groups) d[i1] = make_uint4(pack2(x1.x, x1.y), pack2(x1.z, x1.w), pack2(y1.x, y1.y), pack2(y1.z, y1.w));
+        fence_async_smem();   // the casts -> visible to the bulk stores
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          for (int j = 0; j < ns; ++j) bulk_store(a.params[r * ns + j] + b0, cast[buf], uint32_t(groups) * 16u);
+          bulk_commit();
+        }
+        buf ^= 1;
       }
     }
-    const int64_t n_scalar = head + (len - tail);
+    // unaligned edges (fewer than 16 elements), one element per thread
+    const int64_t n_head = b0 - f0, n_scalar = n_head + (end - b1);
     if (threadIdx.x < n_scalar) {
-      const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
+      const int64_t f = threadIdx.x < n_head ? f0 + threadIdx.x : b1 + (threadIdx.x - n_head);
       for (int r = 0; r < nr; ++r) {
         const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(a.master[f + delta + r * a.rep_stride]));
         for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
       }
     }
   }
+  if (threadIdx.x == 0) bulk_wait_read<0>();   // shared memory must outlive the stores' reads
 }
 
 cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream) {

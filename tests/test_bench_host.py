@@ -96,3 +96,16 @@ def test_cpu_sample_is_whole_params_and_skips_embeddings():
     from synth_inputs import workload
     shapes, n = bench.cpu_sample_shapes(workload(1).shapes)
     assert shapes[0] == (1024,) and n <= 16_000_000 and len(shapes) == 12
+
+
+def test_rank_count_override_and_param_slice():
+    w, shapes, label = bench.resolve_workload("qwen3_0p6b_fsdp2", "1:45", 24)
+    assert w.n_d == 24 and w.mode == "fsdp2" and len(shapes) == 44
+    assert label == "qwen3_0p6b_fsdp2@N_d=24[1:45]"
+    w, _, label = bench.resolve_workload("5", None, 6)          # HSDP: 2 groups of 3
+    assert (w.n_d, w.n_rep, label) == (6, 2, "qwen3_0p6b_hsdp_2x4@N_d=6")
+    w, _, label = bench.resolve_workload("1", None, 8)          # its own N_d: unchanged
+    assert label == "qwen3_0p6b_fsdp2"
+    for bad in (7, 0, 65):
+        with pytest.raises(SystemExit):
+            bench.resolve_workload("5" if bad == 7 else "1", None, bad)
