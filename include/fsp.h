@@ -26,12 +26,18 @@
  * Conventions for every function below:
  *   - Return FSP_OK or an error status; fsp_last_error() then gives a
  *     one-line, thread-local description.  Argument errors are detected on the
- *     host before anything is launched; no function traps, asserts or waits on
- *     the device.
+ *     host before anything is launched; no function traps or asserts on the
+ *     device, and the only device-side waits are the step kernel's bounded
+ *     waits on its own copy pipeline (see fsp_device_error).
  *   - The caller owns every device buffer and the CUDA stream.  The library
  *     owns plans and, per device, a small read-only table of work tiles that a
  *     plan uploads on its first step on that device (one cudaMalloc and one
  *     synchronous copy; make that first call outside any stream capture).
+ *     It also owns one CUDA memory pool per device: a step whose plan has at
+ *     least 16 work tiles per SM takes an 8-byte tile counter from it on the
+ *     step's stream, zeroed before the kernel and freed after it
+ *     (stream-ordered, so concurrent steps and CUDA-graph replays each get
+ *     their own; the kernel hands its tiles out in order from it).
  *   - Steps are asynchronous on the given stream (NULL = legacy default
  *     stream) and run on the current CUDA device.
  *   - A plan may be used from several threads at once; fsp_plan_destroy must
@@ -214,15 +220,19 @@ fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void* const* gr
  *      (the rank-ordered fp32 fold / N_d) is stored into its owner's slice of
  *      the owner's own grad buffer ("07 · 显存模型", section 2.1 item 1); the
  *      rest of each grad buffer is left as it was;
- *   2. norm = sqrt(sum of squares of every reduced element), taken in fp64,
- *      and coefficient = min(1, max_norm / (norm + 1e-6)) rounded to fp32
- *      (the pages are silent on clipping; this is clip_grad_norm_'s rule);
+ *   2. norm = sqrt(sum of squares of every reduced element) to fp64 accuracy
+ *      (each thread's squares summed as a pair of floats - Dot2 of Ogita,
+ *      Rump and Oishi 2005 - one fp64 partial per work tile, the partials
+ *      added in an order fixed by the plan), and coefficient = min(1,
+ *      max_norm / (norm + 1e-6)) rounded to fp32 (the pages are silent on
+ *      clipping; this is clip_grad_norm_'s rule);
  *   3. AdamW on coefficient * gradient (one fp32 multiply), bf16 cast and
  *      all-gather, as in fsp_sharded_step.
  *   max_norm: finite, > 0.  norm_out: device, 2 floats, 16-byte aligned;
- *   receives {norm, coefficient}.  Three kernels on `cuda_stream`; the plan
- *   owns a small per-device array of partial sums (allocated on first use),
- *   so clipped steps on one plan must be ordered on the device. */
+ *   receives {norm, coefficient}.  Four kernels on `cuda_stream`; the plan
+ *   owns a per-device array of partial sums (8 bytes per work tile,
+ *   allocated on first use), so clipped steps on one plan must be ordered on
+ *   the device. */
 fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
                                     float* master, float* exp_avg, float* exp_avg_sq,
                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
@@ -260,8 +270,9 @@ fsp_status fsp_host_step_workspace_bytes(const fsp_plan* plan, int32_t grad_dtyp
  * master / exp_avg / exp_avg_sq on the device, as a pipeline over chunks of
  * about chunk_elems elements: host-to-device copies of chunk k+1's gradient
  * slices, the step kernel on chunk k and device-to-host copies of chunk k-1's
- * bf16 result to every rank's host buffer overlap, on two library-owned copy
- * streams (created once per device, kept until exit) and `cuda_stream`.
+ * bf16 result to every rank's host buffer overlap, on library-owned copy
+ * streams (four per direction, created once per device, kept until exit) and
+ * `cuda_stream`.
  *   host_grads[r], host_params[r]: full_len_padded elements each; only the
  *               P owned elements are copied (padding is left alone).
  *   workspace:  device, 256-byte aligned, at least
@@ -279,7 +290,8 @@ fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_g
  * or the call sits on a path that must never reach cudaMalloc).  The pages
  * have no counterpart: this is a property of the library, not of the step.
  *   Same arguments, results and checks as fsp_sharded_step; it allocates
- *   nothing.  The plan's work-tile list goes into a fixed array of device
+ *   nothing (its kernel takes tiles with a fixed stride, so it needs no
+ *   tile counter).  The plan's work-tile list goes into a fixed array of device
  *   memory declared by the library (262144 tiles, 8 MiB, present on every
  *   device that loads the library until the process exits), copied there on
  *   `cuda_stream` before the kernel on every call.  Plans with more tiles
