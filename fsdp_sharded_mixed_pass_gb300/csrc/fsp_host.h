@@ -28,9 +28,10 @@ fsp_status device_tiles(const fsp_plan* p, const Tile** out);
 void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step);
 void set_mesh(StepArgs& a, const fsp_plan* p);
 // Launches the step kernel for `a` (clip: the clipped update).
-// `ordered`: the bulk kernel may take its tiles in order from a counter of its
-// own (allocated from a library pool on `stream`, freed after the launch);
-// false keeps the static tile stride and allocates nothing.
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false, bool ordered = true);
+// On plans with many tiles per CTA the bulk kernel takes its tiles in order
+// from a counter: `fixed_ctr` when given (zeroed here on `stream`), else one
+// allocated from a library pool on `stream` and freed after the launch.
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false,
+                  unsigned long long* fixed_ctr = nullptr);
 
 }  // namespace fsp

@@ -231,7 +231,7 @@ constexpr int64_t kOrderedMinTilesPerCta = 16;
 
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, bool ordered) {
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned long long* fixed_ctr) {
   const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
                        : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
                                                 : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
@@ -243,7 +243,12 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, bool orde
   grid = int(std::min<int64_t>(k.bulk ? grid : int64_t(INT32_MAX), a.n_tiles));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.tile_ctr = nullptr;
-  if (ordered && k.bulk && a.n_tiles >= kOrderedMinTilesPerCta * grid) {
+  const bool ordered = k.bulk && a.n_tiles >= kOrderedMinTilesPerCta * grid;
+  if (ordered && fixed_ctr) {
+    cudaError_t e = cudaMemsetAsync(fixed_ctr, 0, sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemsetAsync (tile counter)", e));
+    a.tile_ctr = fixed_ctr;
+  } else if (ordered) {
     cudaMemPool_t pool = nullptr;
     s = counter_pool(&pool);
     if (s != FSP_OK) return s;
@@ -259,7 +264,7 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, bool orde
   }
   void* args[] = {&a};
   cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(k.threads), args, size_t(k.smem), st);
-  if (a.tile_ctr) {
+  if (a.tile_ctr && a.tile_ctr != fixed_ctr) {
     const cudaError_t f = cudaFreeAsync(a.tile_ctr, st);
     if (e == cudaSuccess) e = f;
   }
@@ -497,7 +502,8 @@ extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* c
 // point instead keeps the tile list in a fixed array of device memory that
 // the library declares at file scope (kNoAllocMaxTiles tiles, 8 MiB, held on
 // every device that loads the library until the process exits), rewrites it
-// with a stream-ordered copy on every call, and runs the same kernel on it.
+// with a stream-ordered copy on every call, and runs the same kernel on it;
+// its tile counter is a second file-scope variable, zeroed on the stream.
 
 namespace fsp {
 namespace {
@@ -506,25 +512,37 @@ constexpr int64_t kNoAllocMaxTiles = 262144;   // 8 MiB of 32-byte tile descript
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) Tile g_noalloc_tiles[kNoAllocMaxTiles];
+// The kernel's tile counter for this entry (zeroed on the stream before each launch).
+static __device__ __align__(8) unsigned long long g_noalloc_tile_ctr;
 
-// Device address of g_noalloc_tiles on each device (the name itself is a host
-// stand-in in host code), resolved once per device with that device current.
+// Device addresses of g_noalloc_tiles and g_noalloc_tile_ctr on each device
+// (the names themselves are host stand-ins in host code), resolved once per
+// device with that device current.
+struct NoAllocAddrs {
+  Tile* tiles = nullptr;
+  unsigned long long* ctr = nullptr;
+};
 std::mutex g_noalloc_mu;
-Tile* g_noalloc_addr[kNoAllocMaxDevices] = {};
+NoAllocAddrs g_noalloc_addr[kNoAllocMaxDevices] = {};
 
-fsp_status noalloc_tiles_on_current_device(Tile** out) {
+fsp_status noalloc_arrays_on_current_device(NoAllocAddrs* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
   if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FSP_EUNSUPPORTED, "device ordinal above 63");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_tiles);
+  NoAllocAddrs& d = g_noalloc_addr[dev];
+  if (!d.tiles) {
+    void* tiles = nullptr;
+    void* ctr = nullptr;
+    e = cudaGetSymbolAddress(&tiles, g_noalloc_tiles);
     if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetSymbolAddress(g_noalloc_tiles)", e));
-    g_noalloc_addr[dev] = static_cast<Tile*>(ptr);
+    e = cudaGetSymbolAddress(&ctr, g_noalloc_tile_ctr);
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetSymbolAddress(g_noalloc_tile_ctr)", e));
+    d.ctr = static_cast<unsigned long long*>(ctr);
+    d.tiles = static_cast<Tile*>(tiles);
   }
-  *out = g_noalloc_addr[dev];
+  *out = d;
   return FSP_OK;
 }
 
@@ -580,9 +598,10 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
     if (s != FSP_OK) return s;
   }
 
-  Tile* tiles = nullptr;
-  fsp_status s = noalloc_tiles_on_current_device(&tiles);
+  NoAllocAddrs arrays;
+  fsp_status s = noalloc_arrays_on_current_device(&arrays);
   if (s != FSP_OK) return s;
+  Tile* tiles = arrays.tiles;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(tiles, p->tiles.data(), p->tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemcpyAsync (tile list)", e));
@@ -601,7 +620,7 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   a.n_tiles = int64_t(p->tiles.size());
   set_mesh(a, p);
   set_coeffs(a, hp, step);
-  return launch(a, dtype, st, false, /*ordered=*/false);   // static tile stride: no counter to allocate
+  return launch(a, dtype, st, false, arrays.ctr);   // the library's counter: nothing to allocate
 }
 
 }  // namespace

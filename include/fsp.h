@@ -290,8 +290,8 @@ fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_g
  * or the call sits on a path that must never reach cudaMalloc).  The pages
  * have no counterpart: this is a property of the library, not of the step.
  *   Same arguments, results and checks as fsp_sharded_step; it allocates
- *   nothing (its kernel takes tiles with a fixed stride, so it needs no
- *   tile counter).  The plan's work-tile list goes into a fixed array of device
+ *   nothing (the kernel's tile counter is a library variable too, zeroed on
+ *   `cuda_stream`).  The plan's work-tile list goes into a fixed array of device
  *   memory declared by the library (262144 tiles, 8 MiB, present on every
  *   device that loads the library until the process exits), copied there on
  *   `cuda_stream` before the kernel on every call.  Plans with more tiles

@@ -10,8 +10,8 @@ from oracle import plan as OP
 from oracle import step as OS
 from synth_inputs import workload
 
-from gpu_cases import (HP, SCALED_BOUND, DeviceCase, OracleCase, ensure_built, state_errors, ulp_dist,
-                       within_tol)
+from gpu_cases import (HP, SCALED_BOUND, DeviceCase, OracleCase, check_params, ensure_built, param_ulp_allowance,
+                       state_errors, ulp_dist, within_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,9 +43,11 @@ def _check(dev, ora, norm, coef, o_norm, o_coef):
     for name, g_, o_, e in zip(("master", "m", "v"), gots, ora.state, errs):
         assert within_tol(g_, o_[si]).all(), name
         assert (e <= SCALED_BOUND * 2 ** 24).all(), f"{name}: {e.max():.1f}"
+    p0 = dev.params[0].bits()
+    assert np.array_equal(p0[ora.fi], OS.bf16_rne(gots[0])), "params != bf16_rne(device master)"
     for q in range(len(dev.params)):
-        assert ulp_dist(dev.params[q].bits(), ora.params[q]).max(initial=0) <= 1
-        assert np.array_equal(dev.params[q].bits(), dev.params[0].bits())
+        assert np.array_equal(dev.params[q].bits(), p0)
+        check_params(dev.params[q].bits(), ora.params[q], ora.fi, gots[0], ora.state[0][si], f"param copy {q}")
     assert dev.all_guards_intact() and fsp.device_error() == 0
 
 
@@ -119,7 +121,8 @@ def test_clipped_full_size(idx):
         for name, g_, r_, e in zip(("master", "m", "v"), got, (th, mm, vv), state_errors(got, (th, mm, vv), olds)):
             assert within_tol(g_, r_).all() and (e <= SCALED_BOUND * 2 ** 24).all(), name
         p0 = dev.params[0].t.view(torch.int16)[torch.from_numpy(f).cuda()].cpu().numpy().view(np.uint16)
-        assert ulp_dist(p0, OS.bf16_rne(th)).max() <= 1
+        assert np.array_equal(p0, OS.bf16_rne(got[0])), "params != bf16_rne(device master)"
+        assert (ulp_dist(p0, OS.bf16_rne(th)) <= param_ulp_allowance(got[0], th)).all()
         assert fsp.device_error() == 0
     finally:
         del dev

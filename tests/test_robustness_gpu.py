@@ -10,7 +10,7 @@ import torch
 import fsdp_sharded_mixed_pass_gb300 as fsp
 from synth_inputs import workload
 
-from gpu_cases import HP, DeviceCase, ensure_built
+from gpu_cases import HP, DeviceCase, OracleCase, compare, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -124,32 +124,39 @@ def test_first_use_of_a_plan_from_several_host_threads():
 
 # --- tiles handed out in order from a per-launch counter (plans with many tiles per CTA) ---
 
-BIG = ((6100, 4096), (4099,), (77, 3))   # ~25M elements: thousands of tiles per CTA group
+BIG = ((3000, 4096), (4099,), (77, 3))   # ~12.3M elements: at least 16 tiles per CTA on 152 SMs
 
 
 def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def _noalloc(case, t, stream):
-    """The no-allocation entry keeps the static tile stride: the reference schedule."""
-    grads, state, params = _step_args(case)
-    fsp.sharded_step_noalloc(case.plan, grads, *state, params, HP, t, stream=stream)
-
-
 @pytest.mark.parametrize("n_d,mode,n_rep,gd", [(4, "fsdp2", 1, "f32"), (8, "hsdp", 2, "f32"), (6, "fsdp2", 1, "bf16")])
-def test_ordered_tiles_equal_static_stride(n_d, mode, n_rep, gd):
-    ordered = DeviceCase(BIG, n_d, mode, gd, 51, n_rep)
-    static = DeviceCase(BIG, n_d, mode, gd, 51, n_rep)
-    assert ordered.plan.n_tiles >= 16 * _sms()     # large enough for the counter schedule
+def test_ordered_tiles_match_the_oracle(n_d, mode, n_rep, gd):
+    """A tile skipped or taken twice by the counter schedule shows up here: a
+    sentinel left in place, or state updated twice."""
+    dev = DeviceCase(BIG, n_d, mode, gd, 51, n_rep)
+    assert dev.plan.n_tiles >= 16 * _sms()      # large enough for the counter schedule
+    ora = OracleCase(BIG, n_d, mode, gd, 51, n_rep)
+    dev.step(10)
+    ora.step(10)
+    torch.cuda.synchronize()
+    compare(dev, ora)
+
+
+def test_noalloc_counter_schedule_equals_the_step():
+    ref = DeviceCase(BIG, 4, "fsdp2", "f32", 52)
+    new = DeviceCase(BIG, 4, "fsdp2", "f32", 52)
+    assert ref.plan.n_tiles >= 16 * _sms()
     stream = torch.cuda.current_stream()
     for t in (10, 11):
-        ordered.step(t, debug=False)
-        _noalloc(static, t, stream)
+        ref.step(t, debug=False)
+        grads, state, params = _step_args(new)
+        fsp.sharded_step_noalloc(new.plan, grads, *state, params, HP, t, stream=stream)
     torch.cuda.synchronize()
-    for a, b in zip(_bits(ordered), _bits(static)):
+    for a, b in zip(_bits(ref), _bits(new)):
         assert np.array_equal(a, b)
-    assert ordered.all_guards_intact() and static.all_guards_intact()
+    assert new.all_guards_intact()
     assert fsp.device_error() == 0
 
 
