@@ -1,0 +1,154 @@
+// Passes 1 and 2 of the Megatron distributed-optimizer flow with global-norm
+// clipping ("07 · 显存模型", section 2.1 item 1: the reduce-scatter result
+// lands in the rank's own slice of its grad buffer; the clipping rule itself
+// is PyTorch's clip_grad_norm_, the pages being silent on it).  Pass 3, the
+// clipped AdamW + cast + all-gather, is sharded_step_kernel<..., kClip> in
+// fsp_kernels.cuh.
+//
+//  * rs_writeback_norm_kernel<N_d>: one CTA per tile; reduce-scatter into the
+//    owners' slices and the tile's sum of squares.
+//  * norm_block_sums_kernel, norm_finalize_kernel: the tiles' sums added in an
+//    order fixed by the plan; the norm and the clip coefficient.
+#pragma once
+
+#include <cstdint>
+
+#include "fsp_args.h"
+#include "fsp_kernels.cuh"
+
+namespace fsp {
+
+// ---- distributed-optimizer pass 1: reduce-scatter into the owner's slice + norm ----
+
+// A sum of squares carried as an unevaluated pair of floats, hi + lo, in about
+// twice fp32's precision: the Dot2 scheme of Ogita, Rump and Oishi ("Accurate
+// sum and dot product", SIAM J. Sci. Comput. 26(6), 2005).  Each square is
+// split exactly into p + e (p = fl(x x), e = fma(x, x, -p)); p joins hi through
+// Knuth's TwoSum, whose rounding error goes to lo together with e.  The _rn
+// intrinsics keep the compiler from fusing these steps into FMAs.  GB300 runs
+// fp32 far faster than fp64, so the per-element work stays off the fp64 pipe.
+struct SumSq2 {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = fmaf(x, x, -p);
+    const float s = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+  }
+  __device__ __forceinline__ double value() const { return double(hi) + double(lo); }
+};
+
+// Every element's averaged gradient (rank-ordered fp32 fold / N_d) is written
+// into its owner's slice of that rank's own grad buffer (fp32), and each CTA
+// leaves the sum of squares of the elements it reduced in partials[cta]: each
+// thread's in SumSq2, the CTA's threads added in fp64 in a fixed order.
+// Launched with one CTA per tile: one partial per tile, a grouping fixed by the
+// plan alone.  One replica group (FSDP2 / DistOpt).  NT > 0: N_d fixed; 0: a.n_d.
+template <int NT>
+__global__ void __launch_bounds__(kGenericThreads) rs_writeback_norm_kernel(const __grid_constant__ StepArgs a,
+                                                                            double* partials) {
+  const int n = NT > 0 ? NT : a.n_d;
+  SumSq2 sq;
+  for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const int64_t f0 = tile.full_begin, len = tile.len;
+    float* own = static_cast<float*>(const_cast<void*>(a.grads[tile.rank]));
+    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
+    const int64_t groups = (len - head) >> 2;
+    const int64_t tail = head + groups * 4;
+    for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+      const int64_t f = f0 + head + 4 * i;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(NT > 0 ? NT : 1)
+      for (int q = 0; q < n; ++q) add4(acc, GradIO<float>::load4(a.grads[q], f));
+      acc.x = acc.x / float(n);
+      acc.y = acc.y / float(n);
+      acc.z = acc.z / float(n);
+      acc.w = acc.w / float(n);
+      *reinterpret_cast<float4*>(own + f) = acc;
+      sq.add(acc.x);
+      sq.add(acc.y);
+      sq.add(acc.z);
+      sq.add(acc.w);
+    }
+    const int64_t n_scalar = head + (len - tail);
+    if (threadIdx.x < n_scalar) {
+      const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
+      float acc = 0.f;
+#pragma unroll(NT > 0 ? NT : 1)
+      for (int q = 0; q < n; ++q) acc += GradIO<float>::load1(a.grads[q], f);
+      acc = acc / float(n);
+      own[f] = acc;
+      sq.add(acc);
+    }
+  }
+  // CTA sum in a fixed order: warp shuffles, then warp 0 over the warp sums
+  __shared__ double warp_sums[kGenericThreads / 32];
+  double x = sq.value();
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  if (threadIdx.x % 32 == 0) warp_sums[threadIdx.x / 32] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    for (int w = 0; w < kGenericThreads / 32; ++w) total += warp_sums[w];
+    partials[blockIdx.x] = total;
+  }
+}
+
+// pass 2a: out[b] = the sum of partials[b * kNormBlock, (b + 1) * kNormBlock),
+// four strided values per thread, then a tree over the threads (fixed order).
+constexpr int kNormBlockThreads = 1024;
+constexpr int kNormBlock = 4 * kNormBlockThreads;
+__global__ void __launch_bounds__(kNormBlockThreads) norm_block_sums_kernel(const double* partials, int n_partials,
+                                                                           double* out) {
+  __shared__ double s[kNormBlockThreads];
+  const int64_t base = int64_t(blockIdx.x) * kNormBlock;
+  double x = 0.0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t i = base + threadIdx.x + k * kNormBlockThreads;
+    if (i < n_partials) x += partials[i];
+  }
+  s[threadIdx.x] = x;
+  __syncthreads();
+  for (int w = kNormBlockThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[blockIdx.x] = s[0];
+}
+
+// pass 2b: out = {sqrt(sum of partials), min(1, max_norm / (norm + 1e-6))};
+// the partials are added in a fixed order for a given count (eight strided
+// sums per thread, their pairwise sum, then a tree over the threads).
+constexpr int kNormFinalizeThreads = 1024;
+__global__ void __launch_bounds__(kNormFinalizeThreads) norm_finalize_kernel(const double* partials, int n_partials,
+                                                                             float max_norm, float* out) {
+  __shared__ double s[kNormFinalizeThreads];
+  // eight independent sums per thread keep eight loads in flight
+  constexpr int T = kNormFinalizeThreads;
+  double acc[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
+  int i = threadIdx.x;
+  for (; i + 7 * T < n_partials; i += 8 * T) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] += partials[i + k * T];
+  }
+  for (; i < n_partials; i += T) acc[0] += partials[i];
+  s[threadIdx.x] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  __syncthreads();
+  for (int w = kNormFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(s[0]);
+    const double c = double(max_norm) / (norm + 1e-6);
+    out[0] = float(norm);
+    out[1] = float(c < 1.0 ? c : 1.0);
+  }
+}
+
+}  // namespace fsp

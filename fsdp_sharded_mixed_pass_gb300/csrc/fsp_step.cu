@@ -1,8 +1,9 @@
 // Host side of the fused sharded step: kernel selection and launch, argument
 // checks, and the C entry points that take device buffers (the step, its
 // debug / device-t / clipped / no-allocation variants, the device error word
-// and the bounded-wait self-test).  The kernels are in fsp_kernels.cuh; the
-// host-buffer pipeline is in fsp_host.cu and the unshard in fsp_unshard.cu.
+// and the bounded-wait self-test).  The kernels are in fsp_kernels.cuh and
+// fsp_norm_kernels.cuh; the host-buffer pipeline is in fsp_host.cu and the
+// unshard in fsp_unshard.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -15,6 +16,7 @@
 #include "fsp_host.h"
 #include "fsp_internal.h"
 #include "fsp_kernels.cuh"
+#include "fsp_norm_kernels.cuh"
 
 namespace fsp {
 
