@@ -26,6 +26,15 @@ State placement (FSDP2; the pages are silent): the fp32 master/m/v buffers are
     largest rank's extent rounded up to 16.  Gaps and shard padding are never
     written.
 
+Per-parameter buffers ("Parallelism strategies: which state to shard",
+    section 二.5: FSDP2 keeps every parameter, and its gradient, as a tensor of
+    its own; copy-in gathers them before the reduce-scatter, copy-out scatters
+    the all-gather's result back): with param_align = 16 the parameters sit in
+    a virtual full index at offsets rounded up to multiples of 16 elements
+    (our choice, so each tensor's vector boundaries line up with the index);
+    the gaps belong to no rank.  Offsets, segments and state are otherwise as
+    for flat buffers; param_align = 1 is the flat layout.
+
 HSDP ("Parallelism strategies: which state to shard", section 二.6): the N_d
     ranks form an N_r x N_s mesh (replicate, shard); global rank = r * N_s + j.
     Inside each replica group the parameters are FSDP2 Shard(0) over N_s ranks;
@@ -98,17 +107,20 @@ def shard_shape(shape, n_d: int) -> tuple:
     return (shard_rows(shape[0], n_d),) + tuple(shape[1:])
 
 
-def _offsets(shapes):
+def _offsets(shapes, align: int = 1):
+    """Start of each parameter (rounded up to ``align``) and the extent."""
     offs, at = [], 0
     for s in shapes:
+        at = -(-at // align) * align
         offs.append(at)
         at += numel(s)
     return tuple(offs), at
 
 
-def plan_fsdp2(shapes, n_d: int) -> Plan:
+def plan_fsdp2(shapes, n_d: int, param_align: int = 1) -> Plan:
     shapes = tuple(tuple(s) for s in shapes)
-    offs, total = _offsets(shapes)
+    offs, extent = _offsets(shapes, param_align)
+    total = sum(numel(s) for s in shapes)
     cursor = [0] * n_d                    # next free slot within each rank's shard
     local = []                            # (param, rank, full_off, local_state_off, len, padded)
     for i, shape in enumerate(shapes):
@@ -126,7 +138,7 @@ def plan_fsdp2(shapes, n_d: int) -> Plan:
     per_rank = max(cursor) if cursor else 0
     per_rank = -(-per_rank // STATE_ALIGN) * STATE_ALIGN
     segs = tuple(Segment(i, r, f, r * per_rank + s, n, p) for (i, r, f, s, n, p) in local)
-    return Plan("fsdp2", n_d, shapes, offs, total, total, per_rank, segs)
+    return Plan("fsdp2", n_d, shapes, offs, total, extent, per_rank, segs)
 
 
 def plan_distopt(shapes, n_d: int) -> Plan:
@@ -140,9 +152,9 @@ def plan_distopt(shapes, n_d: int) -> Plan:
     return Plan("distopt", n_d, shapes, offs, total, padded, shard, segs)
 
 
-def plan_hsdp(shapes, n_rep: int, n_shard: int) -> Plan:
+def plan_hsdp(shapes, n_rep: int, n_shard: int, param_align: int = 1) -> Plan:
     """N_r replica groups of an N_s-rank FSDP2 layout; segment ranks are global."""
-    inner = plan_fsdp2(shapes, n_shard)
+    inner = plan_fsdp2(shapes, n_shard, param_align)
     copy = n_shard * inner.state_len_per_rank
     segs = tuple(Segment(s.param, r * n_shard + s.rank, s.full_off, r * copy + s.state_off, s.length, s.padded_len)
                  for r in range(n_rep) for s in inner.segments)
@@ -150,15 +162,18 @@ def plan_hsdp(shapes, n_rep: int, n_shard: int) -> Plan:
                 inner.full_len_padded, inner.state_len_per_rank, segs, n_rep)
 
 
-def plan_layout(shapes, n_d: int, mode: str, n_rep: int = 1) -> Plan:
+def plan_layout(shapes, n_d: int, mode: str, n_rep: int = 1, param_align: int = 1) -> Plan:
+    """param_align 16: per-parameter buffers (FSDP2 / HSDP only)."""
+    if param_align not in (1, 16) or (param_align != 1 and mode == "distopt"):
+        raise ValueError("param_align: 1, or 16 for FSDP2 / HSDP")
     if mode == "fsdp2":
-        return plan_fsdp2(shapes, n_d)
+        return plan_fsdp2(shapes, n_d, param_align)
     if mode == "distopt":
         return plan_distopt(shapes, n_d)
     if mode == "hsdp":
         if n_rep < 1 or n_d % n_rep:
             raise ValueError("N_d must be a multiple of the replica count")
-        return plan_hsdp(shapes, n_rep, n_d // n_rep)
+        return plan_hsdp(shapes, n_rep, n_d // n_rep, param_align)
     raise ValueError(mode)
 
 

@@ -166,3 +166,55 @@ def test_workload_layouts():
     assert {1 if len(s) == 1 else s[1] for s in w3.shapes} <= {1, 64, 1024, 4096}
     w4 = workload(4)
     assert len(w4.shapes) == 216 and w4.numel == 1_082_228_736
+
+
+# --- per-parameter buffers: parameters at 16-element-aligned virtual offsets ---
+
+def test_per_param_layout_worked_by_hand():
+    """shapes (3,), (5, 2), (17,) on 2 ranks: offsets 0, 16, 32 (extent 49);
+    dim-0 shards of 2, 3 and 9 rows; state slots by the residue rule."""
+    p = P.plan_layout([(3,), (5, 2), (17,)], 2, "fsdp2", param_align=16)
+    assert p.param_offsets == (0, 16, 32)
+    assert (p.valid_elems, p.full_len_padded) == (3 + 10 + 17, 49)
+    got = [(s.param, s.rank, s.full_off, s.state_off, s.length, s.padded_len) for s in p.segments]
+    assert got == [
+        (0, 0, 0, 0, 2, 2), (0, 1, 2, 48 + 2, 1, 2),
+        (1, 0, 16, 16, 6, 6), (1, 1, 22, 48 + 6, 4, 6),
+        (2, 0, 32, 32, 9, 9), (2, 1, 41, 48 + 25, 8, 9),
+    ]
+    assert p.state_len_per_rank == 48
+
+
+@pytest.mark.parametrize("n_d", [1, 3, 4, 8])
+def test_per_param_layout_properties(n_d):
+    shapes = [(7, 3), (1,), (33,), (16, 2), (5,), (129, 7)]
+    p = P.plan_layout(shapes, n_d, "fsdp2", param_align=16)
+    flat = P.plan_layout(shapes, n_d, "fsdp2")
+    at = 0
+    for off, s in zip(p.param_offsets, shapes):
+        assert off % 16 == 0 and at <= off < at + 16
+        at = off + P.numel(s)
+    assert p.full_len_padded == at and p.valid_elems == flat.valid_elems
+    fi, si = P.owned_indices(p)
+    want = np.concatenate([np.arange(o, o + P.numel(s)) for o, s in zip(p.param_offsets, shapes)])
+    assert np.array_equal(np.sort(fi), want)                     # every element once, gaps nobody's
+    assert len(set(si.tolist())) == si.size
+    for s in p.segments:
+        assert (s.state_off - s.full_off) % 16 == 0
+    # shard heights and lengths are the flat plan's, element for element
+    assert [(s.param, s.rank, s.length, s.padded_len) for s in p.segments] == \
+        [(s.param, s.rank, s.length, s.padded_len) for s in flat.segments]
+
+
+def test_per_param_layout_equals_flat_when_sizes_are_multiples_of_16():
+    shapes = [(16, 3), (32,), (4, 4)]
+    assert P.plan_layout(shapes, 4, "fsdp2", param_align=16) == P.plan_layout(shapes, 4, "fsdp2")
+
+
+def test_per_param_layout_hsdp_and_rejections():
+    p = P.plan_layout([(3,), (5, 2)], 4, "hsdp", n_rep=2, param_align=16)
+    assert p.param_offsets == (0, 16) and p.n_rep == 2
+    with pytest.raises(ValueError):
+        P.plan_layout([(3,)], 2, "distopt", param_align=16)
+    with pytest.raises(ValueError):
+        P.plan_layout([(3,)], 2, "fsdp2", param_align=8)
