@@ -78,6 +78,9 @@ def parse_args(argv=None):
                     help="time the ZeRO-3 step instead: reduce-scatter + AdamW, parameters left sharded")
     ap.add_argument("--unshard", action="store_true",
                     help="time the FSDP2 unshard instead (fp32 shards -> bf16 -> every rank's full buffer)")
+    ap.add_argument("--per-param", action="store_true",
+                    help="every rank's gradient and parameter of every parameter in a tensor of its own "
+                         "(FSDP2 / HSDP; the step reads and writes them in place)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the timed steps in one CUDA graph (removes host launch overhead; small cases)")
     return ap.parse_args(argv)
@@ -258,20 +261,34 @@ def resolve_workload(name: str, param_slice: str | None, n_d: int | None = None)
 
 
 class DeviceWorkload:
-    def __init__(self, w, shapes, device):
+    def __init__(self, w, shapes, device, per_param: bool = False):
         import torch
         import fsdp_sharded_mixed_pass_gb300 as fsp
         from synth_inputs import device as D
         self.w, self.device = w, device
-        self.plan = fsp.plan_layout(shapes, w.n_d, w.mode, n_replicate=w.n_rep)
-        p = self.plan
+        self.per_param = per_param
         gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
-        self.grads = [torch.empty(p.full_len_padded, dtype=gdt, device=device) for _ in range(w.n_d)]
-        for q, g in enumerate(self.grads):
-            D.fill_grad(g, w.data_seed, q, w.grad_dtype)
+        if per_param:
+            # every rank's gradient and bf16 parameter of every parameter as a tensor of its own
+            self.plan = fsp.plan_layout_params(shapes, w.n_d, n_replicate=w.n_rep)
+            p = self.plan
+            sizes = [math.prod(sh) for sh in shapes]
+            self.grads = [[torch.empty(n, dtype=gdt, device=device) for n in sizes] for _ in range(w.n_d)]
+            for q, row in enumerate(self.grads):
+                for g in row:
+                    D.fill_grad(g, w.data_seed, q, w.grad_dtype)
+            self.params = [[torch.zeros(n, dtype=torch.bfloat16, device=device) for n in sizes]
+                           for _ in range(w.n_d)]
+            self.table = fsp.ParamTable(p, self.grads, self.params)
+        else:
+            self.plan = fsp.plan_layout(shapes, w.n_d, w.mode, n_replicate=w.n_rep)
+            p = self.plan
+            self.grads = [torch.empty(p.full_len_padded, dtype=gdt, device=device) for _ in range(w.n_d)]
+            for q, g in enumerate(self.grads):
+                D.fill_grad(g, w.data_seed, q, w.grad_dtype)
+            self.params = [torch.zeros(p.full_len_padded, dtype=torch.bfloat16, device=device) for _ in range(w.n_d)]
         self.state = [torch.zeros(p.state_len_total, dtype=torch.float32, device=device) for _ in range(3)]
         D.fill_state_segments(*self.state, w.data_seed, [(s.full_off, s.state_off, s.length) for s in p.segments])
-        self.params = [torch.zeros(p.full_len_padded, dtype=torch.bfloat16, device=device) for _ in range(w.n_d)]
         torch.cuda.synchronize(device)
         self.t = w.step
         self.clip = None
@@ -281,7 +298,12 @@ class DeviceWorkload:
 
     def step(self, stream):
         import fsdp_sharded_mixed_pass_gb300 as fsp
-        if self.unshard:
+        if self.per_param:
+            if self.unshard:
+                fsp.unshard_params(self.plan, self.table, self.state[0], stream=stream)
+            else:
+                fsp.sharded_step_params(self.plan, self.table, *self.state, self.w.hparams(), self.t, stream=stream)
+        elif self.unshard:
             fsp.unshard(self.plan, self.state[0], self.params, stream=stream)
         elif self.clip is not None:
             fsp.sharded_step_clipped(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
@@ -522,7 +544,9 @@ def run_fsp(args):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
-    wl = DeviceWorkload(w, shapes, dev)
+    if args.per_param and (w.mode == "distopt" or args.clip is not None or args.no_gather):
+        raise SystemExit("--per-param: FSDP2 / HSDP workloads, the plain step or --unshard")
+    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param)
     wl.clip = args.clip
     wl.unshard = args.unshard
     wl.no_gather = args.no_gather
@@ -550,7 +574,7 @@ def run_fsp(args):
     tpe = traffic_per_elem(w.name) if args.n_d in (None, workload_own_n_d(args.workload)) else None
 
     e2e = None
-    if not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather:
+    if not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather and not args.per_param:
         # every rank on this node needs its own host copy of the grads and params
         per_rank = P * w.n_d * (w.grad_bytes + 2)
         local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
@@ -585,14 +609,17 @@ def run_fsp(args):
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (4 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
             if args.unshard else {"flow": "ZeRO-3 step: reduce-scatter + AdamW, no all-gather"}
-            if args.no_gather else {})),
+            if args.no_gather else {}),
+                       **({"buffers": "per-parameter tensors (each rank's gradient and bf16 parameter of each "
+                                      "parameter in a tensor of its own)"} if args.per_param else {})),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
-                     and not args.no_gather else None,
-                     "kernel": "unshard_kernel" if args.unshard else "sharded_step_kernel",
+                     and not args.no_gather and not args.per_param else None,
+                     "kernel": "unshard_kernel" if args.unshard else
+                     "sharded_step_generic_kernel" if args.per_param else "sharded_step_kernel",
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,

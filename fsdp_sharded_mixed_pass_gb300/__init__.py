@@ -10,11 +10,13 @@ fused into one streaming CUDA kernel behind the C ABI in ``include/fsp.h``.
 from .fsp import (  # noqa: F401
     EXPORTS,
     FspError,
+    ParamTable,
     Plan,
     Segment,
     device_error,
     lib,
     plan_layout,
+    plan_layout_params,
     selftest_bounded_wait,
     sharded_step,
     sharded_step_clipped,
@@ -23,5 +25,7 @@ from .fsp import (  # noqa: F401
     sharded_step_host,
     host_step_workspace_bytes,
     sharded_step_noalloc,
+    sharded_step_params,
     unshard,
+    unshard_params,
 )

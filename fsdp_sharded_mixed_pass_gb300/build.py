@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfsp.so")
-SOURCES = ("fsp_plan.cpp", "fsp_step.cu", "fsp_host.cu", "fsp_unshard.cu")
+SOURCES = ("fsp_plan.cpp", "fsp_step.cu", "fsp_host.cu", "fsp_unshard.cu", "fsp_params.cu")
 ARCH = ("-gencode", "arch=compute_103a,code=sm_103a")
 
 

@@ -26,6 +26,11 @@ struct StepArgs {
   float* m;
   float* v;
   float* reduced;   // averaged shard gradient (state layout); nullptr in production
+  // Per-parameter plans: device tables of "virtual base" pointers, entry
+  // param * n_d + q, such that rank q's element at full index f of that
+  // parameter is at base + f; nullptr for full-size buffers (grads / params).
+  const void* const* vgrads;
+  uint16_t* const* vparams;
   const Tile* tiles;
   int64_t n_tiles;
   // Bulk kernel: tiles are taken in order from this counter (zeroed before the

@@ -81,13 +81,9 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
   clear_error();
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!host_grads || !host_params) return fail(FSP_EINVAL, "host_grads or host_params is NULL");
-  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
-  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
   if (chunk_elems < 0) return fail(FSP_EINVAL, "chunk_elems must be >= 0 (0: default)");
-  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
-      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
-    return fail(FSP_EINVAL, "hyper-parameters out of range");
+  if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
   const int n = p->n_d;
   const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
   const size_t sbytes = size_t(p->state_len_total) * 4;

@@ -27,6 +27,8 @@ fsp_status device_tiles(const fsp_plan* p, const Tile** out);
 // AdamW scalars of update t, and the plan's rank layout, into `a`.
 void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step);
 void set_mesh(StepArgs& a, const fsp_plan* p);
+// hp and t within the ranges fsp.h states.
+fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 // Launches the step kernel for `a` (clip: the clipped update).
 // On plans with many tiles per CTA the bulk kernel takes its tiles in order
 // from a counter: `fixed_ctr` when given (zeroed here on `stream`), else one

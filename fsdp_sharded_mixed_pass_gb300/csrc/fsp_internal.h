@@ -25,16 +25,22 @@ constexpr int64_t kTileElems = 4096;
 constexpr int64_t kStateAlign = 16;
 // DistOpt buffers are padded to a multiple of lcm(N_d, this).
 constexpr int64_t kDistOptAlign = 128;
+// Per-parameter plans start every parameter at a multiple of this many
+// elements of the (virtual) full index.
+constexpr int64_t kParamAlign = 16;
 
 // One unit of work for a CTA: `len` elements starting at `full_begin` of every
 // full-size buffer and at `state_begin` of the state buffers, owned by `rank`
-// (the rank whose shard the elements are; replica group 0 for HSDP).  32 bytes
-// so a descriptor is two aligned 16-byte loads.
+// (the rank whose shard the elements are; replica group 0 for HSDP), all in
+// parameter `param` (-1 for a DistOpt shard, which spans parameters).  32
+// bytes so a descriptor is two aligned 16-byte loads.
 struct Tile {
   int64_t full_begin;
   int64_t state_begin;
-  int64_t len;
-  int64_t rank;
+  int32_t len;
+  int32_t rank;
+  int32_t param;
+  int32_t reserved;
 };
 static_assert(sizeof(Tile) == 32, "tile descriptor layout");
 
@@ -47,6 +53,9 @@ struct fsp_plan {
   int32_t n_params = 0;
   int32_t mode = 0;
   int64_t rep_stride = 0; // state elements between two replicas' copies
+  int32_t param_align = 1; // 16: per-parameter buffers (virtual offsets); 1: full-size buffers
+  std::vector<int64_t> param_off;    // each parameter's first full (virtual) index
+  std::vector<int64_t> param_numel;
   int64_t valid_elems = 0;
   int64_t full_len_padded = 0;
   int64_t state_len_per_rank = 0;
@@ -59,6 +68,19 @@ struct fsp_plan {
   mutable std::mutex mu;
   mutable std::map<int, fsp::Tile*> device_tiles;
   mutable std::map<int, double*> device_partials;
+};
+
+// Per-parameter tensors registered for a per-parameter plan on one device
+// (fsp_params.cu): device tables of virtual bases, entry param * n_d + q, such
+// that rank q's element at full index f of that parameter is at base + f.
+struct fsp_param_table {
+  const fsp_plan* plan = nullptr;
+  int device = -1;
+  int32_t grad_dtype = 0;
+  const void** vgrads = nullptr;   // device, n_params * n_d entries
+  uint16_t** vparams = nullptr;    // device, or nullptr: no param tensors
+  // every registered tensor as [begin, end) device addresses, sorted by begin
+  std::vector<std::pair<uintptr_t, uintptr_t>> spans;
 };
 
 namespace fsp {

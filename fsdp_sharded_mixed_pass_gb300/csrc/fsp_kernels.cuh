@@ -104,7 +104,12 @@ struct BulkCfg {
   static constexpr int kParamOff = kStateOff + NR * 3 * E * 4;        // [NR][E] bf16
   static constexpr int kBarrierBytes = 256;                           // full, computed, empty [S]
   static constexpr int kHeaderOff = kBarrierBytes;                    // StageHdr [S]
-  static constexpr int kMetaBytes = kBarrierBytes + 8 * 64;           // barriers + headers
+  // per-parameter tensors: each stage's N grad and N param bases, then the
+  // producer's bases of its current tile
+  static constexpr int kBaseOff = kBarrierBytes + 8 * 64;
+  static constexpr int kBaseStride = 16 * N;
+  static constexpr int kTileBaseOff = kBaseOff + S * kBaseStride;
+  static constexpr int kMetaBytes = (kTileBaseOff + kBaseStride + 127) / 128 * 128;
   static constexpr int kSmemBytes = kMetaBytes + S * kStageBytes;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
   static_assert(3 * S * 8 <= kBarrierBytes, "barrier area");
@@ -174,20 +179,21 @@ struct GradIO<__nv_bfloat16> {
 // all-reduce across groups); with NR = 1 it is the plain rank-ordered fold.
 // kClip: the clipped update - the gradient is already reduced and sits in
 // its owner's slice, and is multiplied by the clip coefficient instead.
+// gb / pb: rank q's grad and param bases (element f is gb[q] + f).
 template <int NS, int NR, typename GradT, bool kClip>
-__device__ __forceinline__ void step_one(const StepArgs& a, const Coeffs& cf, int64_t f, int64_t s, int64_t owner,
-                                         float coef) {
+__device__ __forceinline__ void step_one(const StepArgs& a, const void* const* gb, uint16_t* const* pb,
+                                         const Coeffs& cf, int64_t f, int64_t s, int64_t owner, float coef) {
   const int ns = NS > 0 ? NS : a.n_shard;
   const int nr = NR > 0 ? NR : a.n_rep;
   float acc = 0.f;
   if (kClip) {
-    acc = GradIO<GradT>::load1(a.grads[owner], f) * coef;
+    acc = GradIO<GradT>::load1(gb[owner], f) * coef;
   } else {
 #pragma unroll(NR > 0 ? NR : 1)
     for (int r = 0; r < nr; ++r) {
       float part = 0.f;
 #pragma unroll(NS > 0 ? NS : 1)
-      for (int j = 0; j < ns; ++j) part += GradIO<GradT>::load1(a.grads[r * ns + j], f);
+      for (int j = 0; j < ns; ++j) part += GradIO<GradT>::load1(gb[r * ns + j], f);
       acc = r == 0 ? part : acc + part;
     }
     acc = acc / float(ns * nr);
@@ -204,7 +210,7 @@ __device__ __forceinline__ void step_one(const StepArgs& a, const Coeffs& cf, in
     const uint16_t b = bf16_bits(th);
     if (a.gather) {
 #pragma unroll(NS > 0 ? NS : 1)
-      for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
+      for (int j = 0; j < ns; ++j) pb[r * ns + j][f] = b;
     }
   }
 }
@@ -218,14 +224,15 @@ __device__ __forceinline__ void add4(float4& a, float4 b) {
   a.w += b.w;
 }
 
-// f: full index (multiple of 4); s: state index (same residue mod 16).
+// f: full index (multiple of 4); s: state index (same residue mod 16); gb /
+// pb as for step_one.
 template <typename GradT, bool kClip>
-__device__ __forceinline__ void step_group(const StepArgs& a, const Coeffs& cf, int64_t f, int64_t s, int64_t owner,
-                                           float coef) {
+__device__ __forceinline__ void step_group(const StepArgs& a, const void* const* gb, uint16_t* const* pb,
+                                           const Coeffs& cf, int64_t f, int64_t s, int64_t owner, float coef) {
   const int ns = a.n_shard, nr = a.n_rep;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (kClip) {
-    acc = GradIO<GradT>::load4(a.grads[owner], f);
+    acc = GradIO<GradT>::load4(gb[owner], f);
     acc.x *= coef;
     acc.y *= coef;
     acc.z *= coef;
@@ -233,7 +240,7 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const Coeffs& cf, 
   } else {
     for (int r = 0; r < nr; ++r) {
       float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < ns; ++j) add4(part, GradIO<GradT>::load4(a.grads[r * ns + j], f));
+      for (int j = 0; j < ns; ++j) add4(part, GradIO<GradT>::load4(gb[r * ns + j], f));
       if (r == 0)
         acc = part;
       else
@@ -260,18 +267,33 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const Coeffs& cf, 
     if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + sr), acc);
     if (a.gather) {
       const uint2 b = pack_bf16x4(th);
-      for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(a.params[r * ns + j] + f), b);
+      for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(pb[r * ns + j] + f), b);
     }
   }
 }
 
-// Any N_d up to 64 and any replica grouping.
+// Any N_d up to 64 and any replica grouping; full-size buffers or, with
+// a.vgrads set, per-parameter tensors (each tile's bases from the tables).
 template <typename GradT, bool kClip>
 __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
+  __shared__ const void* tile_gb[kMaxRanks];
+  __shared__ uint16_t* tile_pb[kMaxRanks];
   const float coef = kClip ? a.clip[1] : 1.f;
   const Coeffs cf = coeffs_of(a);
+  const bool per_param = a.vgrads != nullptr;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
+    if (per_param) {
+      __syncthreads();   // the previous tile's bases are no longer read
+      if (threadIdx.x < a.n_d) {
+        const int64_t e = int64_t(tile.param) * a.n_d + threadIdx.x;
+        tile_gb[threadIdx.x] = a.vgrads[e];
+        tile_pb[threadIdx.x] = a.vparams ? a.vparams[e] : nullptr;
+      }
+      __syncthreads();
+    }
+    const void* const* gb = per_param ? tile_gb : a.grads;
+    uint16_t* const* pb = per_param ? tile_pb : a.params;
     const int64_t f0 = tile.full_begin;
     const int64_t delta = tile.state_begin - tile.full_begin;
     const int64_t len = tile.len;
@@ -282,12 +304,12 @@ __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(c
     const int64_t tail = head + groups * 4;
     for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
       const int64_t f = f0 + head + 4 * i;
-      step_group<GradT, kClip>(a, cf, f, f + delta, tile.rank, coef);
+      step_group<GradT, kClip>(a, gb, pb, cf, f, f + delta, tile.rank, coef);
     }
     const int64_t n_scalar = head + (len - tail);
     if (threadIdx.x < n_scalar) {
       const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<0, 0, GradT, kClip>(a, cf, f0 + e, f0 + e + delta, tile.rank, coef);
+      step_one<0, 0, GradT, kClip>(a, gb, pb, cf, f0 + e, f0 + e + delta, tile.rank, coef);
     }
   }
 }
@@ -432,6 +454,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   uint64_t* empty = full + 2 * S;
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + Cfg::kHeaderOff);
   unsigned char* stages = smem + Cfg::kMetaBytes;
+  // per-parameter tensors (a.vgrads set): stage s's rank bases for its tile
+  const bool per_param = a.vgrads != nullptr;
+  auto stage_gb = [&](int s) { return reinterpret_cast<const void**>(smem + Cfg::kBaseOff + s * Cfg::kBaseStride); };
+  auto stage_pb = [&](int s) {
+    return reinterpret_cast<uint16_t**>(smem + Cfg::kBaseOff + s * Cfg::kBaseStride + 8 * N);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -454,17 +482,41 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     uint32_t phase = 0;
     uint32_t used = 0;   // stages that ever received a header (bit s)
     bool ok = true;
-    // the next tile and its descriptor are fetched one tile ahead
+    // the next tile, its descriptor and (per-parameter tensors) its rank
+    // bases are fetched one tile ahead
     int64_t k = 0;
     int64_t t_next = next_tile(a, k++);
     Tile d_next = t_next < a.n_tiles ? a.tiles[t_next] : Tile{0, 0, 0, 0};
+    const void* gb_next[N] = {};
+    uint16_t* pb_next[N] = {};
+    const void** gb = reinterpret_cast<const void**>(smem + Cfg::kTileBaseOff);   // the current tile's
+    uint16_t** pb = reinterpret_cast<uint16_t**>(smem + Cfg::kTileBaseOff + 8 * N);
+    auto fetch_bases = [&](const Tile& d) {
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const int64_t e = int64_t(d.param) * a.n_d + q;
+        gb_next[q] = a.vgrads[e];
+        pb_next[q] = a.vparams ? a.vparams[e] : nullptr;
+      }
+    };
+    if (per_param && t_next < a.n_tiles) fetch_bases(d_next);
     for (;;) {
       const int64_t t = t_next;
       const Tile tile = d_next;
       const bool done = t >= a.n_tiles;
+      if (per_param) {
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          gb[q] = gb_next[q];
+          pb[q] = pb_next[q];
+        }
+      }
       if (!done) {
         t_next = next_tile(a, k++);
-        if (t_next < a.n_tiles) d_next = a.tiles[t_next];
+        if (t_next < a.n_tiles) {
+          d_next = a.tiles[t_next];
+          if (per_param) fetch_bases(d_next);
+        }
       }
       const Body body = done ? Body{0, 0} : tile_body(tile);
       const int64_t delta = tile.state_begin - tile.full_begin;
@@ -486,18 +538,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         h.n_head = first && !done ? int32_t(body.b0 - tile.full_begin) : 0;
         h.n_tail = first && !done ? int32_t(tile.full_begin + tile.len - body.b1) : 0;
         h.rank = int32_t(tile.rank);
+        if (per_param && !done) {
+#pragma unroll
+          for (int q = 0; q < N; ++q) {
+            stage_gb(stage)[q] = gb[q];
+            stage_pb(stage)[q] = pb[q];
+          }
+        }
         const uint32_t bar = smem_addr(&full[stage]);
         if (len > 0) {
           unsigned char* st = stages + stage * Cfg::kStageBytes;
           mbar_arrive_expect_tx(bar, uint32_t(len) * uint32_t(NG * G + NR * 12));
           if (kClip) {   // the reduced gradient, from its owner's slice
-            bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(a.grads[tile.rank]) + c * G,
-                      len * G, bar);
+            const void* own = per_param ? gb[tile.rank] : a.grads[tile.rank];
+            bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(own) + c * G, len * G, bar);
           } else {
 #pragma unroll
             for (int q = 0; q < N; ++q)
               bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G),
-                        static_cast<const unsigned char*>(a.grads[q]) + c * G, len * G, bar);
+                        static_cast<const unsigned char*>(per_param ? gb[q] : a.grads[q]) + c * G, len * G, bar);
           }
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
@@ -544,6 +603,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
       if (h.len > 0) {
         const uint32_t len = uint32_t(h.len);
         unsigned char* st = stages + stage * Cfg::kStageBytes;
+        uint16_t* const* pb = per_param ? stage_pb(stage) : a.params;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const uint32_t th_s = smem_addr(st + Cfg::kStateOff + r * 3 * E * 4);
@@ -554,7 +614,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
           if (a.gather) {
 #pragma unroll
-            for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + h.c, p_s, len * 2);   // the all-gather
+            for (int j = 0; j < NS; ++j) bulk_store(pb[r * NS + j] + h.c, p_s, len * 2);   // the all-gather
           }
         }
         bulk_commit();
@@ -585,7 +645,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
       // unaligned edges of the tile, straight from global memory (fewer than 16 elements)
       if (tid < h.n_head + h.n_tail) {
         const int64_t f = tid < h.n_head ? h.edge_f0 + tid : h.edge_b1 + (tid - h.n_head);
-        step_one<NS, NR, GradT, kClip>(a, cf, f, f + h.delta, h.rank, coef);
+        step_one<NS, NR, GradT, kClip>(a, per_param ? stage_gb(stage) : a.grads,
+                                       per_param ? stage_pb(stage) : a.params, cf, f, f + h.delta, h.rank, coef);
       }
       const int len = h.len;
       const int64_t c = h.c, delta = h.delta;

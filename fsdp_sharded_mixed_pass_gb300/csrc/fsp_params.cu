@@ -1,0 +1,188 @@
+// Per-parameter tensors: the table that registers them (fsp_param_table_create
+// / _destroy) and the step that reads every rank's per-parameter gradients and
+// writes every rank's per-parameter bf16 parameters in place
+// (fsp_sharded_step_params) - FSDP2's copy-in before the reduce-scatter and
+// copy-out after the all-gather folded into the step ("Parallelism
+// strategies: which state to shard", section 二.5).  The unshard into the same
+// tensors is fsp_unshard_params in fsp_unshard.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "fsp_host.h"
+#include "fsp_internal.h"
+
+namespace fsp {
+namespace {
+
+void free_table(fsp_param_table* t) {
+  if (!t) return;
+  if (t->vgrads || t->vparams) {
+    int prev = -1;
+    const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+    if (cudaSetDevice(t->device) == cudaSuccess) {
+      cudaFree(const_cast<void**>(t->vgrads));
+      cudaFree(t->vparams);
+    }
+    if (have_prev) cudaSetDevice(prev);
+  }
+  delete t;
+}
+
+fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t dtype, void* const* param_ptrs,
+                        fsp_param_table** out) {
+  clear_error();
+  if (!out) return fail(FSP_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!p) return fail(FSP_EINVAL, "plan is NULL");
+  if (p->param_align != kParamAlign)
+    return fail(FSP_EINVAL, "the plan is not a per-parameter plan (fsp_plan_layout_params)");
+  if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
+  const int n = p->n_d, np = p->n_params;
+  if (np > 0 && !grad_ptrs) return fail(FSP_EINVAL, "grad_ptrs is NULL");
+  const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
+
+  // host-side checks first (NULL, alignment, overlap), then the driver's
+  std::vector<const void*> vg(size_t(np) * n, nullptr);
+  std::vector<uint16_t*> vp(param_ptrs ? size_t(np) * n : 0, nullptr);
+  std::vector<std::pair<uintptr_t, uintptr_t>> spans;
+  std::vector<std::string> names;
+  for (int q = 0; q < n; ++q) {
+    for (int i = 0; i < np; ++i) {
+      const int64_t numel = p->param_numel[size_t(i)], off = p->param_off[size_t(i)];
+      if (numel == 0) continue;
+      for (int kind = 0; kind < (param_ptrs ? 2 : 1); ++kind) {
+        const void* ptr = kind == 0 ? grad_ptrs[size_t(q) * np + i] : param_ptrs[size_t(q) * np + i];
+        const size_t esz = kind == 0 ? g : 2;
+        const std::string name = std::string(kind == 0 ? "grad_ptrs[" : "param_ptrs[") +
+                                 std::to_string(size_t(q) * np + i) + "]";
+        if (!ptr) return fail(FSP_EINVAL, name + " is NULL");
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return fail(FSP_EINVAL, name + " is not 16-byte aligned");
+        const uintptr_t b = reinterpret_cast<uintptr_t>(ptr);
+        spans.emplace_back(b, b + size_t(numel) * esz);
+        names.push_back(name);
+        // the virtual base: element f of this parameter is at base + f
+        const uintptr_t base = b - uintptr_t(off) * esz;
+        if (kind == 0)
+          vg[size_t(i) * n + q] = reinterpret_cast<const void*>(base);
+        else
+          vp[size_t(i) * n + q] = reinterpret_cast<uint16_t*>(base);
+      }
+    }
+  }
+  std::vector<size_t> order(spans.size());
+  for (size_t k = 0; k < order.size(); ++k) order[k] = k;
+  std::sort(order.begin(), order.end(), [&](size_t x, size_t y) { return spans[x].first < spans[y].first; });
+  for (size_t k = 1; k < order.size(); ++k)
+    if (spans[order[k - 1]].second > spans[order[k]].first)
+      return fail(FSP_EINVAL, names[order[k - 1]] + " overlaps " + names[order[k]]);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  for (size_t k = 0; k < spans.size(); ++k) {
+    fsp_status s = check_allocation(reinterpret_cast<const void*>(spans[k].first), spans[k].second - spans[k].first,
+                                    names[k].c_str());
+    if (s != FSP_OK) return s;
+  }
+
+  fsp_param_table* t = new (std::nothrow) fsp_param_table();
+  if (!t) return fail(FSP_ENOMEM, "host allocation failed");
+  t->plan = p;
+  t->device = dev;
+  t->grad_dtype = dtype;
+  try {
+    t->spans.reserve(spans.size());
+    for (size_t k : order) t->spans.push_back(spans[k]);
+  } catch (const std::bad_alloc&) {
+    delete t;
+    return fail(FSP_ENOMEM, "host allocation failed");
+  }
+  const size_t bytes = std::max<size_t>(1, vg.size()) * sizeof(void*);
+  e = cudaMalloc(reinterpret_cast<void**>(&t->vgrads), bytes);
+  if (e == cudaSuccess && !vg.empty()) e = cudaMemcpy(t->vgrads, vg.data(), vg.size() * sizeof(void*), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && param_ptrs) {
+    e = cudaMalloc(reinterpret_cast<void**>(&t->vparams), bytes);
+    if (e == cudaSuccess && !vp.empty())
+      e = cudaMemcpy(t->vparams, vp.data(), vp.size() * sizeof(void*), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_table(t);
+    return fail(e == cudaErrorMemoryAllocation ? FSP_ENOMEM : FSP_ECUDA, cuda_msg("uploading the tensor table", e));
+  }
+  *out = t;
+  return FSP_OK;
+}
+
+// Whether [ptr, ptr + bytes) overlaps a registered tensor.
+bool overlaps_table(const fsp_param_table* t, const void* ptr, size_t bytes) {
+  if (!bytes) return false;
+  const uintptr_t b = reinterpret_cast<uintptr_t>(ptr), e = b + bytes;
+  auto it = std::lower_bound(t->spans.begin(), t->spans.end(), std::make_pair(e, uintptr_t(0)));
+  return it != t->spans.begin() && std::prev(it)->second > b;
+}
+
+fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                           const fsp_adamw_hparams* hp, int64_t step, void* stream) {
+  clear_error();
+  if (!p || !t) return fail(FSP_EINVAL, "plan or table is NULL");
+  if (t->plan != p) return fail(FSP_EINVAL, "the table was created for another plan");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  if (dev != t->device) return fail(FSP_EINVAL, "the table was created on another device");
+  if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
+  const size_t sbytes = size_t(p->state_len_total) * 4;
+  const Buf state[3] = {{master, sbytes, "master"}, {m, sbytes, "exp_avg"}, {v, sbytes, "exp_avg_sq"}};
+  for (const Buf& b : state) {
+    if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
+    if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
+    if (overlaps_table(t, b.ptr, b.bytes)) return fail(FSP_EINVAL, b.name + " overlaps a registered tensor");
+  }
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(state[i].ptr), b0 = reinterpret_cast<uintptr_t>(state[j].ptr);
+      if (sbytes && a0 < b0 + sbytes && b0 < a0 + sbytes)
+        return fail(FSP_EINVAL, state[i].name + " overlaps " + state[j].name);
+    }
+  if (p->tiles.empty()) return FSP_OK;
+  for (const Buf& b : state) {
+    fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
+    if (s != FSP_OK) return s;
+  }
+  const Tile* tiles = nullptr;
+  fsp_status s = device_tiles(p, &tiles);
+  if (s != FSP_OK) return s;
+  StepArgs a{};
+  a.vgrads = t->vgrads;
+  a.vparams = t->vparams;
+  a.gather = t->vparams ? 1 : 0;
+  a.master = master;
+  a.m = m;
+  a.v = v;
+  a.tiles = tiles;
+  a.n_tiles = int64_t(p->tiles.size());
+  set_mesh(a, p);
+  set_coeffs(a, hp, step);
+  return launch(a, t->grad_dtype, stream);
+}
+
+}  // namespace
+}  // namespace fsp
+
+extern "C" fsp_status fsp_param_table_create(const fsp_plan* plan, const void* const* grad_ptrs, int32_t grad_dtype,
+                                             void* const* param_ptrs, fsp_param_table** out) {
+  return fsp::create_table(plan, grad_ptrs, grad_dtype, param_ptrs, out);
+}
+
+extern "C" void fsp_param_table_destroy(fsp_param_table* table) { fsp::free_table(table); }
+
+extern "C" fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
+                                              float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
+                                              int64_t step, void* cuda_stream) {
+  return fsp::run_step_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, cuda_stream);
+}

@@ -39,7 +39,7 @@ void append_tiles(const fsp_segment& s, std::vector<Tile>& out) {
   const int64_t end = s.full_off + s.len;
   while (f < end) {
     int64_t stop = std::min(end, (f / kTileElems + 1) * kTileElems);
-    out.push_back(Tile{f, s.state_off + (f - s.full_off), stop - f, s.rank});
+    out.push_back(Tile{f, s.state_off + (f - s.full_off), int32_t(stop - f), s.rank, s.param, 0});
     f = stop;
   }
 }
@@ -72,9 +72,12 @@ extern "C" const char* fsp_status_string(fsp_status s) {
 
 namespace {
 
-// Rows (dim 0), cols (product of the other dims) and flat start of each param.
-fsp_status parse_shapes(const int64_t* dims, const int32_t* ndims, int32_t n_params, std::vector<int64_t>& rows,
-                        std::vector<int64_t>& cols, std::vector<int64_t>& start, int64_t& total) {
+// Rows (dim 0), cols (product of the other dims) and start of each param in
+// the full index (rounded up to a multiple of `align`); total = elements,
+// extent = end of the last parameter.
+fsp_status parse_shapes(const int64_t* dims, const int32_t* ndims, int32_t n_params, int64_t align,
+                        std::vector<int64_t>& rows, std::vector<int64_t>& cols, std::vector<int64_t>& start,
+                        int64_t& total, int64_t& extent) {
   if (n_params < 0) return fail(FSP_EINVAL, "fsp_plan_layout: n_params < 0");
   if (n_params > 0 && (!dims || !ndims)) return fail(FSP_EINVAL, "fsp_plan_layout: dims or ndims is NULL");
   rows.assign(n_params, 0);
@@ -82,6 +85,7 @@ fsp_status parse_shapes(const int64_t* dims, const int32_t* ndims, int32_t n_par
   start.assign(n_params, 0);
   int64_t cursor = 0;
   total = 0;
+  extent = 0;
   for (int32_t i = 0; i < n_params; ++i) {
     if (ndims[i] < 1 || ndims[i] > fsp::kMaxDims)
       return fail(FSP_EINVAL, "fsp_plan_layout: ndims[" + std::to_string(i) + "] must be in [1, 8]");
@@ -99,18 +103,19 @@ fsp_status parse_shapes(const int64_t* dims, const int32_t* ndims, int32_t n_par
     cursor += ndims[i];
     cols[i] = c;
     if (rows[i] != 0 && c > fsp::kMaxElems / rows[i]) return fail(FSP_EINVAL, "fsp_plan_layout: parameter too large");
-    start[i] = total;
+    start[i] = fsp::round_up(extent, align);
     total += rows[i] * c;
-    if (total > fsp::kMaxElems) return fail(FSP_EINVAL, "fsp_plan_layout: model too large");
+    extent = start[i] + rows[i] * c;
+    if (extent > fsp::kMaxElems) return fail(FSP_EINVAL, "fsp_plan_layout: model too large");
   }
   return FSP_OK;
 }
 
 // FSDP2 Shard(0) over n_shard ranks, repeated for n_rep replica groups.
 void build_fsdp2(fsp_plan* p, const std::vector<int64_t>& rows, const std::vector<int64_t>& cols,
-                 const std::vector<int64_t>& start, int32_t n_shard, int32_t n_rep) {
+                 const std::vector<int64_t>& start, int64_t extent, int32_t n_shard, int32_t n_rep) {
   const int32_t n_params = int32_t(rows.size());
-  p->full_len_padded = p->valid_elems;
+  p->full_len_padded = extent;
   // each shard rank's local slot for each (param, rank)
   std::vector<int64_t> local(size_t(n_params) * n_shard);
   int64_t widest = 0;
@@ -166,10 +171,10 @@ void build_tiles(fsp_plan* p) {
 }
 
 fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params, int32_t n_rep, int32_t n_shard,
-                     int32_t mode, fsp_plan** out) {
+                     int32_t mode, int32_t param_align, fsp_plan** out) {
   std::vector<int64_t> rows, cols, start;
-  int64_t total = 0;
-  fsp_status st = parse_shapes(dims, ndims, n_params, rows, cols, start, total);
+  int64_t total = 0, extent = 0;
+  fsp_status st = parse_shapes(dims, ndims, n_params, param_align, rows, cols, start, total, extent);
   if (st != FSP_OK) return st;
   fsp_plan* p = new (std::nothrow) fsp_plan();
   if (!p) return fail(FSP_ENOMEM, "fsp_plan_layout: host allocation failed");
@@ -180,6 +185,10 @@ fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params
     p->n_params = n_params;
     p->mode = mode;
     p->valid_elems = total;
+    p->param_align = param_align;
+    p->param_off = start;
+    p->param_numel.resize(size_t(n_params));
+    for (int32_t i = 0; i < n_params; ++i) p->param_numel[size_t(i)] = rows[size_t(i)] * cols[size_t(i)];
     if (mode == FSP_MODE_DISTOPT_FLAT) {
       const int32_t n_d = n_shard;
       const int64_t unit = int64_t(n_d) / fsp::gcd64(n_d, fsp::kDistOptAlign) * fsp::kDistOptAlign;
@@ -198,7 +207,7 @@ fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params
         p->segments.push_back(s);
       }
     } else {
-      build_fsdp2(p, rows, cols, start, n_shard, n_rep);
+      build_fsdp2(p, rows, cols, start, extent, n_shard, n_rep);
     }
     build_tiles(p);
   } catch (const std::bad_alloc&) {
@@ -219,7 +228,7 @@ extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims,
   if (n_d < 1 || n_d > fsp::kMaxRanks) return fail(FSP_EINVAL, "fsp_plan_layout: n_d must be in [1, 64]");
   if (mode != FSP_MODE_FSDP2_SHARD0 && mode != FSP_MODE_DISTOPT_FLAT)
     return fail(FSP_EINVAL, "fsp_plan_layout: unknown mode");
-  return make_plan(dims, ndims, n_params, 1, n_d, mode, out);
+  return make_plan(dims, ndims, n_params, 1, n_d, mode, 1, out);
 }
 
 extern "C" fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* ndims, int32_t n_params,
@@ -229,7 +238,27 @@ extern "C" fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* n
   *out = nullptr;
   if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
     return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: need n_replicate, n_shard >= 1 and their product <= 64");
-  return make_plan(dims, ndims, n_params, n_replicate, n_shard, FSP_MODE_HSDP, out);
+  return make_plan(dims, ndims, n_params, n_replicate, n_shard, FSP_MODE_HSDP, 1, out);
+}
+
+extern "C" fsp_status fsp_plan_layout_params(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                                             int32_t n_replicate, int32_t n_shard, fsp_plan** out) {
+  fsp::clear_error();
+  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_params: out is NULL");
+  *out = nullptr;
+  if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
+    return fail(FSP_EINVAL, "fsp_plan_layout_params: need n_replicate, n_shard >= 1 and their product <= 64");
+  return make_plan(dims, ndims, n_params, n_replicate, n_shard,
+                   n_replicate == 1 ? FSP_MODE_FSDP2_SHARD0 : FSP_MODE_HSDP, int32_t(fsp::kParamAlign), out);
+}
+
+extern "C" fsp_status fsp_plan_param(const fsp_plan* p, int32_t i, int64_t* full_off, int64_t* numel) {
+  fsp::clear_error();
+  if (!p || !full_off || !numel) return fail(FSP_EINVAL, "fsp_plan_param: NULL argument");
+  if (i < 0 || i >= p->n_params) return fail(FSP_EINVAL, "fsp_plan_param: index out of range");
+  *full_off = p->param_off[size_t(i)];
+  *numel = p->param_numel[size_t(i)];
+  return FSP_OK;
 }
 
 extern "C" fsp_status fsp_plan_info_get(const fsp_plan* p, fsp_plan_info* out) {
@@ -247,6 +276,8 @@ extern "C" fsp_status fsp_plan_info_get(const fsp_plan* p, fsp_plan_info* out) {
   out->n_tiles = int64_t(p->tiles.size());
   out->n_replicate = p->n_rep;
   out->n_shard = p->n_shard;
+  out->param_align = p->param_align;
+  out->reserved = 0;
   return FSP_OK;
 }
 

@@ -276,6 +276,15 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned 
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
 
+fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step) {
+  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
+  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
+  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
+      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
+    return fail(FSP_EINVAL, "hyper-parameters out of range");
+  return FSP_OK;
+}
+
 // Host-side checks shared by the device-buffer entry points: arguments,
 // hyper-parameters, NULL / alignment / overlap of every buffer (the step's and
 // `extra`), and - for a non-empty plan - that each lies in a live allocation.
@@ -284,12 +293,8 @@ fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_
                              const std::vector<Buf>& extra) {
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!grads) return fail(FSP_EINVAL, "grad_bufs is NULL");   // param_bufs NULL: no all-gather
-  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
-  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
-  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
-      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
-    return fail(FSP_EINVAL, "hyper-parameters out of range");
+  if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
 
   const int n = p->n_d;
   const size_t gsize = dtype == FSP_DTYPE_F32 ? 4 : 2;
@@ -554,12 +559,8 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
   clear_error();
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
-  if (!hp) return fail(FSP_EINVAL, "hparams is NULL");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
-  if (step < 1) return fail(FSP_EINVAL, "step must be >= 1 (1-based update index)");
-  if (!finite_nonneg(hp->lr) || !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
-      !finite_nonneg(hp->beta1) || !finite_nonneg(hp->beta2) || !(hp->beta1 < 1.f) || !(hp->beta2 < 1.f))
-    return fail(FSP_EINVAL, "hyper-parameters out of range");
+  if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
   if (int64_t(p->tiles.size()) > kNoAllocMaxTiles)
     return fail(FSP_EUNSUPPORTED, "plan needs " + std::to_string(p->tiles.size()) +
                                       " work tiles; fsp_sharded_step_noalloc holds at most 262144");

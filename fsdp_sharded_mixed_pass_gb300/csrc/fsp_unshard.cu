@@ -32,6 +32,10 @@ constexpr int kUnshardThreads = 256;
 struct UnshardArgs {
   const float* master;
   uint16_t* params[kMaxRanks];
+  // per-parameter plans: entry param * n_d + q is rank q's virtual base for
+  // that parameter (element f at base + f); nullptr for full-size buffers
+  uint16_t* const* vparams;
+  int n_d;
   const Tile* tiles;
   int64_t n_tiles;
   int n_rep;
@@ -66,11 +70,19 @@ static_assert(kTileElems == 2 * 8 * kUnshardThreads, "unshard covers a tile in o
 // alternate, so replica r + 1 is cast while r's stores drain.
 __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_constant__ UnshardArgs a) {
   __shared__ __align__(128) uint16_t cast[2][kTileElems];
+  __shared__ uint16_t* tile_pb[kMaxRanks];
   const int ns = a.n_shard, nr = a.n_rep;
   const int i0 = threadIdx.x, i1 = threadIdx.x + kUnshardThreads;
+  const bool per_param = a.vparams != nullptr;
   int buf = 0;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
+    if (per_param) {
+      __syncthreads();   // the previous tile's bases are no longer read
+      if (threadIdx.x < a.n_d) tile_pb[threadIdx.x] = a.vparams[int64_t(tile.param) * a.n_d + threadIdx.x];
+      __syncthreads();
+    }
+    uint16_t* const* pb = per_param ? tile_pb : a.params;
     const int64_t f0 = tile.full_begin, end = f0 + tile.len;
     const int64_t delta = tile.state_begin - tile.full_begin;
     // aligned body [b0, b1): 8-element (16-byte bf16) boundaries of the full index
@@ -97,7 +109,7 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
         fence_async_smem();   // the casts -> visible to the bulk stores
         __syncthreads();
         if (threadIdx.x == 0) {
-          for (int j = 0; j < ns; ++j) bulk_store(a.params[r * ns + j] + b0, cast[buf], uint32_t(groups) * 16u);
+          for (int j = 0; j < ns; ++j) bulk_store(pb[r * ns + j] + b0, cast[buf], uint32_t(groups) * 16u);
           bulk_commit();
         }
         buf ^= 1;
@@ -109,7 +121,7 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
       const int64_t f = threadIdx.x < n_head ? f0 + threadIdx.x : b1 + (threadIdx.x - n_head);
       for (int r = 0; r < nr; ++r) {
         const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(a.master[f + delta + r * a.rep_stride]));
-        for (int j = 0; j < ns; ++j) a.params[r * ns + j][f] = b;
+        for (int j = 0; j < ns; ++j) pb[r * ns + j][f] = b;
       }
     }
   }
@@ -151,6 +163,7 @@ fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* para
   if (s != FSP_OK) return s;
   UnshardArgs a{};
   a.master = master;
+  a.n_d = p->n_d;
   for (int q = 0; q < p->n_d; ++q) a.params[q] = static_cast<uint16_t*>(params[q]);
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
@@ -165,10 +178,47 @@ fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* para
   return FSP_OK;
 }
 
+fsp_status run_unshard_params(const fsp_plan* p, const fsp_param_table* t, const float* master, void* stream) {
+  clear_error();
+  if (!p || !t) return fail(FSP_EINVAL, "plan or table is NULL");
+  if (t->plan != p) return fail(FSP_EINVAL, "the table was created for another plan");
+  if (!t->vparams) return fail(FSP_EINVAL, "the table has no param tensors");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  if (dev != t->device) return fail(FSP_EINVAL, "the table was created on another device");
+  const size_t sbytes = size_t(p->state_len_total) * 4;
+  if (!master && sbytes) return fail(FSP_EINVAL, "master is NULL");
+  if (reinterpret_cast<uintptr_t>(master) % 16 != 0) return fail(FSP_EINVAL, "master is not 16-byte aligned");
+  if (p->tiles.empty()) return FSP_OK;
+  fsp_status s = check_allocation(master, sbytes, "master");
+  if (s != FSP_OK) return s;
+  const Tile* tiles = nullptr;
+  s = device_tiles(p, &tiles);
+  if (s != FSP_OK) return s;
+  UnshardArgs a{};
+  a.master = master;
+  a.vparams = t->vparams;
+  a.n_d = p->n_d;
+  a.tiles = tiles;
+  a.n_tiles = int64_t(p->tiles.size());
+  a.n_rep = p->n_rep;
+  a.n_shard = p->n_shard;
+  a.rep_stride = p->n_rep > 1 ? p->rep_stride : 0;
+  e = launch_unshard(a, int(std::min<int64_t>(INT32_MAX, a.n_tiles)), stream);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("unshard kernel launch", e));
+  return FSP_OK;
+}
+
 }  // namespace
 }  // namespace fsp
 
 extern "C" fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs,
                                   void* cuda_stream) {
   return fsp::run_unshard(plan, master, param_bufs, cuda_stream);
+}
+
+extern "C" fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,
+                                         void* cuda_stream) {
+  return fsp::run_unshard_params(plan, table, master, cuda_stream);
 }

@@ -18,8 +18,11 @@ MODES = {"fsdp2": 0, "distopt": 1, "hsdp": 2}
 DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
-EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
-           "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug", "fsp_host_step_workspace_bytes", "fsp_sharded_step_host",
+EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
+           "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
+           "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
+           "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
+           "fsp_sharded_step_params", "fsp_unshard_params",
            "fsp_sharded_step_noalloc", "fsp_unshard", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
 
@@ -35,7 +38,8 @@ class _PlanInfo(ctypes.Structure):
                 ("tile_elems", ctypes.c_int32), ("valid_elems", ctypes.c_int64),
                 ("full_len_padded", ctypes.c_int64), ("state_len_per_rank", ctypes.c_int64),
                 ("state_len_total", ctypes.c_int64), ("n_segments", ctypes.c_int64), ("n_tiles", ctypes.c_int64),
-                ("n_replicate", ctypes.c_int32), ("n_shard", ctypes.c_int32)]
+                ("n_replicate", ctypes.c_int32), ("n_shard", ctypes.c_int32), ("param_align", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class _Segment(ctypes.Structure):
@@ -69,6 +73,14 @@ def lib():
                                   ctypes.POINTER(vp)]
     L.fsp_plan_layout_hsdp.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32,
                                        i32, ctypes.POINTER(vp)]
+    L.fsp_plan_layout_params.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32,
+                                         i32, ctypes.POINTER(vp)]
+    L.fsp_plan_param.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+    L.fsp_param_table_create.argtypes = [vp, ctypes.POINTER(vp), i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.fsp_param_table_destroy.argtypes = [vp]
+    L.fsp_param_table_destroy.restype = None
+    L.fsp_sharded_step_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, vp]
+    L.fsp_unshard_params.argtypes = [vp, vp, vp, vp]
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
     L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
@@ -84,8 +96,9 @@ def lib():
     L.fsp_sharded_step_device_t.restype = ctypes.c_int
     L.fsp_unshard.argtypes = [vp, vp, ctypes.POINTER(vp), vp]
     L.fsp_unshard.restype = ctypes.c_int
-    for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step",
-               "fsp_sharded_step_debug", "fsp_sharded_step_noalloc"):
+    for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param",
+               "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
+               "fsp_sharded_step_noalloc", "fsp_param_table_create", "fsp_sharded_step_params", "fsp_unshard_params"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
     L.fsp_host_step_workspace_bytes.restype = ctypes.c_int
@@ -139,7 +152,9 @@ class Plan:
         self.n_tiles = info.n_tiles
         self.n_replicate = info.n_replicate
         self.n_shard = info.n_shard
+        self.param_align = info.param_align
         self._segments = None
+        self._param_offsets = None
 
     @property
     def handle(self):
@@ -154,6 +169,18 @@ class Plan:
                 out.append(Segment(seg.param, seg.rank, seg.full_off, seg.state_off, seg.len, seg.padded_len))
             self._segments = tuple(out)
         return self._segments
+
+    @property
+    def param_offsets(self) -> tuple:
+        """Each parameter's first full index (virtual for per-parameter plans)."""
+        if self._param_offsets is None:
+            off, n = ctypes.c_int64(), ctypes.c_int64()
+            out = []
+            for i in range(self.n_params):
+                _check(lib().fsp_plan_param(self._h, i, ctypes.byref(off), ctypes.byref(n)), "fsp_plan_param")
+                out.append(off.value)
+            self._param_offsets = tuple(out)
+        return self._param_offsets
 
     def ledger(self, grad_dtype: str = "f32") -> dict:
         led = _Ledger()
@@ -192,6 +219,76 @@ def plan_layout(shapes, n_d: int, mode: str = "fsdp2", n_replicate: int = 1) -> 
         _check(lib().fsp_plan_layout(dims_arr, nd_arr, len(shapes), int(n_d), MODES[mode], ctypes.byref(out)),
                "fsp_plan_layout")
     return Plan(out.value, shapes, mode)
+
+
+def plan_layout_params(shapes, n_d: int, n_replicate: int = 1) -> Plan:
+    """Per-parameter plan (``fsp_plan_layout_params``): FSDP2 over ``n_d``
+    ranks, or HSDP with ``n_replicate`` groups of ``n_d // n_replicate``; the
+    step then reads and writes each rank's per-parameter tensors in place."""
+    shapes = [tuple(int(d) for d in s) for s in shapes]
+    dims = [d for s in shapes for d in s]
+    nd = [len(s) for s in shapes]
+    dims_arr = (ctypes.c_int64 * max(1, len(dims)))(*dims)
+    nd_arr = (ctypes.c_int32 * max(1, len(nd)))(*nd)
+    if n_replicate < 1 or n_d % n_replicate:
+        raise ValueError("n_d must be a multiple of n_replicate")
+    out = ctypes.c_void_p()
+    _check(lib().fsp_plan_layout_params(dims_arr, nd_arr, len(shapes), int(n_replicate), int(n_d // n_replicate),
+                                        ctypes.byref(out)), "fsp_plan_layout_params")
+    return Plan(out.value, shapes, "fsdp2" if n_replicate == 1 else "hsdp")
+
+
+class ParamTable:
+    """Per-parameter tensors registered for a per-parameter plan
+    (``fsp_param_table_create``): ``grads[q][i]`` is rank q's gradient of
+    parameter i, ``params[q][i]`` its bf16 parameter tensor (or ``params=None``).
+    Keeps references to the tensors so they outlive the table."""
+
+    def __init__(self, plan: Plan, grads, params=None, grad_dtype: str | None = None):
+        if len(grads) != plan.n_d or any(len(g) != plan.n_params for g in grads):
+            raise ValueError(f"need {plan.n_d} x {plan.n_params} gradient tensors")
+        if params is not None and (len(params) != plan.n_d or any(len(x) != plan.n_params for x in params)):
+            raise ValueError(f"need {plan.n_d} x {plan.n_params} param tensors")
+        gd = grad_dtype or (_grad_dtype([grads[0][0]], None) if plan.n_params else "f32")
+        self.plan, self.grad_dtype = plan, gd
+        self._refs = (grads, params)
+        n = plan.n_d * plan.n_params
+        g = (ctypes.c_void_p * max(1, n))(*[_ptr(x) for row in grads for x in row])
+        p = None if params is None else (ctypes.c_void_p * max(1, n))(*[_ptr(x) for row in params for x in row])
+        out = ctypes.c_void_p()
+        _check(lib().fsp_param_table_create(plan.handle, g, DTYPES[gd], p, ctypes.byref(out)),
+               "fsp_param_table_create")
+        self._h = out
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            lib().fsp_param_table_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def sharded_step_params(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_sq, hparams: dict, step: int,
+                        stream=None) -> None:
+    """The fused step on the per-parameter tensors of ``table`` (asynchronous)."""
+    _check(lib().fsp_sharded_step_params(plan.handle, table.handle, ctypes.c_void_p(_ptr(master)),
+                                         ctypes.c_void_p(_ptr(exp_avg)), ctypes.c_void_p(_ptr(exp_avg_sq)),
+                                         ctypes.byref(_hp(hparams)), int(step),
+                                         ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_params")
+
+
+def unshard_params(plan: Plan, table: ParamTable, master, stream=None) -> None:
+    """FSDP2 unshard into the per-parameter bf16 tensors of ``table``."""
+    _check(lib().fsp_unshard_params(plan.handle, table.handle, ctypes.c_void_p(_ptr(master)),
+                                    ctypes.c_void_p(_stream_handle(stream))), "fsp_unshard_params")
 
 
 def _ptr(x) -> int:

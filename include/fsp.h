@@ -116,6 +116,8 @@ typedef struct {
   int64_t n_tiles;
   int32_t n_replicate;          /* N_r: HSDP replica groups (1 otherwise)            */
   int32_t n_shard;              /* N_s: ranks per shard group (n_d otherwise)         */
+  int32_t param_align;          /* 16: per-parameter plan (fsp_plan_layout_params); 1 */
+  int32_t reserved;
 } fsp_plan_info;
 
 /* One contiguous run of a rank's shard.  Elements [full_off, full_off + len)
@@ -167,6 +169,26 @@ fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_
  * n_shard-rank FSDP2 state (state_len_total covers all of them). */
 fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* ndims, int32_t n_params,
                                 int32_t n_replicate, int32_t n_shard, fsp_plan** out);
+
+/* Per-parameter plan: FSDP2 (n_replicate == 1) or HSDP over n_replicate groups
+ * of n_shard ranks, for steps that read each rank's gradient of each
+ * parameter from a tensor of its own and write its bf16 parameter into a
+ * tensor of its own - FSDP2's per-parameter tensors, whose copy-in before the
+ * reduce-scatter and copy-out after the all-gather the step then does in
+ * place ("Parallelism strategies: which state to shard", section 二.5).
+ * Parameter i occupies [full_off_i, full_off_i + numel_i) of a virtual full
+ * index, full_off_i being the previous parameter's end rounded up to a
+ * multiple of 16 (fsp_plan_param); shards, segments, state placement and
+ * tiles follow from that index exactly as for fsp_plan_layout /
+ * fsp_plan_layout_hsdp (full_len_padded is the index's extent; the gaps belong
+ * to no rank).  Use with fsp_param_table_create, fsp_sharded_step_params and
+ * fsp_unshard_params. */
+fsp_status fsp_plan_layout_params(const int64_t* dims, const int32_t* ndims, int32_t n_params,
+                                  int32_t n_replicate, int32_t n_shard, fsp_plan** out);
+
+/* Parameter i's first full (virtual, for per-parameter plans) index and its
+ * number of elements (0 <= i < n_params). */
+fsp_status fsp_plan_param(const fsp_plan* plan, int32_t i, int64_t* full_off, int64_t* numel);
 
 fsp_status fsp_plan_info_get(const fsp_plan* plan, fsp_plan_info* out);
 
@@ -284,6 +306,48 @@ fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_g
                                  float* master, float* exp_avg, float* exp_avg_sq, void* const* host_params,
                                  const fsp_adamw_hparams* hp, int64_t step, void* workspace,
                                  size_t workspace_bytes, int64_t chunk_elems, void* cuda_stream);
+
+/* The per-parameter tensors of a per-parameter plan, registered once on the
+ * current device (the library uploads a table of their addresses; steps read
+ * and write the tensors through it until it is destroyed).
+ *   grad_ptrs:  host array of n_d * n_params device pointers; entry
+ *               q * n_params + i is rank q's gradient of parameter i
+ *               (numel_i elements of grad_dtype, the unsharded gradient), only
+ *               read by the step.
+ *   param_ptrs: host array of n_d * n_params device pointers to bf16 tensors
+ *               of numel_i elements (rank q's unsharded parameter i), written
+ *               by the step's all-gather and by fsp_unshard_params; NULL for a
+ *               table that only reduces (steps then leave the parameters
+ *               sharded, as fsp_sharded_step with param_bufs = NULL).
+ * Every pointer must be 16-byte aligned and lie in a live allocation holding
+ * its tensor (NULL only for a parameter with 0 elements); no two tensors may
+ * overlap.  The plan must come from fsp_plan_layout_params and outlive the
+ * table.  Synchronous (allocates and uploads); free with
+ * fsp_param_table_destroy. */
+typedef struct fsp_param_table fsp_param_table;
+fsp_status fsp_param_table_create(const fsp_plan* plan, const void* const* grad_ptrs, int32_t grad_dtype,
+                                  void* const* param_ptrs, fsp_param_table** out);
+
+/* Frees the table (its device memory); NULL is a no-op.  Must not race with a
+ * call or an in-flight step that uses it. */
+void fsp_param_table_destroy(fsp_param_table* table);
+
+/* fsp_sharded_step on the tensors of `table` (a table of this plan, created on
+ * the current device): the reduce-scatter reads every rank's per-parameter
+ * gradient tensors in place and the all-gather writes every rank's
+ * per-parameter bf16 tensors (none when the table has no param tensors).
+ * master / exp_avg / exp_avg_sq and every other rule as fsp_sharded_step;
+ * the results are those of fsp_sharded_step on full-size buffers holding the
+ * same values at the plan's full indices (the same kernels: the rank bases of
+ * each tile come from the table). */
+fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
+                                   float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp, int64_t step,
+                                   void* cuda_stream);
+
+/* fsp_unshard into the per-parameter bf16 tensors of `table` (which must have
+ * them). */
+fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,
+                              void* cuda_stream);
 
 /* fsp_sharded_step for callers that cannot allocate device memory (a
  * framework's allocator owns the device, a fixed memory pool must not grow,

@@ -271,3 +271,71 @@ def test_build_is_free_of_compiler_warnings():
         pytest.skip("library built without a log")
     text = open(log).read()
     assert "warning" not in text.lower(), [l for l in text.splitlines() if "warning" in l.lower()][:5]
+
+
+# ---- per-parameter plans and tensor tables ---------------------------------------
+
+@pytest.mark.parametrize("n_rep,n_shard", [(1, 1), (1, 3), (1, 8), (2, 2), (2, 4), (1, 16)])
+def test_per_param_planner_matches_oracle(n_rep, n_shard):
+    rng = np.random.default_rng(n_rep * 17 + n_shard)
+    shapes = [tuple([int(rng.integers(0, 3 * n_shard + 40))] + [int(rng.choice([1, 3, 7, 64]))
+                                                                 for _ in range(int(rng.integers(0, 3)))])
+              for _ in range(int(rng.integers(1, 30)))]
+    n_d = n_rep * n_shard
+    lib_plan = fsp.plan_layout_params(shapes, n_d, n_replicate=n_rep)
+    o = OP.plan_layout(shapes, n_d, "hsdp" if n_rep > 1 else "fsdp2", n_rep=n_rep, param_align=16)
+    _compare_plans(lib_plan, o)
+    assert lib_plan.param_offsets == o.param_offsets
+    assert lib_plan.param_align == 16
+    assert fsp.plan_layout(shapes, n_d, "fsdp2").param_align == 1
+
+
+def test_per_param_worked_example_through_the_abi():
+    p = fsp.plan_layout_params([(3,), (5, 2), (17,)], 2)
+    assert p.param_offsets == (0, 16, 32) and (p.valid_elems, p.full_len_padded) == (30, 49)
+    assert sorted((s.param, s.rank, s.full_off, s.state_off, s.length) for s in p.segments) == [
+        (0, 0, 0, 0, 2), (0, 1, 2, 50, 1), (1, 0, 16, 16, 6), (1, 1, 22, 54, 4), (2, 0, 32, 32, 9), (2, 1, 41, 73, 8)]
+
+
+def test_param_table_rejects_on_host():
+    L = B.lib()
+    flat = fsp.plan_layout([(64, 8), (5,)], 2)
+    pp = fsp.plan_layout_params([(64, 8), (5,)], 2)
+    base = 1 << 40
+
+    def ptrs(plan, shift=0, stride=1 << 20, nulls=()):
+        vals = [0 if k in nulls else base + k * stride + shift for k in range(plan.n_d * plan.n_params)]
+        return (ctypes.c_void_p * len(vals))(*vals)
+
+    out = ctypes.c_void_p()
+    st = L.fsp_param_table_create(flat.handle, ptrs(flat), 0, None, ctypes.byref(out))
+    assert st == B.FSP_EINVAL and "per-parameter" in L.fsp_last_error().decode()
+    assert L.fsp_param_table_create(pp.handle, None, 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp), 7, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, shift=4), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert "aligned" in L.fsp_last_error().decode()
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, nulls=(1,)), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    # 64 x 8 fp32 = 2 KiB tensors 1 KiB apart overlap
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, stride=1024), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert "overlaps" in L.fsp_last_error().decode()
+    # a param tensor on top of a grad tensor
+    g = ptrs(pp)
+    prm = (ctypes.c_void_p * 4)(*[g[k] for k in range(4)])
+    assert L.fsp_param_table_create(pp.handle, g, 0, prm, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, g, 0, None, None) == B.FSP_EINVAL
+    assert L.fsp_sharded_step_params(None, None, None, None, None, None, 1, None) == B.FSP_EINVAL
+    assert L.fsp_unshard_params(pp.handle, None, None, None) == B.FSP_EINVAL
+    L.fsp_param_table_destroy(None)
+
+
+def test_per_param_layout_rejects():
+    L = B.lib()
+    d = (ctypes.c_int64 * 1)(4)
+    nd = (ctypes.c_int32 * 1)(1)
+    out = ctypes.c_void_p()
+    for nr, ns in ((0, 4), (2, 0), (8, 9)):
+        assert L.fsp_plan_layout_params(d, nd, 1, nr, ns, ctypes.byref(out)) == B.FSP_EINVAL
+    p = fsp.plan_layout_params([(4,)], 2)
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    assert L.fsp_plan_param(p.handle, 1, ctypes.byref(a), ctypes.byref(b)) == B.FSP_EINVAL
+    assert L.fsp_plan_param(p.handle, 0, ctypes.byref(a), ctypes.byref(b)) == B.FSP_OK and (a.value, b.value) == (0, 4)
