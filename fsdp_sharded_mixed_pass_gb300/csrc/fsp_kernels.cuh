@@ -549,14 +549,20 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         if (len > 0) {
           unsigned char* st = stages + stage * Cfg::kStageBytes;
           mbar_arrive_expect_tx(bar, uint32_t(len) * uint32_t(NG * G + NR * 12));
+          // (separate paths, so that full-size buffers read their bases straight from the arguments)
           if (kClip) {   // the reduced gradient, from its owner's slice
             const void* own = per_param ? gb[tile.rank] : a.grads[tile.rank];
             bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(own) + c * G, len * G, bar);
+          } else if (per_param) {
+#pragma unroll
+            for (int q = 0; q < N; ++q)
+              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(gb[q]) + c * G,
+                        len * G, bar);
           } else {
 #pragma unroll
             for (int q = 0; q < N; ++q)
-              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G),
-                        static_cast<const unsigned char*>(per_param ? gb[q] : a.grads[q]) + c * G, len * G, bar);
+              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+                        len * G, bar);
           }
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
@@ -603,7 +609,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
       if (h.len > 0) {
         const uint32_t len = uint32_t(h.len);
         unsigned char* st = stages + stage * Cfg::kStageBytes;
-        uint16_t* const* pb = per_param ? stage_pb(stage) : a.params;
+        uint16_t* const* spb = stage_pb(stage);
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const uint32_t th_s = smem_addr(st + Cfg::kStateOff + r * 3 * E * 4);
@@ -612,9 +618,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.master + s, th_s, len * 4);
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
-          if (a.gather) {
+          if (a.gather && per_param) {   // the all-gather
 #pragma unroll
-            for (int j = 0; j < NS; ++j) bulk_store(pb[r * NS + j] + h.c, p_s, len * 2);   // the all-gather
+            for (int j = 0; j < NS; ++j) bulk_store(spb[r * NS + j] + h.c, p_s, len * 2);
+          } else if (a.gather) {
+#pragma unroll
+            for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + h.c, p_s, len * 2);
           }
         }
         bulk_commit();
