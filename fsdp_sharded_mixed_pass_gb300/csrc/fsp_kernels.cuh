@@ -17,20 +17,25 @@
 //  * sharded_step_kernel<NS, NR, GradT, kClip> (N_d = NS x NR known at compile
 //    time; NR > 1 is HSDP: NR replica groups of NS shard ranks, each group with
 //    its own copy of the fp32 state): one CTA per SM, warp-specialised.  A
-//    producer thread streams every chunk of up to E aligned elements of the
-//    N_d gradient slices and the NR x 3 state slices into a ring of S
-//    shared-memory stages with 1-D bulk asynchronous copies (cp.async.bulk,
-//    completion counted on an mbarrier); eight consumer warps fold, update and
-//    cast from shared memory, leaving the new master/m/v in place and one bf16
+//    producer thread takes tiles in order from the launch's counter (or with
+//    a fixed stride on small plans) and streams every chunk of up to E
+//    aligned elements of the N_d gradient slices and the NR x 3 state slices
+//    into a ring of S shared-memory stages with 1-D bulk asynchronous copies
+//    (cp.async.bulk, completion counted on an mbarrier), each stage with a
+//    header saying what it holds; eight consumer warps fold, update and cast
+//    from shared memory, leaving the new master/m/v in place and one bf16
 //    tile per replica group beside them; a storer thread writes the chunk back
 //    with bulk stores: the state slices and the same bf16 tile to each rank of
 //    the group (the all-gather is N_s bulk copies of one tile).  Segment edges
 //    that are not 16-byte aligned take a scalar path from global memory.
+//    Per-parameter tensors: the producer reads each tile's rank bases from
+//    the registered table and passes them on beside the stage.
 //    kClip: the clipped update of the distributed-optimizer flow - one slice,
 //    the already-reduced gradient in its owner's grad buffer, scaled by the
 //    clip coefficient.
 //  * sharded_step_generic_kernel<GradT, kClip> (any N_d up to 64, any
-//    grouping): the same arithmetic with vectorised per-thread loads/stores.
+//    grouping): the same arithmetic with vectorised per-thread loads/stores,
+//    one CTA per tile.
 //  (Passes 1 and 2 of the clipped flow - the reduce-scatter written back into
 //  the owners' slices, the global norm - are in fsp_norm_kernels.cuh.)
 //  * step_advance_kernel: t += 1 for steps whose update index is in device
