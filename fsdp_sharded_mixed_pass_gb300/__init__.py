@@ -20,6 +20,7 @@ from .fsp import (  # noqa: F401
     selftest_bounded_wait,
     sharded_step,
     sharded_step_clipped,
+    sharded_step_clipped_params,
     sharded_step_debug,
     sharded_step_device_t,
     sharded_step_host,

@@ -277,8 +277,33 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const void* const*
   }
 }
 
+// One tile of the generic kernel with rank bases gb / pb.
+template <typename GradT, bool kClip>
+__device__ __forceinline__ void generic_tile(const StepArgs& a, const Coeffs& cf, const Tile& tile,
+                                             const void* const* gb, uint16_t* const* pb, float coef) {
+  const int64_t f0 = tile.full_begin;
+  const int64_t delta = tile.state_begin - tile.full_begin;
+  const int64_t len = tile.len;
+  // [0, head): before the first multiple of 4; [head, tail): 4-element
+  // groups; [tail, len): the remainder.
+  const int64_t head = min(len, (4 - (f0 & 3)) & 3);
+  const int64_t groups = (len - head) >> 2;
+  const int64_t tail = head + groups * 4;
+  for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+    const int64_t f = f0 + head + 4 * i;
+    step_group<GradT, kClip>(a, gb, pb, cf, f, f + delta, tile.rank, coef);
+  }
+  const int64_t n_scalar = head + (len - tail);
+  if (threadIdx.x < n_scalar) {
+    const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
+    step_one<0, 0, GradT, kClip>(a, gb, pb, cf, f0 + e, f0 + e + delta, tile.rank, coef);
+  }
+}
+
 // Any N_d up to 64 and any replica grouping; full-size buffers or, with
 // a.vgrads set, per-parameter tensors (each tile's bases from the tables).
+// The two cases are separate paths, so that full-size buffers read their
+// bases straight from the argument block.
 template <typename GradT, bool kClip>
 __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(const __grid_constant__ StepArgs a) {
   __shared__ const void* tile_gb[kMaxRanks];
@@ -296,25 +321,9 @@ __global__ void __launch_bounds__(kGenericThreads) sharded_step_generic_kernel(c
         tile_pb[threadIdx.x] = a.vparams ? a.vparams[e] : nullptr;
       }
       __syncthreads();
-    }
-    const void* const* gb = per_param ? tile_gb : a.grads;
-    uint16_t* const* pb = per_param ? tile_pb : a.params;
-    const int64_t f0 = tile.full_begin;
-    const int64_t delta = tile.state_begin - tile.full_begin;
-    const int64_t len = tile.len;
-    // [0, head): before the first multiple of 4; [head, tail): 4-element
-    // groups; [tail, len): the remainder.
-    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
-    const int64_t groups = (len - head) >> 2;
-    const int64_t tail = head + groups * 4;
-    for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
-      const int64_t f = f0 + head + 4 * i;
-      step_group<GradT, kClip>(a, gb, pb, cf, f, f + delta, tile.rank, coef);
-    }
-    const int64_t n_scalar = head + (len - tail);
-    if (threadIdx.x < n_scalar) {
-      const int64_t e = threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head);
-      step_one<0, 0, GradT, kClip>(a, gb, pb, cf, f0 + e, f0 + e + delta, tile.rank, coef);
+      generic_tile<GradT, kClip>(a, cf, tile, tile_gb, tile_pb, coef);
+    } else {
+      generic_tile<GradT, kClip>(a, cf, tile, a.grads, a.params, coef);
     }
   }
 }

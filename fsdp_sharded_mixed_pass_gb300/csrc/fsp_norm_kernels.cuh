@@ -42,47 +42,64 @@ struct SumSq2 {
 };
 
 // Every element's averaged gradient (rank-ordered fp32 fold / N_d) is written
-// into its owner's slice of that rank's own grad buffer (fp32), and each CTA
+// into its owner's slice of that rank's own grad buffer (fp32; per-parameter
+// tensors: of the owner's tensor, bases from the registered table), and each CTA
 // leaves the sum of squares of the elements it reduced in partials[cta]: each
 // thread's in SumSq2, the CTA's threads added in fp64 in a fixed order.
 // Launched with one CTA per tile: one partial per tile, a grouping fixed by the
 // plan alone.  One replica group (FSDP2 / DistOpt).  NT > 0: N_d fixed; 0: a.n_d.
+// One tile of pass 1 with rank bases gb.
+template <int NT>
+__device__ __forceinline__ void rs_writeback_tile(const StepArgs& a, const Tile& tile, const void* const* gb,
+                                                  SumSq2& sq) {
+  const int n = NT > 0 ? NT : a.n_d;
+  const int64_t f0 = tile.full_begin, len = tile.len;
+  float* own = static_cast<float*>(const_cast<void*>(gb[tile.rank]));
+  const int64_t head = min(len, (4 - (f0 & 3)) & 3);
+  const int64_t groups = (len - head) >> 2;
+  const int64_t tail = head + groups * 4;
+  for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+    const int64_t f = f0 + head + 4 * i;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(NT > 0 ? NT : 1)
+    for (int q = 0; q < n; ++q) add4(acc, GradIO<float>::load4(gb[q], f));
+    acc.x = acc.x / float(n);
+    acc.y = acc.y / float(n);
+    acc.z = acc.z / float(n);
+    acc.w = acc.w / float(n);
+    *reinterpret_cast<float4*>(own + f) = acc;
+    sq.add(acc.x);
+    sq.add(acc.y);
+    sq.add(acc.z);
+    sq.add(acc.w);
+  }
+  const int64_t n_scalar = head + (len - tail);
+  if (threadIdx.x < n_scalar) {
+    const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
+    float acc = 0.f;
+#pragma unroll(NT > 0 ? NT : 1)
+    for (int q = 0; q < n; ++q) acc += GradIO<float>::load1(gb[q], f);
+    acc = acc / float(n);
+    own[f] = acc;
+    sq.add(acc);
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kGenericThreads) rs_writeback_norm_kernel(const __grid_constant__ StepArgs a,
                                                                             double* partials) {
-  const int n = NT > 0 ? NT : a.n_d;
+  __shared__ const void* tile_gb[kMaxRanks];
+  const bool per_param = a.vgrads != nullptr;
   SumSq2 sq;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
-    const int64_t f0 = tile.full_begin, len = tile.len;
-    float* own = static_cast<float*>(const_cast<void*>(a.grads[tile.rank]));
-    const int64_t head = min(len, (4 - (f0 & 3)) & 3);
-    const int64_t groups = (len - head) >> 2;
-    const int64_t tail = head + groups * 4;
-    for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
-      const int64_t f = f0 + head + 4 * i;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll(NT > 0 ? NT : 1)
-      for (int q = 0; q < n; ++q) add4(acc, GradIO<float>::load4(a.grads[q], f));
-      acc.x = acc.x / float(n);
-      acc.y = acc.y / float(n);
-      acc.z = acc.z / float(n);
-      acc.w = acc.w / float(n);
-      *reinterpret_cast<float4*>(own + f) = acc;
-      sq.add(acc.x);
-      sq.add(acc.y);
-      sq.add(acc.z);
-      sq.add(acc.w);
-    }
-    const int64_t n_scalar = head + (len - tail);
-    if (threadIdx.x < n_scalar) {
-      const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
-      float acc = 0.f;
-#pragma unroll(NT > 0 ? NT : 1)
-      for (int q = 0; q < n; ++q) acc += GradIO<float>::load1(a.grads[q], f);
-      acc = acc / float(n);
-      own[f] = acc;
-      sq.add(acc);
+    if (per_param) {   // this tile's rank bases from the registered table
+      __syncthreads();
+      if (threadIdx.x < a.n_d) tile_gb[threadIdx.x] = a.vgrads[int64_t(tile.param) * a.n_d + threadIdx.x];
+      __syncthreads();
+      rs_writeback_tile<NT>(a, tile, tile_gb, sq);
+    } else {
+      rs_writeback_tile<NT>(a, tile, a.grads, sq);
     }
   }
   // CTA sum in a fixed order: warp shuffles, then warp 0 over the warp sums

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <new>
 #include <string>
 #include <utility>
@@ -126,9 +127,10 @@ bool overlaps_table(const fsp_param_table* t, const void* ptr, size_t bytes) {
   return it != t->spans.begin() && std::prev(it)->second > b;
 }
 
-fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
-                           const fsp_adamw_hparams* hp, int64_t step, void* stream) {
-  clear_error();
+// Checks shared by the per-parameter steps: plan / table / device, hp and t,
+// and the state buffers (and `extra`) against each other and the tensors.
+fsp_status check_params_step(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                             const fsp_adamw_hparams* hp, int64_t step, const std::vector<Buf>& extra) {
   if (!p || !t) return fail(FSP_EINVAL, "plan or table is NULL");
   if (t->plan != p) return fail(FSP_EINVAL, "the table was created for another plan");
   int dev = 0;
@@ -137,38 +139,73 @@ fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* m
   if (dev != t->device) return fail(FSP_EINVAL, "the table was created on another device");
   if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
   const size_t sbytes = size_t(p->state_len_total) * 4;
-  const Buf state[3] = {{master, sbytes, "master"}, {m, sbytes, "exp_avg"}, {v, sbytes, "exp_avg_sq"}};
-  for (const Buf& b : state) {
+  std::vector<Buf> bufs{{master, sbytes, "master"}, {m, sbytes, "exp_avg"}, {v, sbytes, "exp_avg_sq"}};
+  for (const Buf& b : extra) bufs.push_back(b);
+  for (const Buf& b : bufs) {
     if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
     if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
     if (overlaps_table(t, b.ptr, b.bytes)) return fail(FSP_EINVAL, b.name + " overlaps a registered tensor");
   }
-  for (int i = 0; i < 3; ++i)
-    for (int j = i + 1; j < 3; ++j) {
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(state[i].ptr), b0 = reinterpret_cast<uintptr_t>(state[j].ptr);
-      if (sbytes && a0 < b0 + sbytes && b0 < a0 + sbytes)
-        return fail(FSP_EINVAL, state[i].name + " overlaps " + state[j].name);
+  for (size_t i = 0; i < bufs.size(); ++i)
+    for (size_t j = i + 1; j < bufs.size(); ++j) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(bufs[i].ptr), b0 = reinterpret_cast<uintptr_t>(bufs[j].ptr);
+      if (bufs[i].bytes && bufs[j].bytes && a0 < b0 + bufs[j].bytes && b0 < a0 + bufs[i].bytes)
+        return fail(FSP_EINVAL, bufs[i].name + " overlaps " + bufs[j].name);
     }
   if (p->tiles.empty()) return FSP_OK;
-  for (const Buf& b : state) {
+  for (const Buf& b : bufs) {
     fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
     if (s != FSP_OK) return s;
   }
+  return FSP_OK;
+}
+
+// The argument block of a per-parameter step on the current device.
+fsp_status params_step_args(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                            const fsp_adamw_hparams* hp, int64_t step, StepArgs* a) {
   const Tile* tiles = nullptr;
   fsp_status s = device_tiles(p, &tiles);
   if (s != FSP_OK) return s;
-  StepArgs a{};
-  a.vgrads = t->vgrads;
-  a.vparams = t->vparams;
-  a.gather = t->vparams ? 1 : 0;
-  a.master = master;
-  a.m = m;
-  a.v = v;
-  a.tiles = tiles;
-  a.n_tiles = int64_t(p->tiles.size());
-  set_mesh(a, p);
-  set_coeffs(a, hp, step);
+  *a = StepArgs{};
+  a->vgrads = t->vgrads;
+  a->vparams = t->vparams;
+  a->gather = t->vparams ? 1 : 0;
+  a->master = master;
+  a->m = m;
+  a->v = v;
+  a->tiles = tiles;
+  a->n_tiles = int64_t(p->tiles.size());
+  set_mesh(*a, p);
+  set_coeffs(*a, hp, step);
+  return FSP_OK;
+}
+
+fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                           const fsp_adamw_hparams* hp, int64_t step, void* stream) {
+  clear_error();
+  fsp_status s = check_params_step(p, t, master, m, v, hp, step, {});
+  if (s != FSP_OK || p->tiles.empty()) return s;
+  StepArgs a;
+  s = params_step_args(p, t, master, m, v, hp, step, &a);
+  if (s != FSP_OK) return s;
   return launch(a, t->grad_dtype, stream);
+}
+
+fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                                   const fsp_adamw_hparams* hp, int64_t step, float max_norm, float* norm_out,
+                                   void* stream) {
+  clear_error();
+  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 plans");
+  if (t && t->grad_dtype != FSP_DTYPE_F32)
+    return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 gradient tensors");
+  if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");
+  fsp_status s = check_params_step(p, t, master, m, v, hp, step, {{norm_out, 2 * sizeof(float), "norm_out"}});
+  if (s != FSP_OK) return s;
+  if (p->tiles.empty()) return clipped_empty(norm_out, stream);
+  StepArgs a;
+  s = params_step_args(p, t, master, m, v, hp, step, &a);
+  if (s != FSP_OK) return s;
+  return run_clipped_passes(p, a, max_norm, norm_out, stream);
 }
 
 }  // namespace
@@ -180,6 +217,14 @@ extern "C" fsp_status fsp_param_table_create(const fsp_plan* plan, const void* c
 }
 
 extern "C" void fsp_param_table_destroy(fsp_param_table* table) { fsp::free_table(table); }
+
+extern "C" fsp_status fsp_sharded_step_clipped_params(const fsp_plan* plan, const fsp_param_table* table,
+                                                      float* master, float* exp_avg, float* exp_avg_sq,
+                                                      const fsp_adamw_hparams* hp, int64_t step, float max_norm,
+                                                      float* norm_out, void* cuda_stream) {
+  return fsp::run_step_clipped_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, max_norm, norm_out,
+                                      cuda_stream);
+}
 
 extern "C" fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
                                               float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,

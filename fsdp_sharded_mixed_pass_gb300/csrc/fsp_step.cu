@@ -395,29 +395,11 @@ fsp_status device_partials(const fsp_plan* p, double** out) {
   return FSP_OK;
 }
 
-fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype, float* master, float* m, float* v,
-                            void* const* params, const fsp_adamw_hparams* hp, int64_t step, float max_norm,
-                            float* norm_out, void* stream) {
-  clear_error();
-  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 and DistOpt plans");
-  if (dtype != FSP_DTYPE_F32) return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 grad buffers");
-  if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");
-  std::vector<Buf> extra{{norm_out, 2 * sizeof(float), "norm_out"}};
-  fsp_status s = check_device_step(p, reinterpret_cast<const void* const*>(grads), dtype, master, m, v, params, hp,
-                                   step, extra);
-  if (s != FSP_OK) return s;
-  if (p->tiles.empty()) {   // nothing to reduce: norm 0, coefficient 1
-    const float out[2] = {0.f, 1.f};
-    cudaError_t e = cudaMemcpyAsync(norm_out, out, sizeof(out), cudaMemcpyHostToDevice,
-                                    static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FSP_OK : fail(FSP_ECUDA, cuda_msg("writing norm_out", e));
-  }
-  StepArgs a;
-  s = step_args(p, reinterpret_cast<const void* const*>(grads), master, m, v, params, hp, step, &a);
-  if (s != FSP_OK) return s;
+// Passes 1-3 of the clipped flow for an argument block whose tiles, buffers
+// (or per-parameter tables) and coefficients are set; the plan is non-empty.
+fsp_status run_clipped_passes(const fsp_plan* p, StepArgs& a, float max_norm, float* norm_out, void* stream) {
   double* partials = nullptr;
-  s = device_partials(p, &partials);
+  fsp_status s = device_partials(p, &partials);
   if (s != FSP_OK) return s;
 
   // pass 1: reduce-scatter into the owners' slices and each tile's sum of
@@ -440,7 +422,33 @@ fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("norm kernel launch", e));
   // pass 3: AdamW on the clipped gradient read from the owners' slices
   a.clip = norm_out;
-  return launch(a, dtype, stream, true);
+  return launch(a, FSP_DTYPE_F32, stream, true);
+}
+
+// norm_out = {0, 1} for a plan with nothing to reduce.
+fsp_status clipped_empty(float* norm_out, void* stream) {
+  const float out[2] = {0.f, 1.f};
+  cudaError_t e = cudaMemcpyAsync(norm_out, out, sizeof(out), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSP_OK : fail(FSP_ECUDA, cuda_msg("writing norm_out", e));
+}
+
+fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype, float* master, float* m, float* v,
+                            void* const* params, const fsp_adamw_hparams* hp, int64_t step, float max_norm,
+                            float* norm_out, void* stream) {
+  clear_error();
+  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 and DistOpt plans");
+  if (dtype != FSP_DTYPE_F32) return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 grad buffers");
+  if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");
+  std::vector<Buf> extra{{norm_out, 2 * sizeof(float), "norm_out"}};
+  fsp_status s = check_device_step(p, reinterpret_cast<const void* const*>(grads), dtype, master, m, v, params, hp,
+                                   step, extra);
+  if (s != FSP_OK) return s;
+  if (p->tiles.empty()) return clipped_empty(norm_out, stream);   // nothing to reduce: norm 0, coefficient 1
+  StepArgs a;
+  s = step_args(p, reinterpret_cast<const void* const*>(grads), master, m, v, params, hp, step, &a);
+  if (s != FSP_OK) return s;
+  return run_clipped_passes(p, a, max_norm, norm_out, stream);
 }
 
 }  // namespace fsp

@@ -344,6 +344,15 @@ fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* 
                                    float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp, int64_t step,
                                    void* cuda_stream);
 
+/* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 per-parameter
+ * plan, fp32 gradients; others: FSP_EUNSUPPORTED): every element's averaged
+ * gradient is written back into its owner's slice of the owner's gradient
+ * tensor, then the norm, the coefficient and the clipped update as there.
+ * norm_out: device, 2 floats, 16-byte aligned. */
+fsp_status fsp_sharded_step_clipped_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
+                                           float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
+                                           int64_t step, float max_norm, float* norm_out, void* cuda_stream);
+
 /* fsp_unshard into the per-parameter bf16 tensors of `table` (which must have
  * them). */
 fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,

@@ -180,3 +180,34 @@ def test_per_param_step_equals_flat_step_on_a_large_plan(n_d, mode, n_rep, gd):
     pc.params_match_flat()
     assert pc.guards_intact()
     assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("max_norm", [1e-4, 1e30])
+@pytest.mark.parametrize("shapes", [SHAPES, BIG], ids=["small", "large"])
+def test_per_param_clipped_flow_equals_flat(max_norm, shapes):
+    """The distributed-optimizer flow with clipping on per-parameter tensors:
+    the write-back lands in the owner's slice of the owner's gradient tensor,
+    and norm, coefficient, state and parameters are the flat flow's."""
+    flat = DeviceCase(shapes, 4, "fsdp2", "f32", 89)
+    pc = ParamCase(flat)
+    out_f = torch.zeros(4, dtype=torch.float32, device="cuda")
+    out_p = torch.zeros(4, dtype=torch.float32, device="cuda")
+    fsp.sharded_step_clipped(flat.plan, [g.t for g in flat.grads], *[s.t for s in flat.state],
+                             [p.t for p in flat.params], HP, 10, max_norm, out_f)
+    fsp.sharded_step_clipped_params(pc.plan, pc.table, *[s.t for s in pc.state], HP, 10, max_norm, out_p)
+    torch.cuda.synchronize()
+    nf, cf = out_f[:2].tolist()
+    n_p, c_p = out_p[:2].tolist()
+    # the norm's partial sums group by tile, and the tiles differ (virtual offsets)
+    assert abs(nf - n_p) <= 1e-12 * nf
+    assert cf == c_p
+    assert (cf == 1.0) == (max_norm > 1e20)
+    pc.state_matches_flat()
+    pc.params_match_flat()
+    for q in range(flat.n_d):       # write-back: each gradient tensor equals the flat buffer's slice
+        fb = flat.grads[q].bits()
+        for i, s in enumerate(shapes):
+            n = _numel(s)
+            assert np.array_equal(pc.grads[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n]), f"rank {q} grad {i}"
+    assert pc.guards_intact()
+    assert fsp.device_error() == 0
