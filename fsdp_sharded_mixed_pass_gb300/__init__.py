@@ -27,6 +27,7 @@ from .fsp import (  # noqa: F401
     host_step_workspace_bytes,
     sharded_step_noalloc,
     sharded_step_params,
+    sharded_step_params_device_t,
     unshard,
     unshard_params,
 )

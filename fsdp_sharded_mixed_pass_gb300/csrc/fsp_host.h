@@ -40,5 +40,7 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false,
 // for a plan with nothing to reduce.
 fsp_status run_clipped_passes(const fsp_plan* p, StepArgs& a, float max_norm, float* norm_out, void* stream);
 fsp_status clipped_empty(float* norm_out, void* stream);
+// *step_dev += 1 on `stream` (one thread).
+fsp_status advance_step(int64_t* step_dev, void* stream);
 
 }  // namespace fsp

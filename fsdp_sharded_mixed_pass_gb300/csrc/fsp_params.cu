@@ -191,6 +191,28 @@ fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* m
   return launch(a, t->grad_dtype, stream);
 }
 
+fsp_status run_step_params_device_t(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                                    const fsp_adamw_hparams* hp, int64_t* step_dev, int32_t advance, void* stream) {
+  clear_error();
+  if (!step_dev) return fail(FSP_EINVAL, "step_dev is NULL");
+  if (reinterpret_cast<uintptr_t>(step_dev) % 8 != 0) return fail(FSP_EINVAL, "step_dev is not 8-byte aligned");
+  // t only enters the bias corrections, which the kernel recomputes from *step_dev
+  fsp_status s = check_params_step(p, t, master, m, v, hp, 1, {});
+  if (s != FSP_OK) return s;
+  if (overlaps_table(t, step_dev, sizeof(int64_t))) return fail(FSP_EINVAL, "step_dev overlaps a registered tensor");
+  s = check_allocation(step_dev, sizeof(int64_t), "step_dev");
+  if (s != FSP_OK) return s;
+  if (!p->tiles.empty()) {
+    StepArgs a;
+    s = params_step_args(p, t, master, m, v, hp, 1, &a);
+    if (s != FSP_OK) return s;
+    a.step_dev = step_dev;
+    s = launch(a, t->grad_dtype, stream);
+    if (s != FSP_OK) return s;
+  }
+  return advance ? advance_step(step_dev, stream) : FSP_OK;
+}
+
 fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
                                    const fsp_adamw_hparams* hp, int64_t step, float max_norm, float* norm_out,
                                    void* stream) {
@@ -217,6 +239,13 @@ extern "C" fsp_status fsp_param_table_create(const fsp_plan* plan, const void* c
 }
 
 extern "C" void fsp_param_table_destroy(fsp_param_table* table) { fsp::free_table(table); }
+
+extern "C" fsp_status fsp_sharded_step_params_device_t(const fsp_plan* plan, const fsp_param_table* table,
+                                                       float* master, float* exp_avg, float* exp_avg_sq,
+                                                       const fsp_adamw_hparams* hp, int64_t* step_dev,
+                                                       int32_t advance, void* cuda_stream) {
+  return fsp::run_step_params_device_t(plan, table, master, exp_avg, exp_avg_sq, hp, step_dev, advance, cuda_stream);
+}
 
 extern "C" fsp_status fsp_sharded_step_clipped_params(const fsp_plan* plan, const fsp_param_table* table,
                                                       float* master, float* exp_avg, float* exp_avg_sq,

@@ -425,6 +425,12 @@ fsp_status run_clipped_passes(const fsp_plan* p, StepArgs& a, float max_norm, fl
   return launch(a, FSP_DTYPE_F32, stream, true);
 }
 
+fsp_status advance_step(int64_t* step_dev, void* stream) {
+  step_advance_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(step_dev);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FSP_OK : fail(FSP_ECUDA, cuda_msg("step counter advance", e));
+}
+
 // norm_out = {0, 1} for a plan with nothing to reduce.
 fsp_status clipped_empty(float* norm_out, void* stream) {
   const float out[2] = {0.f, 1.f};
@@ -491,11 +497,7 @@ extern "C" fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void
     s = launch(a, grad_dtype, cuda_stream);
     if (s != FSP_OK) return s;
   }
-  if (advance) {
-    step_advance_kernel<<<1, 1, 0, st>>>(step_dev);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("step counter advance", e));
-  }
+  if (advance) return advance_step(step_dev, st);
   return FSP_OK;
 }
 

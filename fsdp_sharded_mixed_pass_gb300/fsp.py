@@ -22,7 +22,8 @@ EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", 
            "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
-           "fsp_sharded_step_params", "fsp_sharded_step_clipped_params", "fsp_unshard_params",
+           "fsp_sharded_step_params", "fsp_sharded_step_params_device_t", "fsp_sharded_step_clipped_params",
+           "fsp_unshard_params",
            "fsp_sharded_step_noalloc", "fsp_unshard", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
 
@@ -81,6 +82,7 @@ def lib():
     L.fsp_param_table_destroy.restype = None
     L.fsp_sharded_step_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, vp]
     L.fsp_unshard_params.argtypes = [vp, vp, vp, vp]
+    L.fsp_sharded_step_params_device_t.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), vp, i32, vp]
     L.fsp_sharded_step_clipped_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, ctypes.c_float,
                                                   vp, vp]
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
@@ -101,7 +103,7 @@ def lib():
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param",
                "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
                "fsp_sharded_step_noalloc", "fsp_param_table_create", "fsp_sharded_step_params",
-               "fsp_sharded_step_clipped_params", "fsp_unshard_params"):
+               "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
     L.fsp_host_step_workspace_bytes.restype = ctypes.c_int
@@ -286,6 +288,16 @@ def sharded_step_params(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_
                                          ctypes.c_void_p(_ptr(exp_avg)), ctypes.c_void_p(_ptr(exp_avg_sq)),
                                          ctypes.byref(_hp(hparams)), int(step),
                                          ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_params")
+
+
+def sharded_step_params_device_t(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_sq, hparams: dict,
+                                 step_dev, advance: bool = True, stream=None) -> None:
+    """``sharded_step_params`` with t read from (and advanced in) device memory."""
+    _check(lib().fsp_sharded_step_params_device_t(plan.handle, table.handle, ctypes.c_void_p(_ptr(master)),
+                                                  ctypes.c_void_p(_ptr(exp_avg)), ctypes.c_void_p(_ptr(exp_avg_sq)),
+                                                  ctypes.byref(_hp(hparams)), ctypes.c_void_p(_ptr(step_dev)),
+                                                  1 if advance else 0, ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_sharded_step_params_device_t")
 
 
 def sharded_step_clipped_params(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_sq, hparams: dict,

@@ -344,6 +344,13 @@ fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* 
                                    float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp, int64_t step,
                                    void* cuda_stream);
 
+/* fsp_sharded_step_params with the update index in device memory, as
+ * fsp_sharded_step_device_t (for a step captured once in a CUDA graph and
+ * replayed: t = *step_dev, then *step_dev += 1 when `advance` is non-zero). */
+fsp_status fsp_sharded_step_params_device_t(const fsp_plan* plan, const fsp_param_table* table, float* master,
+                                            float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
+                                            int64_t* step_dev, int32_t advance, void* cuda_stream);
+
 /* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 per-parameter
  * plan, fp32 gradients; others: FSP_EUNSUPPORTED): every element's averaged
  * gradient is written back into its owner's slice of the owner's gradient

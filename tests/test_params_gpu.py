@@ -211,3 +211,30 @@ def test_per_param_clipped_flow_equals_flat(max_norm, shapes):
             assert np.array_equal(pc.grads[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n]), f"rank {q} grad {i}"
     assert pc.guards_intact()
     assert fsp.device_error() == 0
+
+
+def test_per_param_device_t_replayed_in_a_cuda_graph():
+    """One captured per-parameter step with t in device memory, replayed twice,
+    equals the flat step at t = 10 and 11."""
+    flat = DeviceCase(SHAPES, 8, "fsdp2", "f32", 97)
+    pc = ParamCase(flat)
+    t_dev = torch.tensor([10], dtype=torch.int64, device="cuda")
+    # first use of the plan outside capture, on scratch copies of the state (the
+    # parameter tensors it writes are rewritten by every later step)
+    scratch = [s.t.clone() for s in pc.state]
+    fsp.sharded_step_params_device_t(pc.plan, pc.table, *scratch, HP, torch.ones(1, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fsp.sharded_step_params_device_t(pc.plan, pc.table, *[s.t for s in pc.state], HP, t_dev, stream=stream)
+    g.replay()
+    g.replay()
+    flat.step(10, debug=False)
+    flat.step(11, debug=False)
+    torch.cuda.synchronize()
+    assert int(t_dev.item()) == 12
+    pc.state_matches_flat()
+    pc.params_match_flat()
+    assert fsp.device_error() == 0
