@@ -614,7 +614,7 @@ def run_fsp(args):
                                       "parameter in a tensor of its own)"} if args.per_param else {})),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     "frac": achieved / peak, "frac_of_nominal_8000": achieved / 8000.0, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
                      and not args.no_gather and not args.per_param else None,
