@@ -18,10 +18,14 @@
  * Steps (1)-(3) run as one fused streaming kernel: every gradient is read
  * once, the fp32 state is read and written once, every bf16 copy is written
  * once; the reduced gradient is never stored (except by the debug entry).
- * For N_d in {1..8, 12, 16} the kernel stages the gradient and state slices
- * in shared memory with bulk asynchronous copies and writes the N_d bf16
- * copies as bulk stores of one tile; other N_d (up to 64) use per-thread
- * vector loads and stores.
+ * For N_d in {1..8, 12, 16} (and the HSDP meshes 2x2, 4x2, 8x2, 2x4, 4x4) the
+ * kernel stages the gradient and state slices in shared memory with bulk
+ * asynchronous copies and writes the N_d bf16 copies as bulk stores of one
+ * tile; other N_d (up to 64) use per-thread vector loads and stores.
+ * Gradients and parameters are either one full-size buffer per rank
+ * (fsp_plan_layout / fsp_plan_layout_hsdp with the *_step entries) or one
+ * tensor per parameter per rank (fsp_plan_layout_params with an
+ * fsp_param_table and the *_params entries).
  *
  * Conventions for every function below:
  *   - Return FSP_OK or an error status; fsp_last_error() then gives a
