@@ -76,6 +76,9 @@ def parse_args(argv=None):
                          "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt)")
     ap.add_argument("--no-gather", action="store_true",
                     help="time the ZeRO-3 step instead: reduce-scatter + AdamW, parameters left sharded")
+    ap.add_argument("--writeback", action="store_true",
+                    help="time the step that also writes the averaged gradient into the owners' slices "
+                         "(distributed optimizer; fp32 grads, FSDP2 / DistOpt)")
     ap.add_argument("--unshard", action="store_true",
                     help="time the FSDP2 unshard instead (fp32 shards -> bf16 -> every rank's full buffer)")
     ap.add_argument("--per-param", action="store_true",
@@ -294,6 +297,7 @@ class DeviceWorkload:
         self.clip = None
         self.unshard = False
         self.no_gather = False
+        self.writeback = False
         self.norm_out = torch.zeros(4, dtype=torch.float32, device=device)
 
     def step(self, stream):
@@ -305,6 +309,9 @@ class DeviceWorkload:
                 fsp.sharded_step_params(self.plan, self.table, *self.state, self.w.hparams(), self.t, stream=stream)
         elif self.unshard:
             fsp.unshard(self.plan, self.state[0], self.params, stream=stream)
+        elif self.writeback:
+            fsp.sharded_step_writeback(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
+                                       stream=stream)
         elif self.clip is not None:
             fsp.sharded_step_clipped(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
                                      self.clip, self.norm_out, stream=stream)
@@ -319,6 +326,8 @@ class DeviceWorkload:
             return 4 * w.n_rep + 2 * w.n_d
         if self.no_gather:          # grads in, state in and out, no params
             return w.n_d * w.grad_bytes + 24 * w.n_rep
+        if self.writeback:          # the step plus the owner's averaged slice written back
+            return w.n_d * w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
             return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
@@ -544,12 +553,15 @@ def run_fsp(args):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
-    if args.per_param and (w.mode == "distopt" or args.clip is not None or args.no_gather):
+    if args.per_param and (w.mode == "distopt" or args.clip is not None or args.no_gather or args.writeback):
         raise SystemExit("--per-param: FSDP2 / HSDP workloads, the plain step or --unshard")
+    if args.writeback and (w.grad_dtype != "f32" or w.n_rep != 1):
+        raise SystemExit("--writeback: fp32 gradients, FSDP2 or DistOpt")
     wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param)
     wl.clip = args.clip
     wl.unshard = args.unshard
     wl.no_gather = args.no_gather
+    wl.writeback = args.writeback
     plan = wl.plan
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
@@ -574,7 +586,8 @@ def run_fsp(args):
     tpe = traffic_per_elem(w.name) if args.n_d in (None, workload_own_n_d(args.workload)) else None
 
     e2e = None
-    if not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather and not args.per_param:
+    if (not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather and not args.per_param
+            and not args.writeback):
         # every rank on this node needs its own host copy of the grads and params
         per_rank = P * w.n_d * (w.grad_bytes + 2)
         local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
@@ -609,7 +622,9 @@ def run_fsp(args):
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (4 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
             if args.unshard else {"flow": "ZeRO-3 step: reduce-scatter + AdamW, no all-gather"}
-            if args.no_gather else {}),
+            if args.no_gather else {"flow": "distributed-optimizer step with the averaged gradient written back "
+                                            "into the owners' grad slices (one kernel)"}
+            if args.writeback else {}),
                        **({"buffers": "per-parameter tensors (each rank's gradient and bf16 parameter of each "
                                       "parameter in a tensor of its own)"} if args.per_param else {})),
         "hbm_gbs": achieved,
@@ -617,7 +632,7 @@ def run_fsp(args):
                      "frac": achieved / peak, "frac_of_nominal_8000": achieved / 8000.0, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
-                     and not args.no_gather and not args.per_param else None,
+                     and not args.no_gather and not args.per_param and not args.writeback else None,
                      "kernel": "unshard_kernel" if args.unshard else
                      "sharded_step_generic_kernel" if args.per_param else "sharded_step_kernel",
                      "kernel_src": kernel_src_hash()},

@@ -28,6 +28,7 @@ from .fsp import (  # noqa: F401
     sharded_step_noalloc,
     sharded_step_params,
     sharded_step_params_device_t,
+    sharded_step_writeback,
     unshard,
     unshard_params,
 )

@@ -202,6 +202,7 @@ __device__ __forceinline__ void step_one(const StepArgs& a, const void* const* g
       acc = r == 0 ? part : acc + part;
     }
     acc = acc / float(ns * nr);
+    if (a.writeback) const_cast<float*>(static_cast<const float*>(gb[owner]))[f] = acc;   // fp32, one group
   }
 #pragma unroll(NR > 0 ? NR : 1)
   for (int r = 0; r < nr; ++r) {
@@ -256,6 +257,8 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const void* const*
     acc.y = acc.y / nd;
     acc.z = acc.z / nd;
     acc.w = acc.w / nd;
+    if (a.writeback)   // fp32, one replica group
+      __stcs(reinterpret_cast<float4*>(const_cast<float*>(static_cast<const float*>(gb[owner])) + f), acc);
   }
   for (int r = 0; r < nr; ++r) {
     const int64_t sr = s + r * a.rep_stride;
@@ -640,6 +643,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
             for (int j = 0; j < NS; ++j) bulk_store(a.params[r * NS + j] + h.c, p_s, len * 2);
           }
         }
+        if (sizeof(GradT) == 4 && NR == 1 && !kClip && a.writeback) {   // the owner's averaged slice
+          const void* own = per_param ? stage_gb(stage)[h.rank] : a.grads[h.rank];
+          bulk_store(static_cast<unsigned char*>(const_cast<void*>(own)) + h.c * G,
+                     smem_addr(st + Cfg::kGradOff + h.rank * E * G), len * G);
+        }
         bulk_commit();
         bulk_wait_read_all();   // the stage may be refilled once its bytes have been read out
       }
@@ -700,6 +708,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           acc.y = acc.y / float(N);
           acc.z = acc.z / float(N);
           acc.w = acc.w / float(N);
+          // write-back (fp32, one replica group): the owner's slice in the stage now
+          // holds the averaged gradient; this thread alone read its elements there
+          if (sizeof(GradT) == 4 && NR == 1 && a.writeback)
+            *reinterpret_cast<float4*>(st + Cfg::kGradOff + h.rank * E * G + j * G) = acc;
         }
 #pragma unroll
         for (int r = 0; r < NR; ++r) {

@@ -501,6 +501,25 @@ extern "C" fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void
   return FSP_OK;
 }
 
+extern "C" fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
+                                                 float* master, float* exp_avg, float* exp_avg_sq,
+                                                 void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
+                                                 void* cuda_stream) {
+  using namespace fsp;
+  clear_error();
+  if (plan && plan->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the write-back step is for FSDP2 and DistOpt plans");
+  if (grad_dtype != FSP_DTYPE_F32)
+    return fail(FSP_EUNSUPPORTED, "the write-back step stores the averaged gradient into fp32 grad buffers");
+  const void* const* grads = reinterpret_cast<const void* const*>(grad_bufs);
+  fsp_status s = check_device_step(plan, grads, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, {});
+  if (s != FSP_OK || plan->tiles.empty()) return s;
+  StepArgs a;
+  s = step_args(plan, grads, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
+  if (s != FSP_OK) return s;
+  a.writeback = 1;
+  return launch(a, grad_dtype, cuda_stream);
+}
+
 extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs,
                                              int32_t grad_dtype, float* master, float* exp_avg,
                                              float* exp_avg_sq, void* const* param_bufs,

@@ -21,6 +21,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
            "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
+           "fsp_sharded_step_writeback",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
            "fsp_sharded_step_params", "fsp_sharded_step_params_device_t", "fsp_sharded_step_clipped_params",
            "fsp_unshard_params",
@@ -94,6 +95,7 @@ def lib():
     L.fsp_sharded_step.argtypes = step_args + [vp]
     L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
+    L.fsp_sharded_step_writeback.argtypes = step_args + [vp]
     L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
     L.fsp_sharded_step_clipped.restype = ctypes.c_int
     L.fsp_sharded_step_device_t.argtypes = step_args[:-1] + [vp, i32, vp]
@@ -102,7 +104,7 @@ def lib():
     L.fsp_unshard.restype = ctypes.c_int
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param",
                "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
-               "fsp_sharded_step_noalloc", "fsp_param_table_create", "fsp_sharded_step_params",
+               "fsp_sharded_step_noalloc", "fsp_sharded_step_writeback", "fsp_param_table_create", "fsp_sharded_step_params",
                "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
@@ -375,6 +377,15 @@ def sharded_step_debug(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_debug(*args, ctypes.c_void_p(_ptr(reduced_grad)),
                                         ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_debug")
+
+
+def sharded_step_writeback(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
+                           stream=None, grad_dtype: str | None = None) -> None:
+    """``sharded_step`` that also stores every element's averaged gradient into
+    its owner's slice of the owner's fp32 grad buffer (one pass)."""
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step_writeback(*args, ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_sharded_step_writeback")
 
 
 def sharded_step_noalloc(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,

@@ -264,6 +264,18 @@ fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs
                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                     float max_norm, float* norm_out, void* cuda_stream);
 
+/* fsp_sharded_step that also writes every element's averaged gradient into
+ * its owner's slice of the owner's own grad buffer - the Megatron distributed
+ * optimizer's reduce-scatter, whose result lands in the rank's 1/DP slice of
+ * its full grad buffer ("07 · 显存模型", section 2.1 item 1) - in the same
+ * pass: 4 more bytes per element (76 B for N_d = 8 fp32 instead of 72).  The
+ * rest of each grad buffer is left as it was.  FSDP2 and DistOpt plans with
+ * fp32 grads (others: FSP_EUNSUPPORTED); otherwise as fsp_sharded_step
+ * (param_bufs NULL: no all-gather). */
+fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
+                                      float* master, float* exp_avg, float* exp_avg_sq, void* const* param_bufs,
+                                      const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream);
+
 /* FSDP2 unshard of the plan's parameters (the all-gather before forward and
  * before backward in ZeRO-3 / FSDP2, with a bf16 MixedPrecisionPolicy): every
  * rank's fp32 shard - its owned slots of `master` - is cast to bf16 (round to

@@ -339,3 +339,16 @@ def test_per_param_layout_rejects():
     a, b = ctypes.c_int64(), ctypes.c_int64()
     assert L.fsp_plan_param(p.handle, 1, ctypes.byref(a), ctypes.byref(b)) == B.FSP_EINVAL
     assert L.fsp_plan_param(p.handle, 0, ctypes.byref(a), ctypes.byref(b)) == B.FSP_OK and (a.value, b.value) == (0, 4)
+
+
+def test_writeback_step_rejects_on_host():
+    L = B.lib()
+    hsdp = fsp.plan_layout([(64, 8)], 4, "hsdp", n_replicate=2)
+    fsdp = fsp.plan_layout([(64, 8)], 4)
+    for plan, dtype in ((hsdp, "f32"), (fsdp, "bf16")):
+        grads, state, params = _fakes(plan)
+        args = B._step_args(plan, grads, *state, params, HP, 1, dtype)
+        assert L.fsp_sharded_step_writeback(*args, ctypes.c_void_p(0)) == B.FSP_EUNSUPPORTED
+    grads, state, params = _fakes(fsdp)
+    args = B._step_args(fsdp, grads, *state, params, HP, 0, "f32")
+    assert L.fsp_sharded_step_writeback(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
