@@ -32,6 +32,7 @@ CASES = [
 CASES += [
     (((3001, 7), (12289,), (9, 5)), 8, "hsdp", "f32", 11, 4096),   # 2 x 4 mesh
     (((3001, 7), (12289,), (9, 5)), 6, "hsdp", "bf16", 12, 8192),  # 2 x 3 mesh (generic kernel)
+    (((3000, 4096), (4099,), (77, 3)), 4, "fsdp2", "f32", 13, 0),   # one chunk with tiles in order
 ]
 
 
