@@ -24,9 +24,10 @@ Modules
 Pins (``tests/test_oracle_*.py``, ``-m "not gpu"``) tie every function to
 something other than itself: the pages' worked numbers (``tests/golden/``),
 hand-worked AdamW cases, brute force on tiny inputs, and library routines for
-special cases.  Parity unpinned: the AdamW formula itself - the pages name
-"Adam m/v" as state but never print the update rule, so the decoupled,
-bias-corrected form is a stated reading, pinned only by hand-worked closed
-forms.
+special cases.  The AdamW update rule is a reading, not a page's: the pages
+name "Adam m/v" as state but never print the rule.  The oracle's statement of
+the reading (PyTorch's decoupled, bias-corrected AdamW) is pinned by
+hand-worked closed forms and against torch.optim.AdamW run in fp64; which rule
+the pages' systems use is beyond what the pages fix.
 """
 from . import plan, step, ledger  # noqa: F401

@@ -2,7 +2,8 @@
 
 Each stage is tied to something other than the oracle itself: the pages' worked
 all-reduce = reduce-scatter + all-gather example, hand-worked AdamW cases with
-exactly representable numbers, a library routine for the bf16 cast, exact
+exactly representable numbers, torch.optim.AdamW for the update's form, a
+library routine for the bf16 cast, exact
 rational arithmetic for the averaging, and brute-force agreement between the
 sharded step and the unsharded all-reduce definition.
 """
@@ -144,6 +145,36 @@ def test_adamw_zero_betas():
 # --------------------------------------------------------------------------
 # Stage 3: bf16 cast
 # --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("t", [1, 10, 1000])
+def test_adamw_matches_torch_optim_adamw(t):
+    """The reading 'PyTorch-style decoupled AdamW' checked against an
+    implementation that is not the oracle's: torch.optim.AdamW in fp64, from
+    the same m, v and step count t - 1, one step.  Both round to fp32 at the
+    end; they agree bit for bit except where the two fp64 evaluations straddle
+    an fp32 rounding boundary (then by one ulp)."""
+    n = 100_000
+    idx = np.arange(n)
+    g = S.grad_f32(77, 0, idx)
+    th, m, v = S.master_f32(77, idx), S.adam_m_f32(77, idx), S.adam_v_f32(77, idx)
+    want = O.adamw(th, m, v, g, HP, t)
+    h = O.hparams_f32(HP)
+    p = torch.nn.Parameter(torch.from_numpy(th.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=h["lr"], betas=(h["beta1"], h["beta2"]), eps=h["eps"],
+                            weight_decay=h["weight_decay"], foreach=False)
+    p.grad = torch.from_numpy(g.astype(np.float64))
+    opt.state[p] = {"step": torch.tensor(float(t - 1), dtype=torch.float64),
+                    "exp_avg": torch.from_numpy(m.astype(np.float64)),
+                    "exp_avg_sq": torch.from_numpy(v.astype(np.float64))}
+    opt.step()
+    got = (p.detach().numpy().astype(np.float32), opt.state[p]["exp_avg"].numpy().astype(np.float32),
+           opt.state[p]["exp_avg_sq"].numpy().astype(np.float32))
+    for a, b in zip(got, want):
+        ai = a.view(np.int32).astype(np.int64)
+        bi = b.view(np.int32).astype(np.int64)
+        assert np.abs(ai - bi).max() <= 1
+        assert (ai == bi).mean() > 0.999
+
 
 def test_bf16_rne_hand_cases():
     one = 1.0
