@@ -528,6 +528,10 @@ def time_oracle(w, shapes, seconds: float, use_device: bool, max_reps: int = 100
 
 def config_block(w, label, plan):
     per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+    extra = {}
+    if w.grad_bytes != 4:
+        # the 6 N_d + 24 B/param formula counts 4-byte gradients; with bf16 grads the step moves less
+        extra["bytes_per_param_if_fp32_grads"] = 6 * w.n_d + 24 * w.n_rep
     return {
         "workload": label,
         "n_d": w.n_d,
@@ -536,6 +540,7 @@ def config_block(w, label, plan):
         "grad_dtype": w.grad_dtype,
         "params": plan.valid_elems,
         "bytes_per_param": per,
+        **extra,
         "bytes_per_step": per * plan.valid_elems,
         "parallelism": "replicas",
     }
