@@ -79,6 +79,9 @@ def parse_args(argv=None):
     ap.add_argument("--writeback", action="store_true",
                     help="time the step that also writes the averaged gradient into the owners' slices "
                          "(distributed optimizer; fp32 grads, FSDP2 / DistOpt)")
+    ap.add_argument("--fp32-gather", action="store_true",
+                    help="time the step whose all-gather writes the fp32 master into fp32 param buffers "
+                         "(full-size buffers; with --unshard: the fp32 unshard)")
     ap.add_argument("--unshard", action="store_true",
                     help="time the FSDP2 unshard instead (fp32 shards -> bf16 -> every rank's full buffer)")
     ap.add_argument("--per-param", action="store_true",
@@ -264,7 +267,7 @@ def resolve_workload(name: str, param_slice: str | None, n_d: int | None = None)
 
 
 class DeviceWorkload:
-    def __init__(self, w, shapes, device, per_param: bool = False):
+    def __init__(self, w, shapes, device, per_param: bool = False, fp32_gather: bool = False):
         import torch
         import fsdp_sharded_mixed_pass_gb300 as fsp
         from synth_inputs import device as D
@@ -289,7 +292,9 @@ class DeviceWorkload:
             self.grads = [torch.empty(p.full_len_padded, dtype=gdt, device=device) for _ in range(w.n_d)]
             for q, g in enumerate(self.grads):
                 D.fill_grad(g, w.data_seed, q, w.grad_dtype)
-            self.params = [torch.zeros(p.full_len_padded, dtype=torch.bfloat16, device=device) for _ in range(w.n_d)]
+            pdt = torch.float32 if fp32_gather else torch.bfloat16
+            self.params = [torch.zeros(p.full_len_padded, dtype=pdt, device=device) for _ in range(w.n_d)]
+        self.fp32_gather = fp32_gather
         self.state = [torch.zeros(p.state_len_total, dtype=torch.float32, device=device) for _ in range(3)]
         D.fill_state_segments(*self.state, w.data_seed, [(s.full_off, s.state_off, s.length) for s in p.segments])
         torch.cuda.synchronize(device)
@@ -308,7 +313,10 @@ class DeviceWorkload:
             else:
                 fsp.sharded_step_params(self.plan, self.table, *self.state, self.w.hparams(), self.t, stream=stream)
         elif self.unshard:
-            fsp.unshard(self.plan, self.state[0], self.params, stream=stream)
+            fsp.unshard(self.plan, self.state[0], self.params, stream=stream, fp32=self.fp32_gather)
+        elif self.fp32_gather:
+            fsp.sharded_step_fp32_gather(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
+                                         stream=stream)
         elif self.writeback:
             fsp.sharded_step_writeback(self.plan, self.grads, *self.state, self.params, self.w.hparams(), self.t,
                                        stream=stream)
@@ -322,15 +330,16 @@ class DeviceWorkload:
 
     def bytes_per_param(self) -> int:
         w = self.w
-        if self.unshard:            # fp32 master in, one bf16 per rank of its group out
-            return 4 * w.n_rep + 2 * w.n_d
+        pbytes = 4 if self.fp32_gather else 2
+        if self.unshard:            # fp32 master in, one bf16 (fp32) per rank of its group out
+            return 4 * w.n_rep + pbytes * w.n_d
         if self.no_gather:          # grads in, state in and out, no params
             return w.n_d * w.grad_bytes + 24 * w.n_rep
         if self.writeback:          # the step plus the owner's averaged slice written back
             return w.n_d * w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
             return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
-        return w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+        return w.n_d * w.grad_bytes + 24 * w.n_rep + pbytes * w.n_d
 
 
 def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False,
@@ -562,7 +571,9 @@ def run_fsp(args):
         raise SystemExit("--per-param: FSDP2 / HSDP workloads, the plain step or --unshard")
     if args.writeback and (w.grad_dtype != "f32" or w.n_rep != 1):
         raise SystemExit("--writeback: fp32 gradients, FSDP2 or DistOpt")
-    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param)
+    if args.fp32_gather and (args.per_param or args.clip is not None or args.no_gather or args.writeback):
+        raise SystemExit("--fp32-gather: the plain step or --unshard on full-size buffers")
+    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather)
     wl.clip = args.clip
     wl.unshard = args.unshard
     wl.no_gather = args.no_gather
@@ -592,7 +603,7 @@ def run_fsp(args):
 
     e2e = None
     if (not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather and not args.per_param
-            and not args.writeback):
+            and not args.writeback and not args.fp32_gather):
         # every rank on this node needs its own host copy of the grads and params
         per_rank = P * w.n_d * (w.grad_bytes + 2)
         local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
@@ -630,6 +641,7 @@ def run_fsp(args):
             if args.no_gather else {"flow": "distributed-optimizer step with the averaged gradient written back "
                                             "into the owners' grad slices (one kernel)"}
             if args.writeback else {}),
+                       **({"param_dtype": "fp32 (all-gather of the fp32 master)"} if args.fp32_gather else {}),
                        **({"buffers": "per-parameter tensors (each rank's gradient and bf16 parameter of each "
                                       "parameter in a tensor of its own)"} if args.per_param else {})),
         "hbm_gbs": achieved,
@@ -637,7 +649,8 @@ def run_fsp(args):
                      "frac": achieved / peak, "frac_of_nominal_8000": achieved / 8000.0, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
-                     and not args.no_gather and not args.per_param and not args.writeback else None,
+                     and not args.no_gather and not args.per_param and not args.writeback and not args.fp32_gather
+                     else None,
                      "kernel": "unshard_kernel" if args.unshard else
                      "sharded_step_generic_kernel" if args.per_param else "sharded_step_kernel",
                      "kernel_src": kernel_src_hash()},

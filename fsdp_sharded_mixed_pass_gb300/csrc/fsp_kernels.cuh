@@ -213,8 +213,11 @@ __device__ __forceinline__ void step_one(const StepArgs& a, const void* const* g
     a.m[sr] = mm;
     a.v[sr] = vv;
     if (a.reduced) a.reduced[sr] = acc;
-    const uint16_t b = bf16_bits(th);
-    if (a.gather) {
+    if (a.gather && a.param_f32) {
+#pragma unroll(NS > 0 ? NS : 1)
+      for (int j = 0; j < ns; ++j) reinterpret_cast<float*>(pb[r * ns + j])[f] = th;
+    } else if (a.gather) {
+      const uint16_t b = bf16_bits(th);
 #pragma unroll(NS > 0 ? NS : 1)
       for (int j = 0; j < ns; ++j) pb[r * ns + j][f] = b;
     }
@@ -273,7 +276,9 @@ __device__ __forceinline__ void step_group(const StepArgs& a, const void* const*
     __stcs(reinterpret_cast<float4*>(a.m + sr), mm);
     __stcs(reinterpret_cast<float4*>(a.v + sr), vv);
     if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + sr), acc);
-    if (a.gather) {
+    if (a.gather && a.param_f32) {
+      for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(pb[r * ns + j]) + f), th);
+    } else if (a.gather) {
       const uint2 b = pack_bf16x4(th);
       for (int j = 0; j < ns; ++j) __stcs(reinterpret_cast<uint2*>(pb[r * ns + j] + f), b);
     }
@@ -635,7 +640,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.master + s, th_s, len * 4);
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
-          if (a.gather && per_param) {   // the all-gather
+          if (a.gather && a.param_f32) {   // the all-gather of the fp32 master itself (full-size buffers)
+#pragma unroll
+            for (int j = 0; j < NS; ++j) bulk_store(reinterpret_cast<float*>(a.params[r * NS + j]) + h.c, th_s, len * 4);
+          } else if (a.gather && per_param) {   // the all-gather
 #pragma unroll
             for (int j = 0; j < NS; ++j) bulk_store(spb[r * NS + j] + h.c, p_s, len * 2);
           } else if (a.gather) {
@@ -732,7 +740,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           *reinterpret_cast<float4*>(v_s + j) = vv;
           if (a.reduced) __stcs(reinterpret_cast<float4*>(a.reduced + c + delta + r * a.rep_stride + j), acc);
           // (3) bf16 cast, one tile for the replica group's ranks
-          *reinterpret_cast<uint2*>(p_s + j) = pack_bf16x4(th);
+          if (!a.param_f32) *reinterpret_cast<uint2*>(p_s + j) = pack_bf16x4(th);
         }
       }
       fence_async_smem();   // this thread's shared-memory writes -> visible to the bulk stores

@@ -290,7 +290,7 @@ fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step) {
 // `extra`), and - for a non-empty plan - that each lies in a live allocation.
 fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_t dtype, float* master, float* m,
                              float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
-                             const std::vector<Buf>& extra) {
+                             const std::vector<Buf>& extra, size_t param_size = 2) {
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!grads) return fail(FSP_EINVAL, "grad_bufs is NULL");   // param_bufs NULL: no all-gather
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
@@ -302,7 +302,7 @@ fsp_status check_device_step(const fsp_plan* p, const void* const* grads, int32_
   for (int q = 0; q < n; ++q) {
     bufs.push_back({grads[q], size_t(p->full_len_padded) * gsize, "grad_bufs[" + std::to_string(q) + "]"});
     if (params)
-      bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
+      bufs.push_back({params[q], size_t(p->full_len_padded) * param_size, "param_bufs[" + std::to_string(q) + "]"});
   }
   const size_t sbytes = size_t(p->state_len_total) * 4;
   bufs.push_back({master, sbytes, "master"});
@@ -517,6 +517,23 @@ extern "C" fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* con
   s = step_args(plan, grads, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
   if (s != FSP_OK) return s;
   a.writeback = 1;
+  return launch(a, grad_dtype, cuda_stream);
+}
+
+extern "C" fsp_status fsp_sharded_step_fp32_gather(const fsp_plan* plan, const void* const* grad_bufs,
+                                                   int32_t grad_dtype, float* master, float* exp_avg,
+                                                   float* exp_avg_sq, void* const* param_bufs,
+                                                   const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream) {
+  using namespace fsp;
+  clear_error();
+  if (!param_bufs) return fail(FSP_EINVAL, "param_bufs is NULL");
+  fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                                   {}, 4);
+  if (s != FSP_OK || plan->tiles.empty()) return s;
+  StepArgs a;
+  s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
+  if (s != FSP_OK) return s;
+  a.param_f32 = 1;
   return launch(a, grad_dtype, cuda_stream);
 }
 

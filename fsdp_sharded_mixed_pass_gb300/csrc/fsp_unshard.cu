@@ -36,6 +36,7 @@ struct UnshardArgs {
   // that parameter (element f at base + f); nullptr for full-size buffers
   uint16_t* const* vparams;
   int n_d;
+  int param_f32;   // 1: params[] are fp32 buffers (the master copied, no cast; full-size buffers only)
   const Tile* tiles;
   int64_t n_tiles;
   int n_rep;
@@ -65,11 +66,14 @@ __device__ __forceinline__ void bulk_wait_read() {
 static_assert(kTileElems == 2 * 8 * kUnshardThreads, "unshard covers a tile in one pass of the CTA");
 
 // Per tile and replica group: the threads cast the master's aligned body to
-// bf16 in shared memory, then one thread writes it to each rank of the group
-// with a bulk copy (one 8 KB store per rank for a full tile).  Two buffers
-// alternate, so replica r + 1 is cast while r's stores drain.
+// bf16 in shared memory (kF32: copy it as it is), then one thread writes it to
+// each rank of the group with a bulk copy (one 8 KB store per rank for a full
+// bf16 tile).  Two buffers alternate, so replica r + 1 is cast while r's
+// stores drain.
+template <bool kF32>
 __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_constant__ UnshardArgs a) {
-  __shared__ __align__(128) uint16_t cast[2][kTileElems];
+  constexpr int kOut = kF32 ? 4 : 2;   // bytes per output element
+  __shared__ __align__(128) unsigned char cast[2][kTileElems * kOut];
   __shared__ uint16_t* tile_pb[kMaxRanks];
   const int ns = a.n_shard, nr = a.n_rep;
   const int i0 = threadIdx.x, i1 = threadIdx.x + kUnshardThreads;
@@ -103,13 +107,29 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
         }
         if (threadIdx.x == 0) bulk_wait_read<1>();   // this buffer's previous stores have read it
         __syncthreads();
-        uint4* d = reinterpret_cast<uint4*>(cast[buf]);
-        if (i0 < groups) d[i0] = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(y0.x, y0.y), pack2(y0.z, y0.w));
-        if (i1 < groups) d[i1] = make_uint4(pack2(x1.x, x1.y), pack2(x1.z, x1.w), pack2(y1.x, y1.y), pack2(y1.z, y1.w));
+        if (kF32) {
+          float4* d = reinterpret_cast<float4*>(cast[buf]);
+          if (i0 < groups) {
+            d[2 * i0] = x0;
+            d[2 * i0 + 1] = y0;
+          }
+          if (i1 < groups) {
+            d[2 * i1] = x1;
+            d[2 * i1 + 1] = y1;
+          }
+        } else {
+          uint4* d = reinterpret_cast<uint4*>(cast[buf]);
+          if (i0 < groups)
+            d[i0] = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(y0.x, y0.y), pack2(y0.z, y0.w));
+          if (i1 < groups)
+            d[i1] = make_uint4(pack2(x1.x, x1.y), pack2(x1.z, x1.w), pack2(y1.x, y1.y), pack2(y1.z, y1.w));
+        }
         fence_async_smem();   // the casts -> visible to the bulk stores
         __syncthreads();
         if (threadIdx.x == 0) {
-          for (int j = 0; j < ns; ++j) bulk_store(pb[r * ns + j] + b0, cast[buf], uint32_t(groups) * 16u);
+          for (int j = 0; j < ns; ++j)
+            bulk_store(reinterpret_cast<unsigned char*>(pb[r * ns + j]) + b0 * kOut, cast[buf],
+                       uint32_t(groups) * 8u * kOut);
           bulk_commit();
         }
         buf ^= 1;
@@ -120,8 +140,13 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
     if (threadIdx.x < n_scalar) {
       const int64_t f = threadIdx.x < n_head ? f0 + threadIdx.x : b1 + (threadIdx.x - n_head);
       for (int r = 0; r < nr; ++r) {
-        const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(a.master[f + delta + r * a.rep_stride]));
-        for (int j = 0; j < ns; ++j) pb[r * ns + j][f] = b;
+        const float x = a.master[f + delta + r * a.rep_stride];
+        if (kF32) {
+          for (int j = 0; j < ns; ++j) reinterpret_cast<float*>(pb[r * ns + j])[f] = x;
+        } else {
+          const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+          for (int j = 0; j < ns; ++j) pb[r * ns + j][f] = b;
+        }
       }
     }
   }
@@ -129,19 +154,22 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
 }
 
 cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream) {
-  unshard_kernel<<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (a.param_f32)
+    unshard_kernel<true><<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  else
+    unshard_kernel<false><<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError();
 }
 
 // ---- FSDP2 unshard: host side -----------------------------------------------------------
 
-fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* params, void* stream) {
+fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* params, bool f32, void* stream) {
   clear_error();
   if (!p) return fail(FSP_EINVAL, "plan is NULL");
   if (!params) return fail(FSP_EINVAL, "param_bufs is NULL");
   std::vector<Buf> bufs;
   for (int q = 0; q < p->n_d; ++q)
-    bufs.push_back({params[q], size_t(p->full_len_padded) * 2, "param_bufs[" + std::to_string(q) + "]"});
+    bufs.push_back({params[q], size_t(p->full_len_padded) * (f32 ? 4 : 2), "param_bufs[" + std::to_string(q) + "]"});
   bufs.push_back({master, size_t(p->state_len_total) * 4, "master"});
   for (const Buf& b : bufs) {
     if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
@@ -164,6 +192,7 @@ fsp_status run_unshard(const fsp_plan* p, const float* master, void* const* para
   UnshardArgs a{};
   a.master = master;
   a.n_d = p->n_d;
+  a.param_f32 = f32 ? 1 : 0;
   for (int q = 0; q < p->n_d; ++q) a.params[q] = static_cast<uint16_t*>(params[q]);
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
@@ -215,7 +244,12 @@ fsp_status run_unshard_params(const fsp_plan* p, const fsp_param_table* t, const
 
 extern "C" fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs,
                                   void* cuda_stream) {
-  return fsp::run_unshard(plan, master, param_bufs, cuda_stream);
+  return fsp::run_unshard(plan, master, param_bufs, false, cuda_stream);
+}
+
+extern "C" fsp_status fsp_unshard_fp32(const fsp_plan* plan, const float* master, void* const* param_bufs,
+                                       void* cuda_stream) {
+  return fsp::run_unshard(plan, master, param_bufs, true, cuda_stream);
 }
 
 extern "C" fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,

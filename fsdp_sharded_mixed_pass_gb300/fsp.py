@@ -21,7 +21,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
            "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
-           "fsp_sharded_step_writeback",
+           "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
            "fsp_sharded_step_params", "fsp_sharded_step_params_device_t", "fsp_sharded_step_clipped_params",
            "fsp_unshard_params",
@@ -96,6 +96,8 @@ def lib():
     L.fsp_sharded_step_debug.argtypes = step_args + [vp, vp]
     L.fsp_sharded_step_noalloc.argtypes = step_args + [vp]
     L.fsp_sharded_step_writeback.argtypes = step_args + [vp]
+    L.fsp_sharded_step_fp32_gather.argtypes = step_args + [vp]
+    L.fsp_unshard_fp32.argtypes = [vp, vp, ctypes.POINTER(vp), vp]
     L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
     L.fsp_sharded_step_clipped.restype = ctypes.c_int
     L.fsp_sharded_step_device_t.argtypes = step_args[:-1] + [vp, i32, vp]
@@ -104,7 +106,8 @@ def lib():
     L.fsp_unshard.restype = ctypes.c_int
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param",
                "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
-               "fsp_sharded_step_noalloc", "fsp_sharded_step_writeback", "fsp_param_table_create", "fsp_sharded_step_params",
+               "fsp_sharded_step_noalloc", "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather",
+               "fsp_unshard_fp32", "fsp_param_table_create", "fsp_sharded_step_params",
                "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
@@ -388,6 +391,16 @@ def sharded_step_writeback(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, p
            "fsp_sharded_step_writeback")
 
 
+def sharded_step_fp32_gather(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict,
+                             step: int, stream=None, grad_dtype: str | None = None) -> None:
+    """``sharded_step`` whose all-gather writes the fp32 master into fp32 param buffers."""
+    if param_bufs is None:
+        raise ValueError("param_bufs is required")
+    args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
+    _check(lib().fsp_sharded_step_fp32_gather(*args, ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_sharded_step_fp32_gather")
+
+
 def sharded_step_noalloc(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
                          stream=None, grad_dtype: str | None = None) -> None:
     """``sharded_step`` that allocates no device memory (for callers that cannot
@@ -442,14 +455,16 @@ def sharded_step_clipped(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, par
                                           ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_clipped")
 
 
-def unshard(plan: Plan, master, param_bufs, stream=None) -> None:
-    """FSDP2 unshard: cast every rank's fp32 shard to bf16 and gather it into
-    every rank's full param buffer (of its group).  Asynchronous."""
+def unshard(plan: Plan, master, param_bufs, stream=None, fp32: bool = False) -> None:
+    """FSDP2 unshard: cast every rank's fp32 shard to bf16 (``fp32=True``:
+    copy it as it is into fp32 buffers) and gather it into every rank's full
+    param buffer (of its group).  Asynchronous."""
     if len(param_bufs) != plan.n_d:
         raise ValueError(f"need {plan.n_d} param buffers")
     p = (ctypes.c_void_p * plan.n_d)(*[_ptr(b) for b in param_bufs])
-    _check(lib().fsp_unshard(plan.handle, ctypes.c_void_p(_ptr(master)), p, ctypes.c_void_p(_stream_handle(stream))),
-           "fsp_unshard")
+    fn = lib().fsp_unshard_fp32 if fp32 else lib().fsp_unshard
+    _check(fn(plan.handle, ctypes.c_void_p(_ptr(master)), p, ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_unshard_fp32" if fp32 else "fsp_unshard")
 
 
 def sharded_step_device_t(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step_dev,

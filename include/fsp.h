@@ -276,6 +276,17 @@ fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* const* grad_bu
                                       float* master, float* exp_avg, float* exp_avg_sq, void* const* param_bufs,
                                       const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream);
 
+/* fsp_sharded_step whose all-gather writes the fp32 master itself: FSDP2
+ * with a MixedPrecisionPolicy that keeps parameters in fp32 ("Parallelism
+ * strategies: which state to shard", section 二.5: the policy chooses the
+ * dtype the gathered parameters compute in).  param_bufs: n_d device pointers
+ * to fp32 buffers of full_len_padded elements (owned elements written with the
+ * new master exactly, padding untouched); 4 bytes per element and rank instead
+ * of 2.  Everything else as fsp_sharded_step (param_bufs may not be NULL). */
+fsp_status fsp_sharded_step_fp32_gather(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
+                                        float* master, float* exp_avg, float* exp_avg_sq, void* const* param_bufs,
+                                        const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream);
+
 /* FSDP2 unshard of the plan's parameters (the all-gather before forward and
  * before backward in ZeRO-3 / FSDP2, with a bf16 MixedPrecisionPolicy): every
  * rank's fp32 shard - its owned slots of `master` - is cast to bf16 (round to
@@ -288,6 +299,10 @@ fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* const* grad_bu
  * full_len_padded bf16 each (padding untouched).  Asynchronous on
  * `cuda_stream`; one kernel reading 4 B and writing 2 N_s B per element. */
 fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs, void* cuda_stream);
+
+/* fsp_unshard into fp32 param buffers (full_len_padded fp32 each): the owned
+ * master values copied to every rank of the group, no cast. */
+fsp_status fsp_unshard_fp32(const fsp_plan* plan, const float* master, void* const* param_bufs, void* cuda_stream);
 
 /* As fsp_sharded_step, and also stores the averaged shard gradient of every
  * owned element into reduced_grad (device, fp32, state layout,

@@ -352,3 +352,18 @@ def test_writeback_step_rejects_on_host():
     grads, state, params = _fakes(fsdp)
     args = B._step_args(fsdp, grads, *state, params, HP, 0, "f32")
     assert L.fsp_sharded_step_writeback(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+
+
+def test_fp32_gather_checks_fp32_buffer_sizes_on_host():
+    L = B.lib()
+    plan = fsp.plan_layout([(64, 8)], 4)
+    grads, state, params = _fakes(plan)
+    args = B._step_args(plan, grads, *state, params, HP, 1, "f32")
+    args[6] = None            # param_bufs NULL is not allowed here
+    assert L.fsp_sharded_step_fp32_gather(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+    # fp32 buffers are twice the bf16 size: adjacent fakes laid out for bf16 now overlap
+    g, s, p = _fakes(plan)
+    p = [_Fake(p[0].addr + q * plan.full_len_padded * 2) for q in range(plan.n_d)]
+    args = B._step_args(plan, g, *s, p, HP, 1, "f32")
+    assert L.fsp_sharded_step_fp32_gather(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+    assert "overlaps" in L.fsp_last_error().decode()
