@@ -91,7 +91,8 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
   const char* names[3] = {"master", "exp_avg", "exp_avg_sq"};
   for (int i = 0; i < 3; ++i) {
     if (!state[i] && sbytes) return fail(FSP_EINVAL, std::string(names[i]) + " is NULL");
-    if (reinterpret_cast<uintptr_t>(state[i]) % 16) return fail(FSP_EINVAL, std::string(names[i]) + " is not 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(state[i]) % 16)
+      return fail(FSP_EINVAL, std::string(names[i]) + " is not 16-byte aligned");
   }
   for (int i = 0; i < 3; ++i)
     for (int j = i + 1; j < 3; ++j) {
@@ -236,12 +237,14 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
 
 extern "C" fsp_status fsp_host_step_workspace_bytes(const fsp_plan* plan, int32_t grad_dtype, int64_t chunk_elems,
                                                     size_t* bytes) {
-  fsp::clear_error();
-  if (!plan || !bytes) return fsp::fail(FSP_EINVAL, "NULL argument");
-  if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16) return fsp::fail(FSP_EINVAL, "unknown grad dtype");
-  if (chunk_elems < 0) return fsp::fail(FSP_EINVAL, "chunk_elems must be >= 0 (0: default)");
-  *bytes = fsp::host_workspace_bytes(plan, grad_dtype, chunk_elems);
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!plan || !bytes) return fsp::fail(FSP_EINVAL, "NULL argument");
+    if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16) return fsp::fail(FSP_EINVAL, "unknown grad dtype");
+    if (chunk_elems < 0) return fsp::fail(FSP_EINVAL, "chunk_elems must be >= 0 (0: default)");
+    *bytes = fsp::host_workspace_bytes(plan, grad_dtype, chunk_elems);
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_grads, int32_t grad_dtype,
@@ -249,7 +252,9 @@ extern "C" fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* co
                                             void* const* host_params, const fsp_adamw_hparams* hp, int64_t step,
                                             void* workspace, size_t workspace_bytes, int64_t chunk_elems,
                                             void* cuda_stream) {
-  return fsp::run_step_host(plan, host_grads, grad_dtype, master, exp_avg, exp_avg_sq, host_params, hp, step,
-                            workspace, workspace_bytes, chunk_elems, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_host(plan, host_grads, grad_dtype, master, exp_avg, exp_avg_sq, host_params, hp, step,
+                              workspace, workspace_bytes, chunk_elems, cuda_stream);
+  });
 }
 

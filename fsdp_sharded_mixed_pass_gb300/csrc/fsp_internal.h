@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -88,4 +89,19 @@ namespace fsp {
 // Records the thread-local message behind an error status and returns it.
 fsp_status fail(fsp_status s, const std::string& msg);
 void clear_error();
+// As fail, for a message that must not allocate (a string literal).
+fsp_status fail_static(fsp_status s, const char* msg) noexcept;
+
+// Runs the body of a C entry point: a host allocation failure (or any other
+// C++ exception) becomes a status instead of crossing the C boundary.
+template <typename F>
+fsp_status guard(F&& body) noexcept {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return fail_static(FSP_ENOMEM, "host allocation failed");
+  } catch (...) {
+    return fail_static(FSP_EINVAL, "unexpected host-side error");
+  }
+}
 }  // namespace fsp

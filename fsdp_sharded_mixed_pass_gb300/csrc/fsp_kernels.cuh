@@ -583,7 +583,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           } else {
 #pragma unroll
             for (int q = 0; q < N; ++q)
-              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G), static_cast<const unsigned char*>(a.grads[q]) + c * G,
+              bulk_load(smem_addr(st + Cfg::kGradOff + q * E * G),
+                        static_cast<const unsigned char*>(a.grads[q]) + c * G,
                         len * G, bar);
           }
 #pragma unroll
@@ -642,7 +643,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
           if (a.gather && a.param_f32) {   // the all-gather of the fp32 master itself (full-size buffers)
 #pragma unroll
-            for (int j = 0; j < NS; ++j) bulk_store(reinterpret_cast<float*>(a.params[r * NS + j]) + h.c, th_s, len * 4);
+            for (int j = 0; j < NS; ++j)
+              bulk_store(reinterpret_cast<float*>(a.params[r * NS + j]) + h.c, th_s, len * 4);
           } else if (a.gather && per_param) {   // the all-gather
 #pragma unroll
             for (int j = 0; j < NS; ++j) bulk_store(spb[r * NS + j] + h.c, p_s, len * 2);

@@ -104,7 +104,8 @@ fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t
   }
   const size_t bytes = std::max<size_t>(1, vg.size()) * sizeof(void*);
   e = cudaMalloc(reinterpret_cast<void**>(&t->vgrads), bytes);
-  if (e == cudaSuccess && !vg.empty()) e = cudaMemcpy(t->vgrads, vg.data(), vg.size() * sizeof(void*), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !vg.empty())
+    e = cudaMemcpy(t->vgrads, vg.data(), vg.size() * sizeof(void*), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && param_ptrs) {
     e = cudaMalloc(reinterpret_cast<void**>(&t->vparams), bytes);
     if (e == cudaSuccess && !vp.empty())
@@ -235,7 +236,9 @@ fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, 
 
 extern "C" fsp_status fsp_param_table_create(const fsp_plan* plan, const void* const* grad_ptrs, int32_t grad_dtype,
                                              void* const* param_ptrs, fsp_param_table** out) {
-  return fsp::create_table(plan, grad_ptrs, grad_dtype, param_ptrs, out);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::create_table(plan, grad_ptrs, grad_dtype, param_ptrs, out);
+  });
 }
 
 extern "C" void fsp_param_table_destroy(fsp_param_table* table) { fsp::free_table(table); }
@@ -244,19 +247,25 @@ extern "C" fsp_status fsp_sharded_step_params_device_t(const fsp_plan* plan, con
                                                        float* master, float* exp_avg, float* exp_avg_sq,
                                                        const fsp_adamw_hparams* hp, int64_t* step_dev,
                                                        int32_t advance, void* cuda_stream) {
-  return fsp::run_step_params_device_t(plan, table, master, exp_avg, exp_avg_sq, hp, step_dev, advance, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_params_device_t(plan, table, master, exp_avg, exp_avg_sq, hp, step_dev, advance, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_clipped_params(const fsp_plan* plan, const fsp_param_table* table,
                                                       float* master, float* exp_avg, float* exp_avg_sq,
                                                       const fsp_adamw_hparams* hp, int64_t step, float max_norm,
                                                       float* norm_out, void* cuda_stream) {
-  return fsp::run_step_clipped_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, max_norm, norm_out,
-                                      cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_clipped_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, max_norm, norm_out,
+                                        cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
                                               float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
                                               int64_t step, void* cuda_stream) {
-  return fsp::run_step_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, cuda_stream);
+  });
 }

@@ -46,12 +46,23 @@ void append_tiles(const fsp_segment& s, std::vector<Tile>& out) {
 
 }  // namespace
 
+// The message buffer used when recording a message could itself fail.
+thread_local const char* g_static_error = nullptr;
+
 fsp_status fail(fsp_status s, const std::string& msg) {
+  g_static_error = nullptr;
   g_last_error = msg;
   return s;
 }
-void clear_error() { g_last_error.clear(); }
-const char* last_error() { return g_last_error.c_str(); }
+fsp_status fail_static(fsp_status s, const char* msg) noexcept {
+  g_static_error = msg;
+  return s;
+}
+void clear_error() {
+  g_static_error = nullptr;
+  g_last_error.clear();
+}
+const char* last_error() { return g_static_error ? g_static_error : g_last_error.c_str(); }
 
 }  // namespace fsp
 
@@ -222,92 +233,106 @@ fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params
 
 extern "C" fsp_status fsp_plan_layout(const int64_t* dims, const int32_t* ndims, int32_t n_params,
                                       int32_t n_d, int32_t mode, fsp_plan** out) {
-  fsp::clear_error();
-  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout: out is NULL");
-  *out = nullptr;
-  if (n_d < 1 || n_d > fsp::kMaxRanks) return fail(FSP_EINVAL, "fsp_plan_layout: n_d must be in [1, 64]");
-  if (mode != FSP_MODE_FSDP2_SHARD0 && mode != FSP_MODE_DISTOPT_FLAT)
-    return fail(FSP_EINVAL, "fsp_plan_layout: unknown mode");
-  return make_plan(dims, ndims, n_params, 1, n_d, mode, 1, out);
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!out) return fail(FSP_EINVAL, "fsp_plan_layout: out is NULL");
+    *out = nullptr;
+    if (n_d < 1 || n_d > fsp::kMaxRanks) return fail(FSP_EINVAL, "fsp_plan_layout: n_d must be in [1, 64]");
+    if (mode != FSP_MODE_FSDP2_SHARD0 && mode != FSP_MODE_DISTOPT_FLAT)
+      return fail(FSP_EINVAL, "fsp_plan_layout: unknown mode");
+    return make_plan(dims, ndims, n_params, 1, n_d, mode, 1, out);
+  });
 }
 
 extern "C" fsp_status fsp_plan_layout_hsdp(const int64_t* dims, const int32_t* ndims, int32_t n_params,
                                            int32_t n_replicate, int32_t n_shard, fsp_plan** out) {
-  fsp::clear_error();
-  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: out is NULL");
-  *out = nullptr;
-  if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
-    return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: need n_replicate, n_shard >= 1 and their product <= 64");
-  return make_plan(dims, ndims, n_params, n_replicate, n_shard, FSP_MODE_HSDP, 1, out);
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: out is NULL");
+    *out = nullptr;
+    if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
+      return fail(FSP_EINVAL, "fsp_plan_layout_hsdp: need n_replicate, n_shard >= 1 and their product <= 64");
+    return make_plan(dims, ndims, n_params, n_replicate, n_shard, FSP_MODE_HSDP, 1, out);
+  });
 }
 
 extern "C" fsp_status fsp_plan_layout_params(const int64_t* dims, const int32_t* ndims, int32_t n_params,
                                              int32_t n_replicate, int32_t n_shard, fsp_plan** out) {
-  fsp::clear_error();
-  if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_params: out is NULL");
-  *out = nullptr;
-  if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
-    return fail(FSP_EINVAL, "fsp_plan_layout_params: need n_replicate, n_shard >= 1 and their product <= 64");
-  return make_plan(dims, ndims, n_params, n_replicate, n_shard,
-                   n_replicate == 1 ? FSP_MODE_FSDP2_SHARD0 : FSP_MODE_HSDP, int32_t(fsp::kParamAlign), out);
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!out) return fail(FSP_EINVAL, "fsp_plan_layout_params: out is NULL");
+    *out = nullptr;
+    if (n_replicate < 1 || n_shard < 1 || int64_t(n_replicate) * n_shard > fsp::kMaxRanks)
+      return fail(FSP_EINVAL, "fsp_plan_layout_params: need n_replicate, n_shard >= 1 and their product <= 64");
+    return make_plan(dims, ndims, n_params, n_replicate, n_shard,
+                     n_replicate == 1 ? FSP_MODE_FSDP2_SHARD0 : FSP_MODE_HSDP, int32_t(fsp::kParamAlign), out);
+  });
 }
 
 extern "C" fsp_status fsp_plan_param(const fsp_plan* p, int32_t i, int64_t* full_off, int64_t* numel) {
-  fsp::clear_error();
-  if (!p || !full_off || !numel) return fail(FSP_EINVAL, "fsp_plan_param: NULL argument");
-  if (i < 0 || i >= p->n_params) return fail(FSP_EINVAL, "fsp_plan_param: index out of range");
-  *full_off = p->param_off[size_t(i)];
-  *numel = p->param_numel[size_t(i)];
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!p || !full_off || !numel) return fail(FSP_EINVAL, "fsp_plan_param: NULL argument");
+    if (i < 0 || i >= p->n_params) return fail(FSP_EINVAL, "fsp_plan_param: index out of range");
+    *full_off = p->param_off[size_t(i)];
+    *numel = p->param_numel[size_t(i)];
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_plan_info_get(const fsp_plan* p, fsp_plan_info* out) {
-  fsp::clear_error();
-  if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_info_get: NULL argument");
-  out->n_d = p->n_d;
-  out->n_params = p->n_params;
-  out->mode = p->mode;
-  out->tile_elems = int32_t(fsp::kTileElems);
-  out->valid_elems = p->valid_elems;
-  out->full_len_padded = p->full_len_padded;
-  out->state_len_per_rank = p->state_len_per_rank;
-  out->state_len_total = p->state_len_total;
-  out->n_segments = int64_t(p->segments.size());
-  out->n_tiles = int64_t(p->tiles.size());
-  out->n_replicate = p->n_rep;
-  out->n_shard = p->n_shard;
-  out->param_align = p->param_align;
-  out->reserved = 0;
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_info_get: NULL argument");
+    out->n_d = p->n_d;
+    out->n_params = p->n_params;
+    out->mode = p->mode;
+    out->tile_elems = int32_t(fsp::kTileElems);
+    out->valid_elems = p->valid_elems;
+    out->full_len_padded = p->full_len_padded;
+    out->state_len_per_rank = p->state_len_per_rank;
+    out->state_len_total = p->state_len_total;
+    out->n_segments = int64_t(p->segments.size());
+    out->n_tiles = int64_t(p->tiles.size());
+    out->n_replicate = p->n_rep;
+    out->n_shard = p->n_shard;
+    out->param_align = p->param_align;
+    out->reserved = 0;
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_plan_segment(const fsp_plan* p, int64_t i, fsp_segment* out) {
-  fsp::clear_error();
-  if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_segment: NULL argument");
-  if (i < 0 || i >= int64_t(p->segments.size())) return fail(FSP_EINVAL, "fsp_plan_segment: index out of range");
-  *out = p->segments[size_t(i)];
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_segment: NULL argument");
+    if (i < 0 || i >= int64_t(p->segments.size())) return fail(FSP_EINVAL, "fsp_plan_segment: index out of range");
+    *out = p->segments[size_t(i)];
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_plan_ledger(const fsp_plan* p, int32_t grad_dtype, fsp_ledger* out) {
-  fsp::clear_error();
-  if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_ledger: NULL argument");
-  if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16)
-    return fail(FSP_EINVAL, "fsp_plan_ledger: unknown grad dtype");
-  const double P = double(p->valid_elems), n = double(p->n_d);
-  const double ns = double(p->n_shard), nr = double(p->n_rep);
-  const double g = grad_dtype == FSP_DTYPE_F32 ? 4.0 : 2.0;
-  out->resident_ddp = (2.0 + g + 12.0) * P;
-  out->resident_distopt = (2.0 + g) * P + 12.0 * P / n;
-  out->resident_zero2 = 2.0 * P + (g + 12.0) * P / n;
-  out->resident_fsdp = (2.0 + g + 12.0) * P / n;
-  // collectives of this plan's own layout (the shard group for HSDP)
-  out->reduce_scatter_sent = (ns - 1.0) / ns * g * P;
-  out->all_gather_sent = (ns - 1.0) / ns * 2.0 * P;
-  out->step_hbm_bytes = (n * g + 24.0 * nr + 2.0 * n) * P;
-  out->resident_hsdp = (2.0 + g + 12.0) * P / ns;
-  out->cross_group_all_reduce_sent = nr > 1.0 ? 2.0 * (nr - 1.0) / nr * g * P / ns : 0.0;
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!p || !out) return fail(FSP_EINVAL, "fsp_plan_ledger: NULL argument");
+    if (grad_dtype != FSP_DTYPE_F32 && grad_dtype != FSP_DTYPE_BF16)
+      return fail(FSP_EINVAL, "fsp_plan_ledger: unknown grad dtype");
+    const double P = double(p->valid_elems), n = double(p->n_d);
+    const double ns = double(p->n_shard), nr = double(p->n_rep);
+    const double g = grad_dtype == FSP_DTYPE_F32 ? 4.0 : 2.0;
+    out->resident_ddp = (2.0 + g + 12.0) * P;
+    out->resident_distopt = (2.0 + g) * P + 12.0 * P / n;
+    out->resident_zero2 = 2.0 * P + (g + 12.0) * P / n;
+    out->resident_fsdp = (2.0 + g + 12.0) * P / n;
+    // collectives of this plan's own layout (the shard group for HSDP)
+    out->reduce_scatter_sent = (ns - 1.0) / ns * g * P;
+    out->all_gather_sent = (ns - 1.0) / ns * 2.0 * P;
+    out->step_hbm_bytes = (n * g + 24.0 * nr + 2.0 * n) * P;
+    out->resident_hsdp = (2.0 + g + 12.0) * P / ns;
+    out->cross_group_all_reduce_sent = nr > 1.0 ? 2.0 * (nr - 1.0) / nr * g * P / ns : 0.0;
+    return FSP_OK;
+  });
 }
 
 extern "C" void fsp_plan_destroy(fsp_plan* p) {

@@ -69,7 +69,8 @@ template <int... Ns>
 struct NormKernelTable {
   static KernelInfo get(int n) {
     KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0>), kGenericThreads, 0, false};
-    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0, false},
+    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0,
+                                false},
                  0)
               : 0),
      ...);
@@ -434,7 +435,8 @@ fsp_status advance_step(int64_t* step_dev, void* stream) {
 // norm_out = {0, 1} for a plan with nothing to reduce.
 fsp_status clipped_empty(float* norm_out, void* stream) {
   const float out[2] = {0.f, 1.f};
-  cudaError_t e = cudaMemcpyAsync(norm_out, out, sizeof(out), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      cudaMemcpyAsync(norm_out, out, sizeof(out), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FSP_OK : fail(FSP_ECUDA, cuda_msg("writing norm_out", e));
 }
@@ -463,78 +465,88 @@ extern "C" fsp_status fsp_sharded_step(const fsp_plan* plan, const void* const* 
                                        float* master, float* exp_avg, float* exp_avg_sq,
                                        void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                        void* cuda_stream) {
-  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, false,
-                       nullptr, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, false,
+                         nullptr, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_clipped(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
                                                float* master, float* exp_avg, float* exp_avg_sq,
                                                void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                                float max_norm, float* norm_out, void* cuda_stream) {
-  return fsp::run_step_clipped(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
-                               max_norm, norm_out, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_clipped(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                                 max_norm, norm_out, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void* const* grad_bufs,
                                                 int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
                                                 void* const* param_bufs, const fsp_adamw_hparams* hp,
                                                 int64_t* step_dev, int32_t advance, void* cuda_stream) {
-  using namespace fsp;
-  clear_error();
-  if (!step_dev) return fail(FSP_EINVAL, "step_dev is NULL");
-  if (reinterpret_cast<uintptr_t>(step_dev) % 8 != 0) return fail(FSP_EINVAL, "step_dev is not 8-byte aligned");
-  // t only enters the bias corrections, which the kernel recomputes from *step_dev
-  fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, {});
-  if (s != FSP_OK) return s;
-  s = check_allocation(step_dev, sizeof(int64_t), "step_dev");
-  if (s != FSP_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (!plan->tiles.empty()) {
-    StepArgs a;
-    s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, &a);
+  return fsp::guard([&]() -> fsp_status {
+    using namespace fsp;
+    clear_error();
+    if (!step_dev) return fail(FSP_EINVAL, "step_dev is NULL");
+    if (reinterpret_cast<uintptr_t>(step_dev) % 8 != 0) return fail(FSP_EINVAL, "step_dev is not 8-byte aligned");
+    // t only enters the bias corrections, which the kernel recomputes from *step_dev
+    fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, {});
     if (s != FSP_OK) return s;
-    a.step_dev = step_dev;
-    s = launch(a, grad_dtype, cuda_stream);
+    s = check_allocation(step_dev, sizeof(int64_t), "step_dev");
     if (s != FSP_OK) return s;
-  }
-  if (advance) return advance_step(step_dev, st);
-  return FSP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (!plan->tiles.empty()) {
+      StepArgs a;
+      s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, &a);
+      if (s != FSP_OK) return s;
+      a.step_dev = step_dev;
+      s = launch(a, grad_dtype, cuda_stream);
+      if (s != FSP_OK) return s;
+    }
+    if (advance) return advance_step(step_dev, st);
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* const* grad_bufs, int32_t grad_dtype,
                                                  float* master, float* exp_avg, float* exp_avg_sq,
                                                  void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
                                                  void* cuda_stream) {
-  using namespace fsp;
-  clear_error();
-  if (plan && plan->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the write-back step is for FSDP2 and DistOpt plans");
-  if (grad_dtype != FSP_DTYPE_F32)
-    return fail(FSP_EUNSUPPORTED, "the write-back step stores the averaged gradient into fp32 grad buffers");
-  const void* const* grads = reinterpret_cast<const void* const*>(grad_bufs);
-  fsp_status s = check_device_step(plan, grads, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, {});
-  if (s != FSP_OK || plan->tiles.empty()) return s;
-  StepArgs a;
-  s = step_args(plan, grads, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
-  if (s != FSP_OK) return s;
-  a.writeback = 1;
-  return launch(a, grad_dtype, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    using namespace fsp;
+    clear_error();
+    if (plan && plan->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the write-back step is for FSDP2 and DistOpt plans");
+    if (grad_dtype != FSP_DTYPE_F32)
+      return fail(FSP_EUNSUPPORTED, "the write-back step stores the averaged gradient into fp32 grad buffers");
+    const void* const* grads = reinterpret_cast<const void* const*>(grad_bufs);
+    fsp_status s = check_device_step(plan, grads, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, {});
+    if (s != FSP_OK || plan->tiles.empty()) return s;
+    StepArgs a;
+    s = step_args(plan, grads, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
+    if (s != FSP_OK) return s;
+    a.writeback = 1;
+    return launch(a, grad_dtype, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_fp32_gather(const fsp_plan* plan, const void* const* grad_bufs,
                                                    int32_t grad_dtype, float* master, float* exp_avg,
                                                    float* exp_avg_sq, void* const* param_bufs,
                                                    const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream) {
-  using namespace fsp;
-  clear_error();
-  if (!param_bufs) return fail(FSP_EINVAL, "param_bufs is NULL");
-  fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
-                                   {}, 4);
-  if (s != FSP_OK || plan->tiles.empty()) return s;
-  StepArgs a;
-  s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
-  if (s != FSP_OK) return s;
-  a.param_f32 = 1;
-  return launch(a, grad_dtype, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    using namespace fsp;
+    clear_error();
+    if (!param_bufs) return fail(FSP_EINVAL, "param_bufs is NULL");
+    fsp_status s = check_device_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                                     {}, 4);
+    if (s != FSP_OK || plan->tiles.empty()) return s;
+    StepArgs a;
+    s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
+    if (s != FSP_OK) return s;
+    a.param_f32 = 1;
+    return launch(a, grad_dtype, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs,
@@ -542,8 +554,10 @@ extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* c
                                              float* exp_avg_sq, void* const* param_bufs,
                                              const fsp_adamw_hparams* hp, int64_t step, float* reduced_grad,
                                              void* cuda_stream) {
-  return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, true,
-                       reduced_grad, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step, true,
+                         reduced_grad, cuda_stream);
+  });
 }
 
 // ---- entry point that allocates nothing --------------------------------------
@@ -679,36 +693,42 @@ extern "C" fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void*
                                                int32_t grad_dtype, float* master, float* exp_avg,
                                                float* exp_avg_sq, void* const* param_bufs,
                                                const fsp_adamw_hparams* hp, int64_t step, void* cuda_stream) {
-  return fsp::run_step_noalloc(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
-                               cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_noalloc(plan, grad_bufs, grad_dtype, master, exp_avg, exp_avg_sq, param_bufs, hp, step,
+                                 cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_device_error(uint32_t* bits) {
-  fsp::clear_error();
-  if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, fsp::g_fsp_device_error, sizeof(v));
-  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("reading the device error word", e));
-  const unsigned int zero = 0;
-  e = cudaMemcpyToSymbol(fsp::g_fsp_device_error, &zero, sizeof(zero));
-  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("clearing the device error word", e));
-  *bits = v;
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, fsp::g_fsp_device_error, sizeof(v));
+    if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("reading the device error word", e));
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(fsp::g_fsp_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("clearing the device error word", e));
+    *bits = v;
+    return FSP_OK;
+  });
 }
 
 extern "C" fsp_status fsp_selftest_bounded_wait(uint32_t limit_ms, uint32_t* bits) {
-  fsp::clear_error();
-  if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
-  if (limit_ms < 1 || limit_ms > 2000) return fsp::fail(FSP_EINVAL, "limit_ms must be in [1, 2000]");
-  uint32_t before = 0;
-  fsp_status s = fsp_device_error(&before);   // start from a clear word
-  if (s != FSP_OK) return s;
-  fsp::bounded_wait_selftest_kernel<<<1, 32>>>(uint64_t(limit_ms) * 1000000ull);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("bounded-wait self-test", e));
-  s = fsp_device_error(bits);
-  if (s != FSP_OK) return s;
-  *bits |= before;
-  return FSP_OK;
+  return fsp::guard([&]() -> fsp_status {
+    fsp::clear_error();
+    if (!bits) return fsp::fail(FSP_EINVAL, "bits is NULL");
+    if (limit_ms < 1 || limit_ms > 2000) return fsp::fail(FSP_EINVAL, "limit_ms must be in [1, 2000]");
+    uint32_t before = 0;
+    fsp_status s = fsp_device_error(&before);   // start from a clear word
+    if (s != FSP_OK) return s;
+    fsp::bounded_wait_selftest_kernel<<<1, 32>>>(uint64_t(limit_ms) * 1000000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fsp::fail(FSP_ECUDA, fsp::cuda_msg("bounded-wait self-test", e));
+    s = fsp_device_error(bits);
+    if (s != FSP_OK) return s;
+    *bits |= before;
+    return FSP_OK;
+  });
 }

@@ -244,15 +244,21 @@ fsp_status run_unshard_params(const fsp_plan* p, const fsp_param_table* t, const
 
 extern "C" fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs,
                                   void* cuda_stream) {
-  return fsp::run_unshard(plan, master, param_bufs, false, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_unshard(plan, master, param_bufs, false, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_unshard_fp32(const fsp_plan* plan, const float* master, void* const* param_bufs,
                                        void* cuda_stream) {
-  return fsp::run_unshard(plan, master, param_bufs, true, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_unshard(plan, master, param_bufs, true, cuda_stream);
+  });
 }
 
 extern "C" fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,
                                          void* cuda_stream) {
-  return fsp::run_unshard_params(plan, table, master, cuda_stream);
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_unshard_params(plan, table, master, cuda_stream);
+  });
 }
