@@ -45,10 +45,14 @@ def test_device_t_eager_equals_host_t(mode, n_d, n_rep, dtype):
     assert fsp.device_error() == 0
 
 
-def test_graph_of_one_step_replayed():
-    ref = DeviceCase(SHAPES, 8, "fsdp2", "f32", 62)
-    dev = DeviceCase(SHAPES, 8, "fsdp2", "f32", 62)
-    fresh = DeviceCase(SHAPES, 8, "fsdp2", "f32", 62)
+BIG = [(3000, 4096), (4099,), (77, 3)]   # enough tiles per CTA for the in-order (counter) schedule
+
+
+@pytest.mark.parametrize("shapes", [SHAPES, BIG], ids=["small", "large"])
+def test_graph_of_one_step_replayed(shapes):
+    ref = DeviceCase(shapes, 8, "fsdp2", "f32", 62)
+    dev = DeviceCase(shapes, 8, "fsdp2", "f32", 62)
+    fresh = DeviceCase(shapes, 8, "fsdp2", "f32", 62)
     t = torch.tensor([1], dtype=torch.int64, device="cuda")
     g, s, p = _bufs(dev)
     fsp.sharded_step_device_t(dev.plan, g, *s, p, HP, t, advance=False)   # first call outside capture
