@@ -307,7 +307,7 @@ fsp_status fsp_unshard_fp32(const fsp_plan* plan, const float* master, void* con
 /* As fsp_sharded_step, and also stores the averaged shard gradient of every
  * owned element into reduced_grad (device, fp32, state layout,
  * state_len_total elements; padding slots untouched).  For testing: it adds
- * 8 bytes of traffic per element. */
+ * a 4-byte store per element. */
 fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
                                   float* master, float* exp_avg, float* exp_avg_sq,
                                   void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,
