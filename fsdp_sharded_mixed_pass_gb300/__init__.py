@@ -29,6 +29,7 @@ from .fsp import (  # noqa: F401
     sharded_step_params,
     sharded_step_params_device_t,
     sharded_step_writeback,
+    sharded_step_writeback_params,
     sharded_step_fp32_gather,
     unshard,
     unshard_params,

@@ -214,6 +214,21 @@ fsp_status run_step_params_device_t(const fsp_plan* p, const fsp_param_table* t,
   return advance ? advance_step(step_dev, stream) : FSP_OK;
 }
 
+fsp_status run_step_writeback_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
+                                     const fsp_adamw_hparams* hp, int64_t step, void* stream) {
+  clear_error();
+  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the write-back step is for FSDP2 plans");
+  if (t && t->grad_dtype != FSP_DTYPE_F32)
+    return fail(FSP_EUNSUPPORTED, "the write-back step stores the averaged gradient into fp32 gradient tensors");
+  fsp_status s = check_params_step(p, t, master, m, v, hp, step, {});
+  if (s != FSP_OK || p->tiles.empty()) return s;
+  StepArgs a;
+  s = params_step_args(p, t, master, m, v, hp, step, &a);
+  if (s != FSP_OK) return s;
+  a.writeback = 1;
+  return launch(a, t->grad_dtype, stream);
+}
+
 fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
                                    const fsp_adamw_hparams* hp, int64_t step, float max_norm, float* norm_out,
                                    void* stream) {
@@ -249,6 +264,15 @@ extern "C" fsp_status fsp_sharded_step_params_device_t(const fsp_plan* plan, con
                                                        int32_t advance, void* cuda_stream) {
   return fsp::guard([&]() -> fsp_status {
     return fsp::run_step_params_device_t(plan, table, master, exp_avg, exp_avg_sq, hp, step_dev, advance, cuda_stream);
+  });
+}
+
+extern "C" fsp_status fsp_sharded_step_writeback_params(const fsp_plan* plan, const fsp_param_table* table,
+                                                        float* master, float* exp_avg, float* exp_avg_sq,
+                                                        const fsp_adamw_hparams* hp, int64_t step,
+                                                        void* cuda_stream) {
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_step_writeback_params(plan, table, master, exp_avg, exp_avg_sq, hp, step, cuda_stream);
   });
 }
 

@@ -24,6 +24,7 @@ EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", 
            "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
            "fsp_sharded_step_params", "fsp_sharded_step_params_device_t", "fsp_sharded_step_clipped_params",
+           "fsp_sharded_step_writeback_params",
            "fsp_unshard_params",
            "fsp_sharded_step_noalloc", "fsp_unshard", "fsp_device_error", "fsp_selftest_bounded_wait", "fsp_status_string",
            "fsp_last_error")
@@ -84,6 +85,7 @@ def lib():
     L.fsp_sharded_step_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, vp]
     L.fsp_unshard_params.argtypes = [vp, vp, vp, vp]
     L.fsp_sharded_step_params_device_t.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), vp, i32, vp]
+    L.fsp_sharded_step_writeback_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, vp]
     L.fsp_sharded_step_clipped_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, ctypes.c_float,
                                                   vp, vp]
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
@@ -108,7 +110,8 @@ def lib():
                "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
                "fsp_sharded_step_noalloc", "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather",
                "fsp_unshard_fp32", "fsp_param_table_create", "fsp_sharded_step_params",
-               "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params"):
+               "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params",
+               "fsp_sharded_step_writeback_params"):
         getattr(L, fn).restype = ctypes.c_int
     L.fsp_host_step_workspace_bytes.argtypes = [vp, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
     L.fsp_host_step_workspace_bytes.restype = ctypes.c_int
@@ -303,6 +306,16 @@ def sharded_step_params_device_t(plan: Plan, table: ParamTable, master, exp_avg,
                                                   ctypes.byref(_hp(hparams)), ctypes.c_void_p(_ptr(step_dev)),
                                                   1 if advance else 0, ctypes.c_void_p(_stream_handle(stream))),
            "fsp_sharded_step_params_device_t")
+
+
+def sharded_step_writeback_params(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_sq, hparams: dict,
+                                  step: int, stream=None) -> None:
+    """``sharded_step_writeback`` on the per-parameter tensors of ``table``."""
+    _check(lib().fsp_sharded_step_writeback_params(plan.handle, table.handle, ctypes.c_void_p(_ptr(master)),
+                                                   ctypes.c_void_p(_ptr(exp_avg)), ctypes.c_void_p(_ptr(exp_avg_sq)),
+                                                   ctypes.byref(_hp(hparams)), int(step),
+                                                   ctypes.c_void_p(_stream_handle(stream))),
+           "fsp_sharded_step_writeback_params")
 
 
 def sharded_step_clipped_params(plan: Plan, table: ParamTable, master, exp_avg, exp_avg_sq, hparams: dict,

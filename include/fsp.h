@@ -382,6 +382,14 @@ fsp_status fsp_sharded_step_params_device_t(const fsp_plan* plan, const fsp_para
                                             float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
                                             int64_t* step_dev, int32_t advance, void* cuda_stream);
 
+/* fsp_sharded_step_writeback on the tensors of `table` (an FSDP2
+ * per-parameter plan, fp32 gradients; others: FSP_EUNSUPPORTED): every
+ * element's averaged gradient also lands in its owner's slice of the owner's
+ * gradient tensor, in the same pass. */
+fsp_status fsp_sharded_step_writeback_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
+                                             float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
+                                             int64_t step, void* cuda_stream);
+
 /* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 per-parameter
  * plan, fp32 gradients; others: FSP_EUNSUPPORTED): every element's averaged
  * gradient is written back into its owner's slice of the owner's gradient

@@ -238,3 +238,22 @@ def test_per_param_device_t_replayed_in_a_cuda_graph():
     pc.state_matches_flat()
     pc.params_match_flat()
     assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("shapes", [SHAPES, BIG], ids=["small", "large"])
+def test_per_param_writeback_equals_flat(shapes):
+    flat = DeviceCase(shapes, 4, "fsdp2", "f32", 107)
+    pc = ParamCase(flat)
+    fsp.sharded_step_writeback(flat.plan, [g.t for g in flat.grads], *[s.t for s in flat.state],
+                               [p.t for p in flat.params], HP, 10)
+    fsp.sharded_step_writeback_params(pc.plan, pc.table, *[s.t for s in pc.state], HP, 10)
+    torch.cuda.synchronize()
+    pc.state_matches_flat()
+    pc.params_match_flat()
+    for q in range(flat.n_d):
+        fb = flat.grads[q].bits()
+        for i, s in enumerate(shapes):
+            n = _numel(s)
+            assert np.array_equal(pc.grads[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n]), f"rank {q} grad {i}"
+    assert pc.guards_intact()
+    assert fsp.device_error() == 0
