@@ -44,7 +44,7 @@ struct StepArgs {
   const int64_t* step_dev;  // update index t in device memory (nullptr: t is folded into c)
   int gather;               // 0: ZeRO-3 / FSDP2 reshard - no all-gather, params untouched
   int writeback;            // 1: the averaged gradient also goes into the owner's slice of its fp32 grad buffer
-  int param_f32;            // 1: params[] are fp32 buffers (all-gather of the fp32 master, no bf16 cast)
+  int param_f32;            // 1: the parameter buffers / tensors are fp32 (all-gather of the master, no cast)
   float lr;                 // kept to rebuild c's t-dependent scalars from *step_dev
   Coeffs c;
 };

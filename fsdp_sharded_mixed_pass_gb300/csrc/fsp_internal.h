@@ -78,8 +78,9 @@ struct fsp_param_table {
   const fsp_plan* plan = nullptr;
   int device = -1;
   int32_t grad_dtype = 0;
+  int32_t param_dtype = 1;         // fsp_dtype of the param tensors (FSP_DTYPE_BF16 or FSP_DTYPE_F32)
   const void** vgrads = nullptr;   // device, n_params * n_d entries
-  uint16_t** vparams = nullptr;    // device, or nullptr: no param tensors
+  uint16_t** vparams = nullptr;    // device, or nullptr: no param tensors (fp32 ones are cast back)
   // every registered tensor as [begin, end) device addresses, sorted by begin
   std::vector<std::pair<uintptr_t, uintptr_t>> spans;
 };

@@ -641,7 +641,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           bulk_store(a.master + s, th_s, len * 4);
           bulk_store(a.m + s, th_s + E * 4, len * 4);
           bulk_store(a.v + s, th_s + 2 * E * 4, len * 4);
-          if (a.gather && a.param_f32) {   // the all-gather of the fp32 master itself (full-size buffers)
+          if (a.gather && a.param_f32 && per_param) {   // the all-gather of the fp32 master itself
+#pragma unroll
+            for (int j = 0; j < NS; ++j) bulk_store(reinterpret_cast<float*>(spb[r * NS + j]) + h.c, th_s, len * 4);
+          } else if (a.gather && a.param_f32) {
 #pragma unroll
             for (int j = 0; j < NS; ++j)
               bulk_store(reinterpret_cast<float*>(a.params[r * NS + j]) + h.c, th_s, len * 4);

@@ -35,7 +35,7 @@ void free_table(fsp_param_table* t) {
 }
 
 fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t dtype, void* const* param_ptrs,
-                        fsp_param_table** out) {
+                        int32_t param_dtype, fsp_param_table** out) {
   clear_error();
   if (!out) return fail(FSP_EINVAL, "out is NULL");
   *out = nullptr;
@@ -43,6 +43,8 @@ fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t
   if (p->param_align != kParamAlign)
     return fail(FSP_EINVAL, "the plan is not a per-parameter plan (fsp_plan_layout_params)");
   if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
+  if (param_dtype != FSP_DTYPE_F32 && param_dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown param dtype");
+  const size_t psz = param_dtype == FSP_DTYPE_F32 ? 4 : 2;
   const int n = p->n_d, np = p->n_params;
   if (np > 0 && !grad_ptrs) return fail(FSP_EINVAL, "grad_ptrs is NULL");
   const size_t g = dtype == FSP_DTYPE_F32 ? 4 : 2;
@@ -58,7 +60,7 @@ fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t
       if (numel == 0) continue;
       for (int kind = 0; kind < (param_ptrs ? 2 : 1); ++kind) {
         const void* ptr = kind == 0 ? grad_ptrs[size_t(q) * np + i] : param_ptrs[size_t(q) * np + i];
-        const size_t esz = kind == 0 ? g : 2;
+        const size_t esz = kind == 0 ? g : psz;
         const std::string name = std::string(kind == 0 ? "grad_ptrs[" : "param_ptrs[") +
                                  std::to_string(size_t(q) * np + i) + "]";
         if (!ptr) return fail(FSP_EINVAL, name + " is NULL");
@@ -95,6 +97,7 @@ fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t
   t->plan = p;
   t->device = dev;
   t->grad_dtype = dtype;
+  t->param_dtype = param_dtype;
   try {
     t->spans.reserve(spans.size());
     for (size_t k : order) t->spans.push_back(spans[k]);
@@ -171,6 +174,7 @@ fsp_status params_step_args(const fsp_plan* p, const fsp_param_table* t, float* 
   a->vgrads = t->vgrads;
   a->vparams = t->vparams;
   a->gather = t->vparams ? 1 : 0;
+  a->param_f32 = t->param_dtype == FSP_DTYPE_F32 ? 1 : 0;
   a->master = master;
   a->m = m;
   a->v = v;
@@ -250,9 +254,10 @@ fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, 
 }  // namespace fsp
 
 extern "C" fsp_status fsp_param_table_create(const fsp_plan* plan, const void* const* grad_ptrs, int32_t grad_dtype,
-                                             void* const* param_ptrs, fsp_param_table** out) {
+                                             void* const* param_ptrs, int32_t param_dtype,
+                                             fsp_param_table** out) {
   return fsp::guard([&]() -> fsp_status {
-    return fsp::create_table(plan, grad_ptrs, grad_dtype, param_ptrs, out);
+    return fsp::create_table(plan, grad_ptrs, grad_dtype, param_ptrs, param_dtype, out);
   });
 }
 

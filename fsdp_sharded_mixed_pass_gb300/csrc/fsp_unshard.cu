@@ -36,7 +36,7 @@ struct UnshardArgs {
   // that parameter (element f at base + f); nullptr for full-size buffers
   uint16_t* const* vparams;
   int n_d;
-  int param_f32;   // 1: params[] are fp32 buffers (the master copied, no cast; full-size buffers only)
+  int param_f32;   // 1: the parameter buffers / tensors are fp32 (the master copied, no cast)
   const Tile* tiles;
   int64_t n_tiles;
   int n_rep;
@@ -229,6 +229,7 @@ fsp_status run_unshard_params(const fsp_plan* p, const fsp_param_table* t, const
   a.master = master;
   a.vparams = t->vparams;
   a.n_d = p->n_d;
+  a.param_f32 = t->param_dtype == FSP_DTYPE_F32 ? 1 : 0;
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
   a.n_rep = p->n_rep;

@@ -79,7 +79,7 @@ def lib():
     L.fsp_plan_layout_params.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i32, i32,
                                          i32, ctypes.POINTER(vp)]
     L.fsp_plan_param.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
-    L.fsp_param_table_create.argtypes = [vp, ctypes.POINTER(vp), i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.fsp_param_table_create.argtypes = [vp, ctypes.POINTER(vp), i32, ctypes.POINTER(vp), i32, ctypes.POINTER(vp)]
     L.fsp_param_table_destroy.argtypes = [vp]
     L.fsp_param_table_destroy.restype = None
     L.fsp_sharded_step_params.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(_HParams), i64, vp]
@@ -254,10 +254,11 @@ def plan_layout_params(shapes, n_d: int, n_replicate: int = 1) -> Plan:
 class ParamTable:
     """Per-parameter tensors registered for a per-parameter plan
     (``fsp_param_table_create``): ``grads[q][i]`` is rank q's gradient of
-    parameter i, ``params[q][i]`` its bf16 parameter tensor (or ``params=None``).
-    Keeps references to the tensors so they outlive the table."""
+    parameter i, ``params[q][i]`` its parameter tensor, bf16 or fp32 (or
+    ``params=None``).  Keeps references to the tensors so they outlive the table."""
 
-    def __init__(self, plan: Plan, grads, params=None, grad_dtype: str | None = None):
+    def __init__(self, plan: Plan, grads, params=None, grad_dtype: str | None = None,
+                 param_dtype: str | None = None):
         if len(grads) != plan.n_d or any(len(g) != plan.n_params for g in grads):
             raise ValueError(f"need {plan.n_d} x {plan.n_params} gradient tensors")
         if params is not None and (len(params) != plan.n_d or any(len(x) != plan.n_params for x in params)):
@@ -269,7 +270,12 @@ class ParamTable:
         g = (ctypes.c_void_p * max(1, n))(*[_ptr(x) for row in grads for x in row])
         p = None if params is None else (ctypes.c_void_p * max(1, n))(*[_ptr(x) for row in params for x in row])
         out = ctypes.c_void_p()
-        _check(lib().fsp_param_table_create(plan.handle, g, DTYPES[gd], p, ctypes.byref(out)),
+        if param_dtype is None:
+            import torch
+            first = next((x for row in (params or []) for x in row), None)
+            param_dtype = "f32" if first is not None and getattr(first, "dtype", None) == torch.float32 else "bf16"
+        self.param_dtype = param_dtype
+        _check(lib().fsp_param_table_create(plan.handle, g, DTYPES[gd], p, DTYPES[param_dtype], ctypes.byref(out)),
                "fsp_param_table_create")
         self._h = out
 

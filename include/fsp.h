@@ -345,11 +345,15 @@ fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_g
  *               q * n_params + i is rank q's gradient of parameter i
  *               (numel_i elements of grad_dtype, the unsharded gradient), only
  *               read by the step.
- *   param_ptrs: host array of n_d * n_params device pointers to bf16 tensors
- *               of numel_i elements (rank q's unsharded parameter i), written
- *               by the step's all-gather and by fsp_unshard_params; NULL for a
- *               table that only reduces (steps then leave the parameters
- *               sharded, as fsp_sharded_step with param_bufs = NULL).
+ *   param_ptrs: host array of n_d * n_params device pointers to tensors of
+ *               numel_i elements of param_dtype (rank q's unsharded parameter
+ *               i), written by the step's all-gather and by
+ *               fsp_unshard_params; NULL for a table that only reduces (steps
+ *               then leave the parameters sharded, as fsp_sharded_step with
+ *               param_bufs = NULL).
+ *   param_dtype: FSP_DTYPE_BF16 (the cast master, as fsp_sharded_step) or
+ *               FSP_DTYPE_F32 (the master itself, as
+ *               fsp_sharded_step_fp32_gather).
  * Every pointer must be 16-byte aligned and lie in a live allocation holding
  * its tensor (NULL only for a parameter with 0 elements); no two tensors may
  * overlap.  The plan must come from fsp_plan_layout_params and outlive the
@@ -357,7 +361,7 @@ fsp_status fsp_sharded_step_host(const fsp_plan* plan, const void* const* host_g
  * fsp_param_table_destroy. */
 typedef struct fsp_param_table fsp_param_table;
 fsp_status fsp_param_table_create(const fsp_plan* plan, const void* const* grad_ptrs, int32_t grad_dtype,
-                                  void* const* param_ptrs, fsp_param_table** out);
+                                  void* const* param_ptrs, int32_t param_dtype, fsp_param_table** out);
 
 /* Frees the table (its device memory); NULL is a no-op.  Must not race with a
  * call or an in-flight step that uses it. */

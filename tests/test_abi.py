@@ -308,21 +308,22 @@ def test_param_table_rejects_on_host():
         return (ctypes.c_void_p * len(vals))(*vals)
 
     out = ctypes.c_void_p()
-    st = L.fsp_param_table_create(flat.handle, ptrs(flat), 0, None, ctypes.byref(out))
+    st = L.fsp_param_table_create(flat.handle, ptrs(flat), 0, None, 1, ctypes.byref(out))
     assert st == B.FSP_EINVAL and "per-parameter" in L.fsp_last_error().decode()
-    assert L.fsp_param_table_create(pp.handle, None, 0, None, ctypes.byref(out)) == B.FSP_EINVAL
-    assert L.fsp_param_table_create(pp.handle, ptrs(pp), 7, None, ctypes.byref(out)) == B.FSP_EINVAL
-    assert L.fsp_param_table_create(pp.handle, ptrs(pp, shift=4), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, None, 0, None, 1, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp), 7, None, 1, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, shift=4), 0, None, 1, ctypes.byref(out)) == B.FSP_EINVAL
     assert "aligned" in L.fsp_last_error().decode()
-    assert L.fsp_param_table_create(pp.handle, ptrs(pp, nulls=(1,)), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, nulls=(1,)), 0, None, 1, ctypes.byref(out)) == B.FSP_EINVAL
     # 64 x 8 fp32 = 2 KiB tensors 1 KiB apart overlap
-    assert L.fsp_param_table_create(pp.handle, ptrs(pp, stride=1024), 0, None, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, ptrs(pp, stride=1024), 0, None, 1, ctypes.byref(out)) == B.FSP_EINVAL
     assert "overlaps" in L.fsp_last_error().decode()
     # a param tensor on top of a grad tensor
     g = ptrs(pp)
     prm = (ctypes.c_void_p * 4)(*[g[k] for k in range(4)])
-    assert L.fsp_param_table_create(pp.handle, g, 0, prm, ctypes.byref(out)) == B.FSP_EINVAL
-    assert L.fsp_param_table_create(pp.handle, g, 0, None, None) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, g, 0, prm, 1, ctypes.byref(out)) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, g, 0, None, 1, None) == B.FSP_EINVAL
+    assert L.fsp_param_table_create(pp.handle, g, 0, None, 5, ctypes.byref(out)) == B.FSP_EINVAL   # param dtype
     assert L.fsp_sharded_step_params(None, None, None, None, None, None, 1, None) == B.FSP_EINVAL
     assert L.fsp_unshard_params(pp.handle, None, None, None) == B.FSP_EINVAL
     L.fsp_param_table_destroy(None)

@@ -36,7 +36,7 @@ class ParamCase:
     """The inputs of a flat DeviceCase, copied into per-parameter tensors of a
     per-parameter plan (state keyed by the logical element, like the flat case)."""
 
-    def __init__(self, flat: DeviceCase, n_rep=1, with_params=True):
+    def __init__(self, flat: DeviceCase, n_rep=1, with_params=True, param_dtype=torch.bfloat16):
         self.flat = flat
         shapes, n_d = flat.shapes, flat.n_d
         self.shapes = shapes
@@ -48,7 +48,8 @@ class ParamCase:
             for i, s in enumerate(shapes):
                 n = _numel(s)
                 self.grads[q][i].t.copy_(flat.grads[q].t[self.flat_off[i]:self.flat_off[i] + n])
-        self.params = [[Guarded(_numel(s), torch.bfloat16, PARAM_SENTINEL) for s in shapes] for _ in range(n_d)] \
+        sentinel = PARAM_SENTINEL if param_dtype == torch.bfloat16 else STATE_SENTINEL
+        self.params = [[Guarded(_numel(s), param_dtype, sentinel) for s in shapes] for _ in range(n_d)] \
             if with_params else None
         p = self.plan
         self.state = [Guarded(p.state_len_total, torch.float32, STATE_SENTINEL) for _ in range(3)]
@@ -255,5 +256,38 @@ def test_per_param_writeback_equals_flat(shapes):
         for i, s in enumerate(shapes):
             n = _numel(s)
             assert np.array_equal(pc.grads[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n]), f"rank {q} grad {i}"
+    assert pc.guards_intact()
+    assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("shapes,n_d,n_rep", [(SHAPES, 4, 1), (SHAPES, 8, 2), (SHAPES, 9, 1), (BIG, 4, 1)],
+                         ids=["fsdp2", "hsdp", "per-thread", "large"])
+def test_per_param_fp32_parameters_equal_flat_fp32_gather(shapes, n_d, n_rep):
+    mode = "hsdp" if n_rep > 1 else "fsdp2"
+    flat = DeviceCase(shapes, n_d, mode, "f32", 109, n_rep)
+    pc = ParamCase(flat, n_rep, param_dtype=torch.float32)
+    assert pc.table.param_dtype == "f32"
+    fbufs = [Guarded(flat.plan.full_len_padded, torch.float32, STATE_SENTINEL) for _ in range(n_d)]
+    fsp.sharded_step_fp32_gather(flat.plan, [g.t for g in flat.grads], *[s.t for s in flat.state],
+                                 [b.t for b in fbufs], HP, 10)
+    pc.step(10)
+    torch.cuda.synchronize()
+    pc.state_matches_flat()
+    for q in range(n_d):
+        fb = fbufs[q].bits()
+        for i, s in enumerate(shapes):
+            n = _numel(s)
+            assert np.array_equal(pc.params[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n]), f"rank {q} param {i}"
+    # and the fp32 unshard into the same tensors after wiping them
+    for row in pc.params:
+        for x in row:
+            x.t.view(torch.int32).fill_(-1)
+    fsp.unshard_params(pc.plan, pc.table, pc.state[0].t)
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        fb = fbufs[q].bits()
+        for i, s in enumerate(shapes):
+            n = _numel(s)
+            assert np.array_equal(pc.params[q][i].bits(), fb[pc.flat_off[i]:pc.flat_off[i] + n])
     assert pc.guards_intact()
     assert fsp.device_error() == 0
