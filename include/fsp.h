@@ -62,7 +62,7 @@ typedef enum {
   FSP_EINVAL = 1,        /* bad argument (null, range, alignment, overlap, size) */
   FSP_ENOMEM = 2,        /* host or device allocation failed                       */
   FSP_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed             */
-  FSP_EUNSUPPORTED = 4   /* valid request this build does not handle               */
+  FSP_EUNSUPPORTED = 4   /* valid request the library does not handle              */
 } fsp_status;
 
 typedef enum {
