@@ -368,3 +368,14 @@ def test_fp32_gather_checks_fp32_buffer_sizes_on_host():
     args = B._step_args(plan, g, *s, p, HP, 1, "f32")
     assert L.fsp_sharded_step_fp32_gather(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
     assert "overlaps" in L.fsp_last_error().decode()
+
+
+def test_param_table_wrapper_checks_counts():
+    pp = fsp.plan_layout_params([(64, 8), (5,)], 2)
+    one = [_Fake(1 << 40), _Fake((1 << 40) + 4096)]
+    with pytest.raises(ValueError):
+        fsp.ParamTable(pp, [one], grad_dtype="f32")                       # one rank of two
+    with pytest.raises(ValueError):
+        fsp.ParamTable(pp, [one, one[:1]], grad_dtype="f32")              # a missing tensor
+    with pytest.raises(ValueError):
+        fsp.ParamTable(pp, [one, one], params=[one], grad_dtype="f32", param_dtype="bf16")
