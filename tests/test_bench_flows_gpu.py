@@ -1,0 +1,46 @@
+"""Every flow bench.py times runs and prints one well-formed JSON line (small
+param slices, a few steps)."""
+import json
+import os
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+from gpu_cases import ensure_built  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+FLOWS = [
+    [], ["--clip", "1.0"], ["--writeback"], ["--no-gather"], ["--unshard"], ["--fp32-gather"],
+    ["--fp32-gather", "--unshard"], ["--per-param"], ["--per-param", "--unshard"], ["--graph"],
+    ["--workload", "5"], ["--workload", "4"], ["--n-d", "9"],
+]
+
+
+@pytest.mark.parametrize("flow", FLOWS, ids=[" ".join(f) or "step" for f in FLOWS])
+def test_bench_flow_prints_one_line(flow, capsys):
+    args = ["--param-slice", "1:6", "--steps", "3", "--warmup", "3", "--no-e2e", "--no-cpu-baseline"] + flow
+    bench.main(args)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "roofline", "clocks",
+              "gpu_launches", "config"):
+        assert k in d, k
+    assert d["value"] > 0 and d["roofline"]["achieved"] > 0
+    assert "l2" in d["config"]
+    import fsdp_sharded_mixed_pass_gb300 as fsp
+    assert fsp.device_error() == 0
