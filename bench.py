@@ -517,6 +517,26 @@ def cpu_threads_used() -> int:
     return 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def time_oracle(w, shapes, seconds: float, use_device: bool, max_reps: int = 1000):
     from oracle import step as OS
     op, grads, state, params = oracle_inputs(w, shapes, use_device)
@@ -626,6 +646,7 @@ def run_fsp(args):
         sshapes, _ = cpu_sample_shapes(shapes)
         n, reps, secs = time_oracle(w, sshapes, args.cpu_seconds, use_device=True)
         cpu = {"value": n * reps / secs, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+               "cpu": cpu_model(), "host_cores": os.cpu_count(),
                "sample": f"{len(sshapes)} params ({n} elements) of {w.name}, N_d={w.n_d}, "
                          f"oracle step repeated {reps}x ({secs:.1f} s)"}
 
@@ -707,6 +728,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+                         "cpu": cpu_model(), "host_cores": os.cpu_count(),
                          "sample": f"{len(sshapes)} params ({op.valid_elems} elements) of {w.name} per step, "
                                    f"N_d={w.n_d}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
