@@ -1,10 +1,11 @@
 // Per-parameter tensors: the table that registers them (fsp_param_table_create
-// / _destroy) and the step that reads every rank's per-parameter gradients and
-// writes every rank's per-parameter bf16 parameters in place
-// (fsp_sharded_step_params) - FSDP2's copy-in before the reduce-scatter and
-// copy-out after the all-gather folded into the step ("Parallelism
-// strategies: which state to shard", section 二.5).  The unshard into the same
-// tensors is fsp_unshard_params in fsp_unshard.cu.
+// / _destroy) and the steps that read every rank's per-parameter gradients and
+// write every rank's per-parameter bf16 or fp32 parameters in place
+// (fsp_sharded_step_params and its _device_t, write-back and clipped
+// variants) - FSDP2's copy-in before the reduce-scatter and copy-out after the
+// all-gather folded into the step ("Parallelism strategies: which state to
+// shard", section 二.5).  The unshard into the same tensors is
+// fsp_unshard_params in fsp_unshard.cu.
 #include <cuda_runtime.h>
 
 #include <algorithm>
