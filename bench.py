@@ -12,6 +12,10 @@ per param).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|IDX]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
+Other flows (each reports its own bytes per param): --clip MAX_NORM,
+--writeback, --no-gather, --unshard, --fp32-gather, --per-param; --n-d N and
+--param-slice a:b change the workload, --graph captures the timed steps.
+
 Multi-GPU (torchrun, one rank per GPU): the step does not shard across GPUs
 (the N_d ranks already live on one device), so every GPU runs an independent
 replica; value = all ranks' params / max-over-ranks time ("weak" scaling).
