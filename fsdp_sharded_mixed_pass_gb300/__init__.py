@@ -18,6 +18,7 @@ from .fsp import (  # noqa: F401
     plan_layout,
     plan_layout_params,
     selftest_bounded_wait,
+    shard,
     sharded_step,
     sharded_step_clipped,
     sharded_step_clipped_params,

@@ -240,6 +240,80 @@ fsp_status run_unshard_params(const fsp_plan* p, const fsp_param_table* t, const
   return FSP_OK;
 }
 
+// ---- FSDP2 shard: the inverse of the unshard -------------------------------------------
+
+// Every owned element of the full fp32 parameter buffer goes to its slot of
+// every replica group's master copy ("Parallelism strategies: which state to
+// shard", section 二.5: fully_shard splits each parameter on dim 0 into
+// per-rank DTensor shards).  One CTA per tile; 8-element groups of the full
+// index move as two 16-byte loads and stores (full and state indices share
+// their residue modulo 16), the unaligned edges one element per thread.
+__global__ void __launch_bounds__(kUnshardThreads) shard_kernel(const float* __restrict__ full,
+                                                                float* __restrict__ master, const Tile* tiles,
+                                                                int64_t n_tiles, int n_rep, int64_t rep_stride) {
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tile = tiles[t];
+    const int64_t f0 = tile.full_begin, end = f0 + tile.len;
+    const int64_t delta = tile.state_begin - tile.full_begin;
+    int64_t b0 = (f0 + 7) & ~int64_t(7), b1 = end & ~int64_t(7);
+    if (b1 < b0) b0 = b1 = end;
+    const int64_t groups = (b1 - b0) >> 3;
+    for (int64_t i = threadIdx.x; i < groups; i += kUnshardThreads) {
+      const int64_t f = b0 + 8 * i;
+      const float4 x = __ldcs(reinterpret_cast<const float4*>(full + f));
+      const float4 y = __ldcs(reinterpret_cast<const float4*>(full + f + 4));
+      for (int r = 0; r < n_rep; ++r) {
+        float* dst = master + f + delta + r * rep_stride;
+        __stcs(reinterpret_cast<float4*>(dst), x);
+        __stcs(reinterpret_cast<float4*>(dst + 4), y);
+      }
+    }
+    const int64_t n_head = b0 - f0, n_scalar = n_head + (end - b1);
+    if (threadIdx.x < n_scalar) {
+      const int64_t f = threadIdx.x < n_head ? f0 + threadIdx.x : b1 + (threadIdx.x - n_head);
+      for (int r = 0; r < n_rep; ++r) master[f + delta + r * rep_stride] = full[f];
+    }
+  }
+}
+
+fsp_status run_shard(const fsp_plan* p, const float* full, float* master, float* m, float* v, void* stream) {
+  clear_error();
+  if (!p) return fail(FSP_EINVAL, "plan is NULL");
+  const size_t fbytes = size_t(p->full_len_padded) * 4, sbytes = size_t(p->state_len_total) * 4;
+  std::vector<Buf> bufs{{full, fbytes, "full"}, {master, sbytes, "master"}};
+  if (m) bufs.push_back({m, sbytes, "exp_avg"});
+  if (v) bufs.push_back({v, sbytes, "exp_avg_sq"});
+  for (const Buf& b : bufs) {
+    if (!b.ptr && b.bytes) return fail(FSP_EINVAL, b.name + " is NULL");
+    if (reinterpret_cast<uintptr_t>(b.ptr) % 16 != 0) return fail(FSP_EINVAL, b.name + " is not 16-byte aligned");
+  }
+  for (size_t i = 0; i < bufs.size(); ++i)
+    for (size_t j = i + 1; j < bufs.size(); ++j) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(bufs[i].ptr), b0 = reinterpret_cast<uintptr_t>(bufs[j].ptr);
+      if (bufs[i].bytes && bufs[j].bytes && a0 < b0 + bufs[j].bytes && b0 < a0 + bufs[i].bytes)
+        return fail(FSP_EINVAL, bufs[i].name + " overlaps " + bufs[j].name);
+    }
+  if (p->tiles.empty()) return FSP_OK;
+  for (const Buf& b : bufs) {
+    fsp_status s = check_allocation(b.ptr, b.bytes, b.name.c_str());
+    if (s != FSP_OK) return s;
+  }
+  const Tile* tiles = nullptr;
+  fsp_status s = device_tiles(p, &tiles);
+  if (s != FSP_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (m) e = cudaMemsetAsync(m, 0, sbytes, st);
+  if (e == cudaSuccess && v) e = cudaMemsetAsync(v, 0, sbytes, st);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("zeroing the Adam moments", e));
+  const int64_t n_tiles = int64_t(p->tiles.size());
+  shard_kernel<<<int(std::min<int64_t>(INT32_MAX, n_tiles)), kUnshardThreads, 0, st>>>(
+      full, master, tiles, n_tiles, p->n_rep, p->n_rep > 1 ? p->rep_stride : 0);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("shard kernel launch", e));
+  return FSP_OK;
+}
+
 }  // namespace
 }  // namespace fsp
 
@@ -261,5 +335,12 @@ extern "C" fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_t
                                          void* cuda_stream) {
   return fsp::guard([&]() -> fsp_status {
     return fsp::run_unshard_params(plan, table, master, cuda_stream);
+  });
+}
+
+extern "C" fsp_status fsp_shard(const fsp_plan* plan, const float* full, float* master, float* exp_avg,
+                                float* exp_avg_sq, void* cuda_stream) {
+  return fsp::guard([&]() -> fsp_status {
+    return fsp::run_shard(plan, full, master, exp_avg, exp_avg_sq, cuda_stream);
   });
 }

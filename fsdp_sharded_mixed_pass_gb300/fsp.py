@@ -21,7 +21,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
            "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
-           "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32",
+           "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32", "fsp_shard",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
            "fsp_sharded_step_params", "fsp_sharded_step_params_device_t", "fsp_sharded_step_clipped_params",
            "fsp_sharded_step_writeback_params",
@@ -100,6 +100,7 @@ def lib():
     L.fsp_sharded_step_writeback.argtypes = step_args + [vp]
     L.fsp_sharded_step_fp32_gather.argtypes = step_args + [vp]
     L.fsp_unshard_fp32.argtypes = [vp, vp, ctypes.POINTER(vp), vp]
+    L.fsp_shard.argtypes = [vp, vp, vp, vp, vp, vp]
     L.fsp_sharded_step_clipped.argtypes = step_args + [ctypes.c_float, vp, vp]
     L.fsp_sharded_step_clipped.restype = ctypes.c_int
     L.fsp_sharded_step_device_t.argtypes = step_args[:-1] + [vp, i32, vp]
@@ -109,7 +110,7 @@ def lib():
     for fn in ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param",
                "fsp_plan_info_get", "fsp_plan_segment", "fsp_plan_ledger", "fsp_sharded_step", "fsp_sharded_step_debug",
                "fsp_sharded_step_noalloc", "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather",
-               "fsp_unshard_fp32", "fsp_param_table_create", "fsp_sharded_step_params",
+               "fsp_unshard_fp32", "fsp_shard", "fsp_param_table_create", "fsp_sharded_step_params",
                "fsp_sharded_step_clipped_params", "fsp_sharded_step_params_device_t", "fsp_unshard_params",
                "fsp_sharded_step_writeback_params"):
         getattr(L, fn).restype = ctypes.c_int
@@ -472,6 +473,15 @@ def sharded_step_clipped(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, par
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_clipped(*args, float(max_norm), ctypes.c_void_p(_ptr(norm_out)),
                                           ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_clipped")
+
+
+def shard(plan: Plan, full, master, exp_avg=None, exp_avg_sq=None, stream=None) -> None:
+    """FSDP2 shard: copy every owned element of the full fp32 parameters into
+    ``master`` (every replica copy for HSDP); zero ``exp_avg`` / ``exp_avg_sq``
+    when given.  Asynchronous."""
+    z = lambda x: ctypes.c_void_p(None if x is None else _ptr(x))  # noqa: E731
+    _check(lib().fsp_shard(plan.handle, ctypes.c_void_p(_ptr(full)), ctypes.c_void_p(_ptr(master)), z(exp_avg),
+                           z(exp_avg_sq), ctypes.c_void_p(_stream_handle(stream))), "fsp_shard")
 
 
 def unshard(plan: Plan, master, param_bufs, stream=None, fp32: bool = False) -> None:

@@ -300,6 +300,18 @@ fsp_status fsp_sharded_step_fp32_gather(const fsp_plan* plan, const void* const*
  * `cuda_stream`; one kernel reading 4 B and writing 2 N_s B per element. */
 fsp_status fsp_unshard(const fsp_plan* plan, const float* master, void* const* param_bufs, void* cuda_stream);
 
+/* FSDP2 shard, the inverse of the unshard: every owned element of `full` (the
+ * unsharded fp32 parameters in the plan's full index, full_len_padded
+ * elements; padding ignored) is copied to its slot of `master` - of every
+ * replica group's copy for HSDP - as fully_shard splits each parameter into
+ * per-rank shards ("Parallelism strategies: which state to shard", section
+ * 二.5).  exp_avg / exp_avg_sq, when not NULL, are zeroed (whole buffers): the
+ * state of a fresh optimizer.  Use it to start training from full
+ * parameters or to load a checkpoint.  Shard padding slots of master are
+ * left as they were.  Asynchronous on `cuda_stream`. */
+fsp_status fsp_shard(const fsp_plan* plan, const float* full, float* master, float* exp_avg, float* exp_avg_sq,
+                     void* cuda_stream);
+
 /* fsp_unshard into fp32 param buffers (full_len_padded fp32 each): the owned
  * master values copied to every rank of the group, no cast. */
 fsp_status fsp_unshard_fp32(const fsp_plan* plan, const float* master, void* const* param_bufs, void* cuda_stream);

@@ -285,3 +285,14 @@ def unshard(plan: Plan, master, params) -> None:
     copy-out; "FSDP2 Qwen3 Decoder Layer Walkthrough", section "Step 0")."""
     casts = [bf16_rne(master[seg.state_off:seg.state_off + seg.length]) for seg in plan.segments]
     all_gather(plan, casts, params)
+
+
+def shard(plan: Plan, full, master) -> None:
+    """FSDP2's shard of the full fp32 parameters ("Parallelism strategies:
+    which state to shard", section 二.5: fully_shard splits every parameter on
+    dim 0 into per-rank shards): each owned element goes to its state slot, in
+    every replica group's copy for HSDP (the plan's segments list every copy).
+    Slots no segment owns are left as they were."""
+    full = np.asarray(full, dtype=np.float32)
+    for seg in plan.segments:
+        master[seg.state_off:seg.state_off + seg.length] = full[seg.full_off:seg.full_off + seg.length]

@@ -90,3 +90,29 @@ def test_zero3_step_then_unshard_equals_the_gathering_step(mode, n_d, n_rep):
     for a, b in zip(full.params, z3.params):
         assert np.array_equal(a.bits(), b.bits())
     assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("mode,n_d,n_rep", CASES)
+def test_shard_matches_oracle(mode, n_d, n_rep):
+    """fsp_shard (full fp32 parameters -> every replica's master slots; m, v
+    zeroed) against the oracle's shard, slot for slot."""
+    from oracle import plan as OP
+    from gpu_cases import STATE_SENTINEL
+    shapes = SHAPES
+    dev = DeviceCase(shapes, n_d, mode, "f32", 19, n_rep)
+    oplan = OP.plan_layout(shapes, n_d, mode, n_rep=n_rep)
+    rng = np.random.default_rng(n_d * 7 + n_rep)
+    full_h = rng.standard_normal(dev.plan.full_len_padded).astype(np.float32)
+    full = Guarded(dev.plan.full_len_padded, torch.float32, 0)
+    full.t.copy_(torch.from_numpy(full_h))
+    for s in dev.state:
+        s.raw[s.g:s.g + s.n].view(torch.int32).fill_(int(np.array([STATE_SENTINEL], np.uint32).view(np.int32)[0]))
+    fsp.shard(dev.plan, full.t, dev.state[0].t, dev.state[1].t, dev.state[2].t)
+    want = np.full(oplan.state_len_total, STATE_SENTINEL, np.uint32).view(np.float32)
+    OS.shard(oplan, full_h, want)
+    torch.cuda.synchronize()
+    assert np.array_equal(dev.state[0].bits(), want.view(np.uint32))
+    for s in dev.state[1:]:
+        assert not s.bits().any()                    # the Adam moments start at zero
+    assert dev.all_guards_intact() and full.guards_intact()
+    assert fsp.device_error() == 0
