@@ -35,3 +35,4 @@ from .fsp import (  # noqa: F401
     unshard,
     unshard_params,
 )
+from .optim import ShardedAdamW  # noqa: F401,E402

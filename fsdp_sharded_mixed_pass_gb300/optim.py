@@ -1,0 +1,51 @@
+"""An optimizer-shaped handle over the library: one data-parallel group's plan
+and fp32 master / Adam m / Adam v state on one device, and the update index.
+
+It allocates the state (PyTorch device memory) and calls the C ABI; every
+computation - shard, step, unshard - runs in the library's kernels.
+"""
+from __future__ import annotations
+
+from . import fsp as _fsp
+
+
+class ShardedAdamW:
+    """``ShardedAdamW(shapes, n_d, mode="fsdp2")`` - FSDP2 Shard(0) (``"fsdp2"``),
+    DistOpt flat shards (``"distopt"``) or HSDP (``"hsdp"`` with
+    ``n_replicate`` groups) over ``n_d`` ranks held as buffers on ``device``.
+
+    ``load_full(full)`` shards full fp32 parameters (the plan's full index,
+    ``plan.full_len_padded`` elements) into the master and zeroes m and v;
+    ``step(grad_bufs, param_bufs)`` applies update t + 1 (the fused
+    reduce-scatter + AdamW + bf16 all-gather; ``param_bufs=None`` leaves the
+    parameters sharded); ``unshard(param_bufs)`` gathers the current master.
+    """
+
+    def __init__(self, shapes, n_d: int, mode: str = "fsdp2", n_replicate: int = 1, lr: float = 1e-3,
+                 betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 1e-2, device="cuda"):
+        import torch
+        self.plan = _fsp.plan_layout(shapes, n_d, mode, n_replicate=n_replicate)
+        n = self.plan.state_len_total
+        self.master = torch.zeros(n, dtype=torch.float32, device=device)
+        self.exp_avg = torch.zeros(n, dtype=torch.float32, device=device)
+        self.exp_avg_sq = torch.zeros(n, dtype=torch.float32, device=device)
+        self.hparams = dict(lr=float(lr), beta1=float(betas[0]), beta2=float(betas[1]), eps=float(eps),
+                            weight_decay=float(weight_decay))
+        self.t = 0
+
+    @property
+    def full_len(self) -> int:
+        """Elements of every rank's full gradient / parameter buffer."""
+        return self.plan.full_len_padded
+
+    def load_full(self, full, stream=None) -> None:
+        _fsp.shard(self.plan, full, self.master, self.exp_avg, self.exp_avg_sq, stream=stream)
+        self.t = 0
+
+    def step(self, grad_bufs, param_bufs, stream=None, grad_dtype: str | None = None) -> None:
+        self.t += 1
+        _fsp.sharded_step(self.plan, grad_bufs, self.master, self.exp_avg, self.exp_avg_sq, param_bufs,
+                          self.hparams, self.t, stream=stream, grad_dtype=grad_dtype)
+
+    def unshard(self, param_bufs, stream=None) -> None:
+        _fsp.unshard(self.plan, self.master, param_bufs, stream=stream)

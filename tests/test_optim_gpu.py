@@ -1,0 +1,69 @@
+"""ShardedAdamW - plan, state and update index behind an optimizer-shaped
+handle - against the oracle: shard full parameters, two steps, unshard."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_mixed_pass_gb300 as fsp
+import synth_inputs as S
+from oracle import plan as OP
+from oracle import step as OS
+
+from gpu_cases import HP, ensure_built, param_ulp_allowance, state_errors, ulp_dist, within_tol, SCALED_BOUND
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+SHAPES = [(3001, 7), (12289,), (9, 5), (1,), (5, 4099)]
+
+
+@pytest.mark.parametrize("mode,n_d,n_rep", [("fsdp2", 4, 1), ("distopt", 8, 1), ("hsdp", 8, 2)])
+def test_sharded_adamw_matches_oracle(mode, n_d, n_rep):
+    opt = fsp.ShardedAdamW(SHAPES, n_d, mode, n_replicate=n_rep, lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]),
+                           eps=HP["eps"], weight_decay=HP["weight_decay"])
+    plan = opt.plan
+    n = opt.full_len
+    idx = np.arange(n)
+    full = S.master_f32(23, idx)
+    grads_h = [S.grad_f32(23, q, idx) for q in range(n_d)]
+    opt.load_full(torch.from_numpy(full).cuda())
+    grads = [torch.from_numpy(g).cuda() for g in grads_h]
+    params = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(n_d)]
+    oplan = OP.plan_layout(SHAPES, n_d, mode, n_rep=n_rep)
+    om = np.zeros(oplan.state_len_total, np.float32)
+    OS.shard(oplan, full, om)
+    o_state = [om, np.zeros_like(om), np.zeros_like(om)]
+    o_params = [np.zeros(n, np.uint16) for _ in range(n_d)]
+    for t in (1, 2):
+        prev = [x.copy() for x in o_state]
+        opt.step(grads, params)
+        OS.sharded_step(oplan, grads_h, "f32", *o_state, o_params, HP, t)
+    torch.cuda.synchronize()
+    assert opt.t == 2
+    _, si = OP.owned_indices(oplan)
+    got = [x.cpu().numpy()[si] for x in (opt.master, opt.exp_avg, opt.exp_avg_sq)]
+    want = [x[si] for x in o_state]
+    errs = state_errors(got, want, [x[si] for x in prev])
+    for g, w, e in zip(got, want, errs):
+        assert within_tol(g, w).all() and (e <= SCALED_BOUND * 2 ** 24).all()
+    fi, _ = OP.owned_indices(oplan)
+    allow = param_ulp_allowance(got[0], want[0])
+    for q in range(n_d):
+        pb = params[q].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert (ulp_dist(pb[fi], o_params[q][fi]) <= allow).all()
+    # unshard of the current master reproduces the step's gathered parameters
+    again = [torch.full((n,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16) for _ in range(n_d)]
+    opt.unshard(again)
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        a = again[q].view(torch.int16).cpu().numpy()
+        b = params[q].view(torch.int16).cpu().numpy()
+        assert np.array_equal(a[fi], b[fi])
+    assert fsp.device_error() == 0
