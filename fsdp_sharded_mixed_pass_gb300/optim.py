@@ -43,9 +43,9 @@ class ShardedAdamW:
         self.t = 0
 
     def step(self, grad_bufs, param_bufs, stream=None, grad_dtype: str | None = None) -> None:
-        self.t += 1
         _fsp.sharded_step(self.plan, grad_bufs, self.master, self.exp_avg, self.exp_avg_sq, param_bufs,
-                          self.hparams, self.t, stream=stream, grad_dtype=grad_dtype)
+                          self.hparams, self.t + 1, stream=stream, grad_dtype=grad_dtype)
+        self.t += 1   # only once the step was accepted
 
     def unshard(self, param_bufs, stream=None) -> None:
         _fsp.unshard(self.plan, self.master, param_bufs, stream=stream)
