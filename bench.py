@@ -467,21 +467,37 @@ def host_memory_available() -> int:
 # CPU oracle timing
 # --------------------------------------------------------------------------
 
+def _param_runs(shapes, max_elems):
+    """The workload's params (skipping any single param over 32M elements, e.g.
+    an embedding) cut in order into consecutive runs of about ``max_elems``
+    elements each."""
+    runs, cur, total = [], [], 0
+    for s in shapes:
+        n = math.prod(s)
+        if n > 32_000_000:
+            continue
+        if cur and total + n > max_elems:
+            runs.append((tuple(cur), total))
+            cur, total = [], 0
+        cur.append(s)
+        total += n
+    if cur:
+        runs.append((tuple(cur), total))
+    return runs or [((), 0)]
+
+
 def cpu_sample_shapes(shapes, max_elems=16_000_000):
     """A contiguous run of the workload's params (skipping any single param over
     32M elements, e.g. an embedding) of about ``max_elems`` elements."""
-    out, total = [], 0
-    for s in shapes:
-        n = 1
-        for d in s:
-            n *= d
-        if n > 32_000_000:
-            continue
-        if out and total + n > max_elems:
-            break
-        out.append(s)
-        total += n
-    return tuple(out), total
+    return _param_runs(shapes, max_elems)[0]
+
+
+def cpu_sample_runs(shapes, max_elems, count):
+    """``count`` samples for as many host cores: the consecutive runs of
+    ``_param_runs`` in the workload's order, reused from the start when there
+    are fewer runs than cores."""
+    runs = _param_runs(shapes, max_elems)
+    return [runs[k % len(runs)][0] for k in range(count)]
 
 
 def oracle_inputs(w, shapes, use_device: bool):
@@ -516,9 +532,92 @@ def oracle_inputs(w, shapes, use_device: bool):
     return op, grads, state, params
 
 
-def cpu_threads_used() -> int:
-    # numpy's elementwise kernels run on the calling thread
-    return 1
+# elements of each host core's sample in the all-core oracle timing
+CPU_POOL_ELEMS = 4_000_000
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def pool_size(w, elems_per_worker: int) -> int:
+    """One oracle process per host core, fewer if their inputs and numpy
+    temporaries (about 160 B per element beside the buffers) would take more
+    than half of the available host memory."""
+    per_worker = elems_per_worker * (w.n_d * (w.grad_bytes + 2) + 12 + 160)
+    avail = host_memory_available()
+    k = host_cores()
+    if avail and per_worker:
+        k = min(k, max(1, int(0.5 * avail // per_worker)))
+    return k
+
+
+def _oracle_worker(w, shapes, warmup, steps, seconds, barrier, results):
+    """One host core's share of the oracle timing (a spawned process: numpy
+    runs elementwise work on the calling thread, so one process is one core).
+    It builds its own sample's inputs with the host generator, runs the warm-up
+    steps, waits for the others, then times ``steps`` oracle steps, or as many
+    as fit in ``seconds`` when ``steps`` is 0."""
+    try:
+        from oracle import step as OS
+        op, grads, state, params = oracle_inputs(w, shapes, use_device=False)
+        t = w.step
+        for _ in range(warmup):
+            OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+            t += 1
+        barrier.wait(timeout=900)
+        reps, t0 = 0, time.perf_counter()
+        while (reps < steps) if steps else (time.perf_counter() - t0 < seconds):
+            OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+            reps += 1
+            t += 1
+        results.put((op.valid_elems, reps, time.perf_counter() - t0, None))
+    except BaseException as e:   # reported to the parent, which raises it
+        try:
+            barrier.abort()
+        except Exception:
+            pass
+        results.put((0, 0, 0.0, f"{type(e).__name__}: {e}"))
+
+
+def time_oracle_pool(w, shapes, workers: int, elems_per_worker: int, warmup: int = 0, steps: int = 0,
+                     seconds: float = 10.0, limit_s: float = 1200.0):
+    """The oracle on ``workers`` host cores at once, one spawned process each
+    on its own run of whole params, all timed over the same window.  Returns
+    (elements x steps summed over the processes, the longest process's time,
+    each process's sample size in elements)."""
+    import multiprocessing as mp
+    import queue
+    samples = cpu_sample_runs(shapes, elems_per_worker, workers)
+    ctx = mp.get_context("spawn")   # a fresh interpreter: safe beside this process's CUDA context
+    barrier, results = ctx.Barrier(workers), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w, sm, warmup, steps, seconds, barrier, results),
+                         daemon=True) for sm in samples]
+    for p in procs:
+        p.start()
+    out, deadline = [], time.monotonic() + limit_s
+    try:
+        while len(out) < len(procs):
+            try:
+                out.append(results.get(timeout=5))
+            except queue.Empty:
+                dead = [p.exitcode for p in procs if p.exitcode not in (None, 0)]
+                if dead or time.monotonic() > deadline:
+                    barrier.abort()
+                    raise RuntimeError(f"oracle pool: exit codes {dead}" if dead else "oracle pool: time limit")
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+    errors = [e for *_, e in out if e]
+    if errors:
+        raise RuntimeError(f"oracle pool: {errors[0]}")
+    return sum(n * r for n, r, _, _ in out), max(s for _, _, s, _ in out), [n for n, *_ in out]
 
 
 def cpu_model() -> str:
@@ -649,10 +748,22 @@ def run_fsp(args):
     if dist.world == 1 and not args.no_cpu_baseline:
         sshapes, _ = cpu_sample_shapes(shapes)
         n, reps, secs = time_oracle(w, sshapes, args.cpu_seconds, use_device=True)
-        cpu = {"value": n * reps / secs, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
-               "cpu": cpu_model(), "host_cores": os.cpu_count(),
+        one = {"value": n * reps / secs,
                "sample": f"{len(sshapes)} params ({n} elements) of {w.name}, N_d={w.n_d}, "
                          f"oracle step repeated {reps}x ({secs:.1f} s)"}
+        cpu = {"value": one["value"], "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+               "host_cores": host_cores(), "sample": one["sample"], "value_1_core": one["value"]}
+        k = pool_size(w, CPU_POOL_ELEMS)
+        if k > 1:
+            try:
+                done, psecs, sizes = time_oracle_pool(w, shapes, k, CPU_POOL_ELEMS, seconds=args.cpu_seconds)
+                cpu.update(value=done / psecs, cores=k,
+                           sample=f"{k} processes, one per host core, each repeating the oracle step on its own "
+                                  f"run of whole params of {w.name} ({min(sizes)}-{max(sizes)} elements), "
+                                  f"N_d={w.n_d}, for {psecs:.1f} s",
+                           sample_1_core=one["sample"])
+            except Exception as e:
+                cpu["pool_error"] = str(e)[:300]
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
@@ -697,44 +808,56 @@ def run_reference(args):
     if dist_rank != 0:
         return
     w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
-    # per step, a bounded sample sized so the whole run stays within ~2 minutes
+    # per step and core, a bounded sample sized so the whole run stays within ~2 minutes
     budget_elems = max(100_000, min(16_000_000, int(120 * 15e6 / max(1, args.steps + args.warmup))))
-    sshapes, _ = cpu_sample_shapes(shapes, budget_elems)
-    use_device = False
-    try:
-        import torch
-        use_device = torch.cuda.is_available()
-        if use_device:
-            from synth_inputs import device as D
-            D.lib()
-    except Exception:
+    per_core = min(budget_elems, CPU_POOL_ELEMS)
+    k = pool_size(w, per_core)
+    pool_error = None
+    if k > 1:
+        try:
+            done, secs, sizes = time_oracle_pool(w, shapes, k, per_core, warmup=args.warmup, steps=args.steps)
+            value, sample_elems = done / secs, sum(sizes)
+            sample = (f"{k} processes, one per host core, each stepping the oracle on its own run of whole params "
+                      f"of {w.name} ({min(sizes)}-{max(sizes)} elements) per step, N_d={w.n_d}")
+        except Exception as e:
+            pool_error, k = str(e)[:300], 1
+    if k == 1:
+        sshapes, _ = cpu_sample_shapes(shapes, budget_elems)
         use_device = False
-    from oracle import step as OS
-    op, grads, state, params = oracle_inputs(w, sshapes, use_device)
-    t = w.step
-    for _ in range(args.warmup):
-        OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
-        t += 1
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
-        t += 1
-    secs = time.perf_counter() - t0
-    value = op.valid_elems * args.steps / secs
+        try:
+            import torch
+            use_device = torch.cuda.is_available()
+            if use_device:
+                from synth_inputs import device as D
+                D.lib()
+        except Exception:
+            use_device = False
+        from oracle import step as OS
+        op, grads, state, params = oracle_inputs(w, sshapes, use_device)
+        t = w.step
+        for _ in range(args.warmup):
+            OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+            t += 1
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            OS.sharded_step(op, grads, w.grad_dtype, *state, params, w.hparams(), t)
+            t += 1
+        secs = time.perf_counter() - t0
+        value, sample_elems = op.valid_elems * args.steps / secs, op.valid_elems
+        sample = f"{len(sshapes)} params ({op.valid_elems} elements) of {w.name} per step, N_d={w.n_d}"
     # the config of the workload itself (as the GPU arm reports it), the sample beside it
     full_p = sum(math.prod(sh) for sh in shapes)
     plan_like = type("P", (), {"valid_elems": full_p})
     cfg = config_block(w, label, plan_like)
-    cfg["sample_params"] = op.valid_elems
+    cfg["sample_params"] = sample_elems
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
-                         "cpu": cpu_model(), "host_cores": os.cpu_count(),
-                         "sample": f"{len(sshapes)} params ({op.valid_elems} elements) of {w.name} per step, "
-                                   f"N_d={w.n_d}"},
+        "cpu_baseline": dict({"value": value, "unit": UNIT, "cores": k, "kind": "oracle",
+                              "cpu": cpu_model(), "host_cores": host_cores(), "sample": sample},
+                             **({"pool_error": pool_error} if pool_error else {})),
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

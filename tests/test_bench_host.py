@@ -109,3 +109,43 @@ def test_rank_count_override_and_param_slice():
     for bad in (7, 0, 65):
         with pytest.raises(SystemExit):
             bench.resolve_workload("5" if bad == 7 else "1", None, bad)
+
+
+def test_param_runs_keep_the_params_in_order():
+    from synth_inputs import workload
+    shapes = workload(1).shapes
+    runs = bench._param_runs(shapes, 4_000_000)
+    flat = [s for r, _ in runs for s in r]
+    assert flat == [s for s in shapes if bench.math.prod(s) <= 32_000_000]
+    for r, n in runs:
+        assert n == sum(bench.math.prod(s) for s in r)
+        assert n <= 4_000_000 or len(r) == 1
+    assert bench.cpu_sample_shapes(shapes, 4_000_000) == runs[0]
+    assert bench.cpu_sample_runs(shapes, 4_000_000, len(runs) + 2)[-2:] == [runs[0][0], runs[1][0]]
+
+
+def test_oracle_pool_times_every_process():
+    w, shapes, _ = bench.resolve_workload("0", "0:4", None)
+    done, secs, sizes = bench.time_oracle_pool(w, shapes, 2, 1_000_000, warmup=1, steps=3)
+    assert len(sizes) == 2 and done == 3 * sum(sizes) and secs > 0
+    assert sizes[0] == sum(bench.math.prod(s) for s in bench.cpu_sample_runs(shapes, 1_000_000, 1)[0])
+
+
+def test_oracle_pool_reports_a_failing_process():
+    import dataclasses
+    w, shapes, _ = bench.resolve_workload("0", "0:2", None)
+    with pytest.raises(RuntimeError, match="oracle pool"):
+        bench.time_oracle_pool(dataclasses.replace(w, grad_dtype="f8"), shapes, 2, 1_000_000, steps=1,
+                               limit_s=300)
+
+
+def test_pool_size_respects_host_memory(monkeypatch):
+    w, _, _ = bench.resolve_workload("1", None, None)
+    monkeypatch.setattr(bench, "host_cores", lambda: 16)
+    monkeypatch.setattr(bench, "host_memory_available", lambda: 0)
+    assert bench.pool_size(w, 4_000_000) == 16
+    per = 4_000_000 * (8 * 6 + 12 + 160)
+    monkeypatch.setattr(bench, "host_memory_available", lambda: 6 * per)
+    assert bench.pool_size(w, 4_000_000) == 3
+    monkeypatch.setattr(bench, "host_memory_available", lambda: per)
+    assert bench.pool_size(w, 4_000_000) == 1
