@@ -351,15 +351,18 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
     """Device time of ``steps`` steps on one stream, in ms.
 
     With ``flush_bytes`` > 0 (working sets that fit in L2) every timed step is
-    preceded by an untimed write of ``flush_bytes`` to a scratch buffer, so each
-    step starts from a cold L2; each step then has its own event pair and the
-    result is the sum of the steps' own durations."""
+    preceded by an untimed write of ``flush_bytes`` to a scratch buffer and a
+    read of it back, so each step starts from a cold L2 that holds no line of
+    its own and no dirty line whose write-back the step would pay for; each
+    step then has its own event pair and the result is the sum of the steps'
+    own durations."""
     import torch
     stream = torch.cuda.Stream(device=wl.device)
     for _ in range(warmup):
         wl.step(stream)
     stream.synchronize()
-    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=wl.device) if flush_bytes > 0 else None
+    flush = torch.empty((flush_bytes + 15) // 16 * 16, dtype=torch.uint8, device=wl.device) \
+        if flush_bytes > 0 else None
     graphs = []
     if graph:
         # the K timed launches (each with its own update index t) as one graph,
@@ -393,6 +396,7 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
         else:
             for i in range(steps):
                 flush.fill_(i & 0xFF)
+                flush.view(torch.int32).max()   # read back: only clean lines stay in L2
                 starts[i].record(stream)
                 if graphs:
                     graphs[i].replay()
@@ -680,7 +684,8 @@ def config_block(w, label, plan):
 
 def l2_note(moved: int, flush_bytes: int) -> str:
     if flush_bytes:
-        return f"L2 flushed before every timed step (an untimed {flush_bytes / 1e6:.0f} MB write)"
+        return (f"L2 flushed before every timed step (an untimed {flush_bytes / 1e6:.0f} MB write, "
+                f"then a read of it)")
     return f"inputs larger than L2: every step streams the whole {moved / 1e9:.2f} GB working set"
 
 
