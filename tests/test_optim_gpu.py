@@ -67,3 +67,41 @@ def test_sharded_adamw_matches_oracle(mode, n_d, n_rep):
         b = params[q].view(torch.int16).cpu().numpy()
         assert np.array_equal(a[fi], b[fi])
     assert fsp.device_error() == 0
+
+
+def test_capturable_steps_replay_in_a_graph_bit_for_bit():
+    """capturable=True: t lives on the device; one eager step, then a captured
+    step replayed twice equals three eager steps of the host-t handle."""
+    kw = dict(lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"], weight_decay=HP["weight_decay"])
+    eager = fsp.ShardedAdamW(SHAPES, 4, "fsdp2", **kw)
+    cap = fsp.ShardedAdamW(SHAPES, 4, "fsdp2", capturable=True, **kw)
+    assert cap.capturable and not eager.capturable and cap.t == 0
+    n = eager.full_len
+    idx = np.arange(n)
+    full = torch.from_numpy(S.master_f32(31, idx)).cuda()
+    grads = [torch.from_numpy(S.grad_f32(31, q, idx)).cuda() for q in range(4)]
+    pe = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    pc = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    eager.load_full(full)
+    cap.load_full(full)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    cap.step(grads, pc, stream=stream)                 # eager first step (t = 1)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        cap.step(grads, pc, stream=stream)
+    for _ in range(2):
+        graph.replay()                                   # t = 2, 3
+    for _ in range(3):
+        eager.step(grads, pe)
+    torch.cuda.synchronize()
+    assert cap.t == 3 and eager.t == 3
+    for a, b in zip((cap.master, cap.exp_avg, cap.exp_avg_sq), (eager.master, eager.exp_avg, eager.exp_avg_sq)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    for a, b in zip(pc, pe):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    cap.t = 0                                            # resume index, set on the device
+    cap.load_full(full)
+    torch.cuda.synchronize()
+    assert cap.t == 0
+    assert fsp.device_error() == 0
