@@ -81,7 +81,13 @@ def within_tol(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
 #   m', v':  |old| + |new| bounds every term;
 #   theta':  |theta| + |theta'| bounds theta (1 - lr wd) and u, and u inherits
 #            m''s error: u is proportional to m', and m' can cancel, so u's
-#            error scale is |u| (2|m| + |m'|) / |m'|.
+#            error scale is |u| (2|m| + |m'| + 2^-125) / |m'| - the last term
+#            because below 2^-126 the fp32 grid that m' is rounded to is
+#            evenly spaced at 2^-149 (subnormals), so each of its two
+#            roundings may be off by 2^-150 = 2^-24 * 2^-126 whatever |m'| is;
+#            where m' itself rounds to 0 the whole of u is allowed (such a u
+#            is at most lr / (bc1 eps) times 2^-150: about 2^-132 with the
+#            tests' hyper-parameters at t = 1).
 # Near-cancellation makes ulp distance meaningless (a result can be tiny
 # while its terms are not), and the absolute bar above sees a dropped
 # weight-decay term (lr wd theta) only where |theta| > 0.033, so parity also
@@ -98,13 +104,15 @@ def scaled_err(got: np.ndarray, ref: np.ndarray, old: np.ndarray, extra=0.0) -> 
 
 
 def master_extra_scale(th_old, th_ref, m_old, m_ref, hp=HP) -> np.ndarray:
-    """|u| (2|m| + |m'|) / |m'|: the part of theta''s error scale carried in from m'."""
+    """|u| (2|m| + |m'| + 2^-125) / |m'|: the part of theta''s error scale
+    carried in from m' (the last term: m''s two roundings on the subnormal
+    grid); where the reference m' is 0 it lets theta' miss all of u."""
     decay = 1.0 - float(np.float32(hp["lr"])) * float(np.float32(hp["weight_decay"]))
     u = np.abs(th_old.astype(np.float64) * decay - th_ref.astype(np.float64))
     mo = np.abs(m_old.astype(np.float64))
     mr = np.abs(m_ref.astype(np.float64))
     with np.errstate(divide="ignore", invalid="ignore"):
-        return np.where(mr > 0, u * (2 * mo + mr) / mr, 0.0)
+        return np.where(mr > 0, u * (2 * mo + mr + 2.0 ** -125) / mr, u * 2.0 ** 20)
 
 
 def state_errors(got, ref, old, hp=HP):

@@ -34,6 +34,29 @@ def test_fp32_evaluation_passes():
     assert not _detected([th1, m1, v1], ref, [th, m, v])
 
 
+def test_fp32_evaluation_with_subnormal_moments_passes():
+    """G subnormal and m = v = 0: m' = (1 - b1) G lands on the subnormal grid
+    (a few significant bits) and u = lr m'/(bc1 eps) carries that rounding,
+    amplified by 1/eps, into theta'.  An fp32 evaluation must still pass."""
+    f = np.float32
+    g = (np.arange(1, 2001, dtype=np.float64) * -2.5e-45).astype(f)   # 2 .. 5e-42, on the subnormal grid
+    th = np.zeros_like(g)
+    m = np.zeros_like(g)
+    v = np.zeros_like(g)
+    b1, b2, lr, wd, eps = (f(HP[k]) for k in ("beta1", "beta2", "lr", "weight_decay", "eps"))
+    m1 = (f(1) - b1) * g
+    v1 = (f(1) - b2) * (g * g)
+    bc1, bc2 = f(1 - 0.9 ** 1), f(1 - 0.95 ** 1)
+    th1 = th * (f(1) - lr * wd) - (lr / bc1) * (m1 / (np.sqrt(v1 / bc2) + eps))
+    ref = O.adamw(th, m, v, g, HP, 1)
+    assert np.abs(th1.astype(np.float64) / ref[0] - 1).max() > 1e-4   # far beyond 2^-24 relative ...
+    assert not _detected([th1, m1, v1], ref, [th, m, v])              # ... and still inside the bound
+    # a dropped weight decay on such a theta (here 0) is invisible; on theta = 1e-30 it is not
+    th = np.full_like(g, 1e-30)
+    ref = O.adamw(th, m, v, g, HP, 1)
+    assert _detected(O.adamw(th, m, v, g, dict(HP, weight_decay=0.0), 1), ref, [th, m, v])
+
+
 def test_dropped_weight_decay_is_detected():
     g, th, m, v = _inputs()
     ref = O.adamw(th, m, v, g, HP, 10)
