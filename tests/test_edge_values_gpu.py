@@ -162,3 +162,40 @@ def test_zero_learning_rate_rounds_ties_to_even():
     assert np.all(tb & 0xFFFF == 0x8000)
     assert np.array_equal(p[ties], ((tb >> 16) + ((tb >> 16) & 1)).astype(np.uint16))   # up only from odd
     compare(dev, ora)
+
+
+@pytest.mark.parametrize("max_norm", [1.0, 1e30])
+@pytest.mark.parametrize("n_d,mode", [(4, "fsdp2"), (8, "distopt"), (9, "fsdp2")])
+def test_clipped_flow_on_edge_values(n_d, mode, max_norm):
+    """Write-back, global norm (squares from 1e-82 to 1e34 in one sum) and the
+    clipped update on the same hand-placed values."""
+    from test_clip_gpu import _check, _clipped
+    dev, ora = _case(n_d, mode, "f32")
+    norm, coef = _clipped(dev, 10, max_norm)
+    ora.prev = [a.copy() for a in ora.state]
+    ora.hp = HP
+    o_norm, o_coef = OS.sharded_step_clipped(ora.plan, ora.grads, *ora.state, ora.params, HP, 10, max_norm)
+    _check(dev, ora, norm, coef, o_norm, o_coef)
+    assert (coef < 1.0) == (max_norm < 1e20)
+
+
+@pytest.mark.parametrize("n_d,mode,n_rep", [(4, "fsdp2", 1), (8, "distopt", 1), (8, "hsdp", 2)])
+def test_unshard_of_edge_masters_is_the_exact_cast(n_d, mode, n_rep):
+    """The unshard casts ties, subnormals, signed zeros and 1e30 exactly as
+    the oracle's round-to-nearest-even (and the fp32 unshard copies them)."""
+    dev, ora = _case(n_d, mode, "f32", n_rep)
+    n = dev.plan.full_len_padded
+    bf = [torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(n_d)]
+    f32 = [torch.full((n,), -1, dtype=torch.int32, device="cuda") for _ in range(n_d)]
+    fsp.unshard(dev.plan, dev.state[0].t, [b.view(torch.bfloat16) for b in bf])
+    fsp.unshard(dev.plan, dev.state[0].t, [b.view(torch.float32) for b in f32], fp32=True)
+    o_params = [np.full(n, 0xFFFF, np.uint16) for _ in range(n_d)]
+    OS.unshard(ora.plan, ora.state[0], o_params)
+    torch.cuda.synchronize()
+    fi = ora.fi
+    want32 = np.full(n, 0xFFFFFFFF, np.uint32)
+    want32[fi] = ora.state[0][ora.si].view(np.uint32)
+    for q in range(n_d):
+        assert np.array_equal(bf[q].cpu().numpy().view(np.uint16), o_params[q])   # padding included
+        assert np.array_equal(f32[q].cpu().numpy().view(np.uint32), want32)
+    assert fsp.device_error() == 0
