@@ -6,8 +6,10 @@ check).
 Four gloo processes run the step with real collectives - FSDP2's copy-in of
 each parameter's torch.chunk pieces (padded to the first piece's rows), one
 reduce_scatter_tensor, AdamW on the rank's own shard, the bf16 cast, one
-all_gather_into_tensor and the copy-out; and DistOpt's flat equal shards -
-and every rank's results must equal the single-process oracle bit for bit.
+all_gather_into_tensor and the copy-out; HSDP as 2 replica groups of 2
+(reduce-scatter in the shard group, all-reduce across the replica group,
+gather in the shard group); and DistOpt's flat equal shards - and every
+rank's results must equal the single-process oracle bit for bit.
 The gradients are multiples of 2^-12 small enough that every sum is exact in
 any order, so the collectives' own reduction order cannot matter.  This pins
 the oracle's stage loops (and its plan's shard geometry) to torch.distributed's
@@ -18,6 +20,7 @@ import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -51,11 +54,11 @@ def _state_by_index(n: int):
     return S.master_f32(SEED, idx), S.adam_m_f32(SEED, idx), S.adam_v_f32(SEED, idx)
 
 
-def _all_gather_bits(bits: np.ndarray, world: int) -> np.ndarray:
+def _all_gather_bits(bits: np.ndarray, world: int, group=None) -> np.ndarray:
     """all_gather_into_tensor of bf16 bit patterns (carried as int32: gloo
     gathers no 16-bit integers)."""
     out = torch.zeros(world * bits.size, dtype=torch.int32)
-    dist.all_gather_into_tensor(out, torch.from_numpy(bits.astype(np.int32)))
+    dist.all_gather_into_tensor(out, torch.from_numpy(bits.astype(np.int32)), group=group)
     return out.numpy().astype(np.uint16)
 
 
@@ -68,8 +71,16 @@ def _toy(rank, world):
     return {"shard": shard.tolist(), "gathered": full.tolist()}
 
 
-def _fsdp2(rank, world):
-    plan = OP.plan_layout(SHAPES, world, "fsdp2")
+def _fsdp2(rank, world, n_rep=1):
+    """FSDP2 (n_rep = 1) or HSDP over n_rep replica groups of world // n_rep
+    ranks: reduce-scatter inside the rank's shard group, all-reduce of the
+    shard across the replica group, all-gather inside the shard group."""
+    n_s = world // n_rep
+    groups = [dist.new_group(list(range(r * n_s, (r + 1) * n_s))) for r in range(n_rep)] if n_rep > 1 else [None]
+    across = [dist.new_group(list(range(s, world, n_s))) for s in range(n_s)] if n_rep > 1 else None
+    shard_group = groups[rank // n_s]
+    me = rank % n_s
+    plan = OP.plan_layout(SHAPES, world, "hsdp" if n_rep > 1 else "fsdp2", n_rep=n_rep)
     n = plan.full_len_padded
     grad = torch.from_numpy(_exact_grad(rank, n))
     th, m, v = _state_by_index(n)
@@ -78,21 +89,23 @@ def _fsdp2(rank, world):
     pieces, geometry = [], []
     for i, shape in enumerate(SHAPES):
         t = grad[offs[i]:offs[i] + int(np.prod(shape))].view(shape)
-        ch = torch.chunk(t, world, dim=0)
+        ch = torch.chunk(t, n_s, dim=0)
         rows = ch[0].shape[0]
         cols = t[0].numel()
-        geometry.append((rows * cols, [c.numel() for c in ch] + [0] * (world - len(ch))))
-        pieces.append([c.reshape(-1) for c in ch] + [t.new_zeros(0)] * (world - len(ch)))
+        geometry.append((rows * cols, [c.numel() for c in ch] + [0] * (n_s - len(ch))))
+        pieces.append([c.reshape(-1) for c in ch] + [t.new_zeros(0)] * (n_s - len(ch)))
     block = sum(g[0] for g in geometry)
-    send = torch.zeros(world * block)
-    for r in range(world):
+    send = torch.zeros(n_s * block)
+    for r in range(n_s):
         o = r * block
         for i, (padded, _) in enumerate(geometry):
             p = pieces[i][r]
             send[o:o + p.numel()] = p
             o += padded
     recv = torch.zeros(block)
-    dist.reduce_scatter_tensor(recv, send)
+    dist.reduce_scatter_tensor(recv, send, group=shard_group)
+    if across is not None:
+        dist.all_reduce(recv, group=across[me])
     G = (recv / float(world)).numpy()
     # AdamW on this rank's own segments, state slots from the oracle's plan
     seg = {(s.param, s.rank): s for s in plan.segments}
@@ -103,7 +116,7 @@ def _fsdp2(rank, world):
     o = 0
     checks = []
     for i, (padded, sizes) in enumerate(geometry):
-        k = sizes[rank]
+        k = sizes[me]
         s = seg.get((i, rank))
         checks.append(k == (s.length if s else 0))
         if k:
@@ -114,10 +127,10 @@ def _fsdp2(rank, world):
             var[s.state_off:s.state_off + k] = v1
             cast[o:o + k] = OS.bf16_rne(t1)
         o += padded
-    # all-gather of the bf16 shards, then copy-out into this rank's full buffer
-    gathered = _all_gather_bits(cast, world)
+    # all-gather of the bf16 shards in the shard group, then copy-out into this rank's full buffer
+    gathered = _all_gather_bits(cast, n_s, shard_group)
     params = np.zeros(n, np.uint16)
-    for r in range(world):
+    for r in range(n_s):
         o = r * block
         for i, (padded, sizes) in enumerate(geometry):
             params[offs[i] + sum(sizes[:r]):offs[i] + sum(sizes[:r]) + sizes[r]] = gathered[o:o + sizes[r]]
@@ -143,7 +156,8 @@ def _rank_main(rank, world, port, out_dir, case):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        res = {"toy": _toy, "fsdp2": _fsdp2, "distopt": _distopt}[case](rank, world)
+        res = {"toy": _toy, "fsdp2": _fsdp2, "distopt": _distopt,
+               "hsdp": lambda r, w: _fsdp2(r, w, n_rep=2)}[case](rank, world)
     finally:
         dist.destroy_process_group()
     np.save(os.path.join(out_dir, f"r{rank}.npy"), np.array([res], dtype=object), allow_pickle=True)
@@ -155,8 +169,8 @@ def _run(case, tmp_path):
     return [np.load(tmp_path / f"r{r}.npy", allow_pickle=True)[0] for r in range(WORLD)]
 
 
-def _single_process(mode):
-    plan = OP.plan_layout(SHAPES, WORLD, mode)
+def _single_process(mode, n_rep=1):
+    plan = OP.plan_layout(SHAPES, WORLD, mode, n_rep=n_rep)
     n = plan.full_len_padded
     grads = [_exact_grad(q, n) for q in range(WORLD)]
     fi, si = OP.owned_indices(plan)
@@ -184,9 +198,11 @@ def test_four_processes_reproduce_the_pages_toy(tmp_path):
     assert OS.rs_update_ag(plan, grads, lambda s: np.float32(0.5) * s)[0].tolist() == res[0]["gathered"]
 
 
-def test_fsdp2_with_real_collectives_equals_the_oracle(tmp_path):
-    res = _run("fsdp2", tmp_path)
-    plan, state, params = _single_process("fsdp2")
+@pytest.mark.parametrize("mode,n_rep", [("fsdp2", 1), ("hsdp", 2)])
+def test_fsdp2_with_real_collectives_equals_the_oracle(tmp_path, mode, n_rep):
+    """FSDP2 over 4 ranks, and HSDP as 2 replica groups of 2 (gloo subgroups)."""
+    res = _run(mode, tmp_path)
+    plan, state, params = _single_process(mode, n_rep)
     for r, out in enumerate(res):
         assert all(out["checks"]), "torch.chunk pieces differ from the plan's segment lengths"
         for s in plan.segments:
