@@ -44,7 +44,7 @@ UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = tuple(os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", f)
                    for f in ("fsp_args.h", "fsp_kernels.cuh"))
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sharded_step_kernel_dram_traffic_workloads_1_3_4_5.txt")
 # Working sets under this many L2 sizes get an L2 flush before every timed step.
 L2_FLUSH_FACTOR = 4
 L2_BYTES = 129_000_000      # GB300's L2; the device's own figure is used when a GPU is present
