@@ -149,3 +149,15 @@ def test_pool_size_respects_host_memory(monkeypatch):
     assert bench.pool_size(w, 4_000_000) == 3
     monkeypatch.setattr(bench, "host_memory_available", lambda: per)
     assert bench.pool_size(w, 4_000_000) == 1
+
+
+def test_traffic_record_matches_the_current_kernel_source():
+    """The committed ncu traffic record is found and still belongs to the
+    step kernel's current source (else the bench line reports traffic null)."""
+    from synth_inputs import workload
+    assert os.path.exists(bench.TRAFFIC_FILE)
+    for name in ("qwen3_0p6b_fsdp2", "ragged_500", "dense_1p5b_bf16grad", "qwen3_0p6b_hsdp_2x4"):
+        w = workload(name)
+        algorithmic = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+        tpe = bench.traffic_per_elem(name)
+        assert tpe is not None and 0.95 < tpe / algorithmic < 1.05, name
