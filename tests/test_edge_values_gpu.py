@@ -199,3 +199,41 @@ def test_unshard_of_edge_masters_is_the_exact_cast(n_d, mode, n_rep):
         assert np.array_equal(bf[q].cpu().numpy().view(np.uint16), o_params[q])   # padding included
         assert np.array_equal(f32[q].cpu().numpy().view(np.uint32), want32)
     assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("n_d,mode", [(4, "fsdp2"), (8, "distopt"), (9, "fsdp2")])
+def test_writeback_step_on_edge_values(n_d, mode):
+    """The fused step with the write-back: the owners' grad slices hold the
+    oracle's averaged gradient bit for bit, the rest of every grad buffer is
+    unchanged, and state and params match the oracle as the plain step's do."""
+    dev, ora = _case(n_d, mode, "f32")
+    fsp.sharded_step_writeback(dev.plan, [g.t for g in dev.grads], *[s.t for s in dev.state],
+                               [p.t for p in dev.params], HP, 10)
+    written = [g.copy() for g in ora.grads]
+    OS.reduce_scatter_write_back(ora.plan, written)
+    ora.step(10)                                   # on the gradients as they were before the step
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        assert np.array_equal(dev.grads[q].bits(), written[q].view(np.uint32)), f"grad buffer {q}"
+    compare(dev, ora, check_reduced=False)
+
+
+@pytest.mark.parametrize("n_d,mode,n_rep,gd", [(4, "fsdp2", 1, "f32"), (8, "hsdp", 2, "bf16"), (9, "fsdp2", 1, "f32")])
+def test_per_parameter_tensors_on_edge_values(n_d, mode, n_rep, gd):
+    """The step on per-parameter tensors equals the flat step element for
+    element on the same hand-placed values (state copied slot by slot)."""
+    from test_params_gpu import ParamCase
+    dev, _ = _case(n_d, mode, gd, n_rep)
+    pc = ParamCase(dev, n_rep)
+    flat_seg = {(s.param, s.rank): s for s in dev.plan.segments}
+    for s in pc.plan.segments:
+        f = flat_seg[(s.param, s.rank)]
+        for dst, src in zip(pc.state, dev.state):
+            dst.t[s.state_off:s.state_off + s.length] = src.t[f.state_off:f.state_off + f.length]
+    for t in (1, 10):
+        dev.step(t, debug=False)
+        pc.step(t)
+    torch.cuda.synchronize()
+    pc.state_matches_flat()
+    pc.params_match_flat()
+    assert pc.guards_intact() and dev.all_guards_intact() and fsp.device_error() == 0
