@@ -237,3 +237,30 @@ def test_per_parameter_tensors_on_edge_values(n_d, mode, n_rep, gd):
     pc.state_matches_flat()
     pc.params_match_flat()
     assert pc.guards_intact() and dev.all_guards_intact() and fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("n_d,mode,n_rep", [(4, "fsdp2", 1), (8, "hsdp", 2), (9, "fsdp2", 1)])
+def test_fp32_gather_and_zero3_steps_on_edge_values(n_d, mode, n_rep):
+    """The same state as the plain step on the hand-placed values; the fp32
+    all-gather writes the new master itself, bit for bit, into every rank's
+    buffer (group's for HSDP); the ZeRO-3 step writes no parameter."""
+    plain, ora = _case(n_d, mode, "f32", n_rep)
+    f32, _ = _case(n_d, mode, "f32", n_rep)
+    z3, _ = _case(n_d, mode, "f32", n_rep)
+    n = plain.plan.full_len_padded
+    bufs = [torch.full((n,), -1, dtype=torch.int32, device="cuda") for _ in range(n_d)]
+    plain.step(10, debug=False)
+    fsp.sharded_step_fp32_gather(f32.plan, [g.t for g in f32.grads], *[s.t for s in f32.state],
+                                 [b.view(torch.float32) for b in bufs], HP, 10)
+    fsp.sharded_step(z3.plan, [g.t for g in z3.grads], *[s.t for s in z3.state], None, HP, 10)
+    torch.cuda.synchronize()
+    for a, b, c in zip(plain.state, f32.state, z3.state):
+        assert np.array_equal(a.bits(), b.bits()) and np.array_equal(a.bits(), c.bits())
+    master = plain.state[0].bits()
+    want = np.full(n, 0xFFFFFFFF, np.uint32)
+    want[ora.fi] = master[ora.si]
+    for q in range(n_d):      # (HSDP: each group gathers its own state copy; the copies are equal)
+        assert np.array_equal(bufs[q].cpu().numpy().view(np.uint32), want)
+    for p in z3.params:
+        assert np.all(p.bits() == 0xFFFF)       # untouched: still the sentinel
+    assert fsp.device_error() == 0
