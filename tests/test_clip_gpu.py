@@ -127,3 +127,28 @@ def test_clipped_full_size(idx):
     finally:
         del dev
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", ["fsdp2", "distopt"])
+def test_norm_is_accurate_far_beyond_the_bar(mode):
+    """The norm's squares are summed per thread in an fp32 pair (Dot2), then in
+    fp64, and the result is handed out as fp32: on 12.3 M elements it is the
+    fp32 rounding of an fp64 torch norm of the same reduced gradient (1 ulp at
+    most, for a norm that falls next to a rounding boundary), where the stated
+    bar would allow 1e-6 relative (~17 ulps)."""
+    shapes = [(3000, 4096), (4099,), (77, 3)]
+    dev = DeviceCase(shapes, 8, mode, "f32", 77)
+    try:
+        G = torch.zeros(dev.plan.full_len_padded, dtype=torch.float32, device="cuda")
+        for g in dev.grads:
+            G += g.t
+        G /= 8.0
+        ref = float(torch.sqrt(torch.sum(G[:dev.plan.valid_elems].double() ** 2)))
+        norm, _ = _clipped(dev, 3, 1.0)
+        got = np.array([norm], np.float32).view(np.uint32)
+        want = np.array([ref], np.float32).view(np.uint32)
+        assert ulp_dist(got, want)[0] <= 1, (norm, ref)
+        assert fsp.device_error() == 0
+    finally:
+        del dev
+        torch.cuda.empty_cache()
