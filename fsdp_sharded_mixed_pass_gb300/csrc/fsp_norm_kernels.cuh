@@ -58,7 +58,45 @@ __device__ __forceinline__ void rs_writeback_tile(const StepArgs& a, const Tile&
   const int64_t head = min(len, (4 - (f0 & 3)) & 3);
   const int64_t groups = (len - head) >> 2;
   const int64_t tail = head + groups * 4;
-  for (int64_t i = threadIdx.x; i < groups; i += kGenericThreads) {
+  int64_t i0 = threadIdx.x;
+  if constexpr (NT > 0) {
+    // two groups per round: every load of both before either store (the owner's
+    // slice aliases one of the rank buffers, so the compiler would not reorder)
+    for (; i0 + kGenericThreads < groups; i0 += 2 * kGenericThreads) {
+      const int64_t fa = f0 + head + 4 * i0, fb = fa + 4 * kGenericThreads;
+      float4 xa[NT], xb[NT];
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        xa[q] = GradIO<float>::load4(gb[q], fa);
+        xb[q] = GradIO<float>::load4(gb[q], fb);
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acb = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        add4(acc, xa[q]);
+        add4(acb, xb[q]);
+      }
+      acc.x = acc.x / float(n);
+      acc.y = acc.y / float(n);
+      acc.z = acc.z / float(n);
+      acc.w = acc.w / float(n);
+      acb.x = acb.x / float(n);
+      acb.y = acb.y / float(n);
+      acb.z = acb.z / float(n);
+      acb.w = acb.w / float(n);
+      *reinterpret_cast<float4*>(own + fa) = acc;
+      *reinterpret_cast<float4*>(own + fb) = acb;
+      sq.add(acc.x);
+      sq.add(acc.y);
+      sq.add(acc.z);
+      sq.add(acc.w);
+      sq.add(acb.x);
+      sq.add(acb.y);
+      sq.add(acb.z);
+      sq.add(acb.w);
+    }
+  }
+  for (int64_t i = i0; i < groups; i += kGenericThreads) {
     const int64_t f = f0 + head + 4 * i;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll(NT > 0 ? NT : 1)
