@@ -255,11 +255,12 @@ def clip_coefficient(norm: float, max_norm) -> np.float32:
 
 def sharded_step_clipped(plan: Plan, grads, master, m, v, params, hp: dict, t: int, max_norm):
     """reduce-scatter with write-back -> global norm -> clip -> AdamW -> cast ->
-    all-gather.  Returns (norm, coefficient).  fp32 grads, one replica group."""
-    if plan.n_rep != 1:
-        raise ValueError("clipping is defined here for FSDP2 and DistOpt plans")
+    all-gather.  Returns (norm, coefficient).  fp32 grads.  HSDP: after the
+    all-reduce across replica groups every group's owner holds the same
+    averaged slice, so each group's owner gets it written back, and the norm
+    counts every element once (the first group's segments)."""
     reduced = reduce_scatter_write_back(plan, grads, "f32")
-    norm = global_grad_norm(reduced)
+    norm = global_grad_norm([g for seg, g in zip(plan.segments, reduced) if seg.rank < plan.n_shard])
     coef = clip_coefficient(norm, max_norm)
     casts = []
     for seg, g in zip(plan.segments, reduced):

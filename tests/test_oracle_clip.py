@@ -87,10 +87,53 @@ def test_clipped_step_distopt_matches_fsdp2_per_element():
     assert np.array_equal(out["fsdp2"][3], out["distopt"][3])
 
 
-def test_clipping_rejects_hsdp_and_bf16():
+def test_clipping_rejects_bf16():
     plan = P.plan_hsdp([(8,)], 2, 2)
-    grads, (master, m, v), params = _inputs(plan, "f32", 1)
-    with pytest.raises(ValueError):
-        O.sharded_step_clipped(plan, grads, master, m, v, params, HP, 1, 1.0)
+    grads, _, _ = _inputs(plan, "f32", 1)
     with pytest.raises(ValueError):
         O.reduce_scatter_write_back(P.plan_fsdp2([(8,)], 2), grads[:2], "bf16")
+
+
+@pytest.mark.parametrize("n_rep,n_shard", [(2, 2), (2, 3), (3, 2), (4, 1)])
+@pytest.mark.parametrize("max_norm", [1e-4, 1e30])
+def test_hsdp_clipped_step_equals_the_unsharded_definition(n_rep, n_shard, max_norm):
+    """HSDP with clipping against the plain definition over the full buffer:
+    the grouped all-reduce average, its fp64 norm over every element once, the
+    clipped AdamW; every replica group's state copy and parameters, and every
+    group's owner slices written back with the averaged gradient."""
+    shapes = [(9, 5), (13,), (1,), (2 * n_shard + 1, 3)]
+    plan = P.plan_hsdp(shapes, n_rep, n_shard)
+    grads, (master, m, v), params = _inputs(plan, "f32", 21)
+    n = plan.full_len_padded
+    G = O.all_reduce(grads, "f32", n_rep=n_rep)
+    want_norm = float(np.sqrt(np.sum(G[:plan.valid_elems].astype(np.float64) ** 2)))
+    fi, si = P.owned_indices(plan)
+    th0, m0, v0 = master[si].copy(), m[si].copy(), v[si].copy()
+    norm, coef = O.sharded_step_clipped(plan, grads, master, m, v, params, HP, 7, max_norm)
+    assert norm == pytest.approx(want_norm, rel=1e-12)
+    assert abs(float(coef) - float(O.clip_coefficient(want_norm, max_norm))) <= 2.0 ** -23 * float(coef)
+    assert (coef < 1) == (max_norm < 1)
+    th, mm, vv = O.adamw(th0, m0, v0, (G[fi] * coef).astype(np.float32), HP, 7)
+    assert np.array_equal(master[si], th) and np.array_equal(m[si], mm) and np.array_equal(v[si], vv)
+    for s in plan.segments:   # every group's owner holds the averaged slice
+        assert np.array_equal(grads[s.rank][s.full_off:s.full_off + s.length], G[s.full_off:s.full_off + s.length])
+    cast = np.zeros(n, np.uint16)
+    cast[fi] = O.bf16_rne(th)
+    for q in range(plan.n_d):
+        assert np.array_equal(params[q][:plan.valid_elems], cast[:plan.valid_elems])
+
+
+def test_hsdp_clipped_with_one_group_is_the_fsdp2_flow():
+    shapes = [(9, 5), (13,), (1,)]
+    outs = []
+    for plan in (P.plan_fsdp2(shapes, 3), P.plan_hsdp(shapes, 1, 3)):
+        grads, (master, m, v), params = _inputs(plan, "f32", 22)
+        norm, coef = O.sharded_step_clipped(plan, grads, master, m, v, params, HP, 4, 1e-3)
+        outs.append((norm, coef, master, m, v, params, grads))
+    a, b = outs
+    assert a[0] == b[0] and a[1] == b[1]
+    for x, y in zip(a[2:5], b[2:5]):       # (NaN sentinels in the padding: compare bits)
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    for x, y in zip(a[5] + a[6], b[5] + b[6]):
+        assert np.array_equal(x.view(np.uint16 if x.dtype == np.uint16 else np.uint32),
+                              y.view(np.uint16 if y.dtype == np.uint16 else np.uint32))
