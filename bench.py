@@ -77,7 +77,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clip", type=float, default=None, metavar="MAX_NORM",
                     help="time the distributed-optimizer flow instead: reduce-scatter written back into the "
-                         "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt)")
+                         "owners' grad slices, global norm, clipped AdamW (fp32 grads, FSDP2/DistOpt/HSDP)")
     ap.add_argument("--no-gather", action="store_true",
                     help="time the ZeRO-3 step instead: reduce-scatter + AdamW, parameters left sharded")
     ap.add_argument("--writeback", action="store_true",
@@ -341,8 +341,8 @@ class DeviceWorkload:
             return w.n_d * w.grad_bytes + 24 * w.n_rep
         if self.writeback:          # the step plus the owner's averaged slice written back
             return w.n_d * w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
-        if self.clip is not None:   # pass 1: N_d grads in, 1 out; pass 3: 1 grad + state + N_d params
-            return w.n_d * w.grad_bytes + w.grad_bytes + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+        if self.clip is not None:   # pass 1: N_d grads in, one slice out per group; pass 3: 1 grad + state + params
+            return w.n_d * w.grad_bytes + w.grad_bytes * w.n_rep + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         return w.n_d * w.grad_bytes + 24 * w.n_rep + pbytes * w.n_d
 
 

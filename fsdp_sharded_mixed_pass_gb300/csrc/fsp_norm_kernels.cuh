@@ -5,8 +5,8 @@
 // clipped AdamW + cast + all-gather, is sharded_step_kernel<..., kClip> in
 // fsp_kernels.cuh.
 //
-//  * rs_writeback_norm_kernel<N_d>: one CTA per tile; reduce-scatter into the
-//    owners' slices and the tile's sum of squares.
+//  * rs_writeback_norm_kernel<N_s, N_r>: one CTA per tile; reduce-scatter into
+//    the owners' slices and the tile's sum of squares.
 //  * norm_block_sums_kernel, norm_finalize_kernel: the tiles' sums added in an
 //    order fixed by the plan; the norm and the clip coefficient.
 #pragma once
@@ -47,45 +47,79 @@ struct SumSq2 {
 // leaves the sum of squares of the elements it reduced in partials[cta]: each
 // thread's in SumSq2, the CTA's threads added in fp64 in a fixed order.
 // Launched with one CTA per tile: one partial per tile, a grouping fixed by the
-// plan alone.  One replica group (FSDP2 / DistOpt).  NT > 0: N_d fixed; 0: a.n_d.
+// plan alone.  NS x NR ranks known at compile time (NS = 0: a.n_shard x a.n_rep
+// at run time); NR = 1 is FSDP2 / DistOpt.  HSDP (NR > 1): each replica group's
+// ranks are folded in order, then the groups' sums in group order - the
+// all-reduce across groups - and the result is written to the owner in every
+// group; the tiles cover the first group only, so each element's square is
+// counted once.
+
+// The grouped fold of element f over the ranks' bases gb (ns ranks in each of nr groups).
+__device__ __forceinline__ float fold1(const void* const* gb, int64_t f, int ns, int nr) {
+  float acc = 0.f;
+  for (int r = 0; r < nr; ++r) {
+    float part = 0.f;
+    for (int j = 0; j < ns; ++j) part += GradIO<float>::load1(gb[r * ns + j], f);
+    acc = r == 0 ? part : acc + part;
+  }
+  return acc;
+}
+
+// The grouped fold of N = NS x NR loaded values (rank r * NS + j at x[r * NS + j]).
+template <int NS, int NR>
+__device__ __forceinline__ float4 fold4(const float4* x) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NS; ++j) add4(part, x[r * NS + j]);
+    if (r == 0)
+      acc = part;
+    else
+      add4(acc, part);
+  }
+  return acc;
+}
+
 // One tile of pass 1 with rank bases gb.
-template <int NT>
+template <int NS, int NR>
 __device__ __forceinline__ void rs_writeback_tile(const StepArgs& a, const Tile& tile, const void* const* gb,
                                                   SumSq2& sq) {
-  const int n = NT > 0 ? NT : a.n_d;
+  const int ns = NS > 0 ? NS : a.n_shard, nr = NS > 0 ? NR : a.n_rep;
+  const int n = ns * nr;
   const int64_t f0 = tile.full_begin, len = tile.len;
-  float* own = static_cast<float*>(const_cast<void*>(gb[tile.rank]));
   const int64_t head = min(len, (4 - (f0 & 3)) & 3);
   const int64_t groups = (len - head) >> 2;
   const int64_t tail = head + groups * 4;
   int64_t i0 = threadIdx.x;
-  if constexpr (NT > 0) {
-    // two groups per round: every load of both before either store (the owner's
-    // slice aliases one of the rank buffers, so the compiler would not reorder)
+  if constexpr (NS > 0) {
+    // two groups per round: every load of both before either store (the owners'
+    // slices alias rank buffers, so the compiler would not reorder)
+    constexpr int N = NS * NR;
     for (; i0 + kGenericThreads < groups; i0 += 2 * kGenericThreads) {
       const int64_t fa = f0 + head + 4 * i0, fb = fa + 4 * kGenericThreads;
-      float4 xa[NT], xb[NT];
+      float4 xa[N], xb[N];
 #pragma unroll
-      for (int q = 0; q < NT; ++q) {
+      for (int q = 0; q < N; ++q) {
         xa[q] = GradIO<float>::load4(gb[q], fa);
         xb[q] = GradIO<float>::load4(gb[q], fb);
       }
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acb = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = fold4<NS, NR>(xa), acb = fold4<NS, NR>(xb);
+      acc.x = acc.x / float(N);
+      acc.y = acc.y / float(N);
+      acc.z = acc.z / float(N);
+      acc.w = acc.w / float(N);
+      acb.x = acb.x / float(N);
+      acb.y = acb.y / float(N);
+      acb.z = acb.z / float(N);
+      acb.w = acb.w / float(N);
 #pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        add4(acc, xa[q]);
-        add4(acb, xb[q]);
+      for (int r = 0; r < NR; ++r) {
+        float* own = static_cast<float*>(const_cast<void*>(gb[r * NS + tile.rank]));
+        *reinterpret_cast<float4*>(own + fa) = acc;
+        *reinterpret_cast<float4*>(own + fb) = acb;
       }
-      acc.x = acc.x / float(n);
-      acc.y = acc.y / float(n);
-      acc.z = acc.z / float(n);
-      acc.w = acc.w / float(n);
-      acb.x = acb.x / float(n);
-      acb.y = acb.y / float(n);
-      acb.z = acb.z / float(n);
-      acb.w = acb.w / float(n);
-      *reinterpret_cast<float4*>(own + fa) = acc;
-      *reinterpret_cast<float4*>(own + fb) = acb;
       sq.add(acc.x);
       sq.add(acc.y);
       sq.add(acc.z);
@@ -99,13 +133,20 @@ __device__ __forceinline__ void rs_writeback_tile(const StepArgs& a, const Tile&
   for (int64_t i = i0; i < groups; i += kGenericThreads) {
     const int64_t f = f0 + head + 4 * i;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll(NT > 0 ? NT : 1)
-    for (int q = 0; q < n; ++q) add4(acc, GradIO<float>::load4(gb[q], f));
+    for (int r = 0; r < nr; ++r) {
+      float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < ns; ++j) add4(part, GradIO<float>::load4(gb[r * ns + j], f));
+      if (r == 0)
+        acc = part;
+      else
+        add4(acc, part);
+    }
     acc.x = acc.x / float(n);
     acc.y = acc.y / float(n);
     acc.z = acc.z / float(n);
     acc.w = acc.w / float(n);
-    *reinterpret_cast<float4*>(own + f) = acc;
+    for (int r = 0; r < nr; ++r)
+      *reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(gb[r * ns + tile.rank])) + f) = acc;
     sq.add(acc.x);
     sq.add(acc.y);
     sq.add(acc.z);
@@ -114,16 +155,13 @@ __device__ __forceinline__ void rs_writeback_tile(const StepArgs& a, const Tile&
   const int64_t n_scalar = head + (len - tail);
   if (threadIdx.x < n_scalar) {
     const int64_t f = f0 + (threadIdx.x < head ? int64_t(threadIdx.x) : tail + (threadIdx.x - head));
-    float acc = 0.f;
-#pragma unroll(NT > 0 ? NT : 1)
-    for (int q = 0; q < n; ++q) acc += GradIO<float>::load1(gb[q], f);
-    acc = acc / float(n);
-    own[f] = acc;
+    const float acc = fold1(gb, f, ns, nr) / float(n);
+    for (int r = 0; r < nr; ++r) static_cast<float*>(const_cast<void*>(gb[r * ns + tile.rank]))[f] = acc;
     sq.add(acc);
   }
 }
 
-template <int NT>
+template <int NS, int NR>
 __global__ void __launch_bounds__(kGenericThreads) rs_writeback_norm_kernel(const __grid_constant__ StepArgs a,
                                                                             double* partials) {
   __shared__ const void* tile_gb[kMaxRanks];
@@ -135,9 +173,9 @@ __global__ void __launch_bounds__(kGenericThreads) rs_writeback_norm_kernel(cons
       __syncthreads();
       if (threadIdx.x < a.n_d) tile_gb[threadIdx.x] = a.vgrads[int64_t(tile.param) * a.n_d + threadIdx.x];
       __syncthreads();
-      rs_writeback_tile<NT>(a, tile, tile_gb, sq);
+      rs_writeback_tile<NS, NR>(a, tile, tile_gb, sq);
     } else {
-      rs_writeback_tile<NT>(a, tile, a.grads, sq);
+      rs_writeback_tile<NS, NR>(a, tile, a.grads, sq);
     }
   }
   // CTA sum in a fixed order: warp shuffles, then warp 0 over the warp sums

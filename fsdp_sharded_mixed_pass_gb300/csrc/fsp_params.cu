@@ -238,7 +238,6 @@ fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, 
                                    const fsp_adamw_hparams* hp, int64_t step, float max_norm, float* norm_out,
                                    void* stream) {
   clear_error();
-  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 plans");
   if (t && t->grad_dtype != FSP_DTYPE_F32)
     return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 gradient tensors");
   if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");

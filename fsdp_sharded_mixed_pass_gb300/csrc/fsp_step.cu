@@ -60,24 +60,32 @@ template <typename GradT>
 using Kernels = KernelTable<GradT, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
                             Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>, Mesh<2, 2>, Mesh<4, 2>, Mesh<8, 2>,
                             Mesh<2, 4>, Mesh<4, 4>>;
-// the clipped update exists for one replica group and fp32 grads only
+// the clipped update (fp32 grads): the same meshes
 using ClipKernels = KernelTable<float, Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
-                                Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>>;
+                                Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>, Mesh<2, 2>, Mesh<4, 2>,
+                                Mesh<8, 2>, Mesh<2, 4>, Mesh<4, 4>>;
 
-// Pass 1 of the clipped flow for N_d ranks.
-template <int... Ns>
-struct NormKernelTable {
-  static KernelInfo get(int n) {
-    KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0>), kGenericThreads, 0, false};
-    ((n == Ns ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<Ns>), kGenericThreads, 0,
-                                false},
-                 0)
-              : 0),
+// Pass 1 of the clipped flow for N_s x N_r ranks (the step kernel's meshes;
+// others run the run-time instantiation <0, 0>).
+template <typename... Ms>
+struct NormKernelTable;
+
+template <int... NS, int... NR>
+struct NormKernelTable<Mesh<NS, NR>...> {
+  static KernelInfo get(int n_shard, int n_rep) {
+    KernelInfo k{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<0, 0>), kGenericThreads, 0, false};
+    ((n_shard == NS && n_rep == NR
+          ? (k = KernelInfo{reinterpret_cast<const void*>(&rs_writeback_norm_kernel<NS, NR>), kGenericThreads, 0,
+                            false},
+             0)
+          : 0),
      ...);
     return k;
   }
 };
-using NormKernels = NormKernelTable<1, 2, 3, 4, 5, 6, 7, 8, 12, 16>;
+using NormKernels = NormKernelTable<Mesh<1, 1>, Mesh<2, 1>, Mesh<3, 1>, Mesh<4, 1>, Mesh<5, 1>, Mesh<6, 1>,
+                                    Mesh<7, 1>, Mesh<8, 1>, Mesh<12, 1>, Mesh<16, 1>, Mesh<2, 2>, Mesh<4, 2>,
+                                    Mesh<8, 2>, Mesh<2, 4>, Mesh<4, 4>>;
 
 std::string cuda_msg(const char* what, cudaError_t e) {
   return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -406,7 +414,7 @@ fsp_status run_clipped_passes(const fsp_plan* p, StepArgs& a, float max_norm, fl
   // pass 1: reduce-scatter into the owners' slices and each tile's sum of
   // squares, one CTA per tile (the block scheduler takes the tiles in order)
   if (a.n_tiles > INT32_MAX) return fail(FSP_EUNSUPPORTED, "the clipped step takes at most 2^31 - 1 work tiles");
-  const KernelInfo k1 = NormKernels::get(p->n_d);
+  const KernelInfo k1 = NormKernels::get(p->n_shard, p->n_rep);
   const int grid = int(a.n_tiles);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* args1[] = {&a, &partials};
@@ -445,7 +453,6 @@ fsp_status run_step_clipped(const fsp_plan* p, void* const* grads, int32_t dtype
                             void* const* params, const fsp_adamw_hparams* hp, int64_t step, float max_norm,
                             float* norm_out, void* stream) {
   clear_error();
-  if (p && p->n_rep != 1) return fail(FSP_EUNSUPPORTED, "the clipped step is for FSDP2 and DistOpt plans");
   if (dtype != FSP_DTYPE_F32) return fail(FSP_EUNSUPPORTED, "the clipped step writes back into fp32 grad buffers");
   if (!(std::isfinite(max_norm) && max_norm > 0.f)) return fail(FSP_EINVAL, "max_norm must be finite and > 0");
   std::vector<Buf> extra{{norm_out, 2 * sizeof(float), "norm_out"}};

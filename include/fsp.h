@@ -241,12 +241,16 @@ fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void* const* gr
                                      int32_t advance, void* cuda_stream);
 
 /* The Megatron distributed-optimizer flow with global-norm gradient clipping,
- * for FSDP2 and DistOpt plans with fp32 grads (others: FSP_EUNSUPPORTED):
+ * for FSDP2, DistOpt and HSDP plans with fp32 grads (bf16: FSP_EUNSUPPORTED):
  *   1. reduce-scatter with write-back: every element's averaged gradient
- *      (the rank-ordered fp32 fold / N_d) is stored into its owner's slice of
- *      the owner's own grad buffer ("07 · 显存模型", section 2.1 item 1); the
- *      rest of each grad buffer is left as it was;
- *   2. norm = sqrt(sum of squares of every reduced element) to fp64 accuracy
+ *      (the rank-ordered fp32 fold / N_d; HSDP: the fold inside each replica
+ *      group, then across groups, as fsp_sharded_step) is stored into its
+ *      owner's slice of the owner's own grad buffer ("07 · 显存模型", section
+ *      2.1 item 1) - for HSDP into the owner's slice in every replica group,
+ *      all of which hold the all-reduced slice; the rest of each grad buffer
+ *      is left as it was;
+ *   2. norm = sqrt(sum of squares of every reduced element, each counted
+ *      once) to fp64 accuracy
  *      (each thread's squares summed as a pair of floats - Dot2 of Ogita,
  *      Rump and Oishi 2005 - one fp64 partial per work tile, the partials
  *      added in an order fixed by the plan), and coefficient = min(1,
@@ -406,8 +410,8 @@ fsp_status fsp_sharded_step_writeback_params(const fsp_plan* plan, const fsp_par
                                              float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
                                              int64_t step, void* cuda_stream);
 
-/* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 per-parameter
- * plan, fp32 gradients; others: FSP_EUNSUPPORTED): every element's averaged
+/* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 or HSDP
+ * per-parameter plan, fp32 gradients; bf16: FSP_EUNSUPPORTED): every element's averaged
  * gradient is written back into its owner's slice of the owner's gradient
  * tensor, then the norm, the coefficient and the clipped update as there.
  * norm_out: device, 2 floats, 16-byte aligned. */

@@ -256,7 +256,8 @@ def test_clipped_step_rejects_on_host():
     L = B.lib()
     hsdp = fsp.plan_layout([(64, 8)], 4, "hsdp", n_replicate=2)
     fsdp = fsp.plan_layout([(64, 8)], 4)
-    for plan, dtype, max_norm, want in ((hsdp, "f32", 1.0, B.FSP_EUNSUPPORTED),
+    for plan, dtype, max_norm, want in ((hsdp, "bf16", 1.0, B.FSP_EUNSUPPORTED),
+                                        (hsdp, "f32", -1.0, B.FSP_EINVAL),
                                         (fsdp, "bf16", 1.0, B.FSP_EUNSUPPORTED),
                                         (fsdp, "f32", 0.0, B.FSP_EINVAL),
                                         (fsdp, "f32", float("inf"), B.FSP_EINVAL)):

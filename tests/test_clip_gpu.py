@@ -152,3 +152,23 @@ def test_norm_is_accurate_far_beyond_the_bar(mode):
     finally:
         del dev
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n_rep,n_shard", [(2, 2), (2, 4), (3, 3), (4, 2)])
+@pytest.mark.parametrize("max_norm", [1e-4, 1e30])
+def test_hsdp_clipped_step_matches_oracle(n_rep, n_shard, max_norm):
+    """HSDP meshes: the grouped reduction written back to the owner in every
+    replica group, the norm over each element once, every group's state copy
+    updated with the clipped gradient and gathered within its group."""
+    rng = np.random.default_rng(n_rep * 13 + n_shard)
+    shapes = [(int(rng.integers(1, 3 * n_shard + 5)), int(rng.choice([1, 3, 64]))) for _ in range(5)] + [(4097,)]
+    n_d = n_rep * n_shard
+    dev = DeviceCase(shapes, n_d, "hsdp", "f32", 700 + n_d, n_rep)
+    ora = OracleCase(shapes, n_d, "hsdp", "f32", 700 + n_d, n_rep)
+    for t in (10, 11):
+        norm, coef = _clipped(dev, t, max_norm)
+        ora.prev = [a.copy() for a in ora.state]
+        ora.hp = HP
+        o_norm, o_coef = OS.sharded_step_clipped(ora.plan, ora.grads, *ora.state, ora.params, HP, t, max_norm)
+        _check(dev, ora, norm, coef, o_norm, o_coef)
+        assert (coef < 1.0) == (max_norm < 1e20)

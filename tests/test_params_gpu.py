@@ -184,13 +184,15 @@ def test_per_param_step_equals_flat_step_on_a_large_plan(n_d, mode, n_rep, gd):
 
 
 @pytest.mark.parametrize("max_norm", [1e-4, 1e30])
-@pytest.mark.parametrize("shapes", [SHAPES, BIG], ids=["small", "large"])
-def test_per_param_clipped_flow_equals_flat(max_norm, shapes):
+@pytest.mark.parametrize("shapes,n_d,n_rep", [(SHAPES, 4, 1), (BIG, 4, 1), (SHAPES, 8, 2)],
+                         ids=["small", "large", "hsdp_2x4"])
+def test_per_param_clipped_flow_equals_flat(max_norm, shapes, n_d, n_rep):
     """The distributed-optimizer flow with clipping on per-parameter tensors:
-    the write-back lands in the owner's slice of the owner's gradient tensor,
-    and norm, coefficient, state and parameters are the flat flow's."""
-    flat = DeviceCase(shapes, 4, "fsdp2", "f32", 89)
-    pc = ParamCase(flat)
+    the write-back lands in the owner's slice of the owner's gradient tensor
+    (HSDP: in every replica group), and norm, coefficient, state and
+    parameters are the flat flow's."""
+    flat = DeviceCase(shapes, n_d, "hsdp" if n_rep > 1 else "fsdp2", "f32", 89, n_rep)
+    pc = ParamCase(flat, n_rep)
     out_f = torch.zeros(4, dtype=torch.float32, device="cuda")
     out_p = torch.zeros(4, dtype=torch.float32, device="cuda")
     fsp.sharded_step_clipped(flat.plan, [g.t for g in flat.grads], *[s.t for s in flat.state],
