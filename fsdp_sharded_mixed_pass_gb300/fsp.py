@@ -469,7 +469,7 @@ def sharded_step_clipped(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, par
                          max_norm: float, norm_out, stream=None, grad_dtype: str | None = None) -> None:
     """Reduce-scatter with write-back into the owners' grad slices, global-norm
     clipping, AdamW, cast, all-gather; ``norm_out`` (device, 2 floats) receives
-    {norm, coefficient}.  fp32 grads, FSDP2 or DistOpt plans."""
+    {norm, coefficient}.  fp32 grads; FSDP2, DistOpt or HSDP plans."""
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_clipped(*args, float(max_norm), ctypes.c_void_p(_ptr(norm_out)),
                                           ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_clipped")
