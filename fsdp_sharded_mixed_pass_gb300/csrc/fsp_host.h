@@ -36,7 +36,7 @@ fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false,
                   unsigned long long* fixed_ctr = nullptr);
 // Passes 1-3 of the clipped flow on a prepared argument block (non-empty
-// plan, fp32 grads, one replica group); clipped_empty writes norm_out = {0, 1}
+// plan, fp32 grads; HSDP plans too); clipped_empty writes norm_out = {0, 1}
 // for a plan with nothing to reduce.
 fsp_status run_clipped_passes(const fsp_plan* p, StepArgs& a, float max_norm, float* norm_out, void* stream);
 fsp_status clipped_empty(float* norm_out, void* stream);
