@@ -105,3 +105,44 @@ def test_capturable_steps_replay_in_a_graph_bit_for_bit():
     torch.cuda.synchronize()
     assert cap.t == 0
     assert fsp.device_error() == 0
+
+
+@pytest.mark.parametrize("n_d,n_rep", [(4, 1), (8, 2)])
+def test_optimizer_on_per_parameter_tensors_equals_the_flat_one(n_d, n_rep):
+    """on_tensors: the same parameters loaded per tensor, the same gradients in
+    per-parameter tensors; after two steps every parameter tensor equals the
+    flat optimizer's buffer slice, bit for bit, and so does the unshard."""
+    kw = dict(lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"], weight_decay=HP["weight_decay"])
+    mode = "hsdp" if n_rep > 1 else "fsdp2"
+    flat = fsp.ShardedAdamW(SHAPES, n_d, mode, n_replicate=n_rep, **kw)
+    numel = [int(np.prod(s)) for s in SHAPES]
+    offs = flat.plan.param_offsets
+    n = flat.full_len
+    idx = np.arange(n)
+    full = torch.from_numpy(S.master_f32(41, idx)).cuda()
+    gflat = [torch.from_numpy(S.grad_f32(41, q, idx)).cuda() for q in range(n_d)]
+    pflat = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(n_d)]
+    gt = [[gflat[q][o:o + k].clone().view(s) for o, k, s in zip(offs, numel, SHAPES)] for q in range(n_d)]
+    pt = [[torch.zeros(s, dtype=torch.bfloat16, device="cuda") for s in SHAPES] for _ in range(n_d)]
+    per = fsp.ShardedAdamW.on_tensors(SHAPES, n_d, gt, pt, n_replicate=n_rep, **kw)
+    flat.load_params([full[o:o + k].view(s) for o, k, s in zip(offs, numel, SHAPES)])
+    per.load_params([full[o:o + k].view(s) for o, k, s in zip(offs, numel, SHAPES)])
+    for _ in range(2):
+        flat.step(gflat, pflat)
+        per.step()
+    torch.cuda.synchronize()
+    assert per.t == flat.t == 2
+    def same():
+        for q in range(n_d):
+            for i, (o, k) in enumerate(zip(offs, numel)):
+                assert torch.equal(pt[q][i].reshape(-1).view(torch.int16), pflat[q][o:o + k].view(torch.int16)), (q, i)
+    same()
+    for q in range(n_d):
+        for x in pt[q]:
+            x.zero_()
+    per.unshard()
+    torch.cuda.synchronize()
+    same()
+    with pytest.raises(ValueError):
+        per.step(gflat, pflat)
+    assert fsp.device_error() == 0
