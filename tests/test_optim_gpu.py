@@ -107,8 +107,9 @@ def test_capturable_steps_replay_in_a_graph_bit_for_bit():
     assert fsp.device_error() == 0
 
 
+@pytest.mark.parametrize("capturable", [False, True])
 @pytest.mark.parametrize("n_d,n_rep", [(4, 1), (8, 2)])
-def test_optimizer_on_per_parameter_tensors_equals_the_flat_one(n_d, n_rep):
+def test_optimizer_on_per_parameter_tensors_equals_the_flat_one(n_d, n_rep, capturable):
     """on_tensors: the same parameters loaded per tensor, the same gradients in
     per-parameter tensors; after two steps every parameter tensor equals the
     flat optimizer's buffer slice, bit for bit, and so does the unshard."""
@@ -124,7 +125,7 @@ def test_optimizer_on_per_parameter_tensors_equals_the_flat_one(n_d, n_rep):
     pflat = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(n_d)]
     gt = [[gflat[q][o:o + k].clone().view(s) for o, k, s in zip(offs, numel, SHAPES)] for q in range(n_d)]
     pt = [[torch.zeros(s, dtype=torch.bfloat16, device="cuda") for s in SHAPES] for _ in range(n_d)]
-    per = fsp.ShardedAdamW.on_tensors(SHAPES, n_d, gt, pt, n_replicate=n_rep, **kw)
+    per = fsp.ShardedAdamW.on_tensors(SHAPES, n_d, gt, pt, n_replicate=n_rep, capturable=capturable, **kw)
     flat.load_params([full[o:o + k].view(s) for o, k, s in zip(offs, numel, SHAPES)])
     per.load_params([full[o:o + k].view(s) for o, k, s in zip(offs, numel, SHAPES)])
     for _ in range(2):
