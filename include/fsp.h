@@ -411,16 +411,19 @@ fsp_status fsp_sharded_step_writeback_params(const fsp_plan* plan, const fsp_par
                                              int64_t step, void* cuda_stream);
 
 /* fsp_sharded_step_clipped on the tensors of `table` (an FSDP2 or HSDP
- * per-parameter plan, fp32 gradients; bf16: FSP_EUNSUPPORTED): every element's averaged
- * gradient is written back into its owner's slice of the owner's gradient
- * tensor, then the norm, the coefficient and the clipped update as there.
- * norm_out: device, 2 floats, 16-byte aligned. */
+ * per-parameter plan, fp32 gradients; bf16: FSP_EUNSUPPORTED): every
+ * element's averaged gradient is written back into its owner's slice of the
+ * owner's gradient tensor (HSDP: in every replica group), then the norm, the
+ * coefficient and the clipped update as there.  norm_out: device, 2 floats,
+ * 16-byte aligned. */
 fsp_status fsp_sharded_step_clipped_params(const fsp_plan* plan, const fsp_param_table* table, float* master,
                                            float* exp_avg, float* exp_avg_sq, const fsp_adamw_hparams* hp,
                                            int64_t step, float max_norm, float* norm_out, void* cuda_stream);
 
-/* fsp_unshard into the per-parameter bf16 tensors of `table` (which must have
- * them). */
+/* fsp_unshard into the per-parameter tensors of `table`: the bf16 cast of the
+ * owned master values (an fp32 table: the values themselves) into every rank
+ * of the group.  A table created without param tensors: FSP_EINVAL; a table
+ * of another plan or device: FSP_EINVAL. */
 fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table, const float* master,
                               void* cuda_stream);
 
