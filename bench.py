@@ -13,8 +13,9 @@ per param).
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
 Other flows (each reports its own bytes per param): --clip MAX_NORM,
---writeback, --no-gather, --unshard, --fp32-gather, --per-param; --n-d N and
---param-slice a:b change the workload, --graph captures the timed steps.
+--writeback, --no-gather, --unshard, --fp32-gather, and --per-param (alone or
+with --clip, --writeback or --unshard); --n-d N and --param-slice a:b change
+the workload, --graph captures the timed steps.
 
 Multi-GPU (torchrun, one rank per GPU): the step does not shard across GPUs
 (the N_d ranks already live on one device), so every GPU runs an independent
@@ -250,6 +251,16 @@ def clocks_bad(c: dict) -> bool:
 # workload on the device
 # --------------------------------------------------------------------------
 
+# (N_s, N_r) meshes the library instantiates its bulk-copy step kernel for;
+# other meshes run the per-thread generic kernel.
+BULK_MESHES = frozenset([(n, 1) for n in (1, 2, 3, 4, 5, 6, 7, 8, 12, 16)] + [(2, 2), (4, 2), (8, 2), (2, 4), (4, 4)])
+
+
+def step_kernel_name(w) -> str:
+    """The step kernel a workload's mesh runs (the roofline's dominant kernel)."""
+    return "sharded_step_kernel" if (w.n_d // w.n_rep, w.n_rep) in BULK_MESHES else "sharded_step_generic_kernel"
+
+
 def resolve_workload(name: str, param_slice: str | None, n_d: int | None = None):
     """The named workload, optionally on params a..b-1 only and/or with another
     rank count N_d (HSDP keeps its replica groups; N_d must be a multiple)."""
@@ -314,6 +325,12 @@ class DeviceWorkload:
         if self.per_param:
             if self.unshard:
                 fsp.unshard_params(self.plan, self.table, self.state[0], stream=stream)
+            elif self.clip is not None:
+                fsp.sharded_step_clipped_params(self.plan, self.table, *self.state, self.w.hparams(), self.t,
+                                                self.clip, self.norm_out, stream=stream)
+            elif self.writeback:
+                fsp.sharded_step_writeback_params(self.plan, self.table, *self.state, self.w.hparams(), self.t,
+                                                  stream=stream)
             else:
                 fsp.sharded_step_params(self.plan, self.table, *self.state, self.w.hparams(), self.t, stream=stream)
         elif self.unshard:
@@ -695,8 +712,10 @@ def run_fsp(args):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
-    if args.per_param and (w.mode == "distopt" or args.clip is not None or args.no_gather or args.writeback):
-        raise SystemExit("--per-param: FSDP2 / HSDP workloads, the plain step or --unshard")
+    if args.per_param and (w.mode == "distopt" or args.no_gather):
+        raise SystemExit("--per-param: FSDP2 / HSDP workloads; the plain step, --clip, --writeback or --unshard")
+    if args.clip is not None and w.grad_dtype != "f32":
+        raise SystemExit("--clip: fp32 gradients")
     if args.writeback and (w.grad_dtype != "f32" or w.n_rep != 1):
         raise SystemExit("--writeback: fp32 gradients, FSDP2 or DistOpt")
     if args.fp32_gather and (args.per_param or args.clip is not None or args.no_gather or args.writeback):
@@ -792,8 +811,7 @@ def run_fsp(args):
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
                      and not args.no_gather and not args.per_param and not args.writeback and not args.fp32_gather
                      else None,
-                     "kernel": "unshard_kernel" if args.unshard else
-                     "sharded_step_generic_kernel" if args.per_param else "sharded_step_kernel",
+                     "kernel": "unshard_kernel" if args.unshard else step_kernel_name(w),
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,

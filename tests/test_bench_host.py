@@ -161,3 +161,19 @@ def test_traffic_record_matches_the_current_kernel_source():
         algorithmic = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         tpe = bench.traffic_per_elem(name)
         assert tpe is not None and 0.95 < tpe / algorithmic < 1.05, name
+
+
+def test_roofline_kernel_label_follows_the_mesh():
+    for name, n_d, want in (("1", None, "sharded_step_kernel"), ("1", 9, "sharded_step_generic_kernel"),
+                            ("5", None, "sharded_step_kernel"), ("5", 6, "sharded_step_generic_kernel"),
+                            ("4", None, "sharded_step_kernel"), ("1", 24, "sharded_step_generic_kernel")):
+        w, _, _ = bench.resolve_workload(name, None, n_d)
+        assert bench.step_kernel_name(w) == want, (name, n_d)
+
+
+def test_bulk_mesh_set_mirrors_the_library_table():
+    import re
+    src = open(os.path.join(ROOT, "fsdp_sharded_mixed_pass_gb300", "csrc", "fsp_step.cu")).read()
+    decl = re.search(r"using Kernels = KernelTable<GradT,(.*?)>;", src, re.S).group(1)
+    meshes = {(int(a), int(b)) for a, b in re.findall(r"Mesh<(\d+),\s*(\d+)>", decl)}
+    assert meshes == set(bench.BULK_MESHES)
