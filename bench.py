@@ -14,8 +14,8 @@ per param).
 
 Other flows (each reports its own bytes per param): --clip MAX_NORM,
 --writeback, --no-gather, --unshard, --fp32-gather, and --per-param (alone or
-with --clip, --writeback or --unshard); --n-d N and --param-slice a:b change
-the workload, --graph captures the timed steps.
+with any of those); --n-d N and --param-slice a:b change the workload,
+--graph captures the timed steps.
 
 Multi-GPU (torchrun, one rank per GPU): the step does not shard across GPUs
 (the N_d ranks already live on one device), so every GPU runs an independent
@@ -282,7 +282,8 @@ def resolve_workload(name: str, param_slice: str | None, n_d: int | None = None)
 
 
 class DeviceWorkload:
-    def __init__(self, w, shapes, device, per_param: bool = False, fp32_gather: bool = False):
+    def __init__(self, w, shapes, device, per_param: bool = False, fp32_gather: bool = False,
+                 no_gather: bool = False):
         import torch
         import fsdp_sharded_mixed_pass_gb300 as fsp
         from synth_inputs import device as D
@@ -298,8 +299,10 @@ class DeviceWorkload:
             for q, row in enumerate(self.grads):
                 for g in row:
                     D.fill_grad(g, w.data_seed, q, w.grad_dtype)
-            self.params = [[torch.zeros(n, dtype=torch.bfloat16, device=device) for n in sizes]
-                           for _ in range(w.n_d)]
+            pdt = torch.float32 if fp32_gather else torch.bfloat16
+            # ZeRO-3 (no gather): a table of gradients only
+            self.params = None if no_gather else [[torch.zeros(n, dtype=pdt, device=device) for n in sizes]
+                                                  for _ in range(w.n_d)]
             self.table = fsp.ParamTable(p, self.grads, self.params)
         else:
             self.plan = fsp.plan_layout(shapes, w.n_d, w.mode, n_replicate=w.n_rep)
@@ -712,15 +715,18 @@ def run_fsp(args):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     w, shapes, label = resolve_workload(args.workload, args.param_slice, args.n_d)
-    if args.per_param and (w.mode == "distopt" or args.no_gather):
-        raise SystemExit("--per-param: FSDP2 / HSDP workloads; the plain step, --clip, --writeback or --unshard")
+    if args.per_param and w.mode == "distopt":
+        raise SystemExit("--per-param: FSDP2 / HSDP workloads")
     if args.clip is not None and w.grad_dtype != "f32":
         raise SystemExit("--clip: fp32 gradients")
     if args.writeback and (w.grad_dtype != "f32" or w.n_rep != 1):
         raise SystemExit("--writeback: fp32 gradients, FSDP2 or DistOpt")
-    if args.fp32_gather and (args.per_param or args.clip is not None or args.no_gather or args.writeback):
-        raise SystemExit("--fp32-gather: the plain step or --unshard on full-size buffers")
-    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather)
+    if args.fp32_gather and (args.clip is not None or args.no_gather or args.writeback):
+        raise SystemExit("--fp32-gather: the plain step or --unshard")
+    if args.per_param and args.no_gather and (args.clip is not None or args.writeback or args.unshard):
+        raise SystemExit("--per-param --no-gather: the plain step only (the table has no parameter tensors)")
+    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather,
+                        no_gather=args.no_gather and args.per_param)
     wl.clip = args.clip
     wl.unshard = args.unshard
     wl.no_gather = args.no_gather
