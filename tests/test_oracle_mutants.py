@@ -2,17 +2,22 @@
 
 Each case plants one mistake in the oracle - a floor instead of a ceiling, a
 wrong padding unit, a reversed fold, a truncating cast, a gather that misses
-ranks, ... - and requires that at least one of the pins written against the
-pages, closed forms or library routines then fails.  The mistakes are planted
-with monkeypatch, in the oracle only, and undone after each case."""
+ranks, a wrong byte-ledger or collective-volume formula, ... - and requires
+that at least one of the pins written against the pages, closed forms or
+library routines then fails.  The mistakes are planted with monkeypatch, in
+the oracle only, and undone after each case."""
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
 import test_oracle_clip as TC
 import test_oracle_hsdp as TH
+import test_oracle_ledger as TL
 import test_oracle_plan as TP
 import test_oracle_step as TS
 import test_oracle_unshard as TU
+from oracle import ledger as L
 from oracle import plan as P
 from oracle import step as O
 
@@ -123,6 +128,34 @@ def _shard_first_group_only(mp):
     mp.setattr(O, "shard", shard)
 
 
+# ---- ledger mistakes ---------------------------------------------------------
+
+def _zero2_as_fsdp(mp):
+    orig = L.bytes_per_param
+    mp.setattr(L, "bytes_per_param",
+               lambda scheme, n_d, grad_bytes=4: orig("fsdp" if scheme == "zero2" else scheme, n_d, grad_bytes))
+
+
+def _all_reduce_once(mp):
+    orig = L.coll_bytes
+    mp.setattr(L, "coll_bytes", lambda kind, n, size: orig("all_gather" if kind == "all_reduce" else kind, n, size))
+
+
+def _whole_payload(mp):
+    orig = L.coll_bytes
+    mp.setattr(L, "coll_bytes", lambda kind, n, size: Fraction(size) * (2 if kind == "all_reduce" else 1)
+               if n > 1 and kind != "send_recv" else orig(kind, n, size))
+
+
+def _no_gqa(mp):
+    orig = L.dense_param_count
+    mp.setattr(L, "dense_param_count", lambda h, layers, heads, kv_heads, *a, **k: orig(h, layers, heads, heads, *a, **k))
+
+
+def _state_moved_once(mp):
+    mp.setattr(L, "sharded_step_bytes", lambda n_d, grad_bytes, n_rep=1: n_d * grad_bytes + 12 * n_rep + 2 * n_d)
+
+
 MUTANTS = {
     "floor_chunk": (_floor_chunk, [(TP.test_fsdp2_shards_equal_torch_chunk, (4,)),
                                    (TP.test_qwen3_layer_shard_table_matches_walkthrough, ())]),
@@ -142,6 +175,12 @@ MUTANTS = {
     "clip_without_epsilon": (_clip_without_epsilon, [(TC.test_global_norm_and_coefficient_by_hand, ())]),
     "shard_first_group_only": (_shard_first_group_only,
                                [(TU.test_shard_then_unshard_gives_the_cast_of_every_element, ("hsdp", 8, 2))]),
+    "ledger_zero2_as_fsdp": (_zero2_as_fsdp, [(TL.test_bytes_per_param_tables, (8,))]),
+    "all_reduce_counted_once": (_all_reduce_once, [(TL.test_all_reduce_is_reduce_scatter_plus_all_gather_in_volume, ())]),
+    "collectives_send_the_whole_payload": (_whole_payload, [(TL.test_qwen3_layer_comm_volume, ())]),
+    "param_count_without_gqa": (_no_gqa, [(TL.test_workload_param_counts_follow_the_formula, ()),
+                                          (TL.test_7b_parameter_count_and_ledger, ())]),
+    "state_moved_once": (_state_moved_once, [(TL.test_algorithmic_bytes_per_element, (1, 72))]),
 }
 
 
