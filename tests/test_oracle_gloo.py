@@ -8,7 +8,8 @@ each parameter's torch.chunk pieces (padded to the first piece's rows), one
 reduce_scatter_tensor, AdamW on the rank's own shard, the bf16 cast, one
 all_gather_into_tensor and the copy-out; HSDP as 2 replica groups of 2
 (reduce-scatter in the shard group, all-reduce across the replica group,
-gather in the shard group); and DistOpt's flat equal shards - and every
+gather in the shard group); DistOpt's flat equal shards; and the clipped
+flow (write-back, the norm from an all-reduce of sums of squares) - and every
 rank's results must equal the single-process oracle bit for bit.
 The gradients are multiples of 2^-12 small enough that every sum is exact in
 any order, so the collectives' own reduction order cannot matter.  This pins
@@ -33,6 +34,7 @@ HP = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
 WORLD = 4
 SHAPES = [(7, 5), (13,), (3, 64), (1,), (9, 3), (2, 2, 3)]
 SEED, T = 77, 10
+CLIP = 1e-3   # below the gradients' norm, so the coefficient is < 1
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -71,10 +73,13 @@ def _toy(rank, world):
     return {"shard": shard.tolist(), "gathered": full.tolist()}
 
 
-def _fsdp2(rank, world, n_rep=1):
+def _fsdp2(rank, world, n_rep=1, max_norm=None):
     """FSDP2 (n_rep = 1) or HSDP over n_rep replica groups of world // n_rep
     ranks: reduce-scatter inside the rank's shard group, all-reduce of the
-    shard across the replica group, all-gather inside the shard group."""
+    shard across the replica group, all-gather inside the shard group.  With
+    max_norm: the averaged shard written back into the rank's own gradient
+    buffer, the global norm from an all-reduce (SUM) of the first group's
+    fp64 sums of squares, and AdamW on the clipped gradient."""
     n_s = world // n_rep
     groups = [dist.new_group(list(range(r * n_s, (r + 1) * n_s))) for r in range(n_rep)] if n_rep > 1 else [None]
     across = [dist.new_group(list(range(s, world, n_s))) for s in range(n_s)] if n_rep > 1 else None
@@ -107,8 +112,25 @@ def _fsdp2(rank, world, n_rep=1):
     if across is not None:
         dist.all_reduce(recv, group=across[me])
     G = (recv / float(world)).numpy()
-    # AdamW on this rank's own segments, state slots from the oracle's plan
     seg = {(s.param, s.rank): s for s in plan.segments}
+    coef = np.float32(1.0)
+    wrote = grad.numpy().copy()
+    if max_norm is not None:
+        o, sq = 0, 0.0
+        for i, (padded, sizes) in enumerate(geometry):
+            k = sizes[me]
+            if k:
+                s = seg[(i, rank)]
+                wrote[s.full_off:s.full_off + k] = G[o:o + k]       # the owner's slice of its own buffer
+                if rank < n_s:                                       # each element once: the first group's
+                    sq += float(np.dot(G[o:o + k].astype(np.float64), G[o:o + k].astype(np.float64)))
+            o += padded
+        total = torch.tensor([sq], dtype=torch.float64)
+        dist.all_reduce(total)
+        norm = float(np.sqrt(total.item()))
+        coef = OS.clip_coefficient(norm, max_norm)
+        G = (G * coef).astype(np.float32)
+    # AdamW on this rank's own segments, state slots from the oracle's plan
     master = np.zeros(plan.state_len_total, np.float32)
     mom = np.zeros_like(master)
     var = np.zeros_like(master)
@@ -135,7 +157,10 @@ def _fsdp2(rank, world, n_rep=1):
         for i, (padded, sizes) in enumerate(geometry):
             params[offs[i] + sum(sizes[:r]):offs[i] + sum(sizes[:r]) + sizes[r]] = gathered[o:o + sizes[r]]
             o += padded
-    return {"master": master, "m": mom, "v": var, "params": params, "checks": checks}
+    out = {"master": master, "m": mom, "v": var, "params": params, "checks": checks}
+    if max_norm is not None:
+        out.update(norm=norm, coef=float(coef), grad=wrote)
+    return out
 
 
 def _distopt(rank, world):
@@ -157,7 +182,9 @@ def _rank_main(rank, world, port, out_dir, case):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         res = {"toy": _toy, "fsdp2": _fsdp2, "distopt": _distopt,
-               "hsdp": lambda r, w: _fsdp2(r, w, n_rep=2)}[case](rank, world)
+               "hsdp": lambda r, w: _fsdp2(r, w, n_rep=2),
+               "fsdp2_clip": lambda r, w: _fsdp2(r, w, max_norm=CLIP),
+               "hsdp_clip": lambda r, w: _fsdp2(r, w, n_rep=2, max_norm=CLIP)}[case](rank, world)
     finally:
         dist.destroy_process_group()
     np.save(os.path.join(out_dir, f"r{rank}.npy"), np.array([res], dtype=object), allow_pickle=True)
@@ -226,3 +253,36 @@ def test_distopt_with_real_collectives_equals_the_oracle(tmp_path):
             got = out[name][valid].view(np.uint32)
             assert np.array_equal(got, state[i][lo:lo + got.size].view(np.uint32)), name
         assert np.array_equal(out["params"][:P], params[r][:P])
+
+
+@pytest.mark.parametrize("mode,n_rep", [("fsdp2", 1), ("hsdp", 2)])
+def test_clipped_flow_with_real_collectives_equals_the_oracle(tmp_path, mode, n_rep):
+    """The distributed-optimizer flow with clipping: each rank writes the
+    averaged shard back into its own buffer, the norm comes from an all-reduce
+    of the first group's sums of squares (exact here: the squares of multiples
+    of 2^-12 and their sums are exact in fp64), and every rank's results equal
+    the single-process oracle bit for bit."""
+    res = _run(mode + "_clip", tmp_path)
+    plan = OP.plan_layout(SHAPES, WORLD, mode, n_rep=n_rep)
+    n = plan.full_len_padded
+    grads = [_exact_grad(q, n) for q in range(WORLD)]
+    fi, si = OP.owned_indices(plan)
+    th, m, v = _state_by_index(n)
+    state = []
+    for a in (th, m, v):
+        s = np.zeros(plan.state_len_total, np.float32)
+        s[si] = a[fi]
+        state.append(s)
+    params = [np.zeros(n, np.uint16) for _ in range(WORLD)]
+    norm, coef = OS.sharded_step_clipped(plan, grads, *state, params, HP, T, CLIP)
+    assert coef < 1
+    for r, out in enumerate(res):
+        assert out["norm"] == norm and out["coef"] == float(coef)
+        assert np.array_equal(out["grad"].view(np.uint32), grads[r].view(np.uint32))
+        for sg in plan.segments:
+            if sg.rank != r or not sg.length:
+                continue
+            sl = slice(sg.state_off, sg.state_off + sg.length)
+            for name, k in (("master", 0), ("m", 1), ("v", 2)):
+                assert np.array_equal(out[name][sl].view(np.uint32), state[k][sl].view(np.uint32)), (name, sg)
+        assert np.array_equal(out["params"], params[r])
