@@ -7,8 +7,8 @@
   optimizer (ZeRO-1) shards only the 12 B; ZeRO-2 also shards the grad; ZeRO-3 /
   FSDP shards everything.
 * Per-rank send volume of a collective on n ranks with payload S bytes
-  ("Parallelism strategies: which state to shard", the ``coll_bytes`` listing in
-  its ledger appendix; section 一.1): all-reduce 2(n-1)/n S; all-gather,
+  ("Parallelism strategies: which state to shard", section 一.1 and the volume
+  formulas of its ledger appendix): all-reduce 2(n-1)/n S; all-gather,
   reduce-scatter and all-to-all (n-1)/n S; send/recv S; nothing when n <= 1.
 * Dense GQA/SwiGLU/RMSNorm parameter count with a tied embedding ("07 · 显存模型",
   section 2.2 "参数量估算"):
@@ -69,18 +69,27 @@ def resident_breakdown_distopt(p_shard: int, dp: int, grad_bytes: int = 4) -> di
     }
 
 
+# Ring collectives move the payload in phases.  In one phase the payload is
+# cut into n equal pieces and every rank sends n - 1 of them, so a rank sends
+# (n - 1)/n of the payload per phase.  Reduce-scatter, all-gather and
+# all-to-all take one phase; all-reduce is a reduce-scatter and then an
+# all-gather ("Parallelism strategies: which state to shard", section 一.1),
+# so it takes two.
+RING_PHASES = {"reduce_scatter": 1, "all_gather": 1, "all_to_all": 1, "all_reduce": 2}
+# A point-to-point transfer sends the whole payload once, whatever n is.
+POINT_TO_POINT = ("send_recv",)
+
+
 def coll_bytes(kind: str, n: int, size: float) -> Fraction:
-    """Bytes one rank sends in a collective over ``n`` ranks with payload ``size``."""
-    s = Fraction(size)
-    if n <= 1 and kind != "send_recv":
-        return Fraction(0)
-    if kind == "all_reduce":
-        return 2 * Fraction(n - 1, n) * s
-    if kind in ("all_gather", "reduce_scatter", "all_to_all"):
-        return Fraction(n - 1, n) * s
-    if kind == "send_recv":
-        return s
-    raise ValueError(kind)
+    """Bytes one rank sends in collective ``kind`` over ``n`` ranks with
+    payload ``size`` bytes (a group of one rank sends nothing)."""
+    payload = Fraction(size)
+    if kind in POINT_TO_POINT:
+        return payload
+    if kind not in RING_PHASES:
+        raise ValueError(f"unknown collective {kind!r}")
+    ranks = max(n, 1)
+    return RING_PHASES[kind] * Fraction(ranks - 1, ranks) * payload
 
 
 def dense_param_count(h: int, layers: int, heads: int, kv_heads: int, head_dim: int, ffn: int,
