@@ -30,7 +30,7 @@ def nvcc() -> str:
 def compile_shared(sources, out, includes, extra=()) -> None:
     """Compile ``sources`` in parallel to objects next to ``out``, then link it."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
-    base = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+    base = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off",
             "-Xptxas", "-v", *[f"-I{i}" for i in includes], *extra]
     procs, objs = [], []
     for src in sources:

@@ -9,13 +9,16 @@
 
 namespace fsp {
 
-// Scalars of one AdamW update, from the fp32 hyper-parameters and t in double.
+// Scalars of one AdamW update.  The kernel evaluates the update with float
+// pairs (hi + lo), so every scalar that is not an fp32 number of its own
+// (1 - beta, 1 - lr wd and the two bias-correction factors) is carried as the
+// pair hi = fl(x), lo = fl(x - hi) of its double value.
 struct Coeffs {
-  float beta1, one_minus_beta1;
-  float beta2, one_minus_beta2;
-  float decay;          // 1 - lr * weight_decay
-  float step_size;      // lr / (1 - beta1^t)
-  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+  float beta1, one_minus_beta1_hi, one_minus_beta1_lo;
+  float beta2, one_minus_beta2_hi, one_minus_beta2_lo;
+  float decay_hi, decay_lo;   // 1 - lr * weight_decay
+  float step_hi, step_lo;     // lr / (1 - beta1^t)
+  float isb_hi, isb_lo;       // 1 / sqrt(1 - beta2^t)
   float eps;
 };
 

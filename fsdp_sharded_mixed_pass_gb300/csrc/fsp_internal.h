@@ -48,6 +48,7 @@ static_assert(sizeof(Tile) == 32, "tile descriptor layout");
 }  // namespace fsp
 
 struct fsp_plan {
+  uint64_t uid = 0;       // unique among the process's plans (never reused)
   int32_t n_d = 0;
   int32_t n_rep = 1;      // HSDP replica groups; 1 for FSDP2 and DistOpt
   int32_t n_shard = 0;    // ranks per shard group (= n_d when n_rep == 1)

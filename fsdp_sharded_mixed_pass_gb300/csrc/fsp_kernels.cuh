@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "fsp_args.h"
@@ -71,9 +72,67 @@ static __device__ unsigned int g_fsp_device_error = 0;
 
 constexpr unsigned kErrStepIndex = 8u;   // *step_dev < 1 (treated as 1)
 
+// ---- the t-dependent AdamW scalars, identically on host and device -----------------
+
+// IEEE double operations that no compiler contraction can fuse (the host code
+// is built with -ffp-contract=off), so host and device get the same bits.
+__host__ __device__ __forceinline__ double dmul(double a, double b) {
+#ifdef __CUDA_ARCH__
+  return __dmul_rn(a, b);
+#else
+  return a * b;
+#endif
+}
+__host__ __device__ __forceinline__ double dsub(double a, double b) {
+#ifdef __CUDA_ARCH__
+  return __dsub_rn(a, b);
+#else
+  return a - b;
+#endif
+}
+__host__ __device__ __forceinline__ double ddiv(double a, double b) {
+#ifdef __CUDA_ARCH__
+  return __ddiv_rn(a, b);
+#else
+  return a / b;
+#endif
+}
+__host__ __device__ __forceinline__ double dsqrt(double a) {
+#ifdef __CUDA_ARCH__
+  return __dsqrt_rn(a);
+#else
+  return std::sqrt(a);
+#endif
+}
+
+// hi = fl(x), lo = fl(x - hi): a double as a float pair.
+__host__ __device__ __forceinline__ void split_pair(double x, float& hi, float& lo) {
+  hi = float(x);
+  lo = float(dsub(x, double(hi)));
+}
+
+// b^t for t >= 1 by binary powering (square-and-multiply).
+__host__ __device__ __forceinline__ double pow_int(double b, int64_t t) {
+  double r = 1.0, p = b;
+  for (uint64_t k = uint64_t(t); k != 0; k >>= 1) {
+    if (k & 1u) r = dmul(r, p);
+    p = dmul(p, p);
+  }
+  return r;
+}
+
+// Bias-correction scalars of update t: lr / (1 - beta1^t) and
+// 1 / sqrt(1 - beta2^t), in double, as float pairs.
+__host__ __device__ __forceinline__ void bias_scalars(Coeffs& c, float lr, int64_t t) {
+  const double bc1 = dsub(1.0, pow_int(double(c.beta1), t));
+  const double bc2 = dsub(1.0, pow_int(double(c.beta2), t));
+  split_pair(ddiv(double(lr), bc1), c.step_hi, c.step_lo);
+  split_pair(ddiv(1.0, dsqrt(bc2)), c.isb_hi, c.isb_lo);
+}
+
 // The AdamW scalars of this launch: from the host (c) or, when the update
 // index lives in device memory, with the bias corrections of t = *step_dev
-// computed here in double exactly as the host computes them.
+// computed here exactly as the host computes them.
 __device__ __forceinline__ Coeffs coeffs_of(const StepArgs& a) {
   if (!a.step_dev) return a.c;
   int64_t t = *a.step_dev;
@@ -82,10 +141,7 @@ __device__ __forceinline__ Coeffs coeffs_of(const StepArgs& a) {
     t = 1;
   }
   Coeffs c = a.c;
-  const double bc1 = 1.0 - pow(double(a.c.beta1), double(t));
-  const double bc2 = 1.0 - pow(double(a.c.beta2), double(t));
-  c.step_size = float(double(a.lr) / bc1);
-  c.inv_sqrt_bc2 = float(1.0 / sqrt(bc2));
+  bias_scalars(c, a.lr, t);
   return c;
 }
 
@@ -123,12 +179,131 @@ struct BulkCfg {
 
 // ---- element math -------------------------------------------------------------
 
-// AdamW on one element: updates m, v, theta in place (fp32).
+// Float pairs: a value carried as hi + lo, |lo| <= ulp(hi) / 2 - about 48
+// significant bits.  two_sum is Knuth's error-free sum (TAOCP vol. 2, 4.2.2),
+// fast_two_sum Dekker's (|a| >= |b|, "A floating-point technique for extending
+// the available precision", Numer. Math. 18, 1971), two_prod the exact product
+// with an FMA.  Every step is an explicitly rounded intrinsic, so no compiler
+// contraction changes them.
+struct F2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ F2 fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ F2 two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+
+// (a.hi + a.lo) + (b.hi + b.lo), renormalised.
+__device__ __forceinline__ F2 add_pairs(F2 a, F2 b) {
+  const F2 s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+// Approximate square root and reciprocal (one special-function-unit
+// instruction each; about 2^-22 relative error).
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// AdamW on one element with its intermediate values carried as float pairs
+// (about 2^-44 of the terms' size), each result rounded once to fp32:
+//   m' = b1 m + (1 - b1) G,   v' = b2 v + (1 - b2) G^2,
+//   theta' = theta (1 - lr wd) - u,  u = lr / (1 - b1^t) * m' / (sqrt(v') / sqrt(1 - b2^t) + eps).
+// The square root and the quotient are corrected once each from their fp32
+// values: sqrt(h + l) ~ s + (h - s^2 + l) / (2 s) and n / d ~ q + (n - q d) / d,
+// with the residuals taken with FMAs.  Taken only where theta' cancels.
+__device__ __forceinline__ void adamw_pairs(float g, float& theta, float& m, float& v, const Coeffs& c) {
+  // m' = b1 m + (1 - b1) G
+  F2 gm = two_prod(c.one_minus_beta1_hi, g);
+  gm.lo = __fmaf_rn(c.one_minus_beta1_lo, g, gm.lo);
+  const F2 mp = add_pairs(two_prod(c.beta1, m), gm);
+  // v' = b2 v + (1 - b2) G^2
+  const F2 gg = two_prod(g, g);
+  F2 gv = two_prod(c.one_minus_beta2_hi, gg.hi);
+  gv.lo = __fmaf_rn(c.one_minus_beta2_hi, gg.lo, gv.lo);
+  gv.lo = __fmaf_rn(c.one_minus_beta2_lo, gg.hi, gv.lo);
+  const F2 vp = add_pairs(two_prod(c.beta2, v), gv);
+  // sqrt(v')
+  const float sh = __fsqrt_rn(vp.hi);
+  const float sl = vp.hi > 0.f
+                       ? __fmul_rn(__fadd_rn(__fmaf_rn(-sh, sh, vp.hi), vp.lo), __fmul_rn(0.5f, __frcp_rn(sh)))
+                       : 0.f;
+  // denominator sqrt(v') / sqrt(1 - b2^t) + eps
+  F2 d = two_prod(sh, c.isb_hi);
+  d.lo = __fmaf_rn(sh, c.isb_lo, d.lo);
+  d.lo = __fmaf_rn(sl, c.isb_hi, d.lo);
+  const F2 de = two_sum(d.hi, c.eps);
+  d = fast_two_sum(de.hi, __fadd_rn(de.lo, d.lo));
+  // quotient m' / denominator
+  const float rc = __frcp_rn(d.hi);
+  const float qh = __fmul_rn(mp.hi, rc);
+  float rem = __fmaf_rn(-qh, d.hi, mp.hi);
+  rem = __fadd_rn(rem, mp.lo);
+  rem = __fmaf_rn(-qh, d.lo, rem);
+  const float ql = __fmul_rn(rem, rc);
+  // u = lr / (1 - b1^t) * quotient
+  F2 u = two_prod(qh, c.step_hi);
+  u.lo = __fmaf_rn(qh, c.step_lo, u.lo);
+  u.lo = __fmaf_rn(ql, c.step_hi, u.lo);
+  // theta' = theta (1 - lr wd) - u
+  F2 td = two_prod(theta, c.decay_hi);
+  td.lo = __fmaf_rn(theta, c.decay_lo, td.lo);
+  const F2 r = two_sum(td.hi, -u.hi);
+  theta = __fadd_rn(r.hi, __fadd_rn(r.lo, __fsub_rn(td.lo, u.lo)));
+  m = mp.hi;
+  v = vp.hi;
+}
+
+// theta' is taken from the fp32 evaluation when it is at least this fraction
+// of the size of its terms.
+constexpr float kRefineBelow = 0x1p-10f;
+
+// AdamW on one element, in place (decoupled weight decay on the old theta,
+// bias-corrected moments, eps outside the square root).  First in fp32: there
+// theta' = theta (1 - lr wd) - u is off by a few fp32 ulps of its terms'
+// size, |theta (1 - lr wd)| and |u|'s terms lr / (1 - b1^t) (|b1 m| +
+// |(1 - b1) G|) / denominator.  Where theta' is at least 2^-10 of that size
+// (all but a few elements in a million on the synthetic workloads), that is
+// well under one bf16 ulp of theta'; where it cancels further, a fraction of
+// an fp32 ulp of theta can be many bf16 ulps of the tiny result, and the
+// element is evaluated again with float pairs (adamw_pairs), whose cast then
+// stays within one bf16 ulp of the exact value's.  Every step is an explicitly
+// rounded intrinsic, so every kernel and call site gets the same bits.
 __device__ __forceinline__ void adamw(float g, float& theta, float& m, float& v, const Coeffs& c) {
-  m = fmaf(c.beta1, m, c.one_minus_beta1 * g);
-  v = fmaf(c.beta2, v, c.one_minus_beta2 * (g * g));
-  const float denom = fmaf(sqrtf(v), c.inv_sqrt_bc2, c.eps);
-  theta = fmaf(theta, c.decay, -(c.step_size * (m / denom)));
+  const float m1 = __fmaf_rn(c.beta1, m, __fmul_rn(c.one_minus_beta1_hi, g));
+  const float v1 = __fmaf_rn(c.beta2, v, __fmul_rn(c.one_minus_beta2_hi, __fmul_rn(g, g)));
+  const float r = rcp_approx(__fmaf_rn(sqrt_approx(v1), c.isb_hi, c.eps));
+  const float u = __fmul_rn(c.step_hi, __fmul_rn(m1, r));
+  const float td = __fmul_rn(theta, c.decay_hi);
+  const float t1 = __fsub_rn(td, u);
+  const float u_terms =
+      __fmul_rn(c.step_hi, __fmul_rn(__fadd_rn(fabsf(__fmul_rn(c.beta1, m)), fabsf(__fmul_rn(c.one_minus_beta1_hi, g))), r));
+  if (fabsf(t1) >= __fmul_rn(kRefineBelow, fmaxf(fabsf(td), u_terms))) {
+    theta = t1;
+    m = m1;
+    v = v1;
+    return;
+  }
+  adamw_pairs(g, theta, m, v, c);   // cancellation (or a NaN): the float-pair evaluation
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
@@ -504,40 +679,47 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     uint32_t phase = 0;
     uint32_t used = 0;   // stages that ever received a header (bit s)
     bool ok = true;
-    // the next tile, its descriptor and (per-parameter tensors) its rank
-    // bases are fetched one tile ahead
+    // Look-ahead, so that no load's latency stalls the producer at a tile's
+    // start: tiles are claimed two ahead and their descriptors loaded one
+    // ahead, and (per-parameter tensors) a tile's rank bases are requested
+    // from its descriptor one tile ahead.  At the start of tile T, T + 1's
+    // descriptor and T + 2's index were requested a tile earlier.
     int64_t k = 0;
-    int64_t t_next = next_tile(a, k++);
-    Tile d_next = t_next < a.n_tiles ? a.tiles[t_next] : Tile{0, 0, 0, 0};
-    const void* gb_next[N] = {};
-    uint16_t* pb_next[N] = {};
-    const void** gb = reinterpret_cast<const void**>(smem + Cfg::kTileBaseOff);   // the current tile's
-    uint16_t** pb = reinterpret_cast<uint16_t**>(smem + Cfg::kTileBaseOff + 8 * N);
+    int64_t t_cur = next_tile(a, k++);
+    Tile d_cur = t_cur < a.n_tiles ? a.tiles[t_cur] : Tile{};
+    int64_t t_n1 = t_cur < a.n_tiles ? next_tile(a, k++) : a.n_tiles;
+    Tile d_n1 = t_n1 < a.n_tiles ? a.tiles[t_n1] : Tile{};
+    int64_t t_n2 = t_n1 < a.n_tiles ? next_tile(a, k++) : a.n_tiles;
+    const void* gb[N] = {};      // the current tile's grad bases (registers)
+    const void* gb_n1[N] = {};   // T + 1's, requested one tile ahead
+    uint16_t* pb_n1[N] = {};
+    uint16_t** pb = reinterpret_cast<uint16_t**>(smem + Cfg::kTileBaseOff + 8 * N);   // the current tile's
     auto fetch_bases = [&](const Tile& d) {
 #pragma unroll
       for (int q = 0; q < N; ++q) {
         const int64_t e = int64_t(d.param) * a.n_d + q;
-        gb_next[q] = a.vgrads[e];
-        pb_next[q] = a.vparams ? a.vparams[e] : nullptr;
+        gb_n1[q] = a.vgrads[e];
+        pb_n1[q] = a.vparams ? a.vparams[e] : nullptr;
       }
     };
-    if (per_param && t_next < a.n_tiles) fetch_bases(d_next);
-    for (;;) {
-      const int64_t t = t_next;
-      const Tile tile = d_next;
-      const bool done = t >= a.n_tiles;
-      if (per_param) {
+    if (per_param && t_cur < a.n_tiles) {
+      fetch_bases(d_cur);
 #pragma unroll
-        for (int q = 0; q < N; ++q) {
-          gb[q] = gb_next[q];
-          pb[q] = pb_next[q];
-        }
+      for (int q = 0; q < N; ++q) {
+        gb[q] = gb_n1[q];
+        pb[q] = pb_n1[q];
       }
+    }
+    for (;;) {
+      const Tile tile = d_cur;
+      const bool done = t_cur >= a.n_tiles;
+      Tile d_n2{};
+      int64_t t_n3 = a.n_tiles;
       if (!done) {
-        t_next = next_tile(a, k++);
-        if (t_next < a.n_tiles) {
-          d_next = a.tiles[t_next];
-          if (per_param) fetch_bases(d_next);
+        if (per_param && t_n1 < a.n_tiles) fetch_bases(d_n1);   // T + 1's descriptor landed a tile ago
+        if (t_n2 < a.n_tiles) {
+          d_n2 = a.tiles[t_n2];                                   // T + 2's index was claimed a tile ago
+          t_n3 = next_tile(a, k++);
         }
       }
       const Body body = done ? Body{0, 0} : tile_body(tile);
@@ -573,7 +755,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
           mbar_arrive_expect_tx(bar, uint32_t(len) * uint32_t(NG * G + NR * 12));
           // (separate paths, so that full-size buffers read their bases straight from the arguments)
           if (kClip) {   // the reduced gradient, from its owner's slice
-            const void* own = per_param ? gb[tile.rank] : a.grads[tile.rank];
+            const void* own = per_param ? stage_gb(stage)[tile.rank] : a.grads[tile.rank];
             bulk_load(smem_addr(st + Cfg::kGradOff), static_cast<const unsigned char*>(own) + c * G, len * G, bar);
           } else if (per_param) {
 #pragma unroll
@@ -607,6 +789,19 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         c += E;
       } while (!done && c < body.b1);
       if (!ok || done) break;
+      // T + 1 becomes the current tile
+      t_cur = t_n1;
+      d_cur = d_n1;
+      if (per_param) {
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          gb[q] = gb_n1[q];
+          pb[q] = pb_n1[q];
+        }
+      }
+      t_n1 = t_n2;
+      d_n1 = d_n2;
+      t_n2 = t_n3;
     }
     if (!ok) {
       // Let every issued copy land before this CTA can retire: the most recent

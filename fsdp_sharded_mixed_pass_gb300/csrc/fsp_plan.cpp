@@ -9,6 +9,7 @@
 #include <cuda_runtime_api.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <limits>
 #include <new>
@@ -189,6 +190,8 @@ fsp_status make_plan(const int64_t* dims, const int32_t* ndims, int32_t n_params
   if (st != FSP_OK) return st;
   fsp_plan* p = new (std::nothrow) fsp_plan();
   if (!p) return fail(FSP_ENOMEM, "fsp_plan_layout: host allocation failed");
+  static std::atomic<uint64_t> next_uid{1};
+  p->uid = next_uid.fetch_add(1);
   try {
     p->n_d = n_rep * n_shard;
     p->n_rep = n_rep;

@@ -178,18 +178,17 @@ fsp_status grid_for(const KernelInfo& k, int* grid) {
   return FSP_OK;
 }
 
-// Fills the AdamW scalars of update t (bias corrections in double).
+// Fills the AdamW scalars of update t (in double, as float pairs; the
+// bias corrections through bias_scalars, as the kernels compute them when t
+// is in device memory).
 void set_coeffs(StepArgs& a, const fsp_adamw_hparams* hp, int64_t step) {
   const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  const double bc1 = 1.0 - std::pow(b1, double(step));
-  const double bc2 = 1.0 - std::pow(b2, double(step));
   a.c.beta1 = hp->beta1;
-  a.c.one_minus_beta1 = float(1.0 - b1);
+  split_pair(dsub(1.0, b1), a.c.one_minus_beta1_hi, a.c.one_minus_beta1_lo);
   a.c.beta2 = hp->beta2;
-  a.c.one_minus_beta2 = float(1.0 - b2);
-  a.c.decay = float(1.0 - lr * wd);
-  a.c.step_size = float(lr / bc1);
-  a.c.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+  split_pair(dsub(1.0, b2), a.c.one_minus_beta2_hi, a.c.one_minus_beta2_lo);
+  split_pair(dsub(1.0, dmul(lr, wd)), a.c.decay_hi, a.c.decay_lo);
+  bias_scalars(a.c, hp->lr, step);
   a.c.eps = hp->eps;
   a.lr = hp->lr;
 }
@@ -575,9 +574,10 @@ extern "C" fsp_status fsp_sharded_step_debug(const fsp_plan* plan, const void* c
 // allocates one tile table per plan and device on its first call; this entry
 // point instead keeps the tile list in a fixed array of device memory that
 // the library declares at file scope (kNoAllocMaxTiles tiles, 8 MiB, held on
-// every device that loads the library until the process exits), rewrites it
-// with a stream-ordered copy on every call, and runs the same kernel on it;
-// its tile counter is a second file-scope variable, zeroed on the stream.
+// every device that loads the library until the process exits), copies the
+// plan's list there on the stream when the array does not already hold it,
+// and runs the same kernel on it; its tile counter is a second file-scope
+// variable, zeroed on the stream.
 
 namespace fsp {
 namespace {
@@ -589,34 +589,47 @@ static __device__ __align__(256) Tile g_noalloc_tiles[kNoAllocMaxTiles];
 // The kernel's tile counter for this entry (zeroed on the stream before each launch).
 static __device__ __align__(8) unsigned long long g_noalloc_tile_ctr;
 
-// Device addresses of g_noalloc_tiles and g_noalloc_tile_ctr on each device
-// (the names themselves are host stand-ins in host code), resolved once per
-// device with that device current.
-struct NoAllocAddrs {
+// Per device: the device addresses of g_noalloc_tiles and g_noalloc_tile_ctr
+// (the names themselves are host stand-ins in host code), resolved once with
+// that device current, and the uid of the plan whose tile list the array
+// holds (0: none yet).
+struct NoAllocDevice {
   Tile* tiles = nullptr;
   unsigned long long* ctr = nullptr;
+  uint64_t loaded_uid = 0;
 };
 std::mutex g_noalloc_mu;
-NoAllocAddrs g_noalloc_addr[kNoAllocMaxDevices] = {};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices] = {};
 
-fsp_status noalloc_arrays_on_current_device(NoAllocAddrs* out) {
+// The arrays of the current device; copies plan p's tile list into the tile
+// array on `st` unless the array already holds it (from an earlier call with
+// this plan on this device: calls are ordered by the caller, so that copy has
+// landed before this call's kernel runs).
+fsp_status noalloc_arrays_for(const fsp_plan* p, cudaStream_t st, Tile** tiles, unsigned long long** ctr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
   if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FSP_EUNSUPPORTED, "device ordinal above 63");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  NoAllocAddrs& d = g_noalloc_addr[dev];
+  NoAllocDevice& d = g_noalloc_dev[dev];
   if (!d.tiles) {
-    void* tiles = nullptr;
-    void* ctr = nullptr;
-    e = cudaGetSymbolAddress(&tiles, g_noalloc_tiles);
+    void* tiles_addr = nullptr;
+    void* ctr_addr = nullptr;
+    e = cudaGetSymbolAddress(&tiles_addr, g_noalloc_tiles);
     if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetSymbolAddress(g_noalloc_tiles)", e));
-    e = cudaGetSymbolAddress(&ctr, g_noalloc_tile_ctr);
+    e = cudaGetSymbolAddress(&ctr_addr, g_noalloc_tile_ctr);
     if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetSymbolAddress(g_noalloc_tile_ctr)", e));
-    d.ctr = static_cast<unsigned long long*>(ctr);
-    d.tiles = static_cast<Tile*>(tiles);
+    d.ctr = static_cast<unsigned long long*>(ctr_addr);
+    d.tiles = static_cast<Tile*>(tiles_addr);
   }
-  *out = d;
+  if (d.loaded_uid != p->uid) {
+    d.loaded_uid = 0;   // a failed copy leaves the array's contents unknown
+    e = cudaMemcpyAsync(d.tiles, p->tiles.data(), p->tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemcpyAsync (tile list)", e));
+    d.loaded_uid = p->uid;
+  }
+  *tiles = d.tiles;
+  *ctr = d.ctr;
   return FSP_OK;
 }
 
@@ -624,73 +637,34 @@ fsp_status run_step_noalloc(const fsp_plan* p, const void* const* grads, int32_t
                             float* v, void* const* params, const fsp_adamw_hparams* hp, int64_t step,
                             void* stream) {
   clear_error();
-  if (!p) return fail(FSP_EINVAL, "plan is NULL");
-  if (!grads || !params) return fail(FSP_EINVAL, "grad_bufs or param_bufs is NULL");
-  if (dtype != FSP_DTYPE_F32 && dtype != FSP_DTYPE_BF16) return fail(FSP_EINVAL, "unknown grad dtype");
-  if (fsp_status hs = check_hparams(hp, step); hs != FSP_OK) return hs;
-  if (int64_t(p->tiles.size()) > kNoAllocMaxTiles)
+  if (p && int64_t(p->tiles.size()) > kNoAllocMaxTiles)
     return fail(FSP_EUNSUPPORTED, "plan needs " + std::to_string(p->tiles.size()) +
                                       " work tiles; fsp_sharded_step_noalloc holds at most 262144");
+  // the checks of fsp_sharded_step (host memory only)
+  fsp_status s = check_device_step(p, grads, dtype, master, m, v, params, hp, step, {});
+  if (s != FSP_OK || p->tiles.empty()) return s;
 
-  // The same buffer checks as fsp_sharded_step, on fixed storage.
-  const int n = p->n_d;
-  const size_t gsize = dtype == FSP_DTYPE_F32 ? 4 : 2;
-  const size_t fbytes = size_t(p->full_len_padded), sbytes = size_t(p->state_len_total) * 4;
-  const void* ptrs[2 * kMaxRanks + 3];
-  size_t sizes[2 * kMaxRanks + 3];
-  int nb = 0;
-  for (int q = 0; q < n; ++q) {
-    ptrs[nb] = grads[q];
-    sizes[nb++] = fbytes * gsize;
-    ptrs[nb] = params[q];
-    sizes[nb++] = fbytes * 2;
-  }
-  ptrs[nb] = master;
-  sizes[nb++] = sbytes;
-  ptrs[nb] = m;
-  sizes[nb++] = sbytes;
-  ptrs[nb] = v;
-  sizes[nb++] = sbytes;
-  for (int i = 0; i < nb; ++i) {
-    if (!ptrs[i] && sizes[i]) return fail(FSP_EINVAL, "a buffer is NULL");
-    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0) return fail(FSP_EINVAL, "a buffer is not 16-byte aligned");
-  }
-  for (int i = 0; i < nb; ++i) {
-    for (int j = i + 1; j < nb; ++j) {
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(ptrs[i]), b0 = reinterpret_cast<uintptr_t>(ptrs[j]);
-      if (ptrs[i] && ptrs[j] && sizes[i] && sizes[j] && a0 < b0 + sizes[j] && b0 < a0 + sizes[i])
-        return fail(FSP_EINVAL, "two buffers overlap");
-    }
-  }
-  if (p->tiles.empty()) return FSP_OK;
-  for (int i = 0; i < nb; ++i) {
-    fsp_status s = check_allocation(ptrs[i], sizes[i], "a buffer");
-    if (s != FSP_OK) return s;
-  }
-
-  NoAllocAddrs arrays;
-  fsp_status s = noalloc_arrays_on_current_device(&arrays);
-  if (s != FSP_OK) return s;
-  Tile* tiles = arrays.tiles;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(tiles, p->tiles.data(), p->tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaMemcpyAsync (tile list)", e));
+  Tile* tiles = nullptr;
+  unsigned long long* ctr = nullptr;
+  s = noalloc_arrays_for(p, st, &tiles, &ctr);
+  if (s != FSP_OK) return s;
 
   StepArgs a{};
-  for (int q = 0; q < n; ++q) {
+  for (int q = 0; q < p->n_d; ++q) {
     a.grads[q] = grads[q];
-    a.params[q] = static_cast<uint16_t*>(params[q]);
+    a.params[q] = params ? static_cast<uint16_t*>(params[q]) : nullptr;
   }
+  a.gather = params ? 1 : 0;   // NULL param_bufs: the ZeRO-3 step, as fsp_sharded_step
   a.master = master;
   a.m = m;
   a.v = v;
   a.reduced = nullptr;
-  a.gather = 1;
   a.tiles = tiles;
   a.n_tiles = int64_t(p->tiles.size());
   set_mesh(a, p);
   set_coeffs(a, hp, step);
-  return launch(a, dtype, st, false, arrays.ctr);   // the library's counter: nothing to allocate
+  return launch(a, dtype, st, false, ctr);   // the library's counter: nothing to allocate
 }
 
 }  // namespace

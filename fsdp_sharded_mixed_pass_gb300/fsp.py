@@ -424,8 +424,9 @@ def sharded_step_fp32_gather(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq,
 def sharded_step_noalloc(plan: Plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams: dict, step: int,
                          stream=None, grad_dtype: str | None = None) -> None:
     """``sharded_step`` that allocates no device memory (for callers that cannot
-    call cudaMalloc); see ``fsp_sharded_step_noalloc`` in include/fsp.h for its
-    size limit and the rule that overlapping calls race."""
+    call cudaMalloc; ``param_bufs=None``: the ZeRO-3 step); see
+    ``fsp_sharded_step_noalloc`` in include/fsp.h for its size limit and the
+    rule that overlapping calls race."""
     args = _step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hparams, step, grad_dtype)
     _check(lib().fsp_sharded_step_noalloc(*args, ctypes.c_void_p(_stream_handle(stream))), "fsp_sharded_step_noalloc")
 

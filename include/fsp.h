@@ -431,19 +431,23 @@ fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table
  * framework's allocator owns the device, a fixed memory pool must not grow,
  * or the call sits on a path that must never reach cudaMalloc).  The pages
  * have no counterpart: this is a property of the library, not of the step.
- *   Same arguments, results and checks as fsp_sharded_step; it allocates
- *   nothing (the kernel's tile counter is a library variable too, zeroed on
- *   `cuda_stream`).  The plan's work-tile list goes into a fixed array of device
- *   memory declared by the library (262144 tiles, 8 MiB, present on every
- *   device that loads the library until the process exits), copied there on
- *   `cuda_stream` before the kernel on every call.  Plans with more tiles
- *   (roughly more than 1.07e9 elements) return FSP_EUNSUPPORTED.
+ *   Same arguments, results and checks as fsp_sharded_step (param_bufs NULL:
+ *   the ZeRO-3 step, no all-gather); it allocates no device memory (the
+ *   kernel's tile counter is a library variable too, zeroed on `cuda_stream`).
+ *   The plan's work-tile list lives in a fixed array of device memory declared
+ *   by the library (262144 tiles, 8 MiB, present on every device that loads
+ *   the library until the process exits).  A call copies the list there, on
+ *   `cuda_stream`, only when the array does not already hold this plan's list
+ *   on this device (the first call with the plan, or the first after a call
+ *   with another plan); that copy is from pageable host memory, so such a call
+ *   may wait on the host for earlier work on the stream.  Plans with more
+ *   tiles (roughly more than 1.07e9 elements) return FSP_EUNSUPPORTED.
  *   The first call on a device looks up that array's device address (with the
  *   device current); make that first call before any stream capture.
- *   Every call shares the one array: calls that can overlap on the GPU (other
- *   streams, other threads) race and must be ordered by the caller.  Nothing
- *   in the array needs clearing between calls: each call writes the whole
- *   tile list it uses. */
+ *   Every call shares the one array, which keeps the last list copied into it:
+ *   calls that can overlap on the GPU (other streams, other threads) race and
+ *   must be ordered by the caller.  Nothing in the array needs clearing
+ *   between calls: the kernel reads only the tiles of the plan it runs. */
 fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void* const* grad_bufs, int32_t grad_dtype,
                                     float* master, float* exp_avg, float* exp_avg_sq,
                                     void* const* param_bufs, const fsp_adamw_hparams* hp, int64_t step,

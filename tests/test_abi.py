@@ -380,3 +380,19 @@ def test_param_table_wrapper_checks_counts():
         fsp.ParamTable(pp, [one, one[:1]], grad_dtype="f32")              # a missing tensor
     with pytest.raises(ValueError):
         fsp.ParamTable(pp, [one, one], params=[one], grad_dtype="f32", param_dtype="bf16")
+
+
+def test_noalloc_step_checks_like_the_step_on_host():
+    """The no-allocation entry runs fsp_sharded_step's host checks: the same
+    statuses and the same named messages, before any device call."""
+    L = B.lib()
+    plan = fsp.plan_layout([(64, 8)], 4)
+    g, s, p = _fakes(plan)
+    p = [_Fake(p[0].addr + q * 512) for q in range(plan.n_d)]        # param_bufs[0] overlaps param_bufs[1]
+    for fn in (L.fsp_sharded_step, L.fsp_sharded_step_noalloc):
+        args = B._step_args(plan, g, *s, p, HP, 1, "f32")
+        assert fn(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+        assert L.fsp_last_error().decode() == "param_bufs[0] overlaps param_bufs[1]"
+        args = B._step_args(plan, g, *s, p, HP, 0, "f32")
+        assert fn(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
+        assert "step must be >= 1" in L.fsp_last_error().decode()

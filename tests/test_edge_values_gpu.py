@@ -119,7 +119,7 @@ def test_edge_values_match_oracle(n_d, mode, n_rep, grad_dtype):
         dev.step(t)
         ora.step(t)
         torch.cuda.synchronize()
-        compare(dev, ora)      # reduced gradient bit-exact, state within the bars, params within the allowance
+        compare(dev, ora)      # reduced gradient bit-exact, state within the bars, params within 1 bf16 ulp
         # the next step starts both sides from the device's state: where
         # theta' = theta (1 - lr wd) - u cancels (v = 0 makes u ~ lr m / eps),
         # the few ulps by which two fp32-accurate states differ would

@@ -9,7 +9,7 @@ import synth_inputs as S
 from oracle import plan as OP
 from oracle import step as OS
 
-from gpu_cases import HP, ensure_built, param_ulp_allowance, state_errors, ulp_dist, within_tol, SCALED_BOUND
+from gpu_cases import HP, PARAM_ULP_BAR, ensure_built, state_errors, ulp_dist, within_tol, SCALED_BOUND
 
 pytestmark = pytest.mark.gpu
 
@@ -54,10 +54,9 @@ def test_sharded_adamw_matches_oracle(mode, n_d, n_rep):
     for g, w, e in zip(got, want, errs):
         assert within_tol(g, w).all() and (e <= SCALED_BOUND * 2 ** 24).all()
     fi, _ = OP.owned_indices(oplan)
-    allow = param_ulp_allowance(got[0], want[0])
     for q in range(n_d):
         pb = params[q].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert (ulp_dist(pb[fi], o_params[q][fi]) <= allow).all()
+        assert (ulp_dist(pb[fi], o_params[q][fi]) <= PARAM_ULP_BAR).all()
     # unshard of the current master reproduces the step's gathered parameters
     again = [torch.full((n,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16) for _ in range(n_d)]
     opt.unshard(again)
