@@ -49,6 +49,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sharded_step_kernel_dram_traffic_
 # Working sets under this many L2 sizes get an L2 flush before every timed step.
 L2_FLUSH_FACTOR = 4
 L2_BYTES = 129_000_000      # GB300's L2; the device's own figure is used when a GPU is present
+HOLD_CYCLES = 400_000       # ~0.2 ms of GPU spin before each individually timed (L2-flushed) step
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -92,6 +93,10 @@ def parse_args(argv=None):
     ap.add_argument("--per-param", action="store_true",
                     help="every rank's gradient and parameter of every parameter in a tensor of its own "
                          "(FSDP2 / HSDP; the step reads and writes them in place)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the block that times the other workloads after the default one")
+    ap.add_argument("--workload-steps", type=int, default=20,
+                    help="timed steps per workload in the workloads block")
     ap.add_argument("--graph", action="store_true",
                     help="capture the timed steps in one CUDA graph (removes host launch overhead; small cases)")
     return ap.parse_args(argv)
@@ -373,9 +378,10 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
     With ``flush_bytes`` > 0 (working sets that fit in L2) every timed step is
     preceded by an untimed write of ``flush_bytes`` to a scratch buffer and a
     read of it back, so each step starts from a cold L2 that holds no line of
-    its own and no dirty line whose write-back the step would pay for; each
-    step then has its own event pair and the result is the sum of the steps'
-    own durations."""
+    its own and no dirty line whose write-back the step would pay for, and by
+    a short GPU-side spin that keeps the stream busy while the host enqueues
+    the step; each step then has its own event pair and the result is the sum
+    of the steps' own durations."""
     import torch
     stream = torch.cuda.Stream(device=wl.device)
     for _ in range(warmup):
@@ -417,6 +423,9 @@ def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_
             for i in range(steps):
                 flush.fill_(i & 0xFF)
                 flush.view(torch.int32).max()   # read back: only clean lines stay in L2
+                # hold the GPU (no memory traffic) while the host enqueues the step,
+                # so that the host's launch time is not inside the step's events
+                torch.cuda._sleep(HOLD_CYCLES)
                 starts[i].record(stream)
                 if graphs:
                     graphs[i].replay()
@@ -491,15 +500,28 @@ def host_memory_available() -> int:
 # CPU oracle timing
 # --------------------------------------------------------------------------
 
-def _param_runs(shapes, max_elems):
-    """The workload's params (skipping any single param over 32M elements, e.g.
-    an embedding) cut in order into consecutive runs of about ``max_elems``
-    elements each."""
-    runs, cur, total = [], [], 0
+def _sample_pieces(shapes, max_elems):
+    """The workload's params in order; a param over ``max_elems`` elements (an
+    embedding) is cut into blocks of whole rows of at most ``max_elems``
+    elements, each taken as a param of its own - the step treats every element
+    alike, so a block of rows stands for the rows of the whole param."""
     for s in shapes:
         n = math.prod(s)
-        if n > 32_000_000:
+        if n <= max_elems or len(s) < 2:
+            yield tuple(s)
             continue
+        row = n // s[0]
+        per = max(1, max_elems // row)
+        for r0 in range(0, s[0], per):
+            yield (min(per, s[0] - r0),) + tuple(s[1:])
+
+
+def _param_runs(shapes, max_elems):
+    """The workload's params (oversized ones cut into row blocks) grouped in
+    order into consecutive runs of about ``max_elems`` elements each."""
+    runs, cur, total = [], [], 0
+    for s in _sample_pieces(shapes, max_elems):
+        n = math.prod(s)
         if cur and total + n > max_elems:
             runs.append((tuple(cur), total))
             cur, total = [], 0
@@ -511,16 +533,18 @@ def _param_runs(shapes, max_elems):
 
 
 def cpu_sample_shapes(shapes, max_elems=16_000_000):
-    """A contiguous run of the workload's params (skipping any single param over
-    32M elements, e.g. an embedding) of about ``max_elems`` elements."""
+    """A contiguous run of the workload's params of about ``max_elems``
+    elements (the first of ``_param_runs``)."""
     return _param_runs(shapes, max_elems)[0]
 
 
 def cpu_sample_runs(shapes, max_elems, count):
-    """``count`` samples for as many host cores: the consecutive runs of
-    ``_param_runs`` in the workload's order, reused from the start when there
-    are fewer runs than cores."""
+    """``count`` samples for as many host cores: runs of ``_param_runs`` spread
+    evenly over the workload (so the samples together cover its mix of
+    params), reused from the start when there are fewer runs than cores."""
     runs = _param_runs(shapes, max_elems)
+    if len(runs) > count:
+        return [runs[k * len(runs) // count][0] for k in range(count)]
     return [runs[k % len(runs)][0] for k in range(count)]
 
 
@@ -709,6 +733,56 @@ def l2_note(moved: int, flush_bytes: int) -> str:
     return f"inputs larger than L2: every step streams the whole {moved / 1e9:.2f} GB working set"
 
 
+# The workloads the default run also times, after its headline workload (the
+# one-layer case, the DistOpt layout, the ragged N_d = 6 case, the bf16-grad
+# N_d = 16 stack, the HSDP 2 x 4 mesh), one after another, each freed before
+# the next.
+EXTRA_WORKLOADS = ("qwen3_layer", "qwen3_0p6b_distopt", "ragged_500", "dense_1p5b_bf16grad", "qwen3_0p6b_hsdp_2x4")
+
+
+def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms=None) -> dict:
+    """One workload's line of the workloads block."""
+    P = wl.plan.valid_elems
+    per = wl.bytes_per_param()
+    t = ms / 1e3 / steps
+    gbs = per * P / t / 1e9
+    e = {"workload": label, "n_d": wl.w.n_d, "mode": wl.w.mode, "n_replicate": wl.w.n_rep,
+         "grad_dtype": wl.w.grad_dtype, "params": P, "bytes_per_param": per, "steps": steps,
+         "ms_per_step": ms / steps, "params_per_s": P / t, "hbm_gbs": gbs, "frac_of_measured": gbs / peak,
+         "frac_of_nominal_8000": gbs / 8000.0, "kernel": step_kernel_name(wl.w),
+         "l2": l2_note(per * P, flush_bytes),
+         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "error") if k in clocks}}
+    if graph_ms is not None:
+        e["graph_ms_per_step"] = graph_ms / steps
+    return e
+
+
+def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_slice=None) -> list:
+    """Each named workload (optionally params a..b-1 only) built, timed as the
+    headline one is, and freed."""
+    import torch
+    out = []
+    for name in names:
+        w, shapes, label = resolve_workload(name, param_slice, None)
+        try:
+            wl = DeviceWorkload(w, shapes, dev)
+            flush = 2 * l2 if wl.bytes_per_param() * wl.plan.valid_elems <= L2_FLUSH_FACTOR * l2 else 0
+            ms, clocks = time_device(wl, steps, warmup, dist, clocks_id, False, flush)
+            if clocks_bad(clocks):
+                ms, clocks = time_device(wl, steps, warmup, dist, clocks_id, False, flush)
+            graph_ms = None
+            if flush:   # small enough for launch cost to show: also one CUDA graph per step
+                graph_ms, _ = time_device(wl, steps, warmup, dist, clocks_id, True, flush)
+            out.append(workload_entry(wl, label, ms, steps, clocks, flush, peak, graph_ms))
+            wl.plan.close()
+            del wl
+        except Exception as e:   # one workload failing leaves the others' lines
+            out.append({"workload": label, "error": f"{type(e).__name__}: {e}"[:300]})
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_fsp(args):
     import torch
     dist = Dist(args.gpus)
@@ -774,6 +848,19 @@ def run_fsp(args):
                    "api": f"fsp_sharded_step_host (C ABI): {kind} host grads in, {kind} host bf16 params out, "
                           "chunked H2D / kernel / D2H pipeline"}
 
+    default_run = (args.clip is None and not args.unshard and not args.no_gather and not args.per_param
+                   and not args.writeback and not args.fp32_gather and not args.graph and args.param_slice is None
+                   and args.n_d is None)
+    workloads = None
+    if default_run and dist.world == 1 and not args.no_workloads:
+        headline = workload_entry(wl, label, ms, args.steps, clocks, flush_bytes, peak)
+        wl.plan.close()
+        del wl
+        torch.cuda.empty_cache()
+        names = [n for n in EXTRA_WORKLOADS if n != w.name]
+        workloads = [headline] + time_workloads(names, args.workload_steps, max(3, min(args.warmup, 5)), dist,
+                                                clocks_id, dev, l2, peak)
+
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:
         sshapes, _ = cpu_sample_shapes(shapes)
@@ -821,6 +908,7 @@ def run_fsp(args):
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,
         "cpu_baseline": cpu,
+        **({"workloads": workloads} if workloads is not None else {}),
         "gpu_launches": args.steps * (4 if args.clip is not None else 1),
         "launch": "one CUDA graph of the K steps" if args.graph else "one launch per step from the host",
         "clocks": clocks,
@@ -878,10 +966,15 @@ def run_reference(args):
     full_p = sum(math.prod(sh) for sh in shapes)
     plan_like = type("P", (), {"valid_elems": full_p})
     cfg = config_block(w, label, plan_like)
+    # what was timed: per step a bounded sample of the workload's elements; the
+    # step is elementwise, so the full workload's step takes full_p / value
     cfg["sample_params"] = sample_elems
+    cfg["sample_ms_per_step"] = secs * 1e3 / args.steps
+    cfg["ms_per_step_basis"] = (f"the full workload ({full_p} params) at the measured rate of the "
+                                f"{sample_elems}-element sample (elementwise step)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_p / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
         "cpu_baseline": dict({"value": value, "unit": UNIT, "cores": k, "kind": "oracle",

@@ -44,3 +44,24 @@ def test_bench_flow_prints_one_line(flow, capsys):
     assert "l2" in d["config"]
     import fsdp_sharded_mixed_pass_gb300 as fsp
     assert fsp.device_error() == 0
+
+
+def test_workloads_block_times_each_workload():
+    """The default run's block of the other workloads: one entry each, with
+    its own time, bandwidth and roofline fraction (small slices here)."""
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    dist = bench.Dist(1)
+    try:
+        out = bench.time_workloads(["qwen3_layer", "ragged_500", "dense_1p5b_bf16grad"], 3, 3, dist, None, dev,
+                                   l2, 6698.2, param_slice="1:6")
+    finally:
+        dist.close()
+    assert [e["workload"] for e in out] == ["qwen3_layer[1:6]", "ragged_500[1:6]", "dense_1p5b_bf16grad[1:6]"]
+    for e in out:
+        assert "error" not in e, e
+        assert e["ms_per_step"] > 0 and e["params_per_s"] > 0
+        assert abs(e["hbm_gbs"] - e["bytes_per_param"] * e["params"] / (e["ms_per_step"] / 1e3) / 1e9) < 1e-6 * e["hbm_gbs"]
+        assert e["frac_of_measured"] == e["hbm_gbs"] / 6698.2
+    assert out[0]["bytes_per_param"] == 48 and out[2]["bytes_per_param"] == 88
+    assert "graph_ms_per_step" in out[0]          # small enough for an L2 flush: also a CUDA-graph time

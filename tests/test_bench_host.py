@@ -92,10 +92,11 @@ def test_clock_rejection_rule(clocks, bad):
     assert bench.clocks_bad(clocks) == bad
 
 
-def test_cpu_sample_is_whole_params_and_skips_embeddings():
+def test_cpu_sample_cuts_oversized_params_into_row_blocks():
     from synth_inputs import workload
     shapes, n = bench.cpu_sample_shapes(workload(1).shapes)
-    assert shapes[0] == (1024,) and n <= 16_000_000 and len(shapes) == 12
+    # the 151936 x 1024 embedding comes first: blocks of 15625 whole rows (16,000,000 elements)
+    assert shapes == ((15625, 1024),) and n == 16_000_000
 
 
 def test_rank_count_override_and_param_slice():
@@ -116,12 +117,26 @@ def test_param_runs_keep_the_params_in_order():
     shapes = workload(1).shapes
     runs = bench._param_runs(shapes, 4_000_000)
     flat = [s for r, _ in runs for s in r]
-    assert flat == [s for s in shapes if bench.math.prod(s) <= 32_000_000]
+    # every param in order, an oversized one as consecutive blocks of its rows
+    it = iter(flat)
+    for s in shapes:
+        rows = 0
+        while rows < s[0]:
+            piece = next(it)
+            assert piece[1:] == s[1:]
+            rows += piece[0]
+        assert rows == s[0]
+    assert next(it, None) is None
+    assert sum(n for _, n in runs) == workload(1).numel
     for r, n in runs:
         assert n == sum(bench.math.prod(s) for s in r)
         assert n <= 4_000_000 or len(r) == 1
     assert bench.cpu_sample_shapes(shapes, 4_000_000) == runs[0]
+    # fewer runs than cores: reused from the start; more: spread over the workload
     assert bench.cpu_sample_runs(shapes, 4_000_000, len(runs) + 2)[-2:] == [runs[0][0], runs[1][0]]
+    spread = bench.cpu_sample_runs(shapes, 4_000_000, 4)
+    assert spread == [runs[k * len(runs) // 4][0] for k in range(4)]
+    assert spread[0][0] == (3906, 1024) and spread[-1] != spread[0]   # embedding rows and later layers
 
 
 def test_oracle_pool_times_every_process():
