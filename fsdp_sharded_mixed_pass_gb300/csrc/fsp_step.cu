@@ -680,6 +680,22 @@ extern "C" fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void*
   });
 }
 
+extern "C" fsp_status fsp_plan_tiles(const fsp_plan* plan, fsp_tile* out, int64_t cap, int64_t* n) {
+  return fsp::guard([&]() -> fsp_status {
+    using namespace fsp;
+    clear_error();
+    if (!plan || !n) return fail(FSP_EINVAL, "plan or n is NULL");
+    if (cap < 0 || (cap > 0 && !out)) return fail(FSP_EINVAL, "out is NULL or cap < 0");
+    static_assert(sizeof(fsp_tile) == sizeof(Tile), "fsp_tile mirrors the internal tile");
+    const std::vector<Tile>& tiles = plan->tiles;
+    *n = int64_t(tiles.size());
+    const int64_t k = std::min<int64_t>(cap, int64_t(tiles.size()));
+    for (int64_t i = 0; i < k; ++i)
+      out[i] = fsp_tile{tiles[i].full_begin, tiles[i].state_begin, tiles[i].len, tiles[i].rank, tiles[i].param, 0};
+    return FSP_OK;
+  });
+}
+
 extern "C" fsp_status fsp_device_error(uint32_t* bits) {
   return fsp::guard([&]() -> fsp_status {
     fsp::clear_error();

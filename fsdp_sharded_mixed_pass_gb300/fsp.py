@@ -19,7 +19,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
-           "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_destroy",
+           "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_tiles", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
            "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32", "fsp_shard",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
@@ -43,6 +43,11 @@ class _PlanInfo(ctypes.Structure):
                 ("state_len_total", ctypes.c_int64), ("n_segments", ctypes.c_int64), ("n_tiles", ctypes.c_int64),
                 ("n_replicate", ctypes.c_int32), ("n_shard", ctypes.c_int32), ("param_align", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class _Tile(ctypes.Structure):
+    _fields_ = [("full_begin", ctypes.c_int64), ("state_begin", ctypes.c_int64), ("len", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("param", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class _Segment(ctypes.Structure):
@@ -91,6 +96,7 @@ def lib():
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
     L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
+    L.fsp_plan_tiles.argtypes = [vp, ctypes.POINTER(_Tile), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
     L.fsp_plan_destroy.argtypes = [vp]
     L.fsp_plan_destroy.restype = None
     step_args = [vp, ctypes.POINTER(vp), i32, vp, vp, vp, ctypes.POINTER(vp), ctypes.POINTER(_HParams), i64]
@@ -195,6 +201,15 @@ class Plan:
                 out.append(off.value)
             self._param_offsets = tuple(out)
         return self._param_offsets
+
+    def tiles(self) -> list:
+        """The work tiles as (full_begin, state_begin, len, rank, param) tuples
+        (see ``fsp_plan_tiles``)."""
+        n = ctypes.c_int64()
+        _check(lib().fsp_plan_tiles(self._h, None, 0, ctypes.byref(n)), "fsp_plan_tiles")
+        buf = (_Tile * max(1, n.value))()
+        _check(lib().fsp_plan_tiles(self._h, buf, n.value, ctypes.byref(n)), "fsp_plan_tiles")
+        return [(t.full_begin, t.state_begin, t.len, t.rank, t.param) for t in buf[:n.value]]
 
     def ledger(self, grad_dtype: str = "f32") -> dict:
         led = _Ledger()

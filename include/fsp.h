@@ -202,6 +202,22 @@ fsp_status fsp_plan_segment(const fsp_plan* plan, int64_t i, fsp_segment* out);
 
 fsp_status fsp_plan_ledger(const fsp_plan* plan, int32_t grad_dtype, fsp_ledger* out);
 
+/* One unit of work of the step kernels: `len` elements from full index
+ * `full_begin` (of every rank's buffer) and state index `state_begin`, owned
+ * by rank `rank`, inside parameter `param` (-1: a DistOpt shard). */
+typedef struct {
+  int64_t full_begin, state_begin;
+  int32_t len, rank, param, reserved;
+} fsp_tile;
+
+/* The plan's work tiles (host only, no device call): each non-empty segment
+ * cut at multiples of 4096 elements of the full index, in full-index order.
+ * The step kernels run them in this order (plans with at least 16 tiles per
+ * CTA: taken in order from a counter; smaller ones: CTA b takes tiles b,
+ * b + grid, ...).  The number goes to *n; up to `cap` tiles to `out` (out may
+ * be NULL when cap is 0). */
+fsp_status fsp_plan_tiles(const fsp_plan* plan, fsp_tile* out, int64_t cap, int64_t* n);
+
 /* Frees the plan and its device tile tables.  NULL is a no-op. */
 void fsp_plan_destroy(fsp_plan* plan);
 

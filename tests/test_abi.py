@@ -396,3 +396,39 @@ def test_noalloc_step_checks_like_the_step_on_host():
         args = B._step_args(plan, g, *s, p, HP, 0, "f32")
         assert fn(*args, ctypes.c_void_p(0)) == B.FSP_EINVAL
         assert "step must be >= 1" in L.fsp_last_error().decode()
+
+
+@pytest.mark.parametrize("shapes,n_d,mode,n_rep", [
+    (None, 4, "fsdp2", 1),                                            # the one-layer Qwen3 workload
+    (((3001, 7), (5, 4099), (1,), (12289,), (777, 64)), 6, "fsdp2", 1),
+    (((4097,), (64, 129), (2, 3, 5)), 3, "distopt", 1),
+    (((9,), (1,), (3,), (8193, 2)), 8, "hsdp", 2),
+])
+def test_work_tiles_cover_the_owned_elements_once(shapes, n_d, mode, n_rep):
+    """The kernels' work tiles, against the oracle planner: every owned element
+    of replica group 0 exactly once, at the oracle's state slot, with its
+    owner; tiles in full-index order, none crossing a multiple of 4096."""
+    import numpy as np
+    from oracle import plan as OP
+    from synth_inputs import workload
+    shapes = shapes or workload(0).shapes
+    plan = fsp.plan_layout(shapes, n_d, mode, n_replicate=n_rep)
+    tiles = plan.tiles()
+    assert len(tiles) == plan.n_tiles
+    op = OP.plan_layout(shapes, n_d, mode, n_rep=n_rep)
+    fi, si = OP.owned_indices(op)
+    want = {}
+    for seg in op.segments:
+        if seg.rank < n_d // n_rep:                     # replica group 0 (HSDP); every rank otherwise
+            for x in range(seg.length):
+                want[seg.full_off + x] = (seg.state_off + x, seg.rank)
+    got = {}
+    prev_end = -1
+    for fb, sb, ln, r, pm in tiles:
+        assert ln > 0 and fb >= prev_end and fb // 4096 == (fb + ln - 1) // 4096
+        prev_end = fb + ln
+        for x in range(ln):
+            assert fb + x not in got
+            got[fb + x] = (sb + x, r)
+    assert got == want
+    assert set(want) <= set(fi.tolist())
