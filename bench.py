@@ -635,7 +635,8 @@ def _oracle_worker(w, shapes, warmup, steps, seconds, barrier, results):
 def time_oracle_pool(w, shapes, workers: int, elems_per_worker: int, warmup: int = 0, steps: int = 0,
                      seconds: float = 10.0, limit_s: float = 1200.0):
     """The oracle on ``workers`` host cores at once, one spawned process each
-    on its own run of whole params, all timed over the same window.  Returns
+    on its own run of consecutive params (an oversized one as blocks of its
+    rows), all timed over the same window.  Returns
     (elements x steps summed over the processes, the longest process's time,
     each process's sample size in elements)."""
     import multiprocessing as mp
@@ -876,7 +877,8 @@ def run_fsp(args):
                 done, psecs, sizes = time_oracle_pool(w, shapes, k, CPU_POOL_ELEMS, seconds=args.cpu_seconds)
                 cpu.update(value=done / psecs, cores=k,
                            sample=f"{k} processes, one per host core, each repeating the oracle step on its own "
-                                  f"run of whole params of {w.name} ({min(sizes)}-{max(sizes)} elements), "
+                                  f"run of consecutive params of {w.name}, spread over the workload, params "
+                                  f"larger than a run as blocks of rows ({min(sizes)}-{max(sizes)} elements), "
                                   f"N_d={w.n_d}, for {psecs:.1f} s",
                            sample_1_core=one["sample"])
             except Exception as e:
@@ -934,8 +936,9 @@ def run_reference(args):
         try:
             done, secs, sizes = time_oracle_pool(w, shapes, k, per_core, warmup=args.warmup, steps=args.steps)
             value, sample_elems = done / secs, sum(sizes)
-            sample = (f"{k} processes, one per host core, each stepping the oracle on its own run of whole params "
-                      f"of {w.name} ({min(sizes)}-{max(sizes)} elements) per step, N_d={w.n_d}")
+            sample = (f"{k} processes, one per host core, each stepping the oracle on its own run of consecutive "
+                      f"params of {w.name}, spread over the workload, params larger than a run as blocks of "
+                      f"rows ({min(sizes)}-{max(sizes)} elements) per step, N_d={w.n_d}")
         except Exception as e:
             pool_error, k = str(e)[:300], 1
     if k == 1:

@@ -1,0 +1,76 @@
+"""GPU parity where the master update cancels: theta (1 - lr wd) placed next
+to the step u, at depths from 2^-1 to 2^-30 of theta, so that most elements
+take the kernel's float-pair evaluation and the rest its fp32 one.  Against
+the oracle: state within the bars, params within one bf16 ulp on every
+element.  Inputs are built on the host from the oracle's own update (with the
+weight decay off, theta - theta' is u)."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_mixed_pass_gb300 as fsp
+import synth_inputs as S
+from oracle import step as OS
+
+from gpu_cases import HP, STATE_SENTINEL, DeviceCase, OracleCase, compare, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1000, 64), (4099,), (17, 3)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _upload(buf, bits: np.ndarray) -> None:
+    view = bits.view(np.int32 if bits.dtype.itemsize == 4 else np.int16)
+    buf.raw[buf.g:buf.g + buf.n].copy_(torch.from_numpy(view.copy()).cuda())
+
+
+def _cancelling_case(n_d, t, seed):
+    dev = DeviceCase(SHAPES, n_d, "fsdp2", "f32", seed)
+    ora = OracleCase(SHAPES, n_d, "fsdp2", "f32", seed)
+    n = dev.plan.full_len_padded
+    rng = np.random.default_rng(seed)
+    # every rank holds the same gradient; G is its rank-ordered sum / N_d
+    g = S.grad_f32(seed, 0, np.arange(n))
+    G = OS.average(OS.rank_ordered_sum([g] * n_d), n_d)
+    th, m, v = S.master_f32(seed, np.arange(n)), S.adam_m_f32(seed, np.arange(n)), S.adam_v_f32(seed, np.arange(n))
+    # u from the oracle's update without weight decay, then theta such that
+    # theta (1 - lr wd) = u (1 + e), e of either sign and 2^-1 .. 2^-30 in size
+    th0, _, _ = OS.adamw(th, m, v, G, dict(HP, weight_decay=0.0), t)
+    u = th.astype(np.float64) - th0.astype(np.float64)
+    decay = 1.0 - float(np.float32(HP["lr"])) * float(np.float32(HP["weight_decay"]))
+    e = rng.choice([-1.0, 1.0], n) * 2.0 ** -rng.uniform(1, 30, n)
+    theta = (u / decay * (1.0 + e)).astype(np.float32)
+    keep = rng.random(n) < 0.1            # a tenth keep their ordinary masters
+    theta[keep] = th[keep]
+    for q in range(n_d):
+        _upload(dev.grads[q], g.view(np.uint32))
+        ora.grads[q] = g.copy()
+    for k, full in enumerate((theta, m, v)):
+        slots = np.full(dev.plan.state_len_total, STATE_SENTINEL, np.uint32).view(np.float32)
+        slots[ora.si] = full[ora.fi]
+        _upload(dev.state[k], slots.view(np.uint32))
+        ora.state[k] = slots.copy()
+    torch.cuda.synchronize()
+    return dev, ora
+
+
+@pytest.mark.parametrize("n_d,t", [(4, 10), (8, 1), (4, 1000)])
+def test_cancelling_updates_match_the_oracle(n_d, t):
+    dev, ora = _cancelling_case(n_d, t, seed=70 + n_d + t)
+    before = ora.state[0][ora.si].astype(np.float64)
+    dev.step(t)
+    ora.step(t)
+    torch.cuda.synchronize()
+    after = ora.state[0][ora.si].astype(np.float64)
+    # most elements cancel below 2^-10 of theta: the float-pair path is taken
+    deep = np.abs(after) < 2.0 ** -10 * np.abs(before)
+    assert deep.mean() > 0.5
+    compare(dev, ora)
+    assert fsp.device_error() == 0
