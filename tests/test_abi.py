@@ -432,3 +432,18 @@ def test_work_tiles_cover_the_owned_elements_once(shapes, n_d, mode, n_rep):
             got[fb + x] = (sb + x, r)
     assert got == want
     assert set(want) <= set(fi.tolist())
+
+
+def test_plan_tiles_checks_its_arguments():
+    L = B.lib()
+    plan = fsp.plan_layout([(4099,)], 2)
+    n = ctypes.c_int64()
+    assert L.fsp_plan_tiles(None, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, None, 0, None) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, None, 1, ctypes.byref(n)) == B.FSP_EINVAL      # cap > 0 needs out
+    assert L.fsp_plan_tiles(plan.handle, None, -1, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+    buf = (B._Tile * 1)()                                                             # a short buffer: the first tiles only
+    assert L.fsp_plan_tiles(plan.handle, buf, 1, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+    first = plan.tiles()[0]
+    assert (buf[0].full_begin, buf[0].state_begin, buf[0].len) == first[:3]

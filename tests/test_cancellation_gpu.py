@@ -31,14 +31,14 @@ def _upload(buf, bits: np.ndarray) -> None:
     buf.raw[buf.g:buf.g + buf.n].copy_(torch.from_numpy(view.copy()).cuda())
 
 
-def _cancelling_case(n_d, t, seed):
-    dev = DeviceCase(SHAPES, n_d, "fsdp2", "f32", seed)
-    ora = OracleCase(SHAPES, n_d, "fsdp2", "f32", seed)
+def _cancelling_case(n_d, t, seed, mode="fsdp2", n_rep=1):
+    dev = DeviceCase(SHAPES, n_d, mode, "f32", seed, n_rep)
+    ora = OracleCase(SHAPES, n_d, mode, "f32", seed, n_rep)
     n = dev.plan.full_len_padded
     rng = np.random.default_rng(seed)
-    # every rank holds the same gradient; G is its rank-ordered sum / N_d
+    # every rank holds the same gradient; G is its (grouped) rank-ordered sum / N_d
     g = S.grad_f32(seed, 0, np.arange(n))
-    G = OS.average(OS.rank_ordered_sum([g] * n_d), n_d)
+    G = OS.average(OS.hybrid_sum([g] * n_d, n_rep), n_d)
     th, m, v = S.master_f32(seed, np.arange(n)), S.adam_m_f32(seed, np.arange(n)), S.adam_v_f32(seed, np.arange(n))
     # u from the oracle's update without weight decay, then theta such that
     # theta (1 - lr wd) = u (1 + e), e of either sign and 2^-1 .. 2^-30 in size
@@ -61,9 +61,12 @@ def _cancelling_case(n_d, t, seed):
     return dev, ora
 
 
-@pytest.mark.parametrize("n_d,t", [(4, 10), (8, 1), (4, 1000)])
-def test_cancelling_updates_match_the_oracle(n_d, t):
-    dev, ora = _cancelling_case(n_d, t, seed=70 + n_d + t)
+@pytest.mark.parametrize("n_d,t,mode,n_rep", [(4, 10, "fsdp2", 1), (8, 1, "fsdp2", 1), (4, 1000, "fsdp2", 1),
+                                              (9, 10, "fsdp2", 1), (8, 10, "hsdp", 2), (6, 3, "distopt", 1)])
+def test_cancelling_updates_match_the_oracle(n_d, t, mode, n_rep):
+    """The bulk kernel (N_d 4, 8, 6 and the HSDP 4 x 2 mesh) and the per-thread
+    kernel (N_d 9)."""
+    dev, ora = _cancelling_case(n_d, t, 70 + n_d + t, mode, n_rep)
     before = ora.state[0][ora.si].astype(np.float64)
     dev.step(t)
     ora.step(t)
@@ -73,4 +76,20 @@ def test_cancelling_updates_match_the_oracle(n_d, t):
     deep = np.abs(after) < 2.0 ** -10 * np.abs(before)
     assert deep.mean() > 0.5
     compare(dev, ora)
+    assert fsp.device_error() == 0
+
+
+def test_device_resident_t_gives_the_same_bits_on_cancelling_updates():
+    """The bias-correction scalars (float pairs) computed on the device from a
+    device-resident t equal the host's bit for bit: the float-pair path, which
+    uses their low parts, gives the same state and params."""
+    ref, _ = _cancelling_case(8, 10, 91)
+    dev, _ = _cancelling_case(8, 10, 91)
+    t = torch.tensor([10], dtype=torch.int64, device="cuda")
+    ref.step(10, debug=False)
+    fsp.sharded_step_device_t(dev.plan, [g.t for g in dev.grads], *[s.t for s in dev.state],
+                              [p.t for p in dev.params], HP, t, advance=False)
+    torch.cuda.synchronize()
+    for x, y in zip(ref.state + ref.params, dev.state + dev.params):
+        assert np.array_equal(x.bits(), y.bits())
     assert fsp.device_error() == 0
