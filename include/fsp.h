@@ -11,6 +11,11 @@
  *       "Parallelism strategies: which state to shard", section 二.2.
  *   (2) AdamW on the owner's fp32 master / Adam m / Adam v shard, with no
  *       communication.  "07 · 显存模型", section 2.1 (fp32 master + m/v).
+ *       Each element is updated in fp32; where the new master cancels
+ *       (theta (1 - lr wd) - u below 2^-10 of its terms' size) it is
+ *       evaluated again with pairs of floats (about 2^-44 of the terms'
+ *       size), so every stored fp32 result is close to the exactly rounded
+ *       value and its bf16 cast within one ulp of the exact update's.
  *   (3) cast of the new master to bf16 (round to nearest even) and all-gather
  *       into every rank's full bf16 param buffer.
  *       "FSDP2 Qwen3 Decoder Layer Walkthrough", section "Step 0".
