@@ -727,6 +727,13 @@ def config_block(w, label, plan):
     }
 
 
+def step_config(w, label, plan, flush_bytes: int) -> dict:
+    """The config block of the plain step on a workload: the same dict on both
+    arms (the GPU arm adds the flow's own keys for other flows)."""
+    per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+    return dict(config_block(w, label, plan), bytes_per_param=per, l2=l2_note(per * plan.valid_elems, flush_bytes))
+
+
 def l2_note(moved: int, flush_bytes: int) -> str:
     if flush_bytes:
         return (f"L2 flushed before every timed step (an untimed {flush_bytes / 1e6:.0f} MB write, "
@@ -888,7 +895,7 @@ def run_fsp(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_block(w, label, plan), bytes_per_param=per,
+        "config": dict(step_config(w, label, plan, flush_bytes), bytes_per_param=per,
                        l2=l2_note(per * P, flush_bytes), **(
             {"flow": f"distributed optimizer with clipping, max_norm {args.clip} (4 kernels per step)"}
             if args.clip is not None else {"flow": "FSDP2 unshard (bf16 all-gather of the fp32 shards)"}
@@ -965,21 +972,29 @@ def run_reference(args):
         secs = time.perf_counter() - t0
         value, sample_elems = op.valid_elems * args.steps / secs, op.valid_elems
         sample = f"{len(sshapes)} params ({op.valid_elems} elements) of {w.name} per step, N_d={w.n_d}"
-    # the config of the workload itself (as the GPU arm reports it), the sample beside it
+    # the config of the workload itself, as the GPU arm reports it; what was
+    # timed (a bounded sample of that workload per step) beside it
     full_p = sum(math.prod(sh) for sh in shapes)
     plan_like = type("P", (), {"valid_elems": full_p})
-    cfg = config_block(w, label, plan_like)
-    # what was timed: per step a bounded sample of the workload's elements; the
-    # step is elementwise, so the full workload's step takes full_p / value
-    cfg["sample_params"] = sample_elems
-    cfg["sample_ms_per_step"] = secs * 1e3 / args.steps
-    cfg["ms_per_step_basis"] = (f"the full workload ({full_p} params) at the measured rate of the "
-                                f"{sample_elems}-element sample (elementwise step)")
+    per = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
+    l2 = L2_BYTES
+    try:   # the GPU arm's flush decision uses the device's own L2 size
+        import torch
+        if torch.cuda.is_available():
+            l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or L2_BYTES)
+    except Exception:
+        pass
+    flush_bytes = 2 * l2 if per * full_p <= L2_FLUSH_FACTOR * l2 else 0
+    cfg = step_config(w, label, plan_like, flush_bytes)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_p / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
+        # the step is elementwise: ms_per_step is the whole workload's step at the sample's measured rate
+        "sample": {"params_per_step": sample_elems, "ms_per_step": secs * 1e3 / args.steps,
+                   "ms_per_step_basis": f"the full workload ({full_p} params) at the measured rate of the "
+                                        f"{sample_elems}-element sample"},
         "cpu_baseline": dict({"value": value, "unit": UNIT, "cores": k, "kind": "oracle",
                               "cpu": cpu_model(), "host_cores": host_cores(), "sample": sample},
                              **({"pool_error": pool_error} if pool_error else {})),

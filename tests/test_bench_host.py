@@ -67,6 +67,13 @@ def test_reference_arm_prints_one_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["value"] > 0 and line["unit"] == "params/s"
+    # the workload's own config, as the GPU arm reports it; the timed sample beside it
+    w, shapes, label = bench.resolve_workload("0", "0:4", None)
+    full_p = sum(bench.math.prod(sh) for sh in shapes)
+    flush = 2 * bench.L2_BYTES
+    assert line["config"] == bench.step_config(w, label, type("P", (), {"valid_elems": full_p}), flush)
+    assert line["ms_per_step"] == pytest.approx(full_p / line["value"] * 1e3)
+    assert line["sample"]["params_per_step"] > 0 and line["sample"]["ms_per_step"] > 0
 
 
 def test_reference_arm_other_ranks_print_nothing():
