@@ -31,14 +31,19 @@ def _upload(buf, bits: np.ndarray) -> None:
     buf.raw[buf.g:buf.g + buf.n].copy_(torch.from_numpy(view.copy()).cuda())
 
 
-def _cancelling_case(n_d, t, seed, mode="fsdp2", n_rep=1):
-    dev = DeviceCase(SHAPES, n_d, mode, "f32", seed, n_rep)
-    ora = OracleCase(SHAPES, n_d, mode, "f32", seed, n_rep)
+def _cancelling_case(n_d, t, seed, mode="fsdp2", n_rep=1, grad_dtype="f32"):
+    dev = DeviceCase(SHAPES, n_d, mode, grad_dtype, seed, n_rep)
+    ora = OracleCase(SHAPES, n_d, mode, grad_dtype, seed, n_rep)
     n = dev.plan.full_len_padded
     rng = np.random.default_rng(seed)
     # every rank holds the same gradient; G is its (grouped) rank-ordered sum / N_d
-    g = S.grad_f32(seed, 0, np.arange(n))
-    G = OS.average(OS.hybrid_sum([g] * n_d, n_rep), n_d)
+    if grad_dtype == "f32":
+        g = S.grad_f32(seed, 0, np.arange(n))
+        gw = g
+    else:
+        g = S.grad_bf16_bits(seed, 0, np.arange(n))
+        gw = OS.bf16_bits_to_f32(g)
+    G = OS.average(OS.hybrid_sum([gw] * n_d, n_rep), n_d)
     th, m, v = S.master_f32(seed, np.arange(n)), S.adam_m_f32(seed, np.arange(n)), S.adam_v_f32(seed, np.arange(n))
     # u from the oracle's update without weight decay, then theta such that
     # theta (1 - lr wd) = u (1 + e), e of either sign and 2^-1 .. 2^-30 in size
@@ -50,7 +55,7 @@ def _cancelling_case(n_d, t, seed, mode="fsdp2", n_rep=1):
     keep = rng.random(n) < 0.1            # a tenth keep their ordinary masters
     theta[keep] = th[keep]
     for q in range(n_d):
-        _upload(dev.grads[q], g.view(np.uint32))
+        _upload(dev.grads[q], g.view(np.uint32) if grad_dtype == "f32" else g)
         ora.grads[q] = g.copy()
     for k, full in enumerate((theta, m, v)):
         slots = np.full(dev.plan.state_len_total, STATE_SENTINEL, np.uint32).view(np.float32)
@@ -61,12 +66,14 @@ def _cancelling_case(n_d, t, seed, mode="fsdp2", n_rep=1):
     return dev, ora
 
 
-@pytest.mark.parametrize("n_d,t,mode,n_rep", [(4, 10, "fsdp2", 1), (8, 1, "fsdp2", 1), (4, 1000, "fsdp2", 1),
-                                              (9, 10, "fsdp2", 1), (8, 10, "hsdp", 2), (6, 3, "distopt", 1)])
-def test_cancelling_updates_match_the_oracle(n_d, t, mode, n_rep):
-    """The bulk kernel (N_d 4, 8, 6 and the HSDP 4 x 2 mesh) and the per-thread
-    kernel (N_d 9)."""
-    dev, ora = _cancelling_case(n_d, t, 70 + n_d + t, mode, n_rep)
+@pytest.mark.parametrize("n_d,t,mode,n_rep,gd", [(4, 10, "fsdp2", 1, "f32"), (8, 1, "fsdp2", 1, "f32"),
+                                                 (4, 1000, "fsdp2", 1, "f32"), (9, 10, "fsdp2", 1, "f32"),
+                                                 (8, 10, "hsdp", 2, "f32"), (6, 3, "distopt", 1, "f32"),
+                                                 (16, 10, "fsdp2", 1, "bf16")])
+def test_cancelling_updates_match_the_oracle(n_d, t, mode, n_rep, gd):
+    """The bulk kernel (N_d 4, 8, 6, 16 with bf16 gradients and the HSDP 4 x 2
+    mesh) and the per-thread kernel (N_d 9)."""
+    dev, ora = _cancelling_case(n_d, t, 70 + n_d + t, mode, n_rep, gd)
     before = ora.state[0][ora.si].astype(np.float64)
     dev.step(t)
     ora.step(t)
