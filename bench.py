@@ -15,7 +15,9 @@ per param).
 Other flows (each reports its own bytes per param): --clip MAX_NORM,
 --writeback, --no-gather, --unshard, --fp32-gather, and --per-param (alone or
 with any of those); --n-d N and --param-slice a:b change the workload,
---graph captures the timed steps.
+--layers K steps K copies of it back to back (one plan per layer), --graph
+captures the timed steps.  The default run also times the other workloads
+after the headline one (the "workloads" list of the JSON line).
 
 Multi-GPU (torchrun, one rank per GPU): the step does not shard across GPUs
 (the N_d ranks already live on one device), so every GPU runs an independent
@@ -93,6 +95,8 @@ def parse_args(argv=None):
     ap.add_argument("--per-param", action="store_true",
                     help="every rank's gradient and parameter of every parameter in a tensor of its own "
                          "(FSDP2 / HSDP; the step reads and writes them in place)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="K copies of the workload, one plan each, stepped back to back per step (plain step only)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the block that times the other workloads after the default one")
     ap.add_argument("--workload-steps", type=int, default=20,
@@ -369,6 +373,29 @@ class DeviceWorkload:
         if self.clip is not None:   # pass 1: N_d grads in, one slice out per group; pass 3: 1 grad + state + params
             return w.n_d * w.grad_bytes + w.grad_bytes * w.n_rep + w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         return w.n_d * w.grad_bytes + 24 * w.n_rep + pbytes * w.n_d
+
+
+class LayerStack:
+    """``layers`` independent copies of a workload, each with its own plan and
+    buffers, stepped one after another on one stream: the per-layer steps of a
+    model whose layers each have the workload's size (FSDP2 steps one layer's
+    shards at a time).  Same interface as DeviceWorkload for the timing."""
+
+    def __init__(self, w, shapes, device, layers: int):
+        self.layers = [DeviceWorkload(w, shapes, device) for _ in range(layers)]
+        self.w, self.device = w, device
+        self.plan = type("P", (), {"valid_elems": layers * self.layers[0].plan.valid_elems})
+
+    def step(self, stream):
+        for layer in self.layers:
+            layer.step(stream)
+
+    def bytes_per_param(self) -> int:
+        return self.layers[0].bytes_per_param()
+
+    def close(self):
+        for layer in self.layers:
+            layer.plan.close()
 
 
 def time_device(wl: DeviceWorkload, steps: int, warmup: int, dist: Dist, clocks_id, graph: bool = False,
@@ -745,7 +772,10 @@ def l2_note(moved: int, flush_bytes: int) -> str:
 # one-layer case, the DistOpt layout, the ragged N_d = 6 case, the bf16-grad
 # N_d = 16 stack, the HSDP 2 x 4 mesh), one after another, each freed before
 # the next.
-EXTRA_WORKLOADS = ("qwen3_layer", "qwen3_0p6b_distopt", "ragged_500", "dense_1p5b_bf16grad", "qwen3_0p6b_hsdp_2x4")
+EXTRA_WORKLOADS = ("qwen3_layer", "qwen3_0p6b_distopt", "ragged_500", "dense_1p5b_bf16grad", "qwen3_0p6b_hsdp_2x4",
+                   ("qwen3_layer", 28))
+# (name, K): K copies of the workload stepped back to back (LayerStack) - the
+# one-layer step as it runs in a model of 28 such layers
 
 
 def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms=None) -> dict:
@@ -770,10 +800,13 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
     headline one is, and freed."""
     import torch
     out = []
-    for name in names:
+    for spec in names:
+        name, layers = spec if isinstance(spec, tuple) else (spec, 1)
         w, shapes, label = resolve_workload(name, param_slice, None)
+        if layers > 1:
+            label = f"{label} x{layers} (one plan per layer, stepped back to back)"
         try:
-            wl = DeviceWorkload(w, shapes, dev)
+            wl = LayerStack(w, shapes, dev, layers) if layers > 1 else DeviceWorkload(w, shapes, dev)
             flush = 2 * l2 if wl.bytes_per_param() * wl.plan.valid_elems <= L2_FLUSH_FACTOR * l2 else 0
             ms, clocks = time_device(wl, steps, warmup, dist, clocks_id, False, flush)
             if clocks_bad(clocks):
@@ -781,8 +814,12 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
             graph_ms = None
             if flush:   # small enough for launch cost to show: also one CUDA graph per step
                 graph_ms, _ = time_device(wl, steps, warmup, dist, clocks_id, True, flush)
-            out.append(workload_entry(wl, label, ms, steps, clocks, flush, peak, graph_ms))
-            wl.plan.close()
+            entry = workload_entry(wl, label, ms, steps, clocks, flush, peak, graph_ms)
+            if layers > 1:
+                entry["layers"] = layers
+                entry["ms_per_layer"] = entry["ms_per_step"] / layers
+            out.append(entry)
+            wl.close() if layers > 1 else wl.plan.close()
             del wl
         except Exception as e:   # one workload failing leaves the others' lines
             out.append({"workload": label, "error": f"{type(e).__name__}: {e}"[:300]})
@@ -807,8 +844,15 @@ def run_fsp(args):
         raise SystemExit("--fp32-gather: the plain step or --unshard")
     if args.per_param and args.no_gather and (args.clip is not None or args.writeback or args.unshard):
         raise SystemExit("--per-param --no-gather: the plain step only (the table has no parameter tensors)")
-    wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather,
-                        no_gather=args.no_gather and args.per_param)
+    if args.layers > 1 and (args.clip is not None or args.unshard or args.no_gather or args.per_param
+                            or args.writeback or args.fp32_gather):
+        raise SystemExit("--layers: the plain step only")
+    if args.layers > 1:
+        wl = LayerStack(w, shapes, dev, args.layers)
+        label = f"{label} x{args.layers} (one plan per layer, stepped back to back)"
+    else:
+        wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather,
+                            no_gather=args.no_gather and args.per_param)
     wl.clip = args.clip
     wl.unshard = args.unshard
     wl.no_gather = args.no_gather
@@ -838,7 +882,7 @@ def run_fsp(args):
 
     e2e = None
     if (not args.no_e2e and args.clip is None and not args.unshard and not args.no_gather and not args.per_param
-            and not args.writeback and not args.fp32_gather):
+            and not args.writeback and not args.fp32_gather and args.layers == 1):
         # every rank on this node needs its own host copy of the grads and params
         per_rank = P * w.n_d * (w.grad_bytes + 2)
         local = int(os.environ.get("LOCAL_WORLD_SIZE", dist.world))
@@ -858,14 +902,14 @@ def run_fsp(args):
 
     default_run = (args.clip is None and not args.unshard and not args.no_gather and not args.per_param
                    and not args.writeback and not args.fp32_gather and not args.graph and args.param_slice is None
-                   and args.n_d is None)
+                   and args.n_d is None and args.layers == 1)
     workloads = None
     if default_run and dist.world == 1 and not args.no_workloads:
         headline = workload_entry(wl, label, ms, args.steps, clocks, flush_bytes, peak)
         wl.plan.close()
         del wl
         torch.cuda.empty_cache()
-        names = [n for n in EXTRA_WORKLOADS if n != w.name]
+        names = [n for n in EXTRA_WORKLOADS if n != w.name]   # the headline's own stack entry stays
         workloads = [headline] + time_workloads(names, args.workload_steps, max(3, min(args.warmup, 5)), dist,
                                                 clocks_id, dev, l2, peak)
 
