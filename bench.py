@@ -778,7 +778,7 @@ EXTRA_WORKLOADS = ("qwen3_layer", "qwen3_0p6b_distopt", "ragged_500", "dense_1p5
 # one-layer step as it runs in a model of 28 such layers
 
 
-def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms=None) -> dict:
+def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms_per_step=None) -> dict:
     """One workload's line of the workloads block."""
     P = wl.plan.valid_elems
     per = wl.bytes_per_param()
@@ -790,8 +790,8 @@ def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms=Non
          "frac_of_nominal_8000": gbs / 8000.0, "kernel": step_kernel_name(wl.w),
          "l2": l2_note(per * P, flush_bytes),
          "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "error") if k in clocks}}
-    if graph_ms is not None:
-        e["graph_ms_per_step"] = graph_ms / steps
+    if graph_ms_per_step is not None:
+        e["graph_ms_per_step"] = graph_ms_per_step
     return e
 
 
@@ -808,13 +808,21 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
         try:
             wl = LayerStack(w, shapes, dev, layers) if layers > 1 else DeviceWorkload(w, shapes, dev)
             flush = 2 * l2 if wl.bytes_per_param() * wl.plan.valid_elems <= L2_FLUSH_FACTOR * l2 else 0
-            ms, clocks = time_device(wl, steps, warmup, dist, clocks_id, False, flush)
+            n_steps = steps
+            ms, clocks = time_device(wl, n_steps, warmup, dist, clocks_id, False, flush)
+            if "error" in clocks and ms > 0:
+                # a timed region shorter than the sampler's period saw no clock sample:
+                # time again with enough steps to span ~150 ms (a flushed step takes
+                # ~0.3 ms of wall time with its flush)
+                n_steps = max(n_steps, 500) if flush else max(n_steps, int(math.ceil(n_steps * 150.0 / ms)))
+                ms, clocks = time_device(wl, n_steps, warmup, dist, clocks_id, False, flush)
             if clocks_bad(clocks):
-                ms, clocks = time_device(wl, steps, warmup, dist, clocks_id, False, flush)
+                ms, clocks = time_device(wl, n_steps, warmup, dist, clocks_id, False, flush)
             graph_ms = None
             if flush:   # small enough for launch cost to show: also one CUDA graph per step
-                graph_ms, _ = time_device(wl, steps, warmup, dist, clocks_id, True, flush)
-            entry = workload_entry(wl, label, ms, steps, clocks, flush, peak, graph_ms)
+                g_ms, _ = time_device(wl, steps, warmup, dist, clocks_id, True, flush)
+                graph_ms = g_ms / steps
+            entry = workload_entry(wl, label, ms, n_steps, clocks, flush, peak, graph_ms)
             if layers > 1:
                 entry["layers"] = layers
                 entry["ms_per_layer"] = entry["ms_per_step"] / layers
