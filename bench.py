@@ -805,6 +805,7 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
         w, shapes, label = resolve_workload(name, param_slice, None)
         if layers > 1:
             label = f"{label} x{layers} (one plan per layer, stepped back to back)"
+        wl = None
         try:
             wl = LayerStack(w, shapes, dev, layers) if layers > 1 else DeviceWorkload(w, shapes, dev)
             flush = 2 * l2 if wl.bytes_per_param() * wl.plan.valid_elems <= L2_FLUSH_FACTOR * l2 else 0
@@ -827,12 +828,16 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
                 entry["layers"] = layers
                 entry["ms_per_layer"] = entry["ms_per_step"] / layers
             out.append(entry)
-            wl.close() if layers > 1 else wl.plan.close()
-            del wl
         except Exception as e:   # one workload failing leaves the others' lines
             out.append({"workload": label, "error": f"{type(e).__name__}: {e}"[:300]})
-        torch.cuda.synchronize(dev)
-        torch.cuda.empty_cache()
+        finally:   # the next workload may need the memory
+            if isinstance(wl, LayerStack):
+                wl.close()
+            elif wl is not None:
+                wl.plan.close()
+            del wl
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
     return out
 
 
