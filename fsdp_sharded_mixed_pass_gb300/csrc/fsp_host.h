@@ -33,8 +33,13 @@ fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 // On plans with many tiles per CTA the bulk kernel takes its tiles in order
 // from a counter: `fixed_ctr` when given (zeroed here on `stream`), else one
 // allocated from a library pool on `stream` and freed after the launch.
+// With `step_plan` given, a launch of a large plan (at least 16 tiles per
+// resident CTA) that holds all of that plan's tiles on full-size buffers with
+// the all-gather (no clip, no per-parameter tables) runs on the plan's step
+// tiles instead (the tiles split at multiples of 2048 elements, uploaded once
+// per plan and device).
 fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false,
-                  unsigned long long* fixed_ctr = nullptr);
+                  unsigned long long* fixed_ctr = nullptr, const fsp_plan* step_plan = nullptr);
 // Passes 1-3 of the clipped flow on a prepared argument block (non-empty
 // plan, fp32 grads; HSDP plans too); clipped_empty writes norm_out = {0, 1}
 // for a plan with nothing to reduce.

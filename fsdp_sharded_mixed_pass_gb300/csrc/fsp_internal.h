@@ -70,6 +70,9 @@ struct fsp_plan {
   mutable std::mutex mu;
   mutable std::map<int, fsp::Tile*> device_tiles;
   mutable std::map<int, double*> device_partials;
+  // Per device: `tiles` split at multiples of kStepTileElems (the step
+  // kernels' schedule on full-size buffers) and their number.
+  mutable std::map<int, std::pair<fsp::Tile*, int64_t>> device_step_tiles;
 };
 
 // Per-parameter tensors registered for a per-parameter plan on one device

@@ -147,6 +147,66 @@ fsp_status device_tiles(const fsp_plan* p, const Tile** out) {
   return FSP_OK;
 }
 
+// The step kernels run large plans (at least kOrderedMinTilesPerCta tiles per
+// CTA) on full-size buffers with the all-gather on the plan's tiles split at
+// multiples of this many elements: the CTAs, which take the tiles in order,
+// then work in a narrower window of the buffers.  Measured against the plan's
+// 4096-element tiles (same box, 50 steps, two runs): Qwen3-0.6B FSDP2 5.967 vs
+// 6.008 ms, DistOpt 5.952 vs 5.997, HSDP 2 x 4 8.004 vs 8.054, ragged N_d = 6
+// 11.818 vs 11.870, bf16 grads N_d = 16 13.458 vs 13.468, with write-back 6.330
+// vs 6.369, fp32 gather 7.387 vs 7.424, N_d = 24 (per-thread kernel) 14.49 vs
+// 14.62; 1024 and 1536 were 6-20 % slower, 8192 slower.  Kept on the plan's
+// tiles, where 2048 measured slower: the ZeRO-3 step (4.89 vs 4.61 ms),
+// per-parameter tensors (4.74 vs 4.53), the clipped flow (7.07 vs 6.83) and
+// one-layer slices of 6-7 tiles per CTA (47.4 vs 46.7 and 75.9 vs 73.8 us).
+constexpr int64_t kStepTileElems = 2048;
+static_assert(kTileElems % kStepTileElems == 0, "step tiles split plan tiles");
+
+std::vector<Tile> split_tiles(const std::vector<Tile>& tiles, int64_t unit) {
+  std::vector<Tile> out;
+  out.reserve(tiles.size() * size_t(std::max<int64_t>(1, kTileElems / unit)));
+  for (const Tile& t : tiles) {
+    const int64_t end = t.full_begin + t.len;
+    for (int64_t f = t.full_begin; f < end;) {
+      const int64_t stop = std::min(end, (f / unit + 1) * unit);
+      Tile u = t;
+      u.full_begin = f;
+      u.state_begin = t.state_begin + (f - t.full_begin);
+      u.len = int32_t(stop - f);
+      out.push_back(u);
+      f = stop;
+    }
+  }
+  return out;
+}
+
+// The plan's step tiles on the current device (built and uploaded on first use).
+fsp_status device_step_tiles(const fsp_plan* p, const Tile** out, int64_t* n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
+  std::lock_guard<std::mutex> lock(p->mu);
+  auto it = p->device_step_tiles.find(dev);
+  if (it == p->device_step_tiles.end()) {
+    const std::vector<Tile> host = split_tiles(p->tiles, kStepTileElems);
+    Tile* d = nullptr;
+    e = cudaMalloc(&d, std::max<size_t>(1, host.size()) * sizeof(Tile));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FSP_ENOMEM, cuda_msg("cudaMalloc (step tile table)", e));
+    }
+    e = cudaMemcpy(d, host.data(), host.size() * sizeof(Tile), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      cudaFree(d);
+      return fail(FSP_ECUDA, cuda_msg("cudaMemcpy (step tile table)", e));
+    }
+    it = p->device_step_tiles.emplace(dev, std::make_pair(d, int64_t(host.size()))).first;
+  }
+  *out = it->second.first;
+  *n = it->second.second;
+  return FSP_OK;
+}
+
 // Grid for a kernel on the current device: SM count times resident CTAs
 // (one for the bulk kernel), after allowing its dynamic shared memory.
 // Cached per (kernel, device).
@@ -241,13 +301,20 @@ constexpr int64_t kOrderedMinTilesPerCta = 16;
 
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
-fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned long long* fixed_ctr) {
+fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned long long* fixed_ctr,
+                  const fsp_plan* step_plan) {
   const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
                        : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
                                                 : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
   int grid = 0;
   fsp_status s = grid_for(k, &grid);
   if (s != FSP_OK) return s;
+  if (step_plan && !clip && !a.vgrads && a.gather && a.n_tiles >= kOrderedMinTilesPerCta * grid &&
+      a.n_tiles == int64_t(step_plan->tiles.size())) {
+    // a large plan on full-size buffers with the all-gather: the step tiles
+    s = device_step_tiles(step_plan, &a.tiles, &a.n_tiles);
+    if (s != FSP_OK) return s;
+  }
   // The generic kernel runs one CTA per tile: the block scheduler hands the
   // tiles out in order.  The bulk kernel keeps one CTA per SM.
   grid = int(std::min<int64_t>(k.bulk ? grid : int64_t(INT32_MAX), a.n_tiles));
@@ -376,7 +443,7 @@ fsp_status run_step(const fsp_plan* p, const void* const* grads, int32_t dtype, 
   s = step_args(p, grads, master, m, v, params, hp, step, &a);
   if (s != FSP_OK) return s;
   a.reduced = reduced;
-  return launch(a, dtype, stream);
+  return launch(a, dtype, stream, false, nullptr, p);
 }
 
 // Partial sums of the clipped step's norm, one array per plan and device: one
@@ -507,7 +574,7 @@ extern "C" fsp_status fsp_sharded_step_device_t(const fsp_plan* plan, const void
       s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, 1, &a);
       if (s != FSP_OK) return s;
       a.step_dev = step_dev;
-      s = launch(a, grad_dtype, cuda_stream);
+      s = launch(a, grad_dtype, cuda_stream, false, nullptr, plan);
       if (s != FSP_OK) return s;
     }
     if (advance) return advance_step(step_dev, st);
@@ -532,7 +599,7 @@ extern "C" fsp_status fsp_sharded_step_writeback(const fsp_plan* plan, void* con
     s = step_args(plan, grads, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
     if (s != FSP_OK) return s;
     a.writeback = 1;
-    return launch(a, grad_dtype, cuda_stream);
+    return launch(a, grad_dtype, cuda_stream, false, nullptr, plan);
   });
 }
 
@@ -551,7 +618,7 @@ extern "C" fsp_status fsp_sharded_step_fp32_gather(const fsp_plan* plan, const v
     s = step_args(plan, grad_bufs, master, exp_avg, exp_avg_sq, param_bufs, hp, step, &a);
     if (s != FSP_OK) return s;
     a.param_f32 = 1;
-    return launch(a, grad_dtype, cuda_stream);
+    return launch(a, grad_dtype, cuda_stream, false, nullptr, plan);
   });
 }
 
@@ -680,14 +747,17 @@ extern "C" fsp_status fsp_sharded_step_noalloc(const fsp_plan* plan, const void*
   });
 }
 
-extern "C" fsp_status fsp_plan_tiles(const fsp_plan* plan, fsp_tile* out, int64_t cap, int64_t* n) {
+extern "C" fsp_status fsp_plan_tiles(const fsp_plan* plan, int32_t unit, fsp_tile* out, int64_t cap, int64_t* n) {
   return fsp::guard([&]() -> fsp_status {
     using namespace fsp;
     clear_error();
     if (!plan || !n) return fail(FSP_EINVAL, "plan or n is NULL");
+    if (unit < 0 || unit % 8 != 0 || (unit > 0 && kTileElems % unit != 0))
+      return fail(FSP_EINVAL, "unit must be 0 or a multiple of 8 that divides 4096");
     if (cap < 0 || (cap > 0 && !out)) return fail(FSP_EINVAL, "out is NULL or cap < 0");
     static_assert(sizeof(fsp_tile) == sizeof(Tile), "fsp_tile mirrors the internal tile");
-    const std::vector<Tile>& tiles = plan->tiles;
+    const std::vector<Tile> cut = unit > 0 ? split_tiles(plan->tiles, unit) : std::vector<Tile>();
+    const std::vector<Tile>& tiles = unit > 0 ? cut : plan->tiles;
     *n = int64_t(tiles.size());
     const int64_t k = std::min<int64_t>(cap, int64_t(tiles.size()));
     for (int64_t i = 0; i < k; ++i)

@@ -96,7 +96,7 @@ def lib():
     L.fsp_plan_info_get.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
     L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
-    L.fsp_plan_tiles.argtypes = [vp, ctypes.POINTER(_Tile), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+    L.fsp_plan_tiles.argtypes = [vp, i32, ctypes.POINTER(_Tile), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
     L.fsp_plan_destroy.argtypes = [vp]
     L.fsp_plan_destroy.restype = None
     step_args = [vp, ctypes.POINTER(vp), i32, vp, vp, vp, ctypes.POINTER(vp), ctypes.POINTER(_HParams), i64]
@@ -202,13 +202,14 @@ class Plan:
             self._param_offsets = tuple(out)
         return self._param_offsets
 
-    def tiles(self) -> list:
-        """The work tiles as (full_begin, state_begin, len, rank, param) tuples
-        (see ``fsp_plan_tiles``)."""
+    def tiles(self, unit: int = 0) -> list:
+        """The work tiles as (full_begin, state_begin, len, rank, param) tuples:
+        the plan's own (unit 0) or split at multiples of ``unit`` elements (the
+        step kernels run full-size buffers on unit 2048; see ``fsp_plan_tiles``)."""
         n = ctypes.c_int64()
-        _check(lib().fsp_plan_tiles(self._h, None, 0, ctypes.byref(n)), "fsp_plan_tiles")
+        _check(lib().fsp_plan_tiles(self._h, int(unit), None, 0, ctypes.byref(n)), "fsp_plan_tiles")
         buf = (_Tile * max(1, n.value))()
-        _check(lib().fsp_plan_tiles(self._h, buf, n.value, ctypes.byref(n)), "fsp_plan_tiles")
+        _check(lib().fsp_plan_tiles(self._h, int(unit), buf, n.value, ctypes.byref(n)), "fsp_plan_tiles")
         return [(t.full_begin, t.state_begin, t.len, t.rank, t.param) for t in buf[:n.value]]
 
     def ledger(self, grad_dtype: str = "f32") -> dict:

@@ -39,9 +39,11 @@
  *     device, and the only device-side waits are the step kernel's bounded
  *     waits on its own copy pipeline (see fsp_device_error).
  *   - The caller owns every device buffer and the CUDA stream.  The library
- *     owns plans and, per device, a small read-only table of work tiles that a
- *     plan uploads on its first step on that device (one cudaMalloc and one
- *     synchronous copy; make that first call outside any stream capture).
+ *     owns plans and, per device, small read-only tables of work tiles that a
+ *     plan uploads on its first step on that device (the plan's tiles and, for
+ *     steps with the all-gather on full-size buffers of large plans, the same
+ *     tiles split at 2048 elements; one cudaMalloc and one synchronous copy
+ *     each; make that first call outside any stream capture).
  *     It also owns one CUDA memory pool per device: a step whose plan has at
  *     least 16 work tiles per SM takes an 8-byte tile counter from it on the
  *     step's stream, zeroed before the kernel and freed after it
@@ -215,13 +217,18 @@ typedef struct {
   int32_t len, rank, param, reserved;
 } fsp_tile;
 
-/* The plan's work tiles (host only, no device call): each non-empty segment
- * cut at multiples of 4096 elements of the full index, in full-index order.
- * The step kernels run them in this order (plans with at least 16 tiles per
- * CTA: taken in order from a counter; smaller ones: CTA b takes tiles b,
- * b + grid, ...).  The number goes to *n; up to `cap` tiles to `out` (out may
- * be NULL when cap is 0). */
-fsp_status fsp_plan_tiles(const fsp_plan* plan, fsp_tile* out, int64_t cap, int64_t* n);
+/* The work tiles (host only, no device call).  unit == 0: the plan's tiles,
+ * each non-empty segment cut at multiples of 4096 elements of the full index,
+ * in full-index order - the schedule of small plans, the ZeRO-3 step,
+ * per-parameter tensors, the clipped flow, the unshard and the host-buffer
+ * step.  unit > 0 (a multiple of 8 that divides 4096): those tiles split at
+ * multiples of `unit` elements, in the same order; the step kernels run steps
+ * with the all-gather on full-size buffers of plans with at least 16 tiles
+ * per resident CTA on unit 2048.
+ * Step kernels take the tiles in order from a counter on plans with at least
+ * 16 tiles per CTA, else CTA b takes tiles b, b + grid, ...  The number goes
+ * to *n; up to `cap` tiles to `out` (out may be NULL when cap is 0). */
+fsp_status fsp_plan_tiles(const fsp_plan* plan, int32_t unit, fsp_tile* out, int64_t cap, int64_t* n);
 
 /* Frees the plan and its device tile tables.  NULL is a no-op. */
 void fsp_plan_destroy(fsp_plan* plan);

@@ -438,12 +438,43 @@ def test_plan_tiles_checks_its_arguments():
     L = B.lib()
     plan = fsp.plan_layout([(4099,)], 2)
     n = ctypes.c_int64()
-    assert L.fsp_plan_tiles(None, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
-    assert L.fsp_plan_tiles(plan.handle, None, 0, None) == B.FSP_EINVAL
-    assert L.fsp_plan_tiles(plan.handle, None, 1, ctypes.byref(n)) == B.FSP_EINVAL      # cap > 0 needs out
-    assert L.fsp_plan_tiles(plan.handle, None, -1, ctypes.byref(n)) == B.FSP_EINVAL
-    assert L.fsp_plan_tiles(plan.handle, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+    assert L.fsp_plan_tiles(None, 0, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, 0, None, 0, None) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, 0, None, 1, ctypes.byref(n)) == B.FSP_EINVAL      # cap > 0 needs out
+    assert L.fsp_plan_tiles(plan.handle, 0, None, -1, ctypes.byref(n)) == B.FSP_EINVAL
+    for unit in (-8, 12, 24):                                                              # not 8k dividing 4096
+        assert L.fsp_plan_tiles(plan.handle, unit, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_tiles(plan.handle, 0, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
     buf = (B._Tile * 1)()                                                             # a short buffer: the first tiles only
-    assert L.fsp_plan_tiles(plan.handle, buf, 1, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+    assert L.fsp_plan_tiles(plan.handle, 0, buf, 1, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
     first = plan.tiles()[0]
     assert (buf[0].full_begin, buf[0].state_begin, buf[0].len) == first[:3]
+
+
+@pytest.mark.parametrize("shapes,n_d,mode,unit", [
+    (None, 4, "fsdp2", 2048),                                         # the one-layer Qwen3 workload
+    (((3001, 7), (5, 4099), (1,), (12289,), (777, 64)), 6, "fsdp2", 2048),
+    (((4097,), (64, 129), (2, 3, 5)), 3, "distopt", 1024),
+    (((9,), (1,), (3,)), 2, "fsdp2", 8),
+])
+def test_step_tiles_split_the_plan_tiles(shapes, n_d, mode, unit):
+    """The step kernels' schedule on full-size buffers: the plan's tiles split
+    at multiples of `unit` of the full index, in the same order, every element
+    exactly once with the same owner, parameter and state offset."""
+    from synth_inputs import workload
+    shapes = shapes or workload(0).shapes
+    plan = fsp.plan_layout(shapes, n_d, mode)
+    base = plan.tiles(0)
+    cut = plan.tiles(unit)
+    assert len(cut) >= len(base)
+    it = iter(cut)
+    for fb, sb, ln, r, pm in base:
+        f = fb
+        while f < fb + ln:
+            cf, cs, cl, cr, cp = next(it)
+            assert (cf, cs, cr, cp) == (f, sb + (f - fb), r, pm)
+            assert 0 < cl <= unit and cf // unit == (cf + cl - 1) // unit     # inside one unit
+            assert cf + cl == fb + ln or (cf + cl) % unit == 0                 # cut only at unit multiples
+            f += cl
+        assert f == fb + ln
+    assert next(it, None) is None
