@@ -679,15 +679,18 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     uint32_t phase = 0;
     uint32_t used = 0;   // stages that ever received a header (bit s)
     bool ok = true;
-    // Look-ahead.  Full-size buffers: at a tile's start the next tile is
-    // claimed and its descriptor requested (used a tile later).  Per-parameter
-    // tensors, whose rank bases are read through a tile's descriptor: tiles
-    // are claimed two ahead and descriptors loaded one ahead, and a tile's
-    // bases are requested from its already-loaded descriptor one tile ahead
-    // (kept in registers), so that no load's latency stalls the producer at a
-    // tile's start (measured: the per-parameter ZeRO-3 step 4.54 instead of
-    // 4.98 ms on Qwen3-0.6B).
-    const bool deep = per_param;
+    // Look-ahead.  By default, at a tile's start the next tile is claimed and
+    // its descriptor requested (used a tile later).  Per-parameter tensors,
+    // whose rank bases are read through a tile's descriptor, and the ZeRO-3
+    // step on large plans (no all-gather stores, so nothing hides a stall):
+    // tiles are claimed two ahead and descriptors loaded one ahead, and a
+    // tile's bases are requested from its already-loaded descriptor one tile
+    // ahead (kept in registers), so that no load's latency stalls the producer
+    // at a tile's start.  Measured on Qwen3-0.6B: the per-parameter ZeRO-3 step
+    // 4.54 instead of 4.98 ms, the ZeRO-3 step on full-size buffers 4.51
+    // instead of 4.64; the step with the all-gather is 0.2-0.5 % faster with
+    // the one-tile look-ahead.
+    const bool deep = per_param || (a.tile_ctr != nullptr && !a.gather);
     int64_t k = 0;
     int64_t t_cur = next_tile(a, k++);
     Tile d_cur = t_cur < a.n_tiles ? a.tiles[t_cur] : Tile{};
