@@ -471,7 +471,7 @@ fsp_status fsp_unshard_params(const fsp_plan* plan, const fsp_param_table* table
  *   may wait on the host for earlier work on the stream.  Plans with more
  *   tiles (roughly more than 1.07e9 elements) return FSP_EUNSUPPORTED.
  *   The first call on a device looks up that array's device address (with the
- *   device current); make that first call before any stream capture.
+ *   device current) and keeps it for later calls.
  *   Every call shares the one array, which keeps the last list copied into it:
  *   calls that can overlap on the GPU (other streams, other threads) race and
  *   must be ordered by the caller.  Nothing in the array needs clearing
