@@ -209,7 +209,8 @@ fsp_status run_step_host(const fsp_plan* p, const void* const* host_grads, int32
     }
     a.tiles = dtiles + cuts[k];
     a.n_tiles = int64_t(cuts[k + 1] - cuts[k]);
-    s = launch(a, dtype, cs_main);
+    // (a plain launch: the kernel follows the copies' events, not only the previous chunk's kernel)
+    s = launch(a, dtype, cs_main, false, nullptr, nullptr, false);
     if (s != FSP_OK) {
       cleanup();
       return s;

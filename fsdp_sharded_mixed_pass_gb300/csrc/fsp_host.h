@@ -22,6 +22,9 @@ std::string cuda_msg(const char* what, cudaError_t e);
 bool finite_nonneg(float x);
 // Whether [ptr, ptr + bytes) lies inside one live allocation of the driver.
 fsp_status check_allocation(const void* ptr, size_t bytes, const char* name);
+// Copies a host table into device memory and returns once it has landed
+// (a table that kernels on any stream may read).
+cudaError_t upload_table(void* dst, const void* src, size_t bytes);
 // The plan's tile table on the current device (uploaded on first use).
 fsp_status device_tiles(const fsp_plan* p, const Tile** out);
 // AdamW scalars of update t, and the plan's rank layout, into `a`.
@@ -38,8 +41,12 @@ fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 // the all-gather (no clip, no per-parameter tables) runs on the plan's step
 // tiles instead (the tiles split at multiples of 2048 elements, uploaded once
 // per plan and device).
+// `early_start`: the bulk kernel is launched with programmatic stream
+// serialisation (its prologue may overlap the previous kernel on the stream;
+// it waits for that kernel on the device before reading or writing buffers).
 fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip = false,
-                  unsigned long long* fixed_ctr = nullptr, const fsp_plan* step_plan = nullptr);
+                  unsigned long long* fixed_ctr = nullptr, const fsp_plan* step_plan = nullptr,
+                  bool early_start = true);
 // Passes 1-3 of the clipped flow on a prepared argument block (non-empty
 // plan, fp32 grads; HSDP plans too); clipped_empty writes norm_out = {0, 1}
 // for a plan with nothing to reduce.

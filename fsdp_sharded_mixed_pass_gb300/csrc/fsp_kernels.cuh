@@ -578,6 +578,15 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Programmatic dependent launch.  launch_dependents: the next launch on the
+// stream that allows it may be scheduled (its CTAs take SMs as this grid's
+// CTAs leave them and run up to their own grid_dependency_wait).
+// grid_dependency_wait: returns once the launches this grid depends on have
+// completed and their writes are visible (at once for a launch without the
+// attribute).  A kernel launched with it must read and write nothing that an
+// earlier launch may write before it waits.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // ever arrives at; the wait must give up after `limit_ns` and report through
 // the device error word, exactly as the step kernel's waits do.
@@ -658,6 +667,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     return reinterpret_cast<uint16_t**>(smem + Cfg::kBaseOff + s * Cfg::kBaseStride + 8 * N);
   };
 
+  // The next step launch may start its prologue on the SMs this grid frees;
+  // this grid's own reads of the step's buffers wait for the previous launch
+  // below (the tile list and the per-parameter tables are written by no kernel).
+  launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);                  // producer's arrive (+ the copies' bytes)
@@ -691,6 +704,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
     // instead of 4.64; the step with the all-gather is 0.2-0.5 % faster with
     // the one-tile look-ahead.
     const bool deep = per_param || (a.tile_ctr != nullptr && !a.gather);
+    if (a.tile_ctr) grid_dependency_wait();   // the counter is zeroed just before the launch
     int64_t k = 0;
     int64_t t_cur = next_tile(a, k++);
     Tile d_cur = t_cur < a.n_tiles ? a.tiles[t_cur] : Tile{};
@@ -721,6 +735,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
         pb[q] = pb_n1[q];
       }
     }
+    if (!a.tile_ctr) grid_dependency_wait();   // first descriptors fetched: now the data
     for (;;) {
       const Tile tile = d_cur;
       const bool done = t_cur >= a.n_tiles;
@@ -831,6 +846,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
   if (warp == kConsumerWarps + 1) {
     // ---------------- storer: one thread writes finished stages back ----------------
     if (lane != 0) return;
+    grid_dependency_wait();
     int stage = 0;
     uint32_t phase = 0;
     for (;;) {
@@ -887,6 +903,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) sharded_step_kernel(const __g
 
   // ---------------- consumers: fold, update, cast in shared memory ----------------
   const int tid = threadIdx.x;
+  grid_dependency_wait();   // before the clip coefficient, t in device memory and the tile edges
   const float coef = kClip ? a.clip[1] : 1.f;
   const Coeffs cf = coeffs_of(a);
   int stage = 0;

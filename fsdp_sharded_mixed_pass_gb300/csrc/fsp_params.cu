@@ -109,11 +109,11 @@ fsp_status create_table(const fsp_plan* p, const void* const* grad_ptrs, int32_t
   const size_t bytes = std::max<size_t>(1, vg.size()) * sizeof(void*);
   e = cudaMalloc(reinterpret_cast<void**>(&t->vgrads), bytes);
   if (e == cudaSuccess && !vg.empty())
-    e = cudaMemcpy(t->vgrads, vg.data(), vg.size() * sizeof(void*), cudaMemcpyHostToDevice);
+    e = upload_table(t->vgrads, vg.data(), vg.size() * sizeof(void*));
   if (e == cudaSuccess && param_ptrs) {
     e = cudaMalloc(reinterpret_cast<void**>(&t->vparams), bytes);
     if (e == cudaSuccess && !vp.empty())
-      e = cudaMemcpy(t->vparams, vp.data(), vp.size() * sizeof(void*), cudaMemcpyHostToDevice);
+      e = upload_table(t->vparams, vp.data(), vp.size() * sizeof(void*));
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -120,6 +120,16 @@ fsp_status check_allocation(const void* ptr, size_t bytes, const char* name) {
   return FSP_OK;
 }
 
+// A synchronous cudaMemcpy from pageable host memory may return before its
+// last bytes have reached the device (it is ordered on the legacy stream
+// only); tables that kernels on any stream read later are complete once this
+// returns.
+cudaError_t upload_table(void* dst, const void* src, size_t bytes) {
+  cudaError_t e = cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
+  return e;
+}
+
 fsp_status device_tiles(const fsp_plan* p, const Tile** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -137,7 +147,7 @@ fsp_status device_tiles(const fsp_plan* p, const Tile** out) {
     cudaGetLastError();
     return fail(FSP_ENOMEM, cuda_msg("cudaMalloc (tile table)", e));
   }
-  e = cudaMemcpy(d, p->tiles.data(), bytes, cudaMemcpyHostToDevice);
+  e = upload_table(d, p->tiles.data(), bytes);
   if (e != cudaSuccess) {
     cudaFree(d);
     return fail(FSP_ECUDA, cuda_msg("cudaMemcpy (tile table)", e));
@@ -195,7 +205,7 @@ fsp_status device_step_tiles(const fsp_plan* p, const Tile** out, int64_t* n) {
       cudaGetLastError();
       return fail(FSP_ENOMEM, cuda_msg("cudaMalloc (step tile table)", e));
     }
-    e = cudaMemcpy(d, host.data(), host.size() * sizeof(Tile), cudaMemcpyHostToDevice);
+    e = upload_table(d, host.data(), host.size() * sizeof(Tile));
     if (e != cudaSuccess) {
       cudaFree(d);
       return fail(FSP_ECUDA, cuda_msg("cudaMemcpy (step tile table)", e));
@@ -302,7 +312,7 @@ constexpr int64_t kOrderedMinTilesPerCta = 16;
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
 fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned long long* fixed_ctr,
-                  const fsp_plan* step_plan) {
+                  const fsp_plan* step_plan, bool early_start) {
   const KernelInfo k = clip                     ? ClipKernels::get<true>(a.n_shard, a.n_rep)
                        : dtype == FSP_DTYPE_F32 ? Kernels<float>::get<false>(a.n_shard, a.n_rep)
                                                 : Kernels<__nv_bfloat16>::get<false>(a.n_shard, a.n_rep);
@@ -340,7 +350,21 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned 
     a.tile_ctr = static_cast<unsigned long long*>(ctr);
   }
   void* args[] = {&a};
-  cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(k.threads), args, size_t(k.smem), st);
+  // The bulk kernel allows programmatic stream serialisation: launched right
+  // after another kernel on the stream, its CTAs may start (set up their
+  // barriers, fetch their first tile descriptors) while that kernel's last
+  // CTAs finish, and wait for it on the device before touching its buffers.
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(k.threads);
+  cfg.dynamicSmemBytes = size_t(k.smem);
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = k.bulk && early_start ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
   if (a.tile_ctr && a.tile_ctr != fixed_ctr) {
     const cudaError_t f = cudaFreeAsync(a.tile_ctr, st);
     if (e == cudaSuccess) e = f;

@@ -50,7 +50,12 @@
  *     (stream-ordered, so concurrent steps and CUDA-graph replays each get
  *     their own; the kernel hands its tiles out in order from it).
  *   - Steps are asynchronous on the given stream (NULL = legacy default
- *     stream) and run on the current CUDA device.
+ *     stream) and run on the current CUDA device.  Stream order is kept: the
+ *     bulk step kernel is launched with programmatic stream serialisation, so
+ *     right after another kernel on the stream its CTAs may start and set up
+ *     while that kernel finishes, but they read and write no buffer before it
+ *     has completed.  (The host-buffer entry launches it plainly.)
+ *     "One synchronous copy" above returns only once the table has landed.
  *   - A plan may be used from several threads at once; fsp_plan_destroy must
  *     not race with any call or in-flight step using the same plan.
  */
