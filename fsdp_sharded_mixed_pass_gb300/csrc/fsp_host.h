@@ -40,7 +40,9 @@ fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 // resident CTA) that holds all of that plan's tiles on full-size buffers with
 // the all-gather (no clip, no per-parameter tables) runs on the plan's step
 // tiles instead (the tiles split at multiples of 2048 elements, uploaded once
-// per plan and device).
+// per plan and device); a bulk launch of a smaller plan's tiles over several
+// rounds of CTAs takes them in balanced order where that lowers the busiest
+// CTA's work (uploaded once per plan and device).
 // `early_start`: the bulk kernel is launched with programmatic stream
 // serialisation (its prologue may overlap the previous kernel on the stream;
 // it waits for that kernel on the device before reading or writing buffers).

@@ -194,7 +194,7 @@ fsp_status run_step_params(const fsp_plan* p, const fsp_param_table* t, float* m
   StepArgs a;
   s = params_step_args(p, t, master, m, v, hp, step, &a);
   if (s != FSP_OK) return s;
-  return launch(a, t->grad_dtype, stream);
+  return launch(a, t->grad_dtype, stream, false, nullptr, p);
 }
 
 fsp_status run_step_params_device_t(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,
@@ -213,7 +213,7 @@ fsp_status run_step_params_device_t(const fsp_plan* p, const fsp_param_table* t,
     s = params_step_args(p, t, master, m, v, hp, 1, &a);
     if (s != FSP_OK) return s;
     a.step_dev = step_dev;
-    s = launch(a, t->grad_dtype, stream);
+    s = launch(a, t->grad_dtype, stream, false, nullptr, p);
     if (s != FSP_OK) return s;
   }
   return advance ? advance_step(step_dev, stream) : FSP_OK;
@@ -231,7 +231,7 @@ fsp_status run_step_writeback_params(const fsp_plan* p, const fsp_param_table* t
   s = params_step_args(p, t, master, m, v, hp, step, &a);
   if (s != FSP_OK) return s;
   a.writeback = 1;
-  return launch(a, t->grad_dtype, stream);
+  return launch(a, t->grad_dtype, stream, false, nullptr, p);
 }
 
 fsp_status run_step_clipped_params(const fsp_plan* p, const fsp_param_table* t, float* master, float* m, float* v,

@@ -340,7 +340,8 @@ extern "C" fsp_status fsp_plan_ledger(const fsp_plan* p, int32_t grad_dtype, fsp
 
 extern "C" void fsp_plan_destroy(fsp_plan* p) {
   if (!p) return;
-  if (!p->device_tiles.empty() || !p->device_partials.empty() || !p->device_step_tiles.empty()) {
+  if (!p->device_tiles.empty() || !p->device_partials.empty() || !p->device_step_tiles.empty() ||
+      !p->device_round_tiles.empty()) {
     std::lock_guard<std::mutex> lock(p->mu);
     int prev = -1;
     const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
@@ -353,10 +354,14 @@ extern "C" void fsp_plan_destroy(fsp_plan* p) {
     for (auto& kv : p->device_step_tiles) {
       if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.first);
     }
+    for (auto& kv : p->device_round_tiles) {
+      if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.first);
+    }
     if (have_prev) cudaSetDevice(prev);
     p->device_tiles.clear();
     p->device_partials.clear();
     p->device_step_tiles.clear();
+    p->device_round_tiles.clear();
   }
   delete p;
 }

@@ -19,7 +19,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 # Every symbol include/fsp.h declares.
 EXPORTS = ("fsp_plan_layout", "fsp_plan_layout_hsdp", "fsp_plan_layout_params", "fsp_plan_param", "fsp_plan_info_get",
-           "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_tiles", "fsp_plan_destroy",
+           "fsp_plan_segment", "fsp_plan_ledger", "fsp_plan_tiles", "fsp_plan_round_order", "fsp_plan_destroy",
            "fsp_sharded_step", "fsp_sharded_step_device_t", "fsp_sharded_step_clipped", "fsp_sharded_step_debug",
            "fsp_sharded_step_writeback", "fsp_sharded_step_fp32_gather", "fsp_unshard_fp32", "fsp_shard",
            "fsp_host_step_workspace_bytes", "fsp_sharded_step_host", "fsp_param_table_create", "fsp_param_table_destroy",
@@ -97,6 +97,7 @@ def lib():
     L.fsp_plan_segment.argtypes = [vp, i64, ctypes.POINTER(_Segment)]
     L.fsp_plan_ledger.argtypes = [vp, i32, ctypes.POINTER(_Ledger)]
     L.fsp_plan_tiles.argtypes = [vp, i32, ctypes.POINTER(_Tile), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+    L.fsp_plan_round_order.argtypes = [vp, i32, ctypes.POINTER(_Tile), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
     L.fsp_plan_destroy.argtypes = [vp]
     L.fsp_plan_destroy.restype = None
     step_args = [vp, ctypes.POINTER(vp), i32, vp, vp, vp, ctypes.POINTER(vp), ctypes.POINTER(_HParams), i64]
@@ -210,6 +211,16 @@ class Plan:
         _check(lib().fsp_plan_tiles(self._h, int(unit), None, 0, ctypes.byref(n)), "fsp_plan_tiles")
         buf = (_Tile * max(1, n.value))()
         _check(lib().fsp_plan_tiles(self._h, int(unit), buf, n.value, ctypes.byref(n)), "fsp_plan_tiles")
+        return [(t.full_begin, t.state_begin, t.len, t.rank, t.param) for t in buf[:n.value]]
+
+    def round_order(self, grid: int) -> list:
+        """The tiles in the order a bulk step launch of ``grid`` CTAs strides
+        over them (CTA b takes entries b, b + grid, ...), as ``tiles`` tuples;
+        see ``fsp_plan_round_order``."""
+        n = ctypes.c_int64()
+        _check(lib().fsp_plan_round_order(self._h, int(grid), None, 0, ctypes.byref(n)), "fsp_plan_round_order")
+        buf = (_Tile * max(1, n.value))()
+        _check(lib().fsp_plan_round_order(self._h, int(grid), buf, n.value, ctypes.byref(n)), "fsp_plan_round_order")
         return [(t.full_begin, t.state_begin, t.len, t.rank, t.param) for t in buf[:n.value]]
 
     def ledger(self, grad_dtype: str = "f32") -> dict:

@@ -224,16 +224,29 @@ typedef struct {
 
 /* The work tiles (host only, no device call).  unit == 0: the plan's tiles,
  * each non-empty segment cut at multiples of 4096 elements of the full index,
- * in full-index order - the schedule of small plans, the ZeRO-3 step,
- * per-parameter tensors, the clipped flow, the unshard and the host-buffer
- * step.  unit > 0 (a multiple of 8 that divides 4096): those tiles split at
- * multiples of `unit` elements, in the same order; the step kernels run steps
- * with the all-gather on full-size buffers of plans with at least 16 tiles
- * per resident CTA on unit 2048.
+ * in full-index order - the tiles of small plans (in fsp_plan_round_order's
+ * order), the ZeRO-3 step, per-parameter tensors, the clipped flow, the
+ * unshard and the host-buffer step.  unit > 0 (a multiple of 8 that divides
+ * 4096): those tiles split at multiples of `unit` elements, in the same
+ * order; the step kernels run steps with the all-gather on full-size buffers
+ * of plans with at least 16 tiles per resident CTA on unit 2048.
  * Step kernels take the tiles in order from a counter on plans with at least
- * 16 tiles per CTA, else CTA b takes tiles b, b + grid, ...  The number goes
- * to *n; up to `cap` tiles to `out` (out may be NULL when cap is 0). */
+ * 16 tiles per CTA, else CTA b takes entries b, b + grid, ... of the round
+ * order below.  The number goes to *n; up to `cap` tiles to `out` (out may be
+ * NULL when cap is 0). */
 fsp_status fsp_plan_tiles(const fsp_plan* plan, int32_t unit, fsp_tile* out, int64_t cap, int64_t* n);
+
+/* The order in which the bulk step kernel, launched with `grid` (>= 1) CTAs,
+ * takes the plan's tiles when it strides over them (plans with fewer than 16
+ * tiles per CTA; CTA b takes entries b, b + grid, b + 2 grid, ...).  Host
+ * only.  Each round of `grid` consecutive tiles is handed out longest first
+ * to the CTAs with the fewest 1024-element chunks so far (a partial chunk
+ * counts as one), the CTAs renumbered so that the last, partial round goes to
+ * CTAs 0 .. n - 1; this order is used only where it lowers the busiest CTA's
+ * chunk count, else the plan's own order is (and is what this returns).
+ * Every round holds the same tiles as in the plan's order.  *n, out, cap as
+ * in fsp_plan_tiles; grid < 1: FSP_EINVAL. */
+fsp_status fsp_plan_round_order(const fsp_plan* plan, int32_t grid, fsp_tile* out, int64_t cap, int64_t* n);
 
 /* Frees the plan and its device tile tables.  NULL is a no-op. */
 void fsp_plan_destroy(fsp_plan* plan);

@@ -449,6 +449,47 @@ def test_plan_tiles_checks_its_arguments():
     assert L.fsp_plan_tiles(plan.handle, 0, buf, 1, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
     first = plan.tiles()[0]
     assert (buf[0].full_begin, buf[0].state_begin, buf[0].len) == first[:3]
+    # the round order: same conventions, grid >= 1
+    assert L.fsp_plan_round_order(None, 152, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_round_order(plan.handle, 152, None, 0, None) == B.FSP_EINVAL
+    assert L.fsp_plan_round_order(plan.handle, 152, None, 1, ctypes.byref(n)) == B.FSP_EINVAL
+    for grid in (0, -1):
+        assert L.fsp_plan_round_order(plan.handle, grid, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
+    assert L.fsp_plan_round_order(plan.handle, 1, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+
+
+def _busiest_cta_chunks(tiles, grid):
+    """Most 1024-element chunks (a partial one counting as one) any CTA takes
+    when CTA b takes entries b, b + grid, ... of `tiles`."""
+    load = [0] * grid
+    for i, t in enumerate(tiles):
+        load[i % grid] += -(-t[2] // 1024)
+    return max(load)
+
+
+@pytest.mark.parametrize("n_d,mode,grid", [(4, "fsdp2", 152), (8, "fsdp2", 152), (2, "fsdp2", 152),
+                                           (4, "distopt", 152), (6, "fsdp2", 100), (4, "fsdp2", 7),
+                                           (4, "fsdp2", 1), (4, "fsdp2", 5000)])
+def test_round_order_balances_the_stride(n_d, mode, grid):
+    """The order small plans are strided over: each round of `grid` entries
+    holds exactly the plan's tiles of that round (so the CTAs' window of the
+    buffers is the plan order's), and the busiest CTA's chunk count is below
+    the plain stride's, or the plan's own order is returned.  On the one-layer
+    Qwen3 workload (N_d = 4, 152 CTAs) the busiest CTA goes from 20 chunks to
+    17 against a mean of 15.4."""
+    from synth_inputs import workload
+    plan = fsp.plan_layout(workload(0).shapes, n_d, mode)
+    base = plan.tiles(0)
+    order = plan.round_order(grid)
+    assert len(order) == len(base)
+    for k in range(0, len(base), grid):
+        assert sorted(order[k:k + grid]) == sorted(base[k:k + grid])
+    b, o = _busiest_cta_chunks(base, grid), _busiest_cta_chunks(order, grid)
+    assert o < b or order == base
+    if (n_d, mode, grid) == (4, "fsdp2", 152):
+        assert (o, b) == (17, 20)
+    if grid == 1 or grid >= len(base):      # one CTA, or one partial round: nothing to balance
+        assert order == base
 
 
 @pytest.mark.parametrize("shapes,n_d,mode,unit", [
