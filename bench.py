@@ -15,7 +15,8 @@ per param).
 Other flows (each reports its own bytes per param): --clip MAX_NORM,
 --writeback, --no-gather, --unshard, --fp32-gather, and --per-param (alone or
 with any of those); --n-d N and --param-slice a:b change the workload,
---layers K steps K copies of it back to back (one plan per layer), --graph
+--layers K steps K copies of it back to back (one plan per layer; the plain
+step, --no-gather or --unshard), --graph
 captures the timed steps.  The default run also times the other workloads
 after the headline one (the "workloads" list of the JSON line).
 
@@ -96,7 +97,8 @@ def parse_args(argv=None):
                     help="every rank's gradient and parameter of every parameter in a tensor of its own "
                          "(FSDP2 / HSDP; the step reads and writes them in place)")
     ap.add_argument("--layers", type=int, default=1,
-                    help="K copies of the workload, one plan each, stepped back to back per step (plain step only)")
+                    help="K copies of the workload, one plan each, stepped back to back per step (the plain step, "
+                         "--no-gather or --unshard)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the block that times the other workloads after the default one")
     ap.add_argument("--workload-steps", type=int, default=20,
@@ -857,19 +859,19 @@ def run_fsp(args):
         raise SystemExit("--fp32-gather: the plain step or --unshard")
     if args.per_param and args.no_gather and (args.clip is not None or args.writeback or args.unshard):
         raise SystemExit("--per-param --no-gather: the plain step only (the table has no parameter tensors)")
-    if args.layers > 1 and (args.clip is not None or args.unshard or args.no_gather or args.per_param
-                            or args.writeback or args.fp32_gather):
-        raise SystemExit("--layers: the plain step only")
+    if args.layers > 1 and (args.clip is not None or args.per_param or args.writeback or args.fp32_gather):
+        raise SystemExit("--layers: the plain step, --no-gather or --unshard")
     if args.layers > 1:
         wl = LayerStack(w, shapes, dev, args.layers)
         label = f"{label} x{args.layers} (one plan per layer, stepped back to back)"
     else:
         wl = DeviceWorkload(w, shapes, dev, per_param=args.per_param, fp32_gather=args.fp32_gather,
                             no_gather=args.no_gather and args.per_param)
-    wl.clip = args.clip
-    wl.unshard = args.unshard
-    wl.no_gather = args.no_gather
-    wl.writeback = args.writeback
+    for target in wl.layers if isinstance(wl, LayerStack) else [wl]:
+        target.clip = args.clip
+        target.unshard = args.unshard
+        target.no_gather = args.no_gather
+        target.writeback = args.writeback
     plan = wl.plan
     props = torch.cuda.get_device_properties(dev)
     clocks_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else None
@@ -975,7 +977,7 @@ def run_fsp(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         **({"workloads": workloads} if workloads is not None else {}),
-        "gpu_launches": args.steps * (4 if args.clip is not None else 1),
+        "gpu_launches": args.steps * args.layers * (4 if args.clip is not None else 1),
         "launch": "one CUDA graph of the K steps" if args.graph else "one launch per step from the host",
         "clocks": clocks,
     }

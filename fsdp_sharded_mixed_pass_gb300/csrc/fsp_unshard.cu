@@ -56,6 +56,11 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Programmatic dependent launch: let the next launch on the stream that allows
+// it be scheduled; wait until the launches this grid depends on have completed
+// and their writes are visible (at once for a launch without the attribute).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // At most N committed bulk groups may still be reading shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -78,6 +83,10 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
   const int ns = a.n_shard, nr = a.n_rep;
   const int i0 = threadIdx.x, i1 = threadIdx.x + kUnshardThreads;
   const bool per_param = a.vparams != nullptr;
+  // Launched with programmatic stream serialisation: nothing of the master or
+  // the parameter buffers is touched before the launch before this one is done.
+  launch_dependents();
+  grid_dependency_wait();
   int buf = 0;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
@@ -153,12 +162,22 @@ __global__ void __launch_bounds__(kUnshardThreads) unshard_kernel(const __grid_c
   if (threadIdx.x == 0) bulk_wait_read<0>();   // shared memory must outlive the stores' reads
 }
 
+// Launched with programmatic stream serialisation (see the kernel): right
+// after another kernel on the stream, its CTAs may be scheduled while that
+// kernel's last CTAs finish.
 cudaError_t launch_unshard(const UnshardArgs& a, int grid, void* stream) {
-  if (a.param_f32)
-    unshard_kernel<true><<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  else
-    unshard_kernel<false><<<grid, kUnshardThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kUnshardThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return a.param_f32 ? cudaLaunchKernelEx(&cfg, unshard_kernel<true>, a)
+                     : cudaLaunchKernelEx(&cfg, unshard_kernel<false>, a);
 }
 
 // ---- FSDP2 unshard: host side -----------------------------------------------------------

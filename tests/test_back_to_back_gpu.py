@@ -81,3 +81,36 @@ def test_device_resident_index_advanced_between_launches():
     assert int(t_dev.item()) == 5
     _assert_same(ref, run, "device-resident t")
     assert fsp.device_error() == 0
+
+
+def test_zero3_steps_then_unshard_back_to_back():
+    """ZeRO-3 steps (no all-gather) each followed at once by the unshard of
+    the new master (both kernels may start while the launch before them
+    finishes): every parameter copy must come from the master the step just
+    wrote, as with the host waiting after each launch."""
+    cases = []
+    for _ in range(2):
+        row = []
+        for i, (shapes, n_d, mode, gdt, n_rep) in enumerate(LAYERS):
+            row.append(DeviceCase(shapes, n_d, mode, gdt, 900 + i, n_rep))
+        cases.append(row)
+    ref, run = cases
+
+    def zero3_then_unshard(c, t, sync):
+        st = [s.t for s in c.state]
+        fsp.sharded_step(c.plan, [g.t for g in c.grads], *st, None, HP, t)
+        if sync:
+            torch.cuda.synchronize()
+        fsp.unshard(c.plan, st[0], [q.t for q in c.params])
+        if sync:
+            torch.cuda.synchronize()
+
+    for t in (1, 2, 3):
+        for c in ref:
+            zero3_then_unshard(c, t, True)
+        for c in run:
+            zero3_then_unshard(c, t, False)
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(ref, run)):
+        _assert_same(a, b, f"layer {i}")
+    assert fsp.device_error() == 0
