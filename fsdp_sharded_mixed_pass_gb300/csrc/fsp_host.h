@@ -33,9 +33,10 @@ void set_mesh(StepArgs& a, const fsp_plan* p);
 // hp and t within the ranges fsp.h states.
 fsp_status check_hparams(const fsp_adamw_hparams* hp, int64_t step);
 // Launches the step kernel for `a` (clip: the clipped update).
-// On plans with many tiles per CTA the bulk kernel takes its tiles in order
-// from a counter: `fixed_ctr` when given (zeroed here on `stream`), else one
-// allocated from a library pool on `stream` and freed after the launch.
+// On plans with many tiles per CTA (16, or 128 for the ZeRO-3 step of one
+// replica group) the bulk kernel takes its tiles in order from a counter:
+// `fixed_ctr` when given (zeroed here on `stream`), else one allocated from a
+// library pool on `stream` and freed after the launch.
 // With `step_plan` given, a launch of a large plan (at least 16 tiles per
 // resident CTA) that holds all of that plan's tiles on full-size buffers with
 // the all-gather (no clip, no per-parameter tables) runs on the plan's step

@@ -393,6 +393,15 @@ fsp_status counter_pool(cudaMemPool_t* out) {
 // launch, their copies spread over the whole buffers, and HBM throughput drops
 // (smaller plans finish before that matters).
 constexpr int64_t kOrderedMinTilesPerCta = 16;
+// The ZeRO-3 step of one replica group (no all-gather stores) keeps the fixed
+// stride, in balanced order, up to this many tiles per CTA.  Measured against
+// the counter (same box, two runs): one Qwen3-0.6B layer 129-131 vs 136-137 us
+// (per-parameter tensors 130 vs 137), two layers 250-251 vs 255, one layer of
+// the 1.5B bf16-gradient stack (73 tiles per CTA) 386-387 vs 397-398, four
+// Qwen3-0.6B layers (103) 492 vs 492-493; with the all-gather, or for HSDP,
+// the counter stays ahead from 16 tiles per CTA (one layer with the all-gather
+// 172 vs 184 us, HSDP ZeRO-3 190 vs 192).
+constexpr int64_t kOrderedMinTilesPerCtaZero3 = 128;
 
 // Launches the step for argument block `a` (tiles already on the device);
 // `clip`: the clipped update (a.clip set, fp32 grads, one replica group).
@@ -412,7 +421,8 @@ fsp_status launch(StepArgs& a, int32_t dtype, void* stream, bool clip, unsigned 
   }
   // The generic kernel runs one CTA per tile: the block scheduler hands the
   // tiles out in order.  The bulk kernel keeps one CTA per SM.
-  const bool ordered = k.bulk && a.n_tiles >= kOrderedMinTilesPerCta * grid;
+  const int64_t min_ordered = !a.gather && a.n_rep == 1 ? kOrderedMinTilesPerCtaZero3 : kOrderedMinTilesPerCta;
+  const bool ordered = k.bulk && a.n_tiles >= min_ordered * grid;
   if (step_plan && k.bulk && !ordered && a.n_tiles > grid && a.n_tiles == int64_t(step_plan->tiles.size())) {
     // a small plan's own tiles over several rounds: the balanced order
     const Tile* balanced = nullptr;

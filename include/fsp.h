@@ -45,8 +45,9 @@
  *     tiles split at 2048 elements; one cudaMalloc and one synchronous copy
  *     each; make that first call outside any stream capture).
  *     It also owns one CUDA memory pool per device: a step whose plan has at
- *     least 16 work tiles per SM takes an 8-byte tile counter from it on the
- *     step's stream, zeroed before the kernel and freed after it
+ *     least 16 work tiles per SM (the ZeRO-3 step of one replica group: 128)
+ *     takes an 8-byte tile counter from it on the step's stream, zeroed
+ *     before the kernel and freed after it
  *     (stream-ordered, so concurrent steps and CUDA-graph replays each get
  *     their own; the kernel hands its tiles out in order from it).
  *   - Steps are asynchronous on the given stream (NULL = legacy default
@@ -231,14 +232,15 @@ typedef struct {
  * order; the step kernels run steps with the all-gather on full-size buffers
  * of plans with at least 16 tiles per resident CTA on unit 2048.
  * Step kernels take the tiles in order from a counter on plans with at least
- * 16 tiles per CTA, else CTA b takes entries b, b + grid, ... of the round
- * order below.  The number goes to *n; up to `cap` tiles to `out` (out may be
+ * 16 tiles per CTA (128 for the ZeRO-3 step of one replica group), else CTA
+ * b takes entries b, b + grid, ... of the round order below.  The number goes to *n; up to `cap` tiles to `out` (out may be
  * NULL when cap is 0). */
 fsp_status fsp_plan_tiles(const fsp_plan* plan, int32_t unit, fsp_tile* out, int64_t cap, int64_t* n);
 
 /* The order in which the bulk step kernel, launched with `grid` (>= 1) CTAs,
  * takes the plan's tiles when it strides over them (plans with fewer than 16
- * tiles per CTA; CTA b takes entries b, b + grid, b + 2 grid, ...).  Host
+ * tiles per CTA, or 128 for the ZeRO-3 step of one replica group; CTA b takes
+ * entries b, b + grid, b + 2 grid, ...).  Host
  * only.  Each round of `grid` consecutive tiles is handed out longest first
  * to the CTAs with the fewest 1024-element chunks so far (a partial chunk
  * counts as one), the CTAs renumbered so that the last, partial round goes to
