@@ -775,9 +775,11 @@ def l2_note(moved: int, flush_bytes: int) -> str:
 # N_d = 16 stack, the HSDP 2 x 4 mesh), one after another, each freed before
 # the next.
 EXTRA_WORKLOADS = ("qwen3_layer", "qwen3_0p6b_distopt", "ragged_500", "dense_1p5b_bf16grad", "qwen3_0p6b_hsdp_2x4",
-                   ("qwen3_layer", 28))
-# (name, K): K copies of the workload stepped back to back (LayerStack) - the
-# one-layer step as it runs in a model of 28 such layers
+                   ("qwen3_layer", 28), ("qwen3_0p6b_fsdp2", 28, "1:12"))
+# (name, K[, a:b]): K copies of the workload (of its params a..b-1) stepped back
+# to back (LayerStack) - the one-layer step as it runs in a model of 28 such
+# layers, and the 28 decoder layers of the Qwen3-0.6B stack (params 1..11 are
+# its first layer) stepped one layer at a time
 
 
 def workload_entry(wl, label, ms, steps, clocks, flush_bytes, peak, graph_ms_per_step=None) -> dict:
@@ -803,8 +805,8 @@ def time_workloads(names, steps, warmup, dist, clocks_id, dev, l2, peak, param_s
     import torch
     out = []
     for spec in names:
-        name, layers = spec if isinstance(spec, tuple) else (spec, 1)
-        w, shapes, label = resolve_workload(name, param_slice, None)
+        name, layers, own_slice = (tuple(spec) + (None,))[:3] if isinstance(spec, tuple) else (spec, 1, None)
+        w, shapes, label = resolve_workload(name, own_slice or param_slice, None)
         if layers > 1:
             label = f"{label} x{layers} (one plan per layer, stepped back to back)"
         wl = None

@@ -53,12 +53,14 @@ def test_workloads_block_times_each_workload():
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     dist = bench.Dist(1)
     try:
-        out = bench.time_workloads(["qwen3_layer", "ragged_500", "dense_1p5b_bf16grad", ("qwen3_layer", 3)], 3, 3,
+        out = bench.time_workloads(["qwen3_layer", "ragged_500", "dense_1p5b_bf16grad", ("qwen3_layer", 3),
+                                    ("qwen3_0p6b_fsdp2", 2, "1:3")], 3, 3,
                                    dist, None, dev, l2, 6698.2, param_slice="1:6")
     finally:
         dist.close()
     assert [e["workload"] for e in out] == ["qwen3_layer[1:6]", "ragged_500[1:6]", "dense_1p5b_bf16grad[1:6]",
-                                            "qwen3_layer[1:6] x3 (one plan per layer, stepped back to back)"]
+                                            "qwen3_layer[1:6] x3 (one plan per layer, stepped back to back)",
+                                            "qwen3_0p6b_fsdp2[1:3] x2 (one plan per layer, stepped back to back)"]
     assert out[3]["layers"] == 3 and out[3]["params"] == 3 * out[0]["params"]
     assert out[3]["ms_per_layer"] == out[3]["ms_per_step"] / 3
     for e in out:
