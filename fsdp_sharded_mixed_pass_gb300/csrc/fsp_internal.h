@@ -73,9 +73,10 @@ struct fsp_plan {
   // Per device: `tiles` split at multiples of kStepTileElems (the step
   // kernels' schedule on full-size buffers) and their number.
   mutable std::map<int, std::pair<fsp::Tile*, int64_t>> device_step_tiles;
-  // Per device: `tiles` in the order a fixed-stride launch of `grid` CTAs
-  // takes them with its rounds balanced (balance_rounds), and that grid.
-  mutable std::map<int, std::pair<fsp::Tile*, int>> device_round_tiles;
+  // Per (device, grid): `tiles` in the order a fixed-stride launch of `grid`
+  // CTAs takes them with its rounds balanced (balance_rounds); nullptr where
+  // that order gains nothing (the launch keeps the plan's own order).
+  mutable std::map<std::pair<int, int>, fsp::Tile*> device_round_tiles;
 };
 
 // Per-parameter tensors registered for a per-parameter plan on one device

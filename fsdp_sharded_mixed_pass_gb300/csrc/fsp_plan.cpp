@@ -355,7 +355,7 @@ extern "C" void fsp_plan_destroy(fsp_plan* p) {
       if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.first);
     }
     for (auto& kv : p->device_round_tiles) {
-      if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.first);
+      if (kv.second && cudaSetDevice(kv.first.first) == cudaSuccess) cudaFree(kv.second);
     }
     if (have_prev) cudaSetDevice(prev);
     p->device_tiles.clear();

@@ -275,12 +275,9 @@ fsp_status device_round_tiles(const fsp_plan* p, int grid, const Tile** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FSP_ECUDA, cuda_msg("cudaGetDevice", e));
   std::lock_guard<std::mutex> lock(p->mu);
-  auto it = p->device_round_tiles.find(dev);
-  if (it != p->device_round_tiles.end() && it->second.second != grid) {
-    cudaFree(it->second.first);
-    p->device_round_tiles.erase(it);
-    it = p->device_round_tiles.end();
-  }
+  // one table per grid: a launch of another kernel of this plan may still read
+  // the table of its own grid
+  auto it = p->device_round_tiles.find({dev, grid});
   if (it == p->device_round_tiles.end()) {
     const std::vector<Tile> host = balance_rounds(p->tiles, grid);
     Tile* d = nullptr;
@@ -296,9 +293,9 @@ fsp_status device_round_tiles(const fsp_plan* p, int grid, const Tile** out) {
         return fail(FSP_ECUDA, cuda_msg("cudaMemcpy (balanced tile table)", e));
       }
     }
-    it = p->device_round_tiles.emplace(dev, std::make_pair(d, grid)).first;
+    it = p->device_round_tiles.emplace(std::make_pair(dev, grid), d).first;
   }
-  *out = it->second.first;
+  *out = it->second;
   return FSP_OK;
 }
 
