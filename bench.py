@@ -171,21 +171,39 @@ def workload_own_n_d(name: str) -> int:
     return (S.workload(int(name)) if name.isdigit() else S.workload(name)).n_d
 
 
+def _traffic_record() -> dict:
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    return kv
+
+
 def traffic_per_elem(workload_name: str):
     """ncu DRAM bytes per element of the step kernel, if the committed capture
     was taken on the current kernel source and workload family."""
     try:
-        kv = {}
-        with open(TRAFFIC_FILE) as f:
-            for line in f:
-                if ":" in line and not line.startswith("#"):
-                    k, v = line.split(":", 1)
-                    kv[k.strip()] = v.strip()
+        kv = _traffic_record()
         if kv.get("kernel_src") != kernel_src_hash():
             return None
         return float(kv[f"bytes_per_elem.{workload_name}"])
     except Exception:
         return None
+
+
+def traffic_basis(workload_name: str, elems: int) -> str | None:
+    """How the reported traffic was obtained: one captured launch of this size,
+    or a smaller one scaled by the elements."""
+    try:
+        n = int(_traffic_record()[f"elements.{workload_name}"])
+    except Exception:
+        return None
+    what = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch"
+    if n == elems:
+        return f"{what} of this size ({n} elements)"
+    return f"{what} of {n} elements, scaled to {elems}"
 
 
 class ClockSampler:
@@ -974,6 +992,9 @@ def run_fsp(args):
                      "traffic": tpe * P if tpe is not None and args.clip is None and not args.unshard
                      and not args.no_gather and not args.per_param and not args.writeback and not args.fp32_gather
                      else None,
+                     "traffic_basis": traffic_basis(w.name, P) if tpe is not None and args.clip is None
+                     and not args.unshard and not args.no_gather and not args.per_param and not args.writeback
+                     and not args.fp32_gather else None,
                      "kernel": "unshard_kernel" if args.unshard else step_kernel_name(w),
                      "kernel_src": kernel_src_hash()},
         "e2e": e2e,

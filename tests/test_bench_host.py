@@ -183,6 +183,10 @@ def test_traffic_record_matches_the_current_kernel_source():
         algorithmic = w.n_d * w.grad_bytes + 24 * w.n_rep + 2 * w.n_d
         tpe = bench.traffic_per_elem(name)
         assert tpe is not None and 0.95 < tpe / algorithmic < 1.05, name
+    # the headline workload's figure is a capture of its whole launch
+    P = 596049920
+    assert bench.traffic_basis("qwen3_0p6b_fsdp2", P).endswith(f"of this size ({P} elements)")
+    assert "scaled to" in bench.traffic_basis("ragged_500", 1407887633)
 
 
 def test_roofline_kernel_label_follows_the_mesh():
