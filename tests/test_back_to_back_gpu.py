@@ -114,3 +114,34 @@ def test_zero3_steps_then_unshard_back_to_back():
     for i, (a, b) in enumerate(zip(ref, run)):
         _assert_same(a, b, f"layer {i}")
     assert fsp.device_error() == 0
+
+
+def test_layer_stack_replayed_from_one_graph():
+    """The five plans' steps with the update index in device memory, captured
+    once in one CUDA graph (consecutive launches joined by programmatic
+    edges) and replayed: equal to the steps with host waits."""
+    ref, run = _cases(700), _cases(700)
+    for t in (1, 2, 3):
+        for c in ref:
+            c.step(t, debug=False)
+            torch.cuda.synchronize()
+    t_devs = [torch.ones(1, dtype=torch.int64, device="cuda") for _ in run]
+
+    def step_all(stream):
+        for c, t_dev in zip(run, t_devs):
+            fsp.sharded_step_device_t(c.plan, [g.t for g in c.grads], *[s.t for s in c.state],
+                                      [q.t for q in c.params], HP, t_dev, stream=stream)
+
+    side = torch.cuda.Stream()
+    step_all(side)          # t = 1, eager: every device table is uploaded outside the capture
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side, capture_error_mode="relaxed"):
+        step_all(side)
+    graph.replay()          # t = 2
+    graph.replay()          # t = 3
+    torch.cuda.synchronize()
+    assert [int(t.item()) for t in t_devs] == [4] * len(run)
+    for i, (a, b) in enumerate(zip(ref, run)):
+        _assert_same(a, b, f"layer {i}")
+    assert fsp.device_error() == 0
