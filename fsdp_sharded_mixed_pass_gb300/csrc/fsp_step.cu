@@ -237,6 +237,7 @@ int64_t busiest_cta_chunks(const std::vector<Tile>& tiles, int grid) {
 
 std::vector<Tile> balance_rounds(const std::vector<Tile>& tiles, int grid) {
   const size_t n_tiles = tiles.size(), g = size_t(grid);
+  if (n_tiles <= g) return tiles;   // one round, one tile per CTA: nothing to balance
   auto chunks = tile_chunks;
   std::vector<int64_t> load(g, 0);
   std::vector<size_t> owner(n_tiles);   // virtual CTA of each tile
@@ -898,7 +899,9 @@ extern "C" fsp_status fsp_plan_round_order(const fsp_plan* plan, int32_t grid, f
     if (grid < 1) return fail(FSP_EINVAL, "grid must be >= 1");
     if (cap < 0 || (cap > 0 && !out)) return fail(FSP_EINVAL, "out is NULL or cap < 0");
     std::vector<Tile> order = balance_rounds(plan->tiles, grid);
-    if (busiest_cta_chunks(order, grid) >= busiest_cta_chunks(plan->tiles, grid)) order = plan->tiles;
+    if (plan->tiles.size() <= size_t(grid) ||
+        busiest_cta_chunks(order, grid) >= busiest_cta_chunks(plan->tiles, grid))
+      order = plan->tiles;
     *n = int64_t(order.size());
     const int64_t k = std::min<int64_t>(cap, int64_t(order.size()));
     for (int64_t i = 0; i < k; ++i)

@@ -456,6 +456,9 @@ def test_plan_tiles_checks_its_arguments():
     for grid in (0, -1):
         assert L.fsp_plan_round_order(plan.handle, grid, None, 0, ctypes.byref(n)) == B.FSP_EINVAL
     assert L.fsp_plan_round_order(plan.handle, 1, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == plan.n_tiles
+    assert L.fsp_plan_round_order(plan.handle, 2 ** 31 - 1, None, 0, ctypes.byref(n)) == B.FSP_OK   # one round
+    empty = fsp.plan_layout([], 2)
+    assert L.fsp_plan_round_order(empty.handle, 152, None, 0, ctypes.byref(n)) == B.FSP_OK and n.value == 0
 
 
 def _busiest_cta_chunks(tiles, grid):
