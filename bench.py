@@ -969,6 +969,15 @@ def run_fsp(args):
                            sample_1_core=one["sample"])
             except Exception as e:
                 cpu["pool_error"] = str(e)[:300]
+        for e in workloads or []:
+            if e.get("workload") == "qwen3_layer" and "error" not in e:
+                # the one-layer workload's oracle step on one core too (its whole plan)
+                import synth_inputs as S
+                w0 = S.workload("qwen3_layer")
+                n0, r0, s0 = time_oracle(w0, w0.shapes, min(args.cpu_seconds, 3.0), use_device=True)
+                e["cpu_oracle_1_core"] = {"value": n0 * r0 / s0, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                          "sample": f"the whole plan ({n0} elements), oracle step repeated "
+                                                    f"{r0}x ({s0:.1f} s)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
