@@ -27,6 +27,7 @@ FLOWS = [
     [], ["--clip", "1.0"], ["--writeback"], ["--no-gather"], ["--unshard"], ["--fp32-gather"],
     ["--fp32-gather", "--unshard"], ["--per-param"], ["--per-param", "--unshard"], ["--graph"],
     ["--workload", "5"], ["--workload", "4"], ["--n-d", "9"], ["--workload", "0", "--layers", "3"],
+    ["--workload", "0", "--layers", "3", "--unshard"], ["--workload", "0", "--layers", "3", "--no-gather"],
 ]
 
 
@@ -42,6 +43,8 @@ def test_bench_flow_prints_one_line(flow, capsys):
         assert k in d, k
     assert d["value"] > 0 and d["roofline"]["achieved"] > 0
     assert "l2" in d["config"]
+    layers = int(flow[flow.index("--layers") + 1]) if "--layers" in flow else 1
+    assert d["gpu_launches"] == 3 * layers * (4 if "--clip" in flow else 1)
     import fsdp_sharded_mixed_pass_gb300 as fsp
     assert fsp.device_error() == 0
 
