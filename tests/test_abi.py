@@ -495,6 +495,25 @@ def test_round_order_balances_the_stride(n_d, mode, grid):
         assert order == base
 
 
+def test_round_order_on_random_plans():
+    """Random ragged plans and grids: the round order is a permutation of the
+    plan's tiles within every round (so the last, partial round only ever
+    holds the plan's last tiles, at CTAs 0 .. n - 1), and never leaves a CTA
+    busier than the plain stride does."""
+    rng = np.random.default_rng(20261202)
+    for _ in range(40):
+        n_d = int(rng.integers(1, 17))
+        shapes = [(int(rng.integers(1, 9000)),) if rng.random() < 0.4 else
+                  (int(rng.integers(1, 3000)), int(rng.integers(1, 700))) for _ in range(int(rng.integers(1, 30)))]
+        plan = fsp.plan_layout(shapes, n_d, "fsdp2" if rng.random() < 0.7 else "distopt")
+        base = plan.tiles(0)
+        grid = int(rng.integers(1, max(2, len(base))))
+        order = plan.round_order(grid)
+        for k in range(0, len(base), grid):
+            assert sorted(order[k:k + grid]) == sorted(base[k:k + grid])
+        assert _busiest_cta_chunks(order, grid) <= _busiest_cta_chunks(base, grid)
+
+
 @pytest.mark.parametrize("shapes,n_d,mode,unit", [
     (None, 4, "fsdp2", 2048),                                         # the one-layer Qwen3 workload
     (((3001, 7), (5, 4099), (1,), (12289,), (777, 64)), 6, "fsdp2", 2048),
