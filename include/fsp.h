@@ -52,10 +52,11 @@
  *     their own; the kernel hands its tiles out in order from it).
  *   - Steps are asynchronous on the given stream (NULL = legacy default
  *     stream) and run on the current CUDA device.  Stream order is kept: the
- *     bulk step kernel is launched with programmatic stream serialisation, so
- *     right after another kernel on the stream its CTAs may start and set up
- *     while that kernel finishes, but they read and write no buffer before it
- *     has completed.  (The host-buffer entry launches it plainly.)
+ *     bulk step kernel and the unshard kernel are launched with programmatic
+ *     stream serialisation, so right after another kernel on the stream their
+ *     CTAs may start and set up while that kernel finishes, but they read and
+ *     write no buffer before it has completed.  (The host-buffer entry
+ *     launches the step kernel plainly.)
  *     "One synchronous copy" above returns only once the table has landed.
  *   - A plan may be used from several threads at once; fsp_plan_destroy must
  *     not race with any call or in-flight step using the same plan.
